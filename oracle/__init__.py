@@ -1,0 +1,145 @@
+"""FP64 CPU oracle for attention + JVP and the TrigFlow helpers.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  It shares no code
+with the CUDA library and never imports it; its inputs are plain numpy arrays.
+
+The arithmetic lives in ``attn_jvp_oracle.c`` (plain C, FP64, two-pass
+softmax), following the page "带分数正则的一致性蒸馏" (gitcode.csdn.net):
+section 注意力 (attention) for O = softmax(s Q K^T) V and its JVP
+t_o = P t_v + t_p V, t_p = P (.) t_s - (P t_s^T) P, t_s = (t_q K^T + Q t_k^T) s;
+section 前向 (forward) for the natural-log LSE; section 时间步转换 (timestep
+conversion) for the TrigFlow wrapper coefficients and x_t = cos t x0 + sin t eps.
+The key-chunk merge is exact algebra on those definitions (the pages have no
+key split).
+
+Parity pins for every function here are in tests/test_oracle.py; none is unpinned.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import _build
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        dp = ctypes.POINTER(ctypes.c_double)
+        i64 = ctypes.c_int64
+        lib.oracle_attn_jvp_rows.argtypes = [dp] * 6 + [i64, i64, i64, i64, ctypes.c_double] + [dp] * 4 + [ctypes.c_int]
+        lib.oracle_attn_jvp_rows.restype = ctypes.c_int
+        lib.oracle_merge_chunks.argtypes = [dp] * 4 + [i64, i64, i64] + [dp] * 4
+        lib.oracle_merge_chunks.restype = ctypes.c_int
+        lib.oracle_trigflow_coeffs.argtypes = [ctypes.c_double, ctypes.c_double, dp]
+        lib.oracle_trigflow_coeffs.restype = ctypes.c_int
+        lib.oracle_trigflow_tangent.argtypes = [dp, dp, dp, i64, i64, dp]
+        lib.oracle_trigflow_tangent.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _f64(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def default_threads():
+    """Host threads the oracle uses by default: every core this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover - non-Linux
+        return os.cpu_count() or 1
+
+
+def attn_jvp(q, k, v, qt, kt, vt, scale, rows=None, nthreads=None):
+    """Attention output, its tangent, LSE and mu in FP64.
+
+    q, qt: [..., Nq, d]; k, kt: [..., Nk, d]; v, vt: [..., Nk, dv] with the
+    same leading dims (one independent head per leading index).  ``rows``:
+    optional 1-D array of query-row indices evaluated in every head (rows are
+    independent, so a subset is exact for those rows).  Returns (o, ot, lse, mu)
+    with shapes [..., R, dv], [..., R, dv], [..., R], [..., R].
+    """
+    lib = _load()
+    q, qt, k, kt, v, vt = (_f64(x) for x in (q, qt, k, kt, v, vt))
+    lead = q.shape[:-2]
+    d = q.shape[-1]
+    dv = v.shape[-1]
+    nk = k.shape[-2]
+    if not (k.shape[:-2] == v.shape[:-2] == lead and kt.shape == k.shape and vt.shape == v.shape
+            and qt.shape == q.shape and k.shape[-1] == d and v.shape[-2] == nk):
+        raise ValueError("oracle.attn_jvp: inconsistent shapes")
+    heads = int(np.prod(lead)) if lead else 1
+    qf, qtf = q.reshape(heads, q.shape[-2], d), qt.reshape(heads, q.shape[-2], d)
+    kf, ktf = k.reshape(heads, nk, d), kt.reshape(heads, nk, d)
+    vf, vtf = v.reshape(heads, nk, dv), vt.reshape(heads, nk, dv)
+    if rows is not None:
+        rows = np.asarray(rows, dtype=np.int64)
+        qf = np.ascontiguousarray(qf[:, rows])
+        qtf = np.ascontiguousarray(qtf[:, rows])
+    R = qf.shape[1]
+    o = np.empty((heads, R, dv))
+    ot = np.empty((heads, R, dv))
+    lse = np.empty((heads, R))
+    mu = np.empty((heads, R))
+    nthreads = nthreads or default_threads()
+    for h in range(heads):
+        args = [np.ascontiguousarray(x[h]) for x in (qf, qtf, kf, ktf, vf, vtf)]
+        outs = [o[h], ot[h], lse[h], mu[h]]
+        rc = lib.oracle_attn_jvp_rows(*[_ptr(a) for a in args], R, nk, d, dv, float(scale),
+                                      *[_ptr(a) for a in outs], int(nthreads))
+        if rc != 0:
+            raise RuntimeError("oracle_attn_jvp_rows failed (%d)" % rc)
+    shape_rows = lead + (R,)
+    return (o.reshape(shape_rows + (dv,)), ot.reshape(shape_rows + (dv,)),
+            lse.reshape(shape_rows), mu.reshape(shape_rows))
+
+
+def merge_chunks(o_c, ot_c, lse_c, mu_c):
+    """Exact merge of key-chunk partials: o_c/ot_c [C, ..., d], lse_c/mu_c [C, ...]."""
+    lib = _load()
+    o_c, ot_c, lse_c, mu_c = (_f64(x) for x in (o_c, ot_c, lse_c, mu_c))
+    C = o_c.shape[0]
+    d = o_c.shape[-1]
+    rows = int(np.prod(o_c.shape[1:-1])) if o_c.ndim > 2 else 1
+    o = np.empty(o_c.shape[1:])
+    ot = np.empty(o_c.shape[1:])
+    lse = np.empty(lse_c.shape[1:])
+    mu = np.empty(lse_c.shape[1:])
+    rc = lib.oracle_merge_chunks(_ptr(o_c), _ptr(ot_c), _ptr(lse_c), _ptr(mu_c), C, rows, d,
+                                 _ptr(o), _ptr(ot), _ptr(lse), _ptr(mu))
+    if rc != 0:
+        raise RuntimeError("oracle_merge_chunks failed (%d)" % rc)
+    return o, ot, lse, mu
+
+
+def trigflow_coeffs(t, tau=1000.0):
+    """(c_skip, c_out, c_in, c_noise) in FP64 for TrigFlow time t (scalar)."""
+    lib = _load()
+    out = np.empty(4)
+    rc = lib.oracle_trigflow_coeffs(float(t), float(tau), _ptr(out))
+    if rc != 0:
+        raise ValueError("trigflow_coeffs: cos t + sin t <= 0")
+    return tuple(float(x) for x in out)
+
+
+def trigflow_tangent(x0, eps, t):
+    """dx_t/dt = -sin t x0 + cos t eps in FP64; x0/eps [B, ...], t [B]."""
+    lib = _load()
+    x0, eps, t = _f64(x0), _f64(eps), _f64(t)
+    B = x0.shape[0]
+    M = int(np.prod(x0.shape[1:])) if x0.ndim > 1 else 1
+    out = np.empty_like(x0)
+    rc = lib.oracle_trigflow_tangent(_ptr(x0), _ptr(eps), _ptr(t), B, M, _ptr(out))
+    if rc != 0:
+        raise RuntimeError("oracle_trigflow_tangent failed")
+    return out

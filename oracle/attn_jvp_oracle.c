@@ -1,0 +1,244 @@
+/*
+ * FP64 CPU oracle for the forward-mode JVP through softmax attention and for
+ * the TrigFlow helpers.  TEST INFRASTRUCTURE ONLY: the tests, the smoke check
+ * and the benchmark's CPU-baseline leg call it; the product path never does.
+ * It shares no code, header or constant with the CUDA library.
+ *
+ * Sources (all on the page "带分数正则的一致性蒸馏" — consistency distillation
+ * with score regularisation — a gitcode.csdn.net write-up of rCM/sCM):
+ *   - section 注意力 (attention), "naive_scaled_dot_product_attention":
+ *       O = softmax(s * Q K^T) V, softmax along the key axis.
+ *   - section 注意力, the JVP paragraph: by the chain rule
+ *       t_o = P t_v + t_p V,  t_p = P (.) t_s - (P t_s^T) P,  t_s = t_q K^T + Q t_k^T
+ *     (the prose drops the scale; the kernel listing in section 前向 (forward)
+ *     multiplies t_s by sm_scale, the derivative of s * Q K^T, and so do we).
+ *   - section 前向 (forward): the LSE output is the natural-log log-sum-exp
+ *     of the scaled scores, one float per query row.
+ *   - section 时间步转换 (timestep conversion): the RectifiedFlow_TrigFlowWrapper
+ *     coefficients and the TrigFlow forward process x_t = cos t x0 + sin t eps.
+ *
+ * Every step below is the plain definition, computed in the order written on
+ * the page: two passes over the keys for the softmax (max, then exponentials),
+ * then the value sums.  No blocking, no online rescaling, no fusion.
+ *
+ * Parity pins (tests/test_oracle.py): library SDPA and logsumexp in FP64,
+ * central finite differences of O and LSE, torch.func.jvp autodiff, linearity,
+ * zero tangents, constant-V rows, one-key and two-key closed forms, the
+ * mu shift identity, and for TrigFlow the values printed on the page.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+/* ------------------------------------------------------------------------ */
+/* Attention + JVP, one head, arbitrary query rows                          */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    const double *q, *qt;           /* [R, d]   query rows and their tangents  */
+    const double *k, *kt;           /* [Nk, d]  keys and their tangents        */
+    const double *v, *vt;           /* [Nk, dv] values and their tangents      */
+    int64_t R, Nk, d, dv;
+    double scale;
+    double *o, *ot, *lse, *mu;      /* [R, dv], [R, dv], [R], [R]              */
+    int64_t row_begin, row_end;
+    int status;
+} head_job;
+
+static void one_row(const head_job *J, int64_t i, double *S, double *St, double *P)
+{
+    const int64_t d = J->d, dv = J->dv, Nk = J->Nk;
+    const double *qi = J->q + i * d, *qti = J->qt + i * d;
+
+    /* Step 1: scores S_ij = s * q_i . k_j and their tangents
+     *         St_ij = s * (qt_i . k_j + q_i . kt_j).                         */
+    for (int64_t j = 0; j < Nk; ++j) {
+        const double *kj = J->k + j * d, *ktj = J->kt + j * d;
+        double a = 0.0, b = 0.0;
+        for (int64_t c = 0; c < d; ++c) {
+            a += qi[c] * kj[c];
+            b += qti[c] * kj[c] + qi[c] * ktj[c];
+        }
+        S[j] = J->scale * a;
+        St[j] = J->scale * b;
+    }
+
+    /* Step 2: softmax along the keys, max first for the exponentials.       */
+    double m = -INFINITY;
+    for (int64_t j = 0; j < Nk; ++j)
+        if (S[j] > m) m = S[j];
+    double l = 0.0;
+    for (int64_t j = 0; j < Nk; ++j) {
+        P[j] = exp(S[j] - m);
+        l += P[j];
+    }
+    for (int64_t j = 0; j < Nk; ++j) P[j] /= l;
+
+    /* Step 3: O_i = sum_j P_ij v_j and LSE_i = ln sum_j exp(S_ij).          */
+    double *oi = J->o + i * dv;
+    for (int64_t c = 0; c < dv; ++c) oi[c] = 0.0;
+    for (int64_t j = 0; j < Nk; ++j) {
+        const double *vj = J->v + j * dv;
+        for (int64_t c = 0; c < dv; ++c) oi[c] += P[j] * vj[c];
+    }
+    J->lse[i] = m + log(l);
+
+    /* Step 4: mu_i = sum_j P_ij St_ij (the row sum of P (.) t_s), then the
+     * tangent  t_o = P t_v + t_p V  with  t_p_ij = P_ij (St_ij - mu_i).      */
+    double mu = 0.0;
+    for (int64_t j = 0; j < Nk; ++j) mu += P[j] * St[j];
+    J->mu[i] = mu;
+    double *oti = J->ot + i * dv;
+    for (int64_t c = 0; c < dv; ++c) oti[c] = 0.0;
+    for (int64_t j = 0; j < Nk; ++j) {
+        const double *vj = J->v + j * dv, *vtj = J->vt + j * dv;
+        const double tp = P[j] * (St[j] - mu);
+        for (int64_t c = 0; c < dv; ++c) oti[c] += P[j] * vtj[c] + tp * vj[c];
+    }
+}
+
+static void *head_worker(void *arg)
+{
+    head_job *J = (head_job *)arg;
+    double *buf = (double *)malloc(sizeof(double) * 3 * (size_t)J->Nk);
+    if (!buf) { J->status = -1; return NULL; }
+    for (int64_t i = J->row_begin; i < J->row_end; ++i)
+        one_row(J, i, buf, buf + J->Nk, buf + 2 * J->Nk);
+    free(buf);
+    J->status = 0;
+    return NULL;
+}
+
+/* Returns 0 on success, -1 on bad arguments or allocation failure. */
+int oracle_attn_jvp_rows(const double *q, const double *qt,
+                         const double *k, const double *kt,
+                         const double *v, const double *vt,
+                         int64_t R, int64_t Nk, int64_t d, int64_t dv, double scale,
+                         double *o, double *ot, double *lse, double *mu,
+                         int nthreads)
+{
+    if (!q || !qt || !k || !kt || !v || !vt || !o || !ot || !lse || !mu) return -1;
+    if (R < 0 || Nk < 1 || d < 1 || dv < 1) return -1;
+    if (R == 0) return 0;
+    if (nthreads < 1) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > R) nthreads = (int)R;
+
+    head_job *jobs = (head_job *)calloc((size_t)nthreads, sizeof(head_job));
+    pthread_t *tid = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    char *started = (char *)calloc((size_t)nthreads, 1);
+    if (!jobs || !tid || !started) { free(jobs); free(tid); free(started); return -1; }
+    int rc = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        head_job *J = &jobs[t];
+        J->q = q; J->qt = qt; J->k = k; J->kt = kt; J->v = v; J->vt = vt;
+        J->R = R; J->Nk = Nk; J->d = d; J->dv = dv; J->scale = scale;
+        J->o = o; J->ot = ot; J->lse = lse; J->mu = mu;
+        J->row_begin = R * t / nthreads;
+        J->row_end = R * (t + 1) / nthreads;
+        J->status = -1;
+        if (pthread_create(&tid[t], NULL, head_worker, J) == 0)
+            started[t] = 1;
+        else
+            head_worker(J);   /* no thread available: run the slice here */
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        if (started[t]) pthread_join(tid[t], NULL);
+        if (jobs[t].status != 0) rc = -1;
+    }
+    free(jobs);
+    free(tid);
+    free(started);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Exact merge of key-chunk partial results                                 */
+/* ------------------------------------------------------------------------ */
+/*
+ * The pages do not describe a key split; this is exact algebra on the
+ * definitions above.  For chunk c with partial softmax normaliser l_c:
+ *   O_c = sum_{j in c} e^{S_j} v_j / l_c,   mu_c = sum_{j in c} e^{S_j} St_j / l_c,
+ *   Ot_c = sum_{j in c} e^{S_j} (St_j v_j + vt_j) / l_c - mu_c O_c,
+ *   LSE_c = ln l_c  (up to the common max, which cancels).
+ * With l = sum_c l_c the full-row weights are w_c = l_c / l = e^{LSE_c - LSE},
+ * LSE = ln sum_c e^{LSE_c}, and
+ *   O = sum_c w_c O_c,  mu = sum_c w_c mu_c,  Ot = sum_c w_c (Ot_c + mu_c O_c) - mu O.
+ * Layout: partials [C, rows, d] and [C, rows]; outputs [rows, d] and [rows].
+ */
+int oracle_merge_chunks(const double *o_c, const double *ot_c,
+                        const double *lse_c, const double *mu_c,
+                        int64_t C, int64_t rows, int64_t d,
+                        double *o, double *ot, double *lse, double *mu)
+{
+    if (!o_c || !ot_c || !lse_c || !mu_c || !o || !ot || !lse || !mu) return -1;
+    if (C < 1 || rows < 0 || d < 1) return -1;
+    for (int64_t i = 0; i < rows; ++i) {
+        double m = -INFINITY;
+        for (int64_t c = 0; c < C; ++c)
+            if (lse_c[c * rows + i] > m) m = lse_c[c * rows + i];
+        double l = 0.0;
+        for (int64_t c = 0; c < C; ++c) l += exp(lse_c[c * rows + i] - m);
+        const double L = m + log(l);
+        lse[i] = L;
+        double mui = 0.0;
+        for (int64_t c = 0; c < C; ++c)
+            mui += exp(lse_c[c * rows + i] - L) * mu_c[c * rows + i];
+        mu[i] = mui;
+        for (int64_t e = 0; e < d; ++e) {
+            double oe = 0.0, te = 0.0;
+            for (int64_t c = 0; c < C; ++c) {
+                const double w = exp(lse_c[c * rows + i] - L);
+                const double oce = o_c[(c * rows + i) * d + e];
+                oe += w * oce;
+                te += w * (ot_c[(c * rows + i) * d + e] + mu_c[c * rows + i] * oce);
+            }
+            o[i * d + e] = oe;
+            ot[i * d + e] = te - mui * oe;
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* TrigFlow helpers (section 时间步转换, timestep conversion)                */
+/* ------------------------------------------------------------------------ */
+/*
+ * RectifiedFlow_TrigFlowWrapper, sigma_data = 1: for a TrigFlow time t,
+ *   c_skip = 1 / (cos t + sin t)
+ *   c_out  = -sin t / (cos t + sin t)
+ *   c_in   = 1 / (cos t + sin t)
+ *   c_noise = tau * sin t / (cos t + sin t)     (tau = t_scaling_factor)
+ * out = {c_skip, c_out, c_in, c_noise}.  Returns -1 where cos t + sin t <= 0.
+ */
+int oracle_trigflow_coeffs(double t, double tau, double *out)
+{
+    if (!out) return -1;
+    const double c = cos(t), s = sin(t);
+    const double den = c + s;
+    if (!(den > 0.0)) return -1;
+    out[0] = 1.0 / den;
+    out[1] = -s / den;
+    out[2] = 1.0 / den;
+    out[3] = tau * s / den;
+    return 0;
+}
+
+/*
+ * Time derivative of the TrigFlow forward process x_t = cos t x0 + sin t eps:
+ *   dx_t/dt = -sin t x0 + cos t eps,  t given per sample b, x0/eps [B, M].
+ */
+int oracle_trigflow_tangent(const double *x0, const double *eps, const double *t,
+                            int64_t B, int64_t M, double *out)
+{
+    if (!x0 || !eps || !t || !out || B < 0 || M < 0) return -1;
+    for (int64_t b = 0; b < B; ++b) {
+        const double s = sin(t[b]), c = cos(t[b]);
+        for (int64_t i = 0; i < M; ++i)
+            out[b * M + i] = -s * x0[b * M + i] + c * eps[b * M + i];
+    }
+    return 0;
+}
