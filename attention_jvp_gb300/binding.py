@@ -1,0 +1,233 @@
+"""Thin ctypes binding of ``libattnjvp.so``: argument marshalling only.
+
+Every function has the name of the C entry point it calls (include/attnjvp.h).
+Tensors are torch tensors on the current CUDA device; torch only provides the
+device memory and the stream.  All arithmetic runs in the library's kernels:
+if the library is missing or fails to load, every call raises — there is no
+fallback path.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libattnjvp.so")
+
+ATTNJVP_OK = 0
+ATTNJVP_EINVAL = -1
+ATTNJVP_EUNSUPPORTED = -2
+ATTNJVP_ECUDA = -3
+ATTNJVP_ETIMEOUT = -4
+
+_lib = None
+
+
+class AttnJvpError(RuntimeError):
+    def __init__(self, fn, code, msg):
+        super().__init__("%s failed (%d): %s" % (fn, code, msg))
+        self.code = code
+
+
+def load(path=None):
+    """Load (once) and return the ctypes handle of the CUDA library."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError("libattnjvp.so not built (%s); run __graft_entry__.build()" % path)
+    lib = ctypes.CDLL(path)
+    vp, i64, fp = ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p
+    lib.attn_jvp_fwd.argtypes = [vp] * 6 + [fp] * 4 + [i64] * 4 + [ctypes.c_float, vp]
+    lib.attn_jvp_fwd_chunk.argtypes = [vp] * 6 + [fp] * 4 + [i64] * 4 + [ctypes.c_float, i64, i64, vp]
+    lib.attn_jvp_merge.argtypes = [vp] * 4 + [i64] + [vp] * 4 + [i64] * 4 + [vp]
+    lib.attn_jvp_cast_f32_bf16.argtypes = [vp, vp, i64, vp]
+    lib.trigflow_coeffs.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.POINTER(ctypes.c_double)]
+    lib.trigflow_tangent.argtypes = [vp, vp, vp, vp, i64, i64, vp]
+    lib.attn_jvp_status.argtypes = [ctypes.c_int]
+    lib.attn_jvp_last_error.restype = ctypes.c_char_p
+    lib.attn_jvp_version.restype = ctypes.c_char_p
+    for name in ("attn_jvp_fwd", "attn_jvp_fwd_chunk", "attn_jvp_merge", "attn_jvp_cast_f32_bf16",
+                 "trigflow_coeffs", "trigflow_tangent", "attn_jvp_status"):
+        getattr(lib, name).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _check(fn, rc):
+    if rc != ATTNJVP_OK:
+        raise AttnJvpError(fn, rc, load().attn_jvp_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _req(t, name, dtype, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s (got %s)" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s (got %s)" % (name, tuple(shape), tuple(t.shape)))
+    return t
+
+
+def attn_jvp_cast_f32_bf16(x, out=None, stream=None):
+    """fp32 -> bf16 on the device (round to nearest even)."""
+    _req(x, "x", torch.float32)
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
+    _req(out, "out", torch.bfloat16, x.shape)
+    _check("attn_jvp_cast_f32_bf16", load().attn_jvp_cast_f32_bf16(_ptr(x), _ptr(out), x.numel(), _stream(stream)))
+    return out
+
+
+def _bf16_inputs(tensors, stream):
+    """bf16 views of the six inputs; fp32 inputs are rounded by the library's cast kernel."""
+    res = []
+    for n, t in zip(("q", "k", "v", "q_t", "k_t", "v_t"), tensors):
+        if isinstance(t, torch.Tensor) and t.dtype == torch.float32:
+            _req(t, n, torch.float32)
+            t = attn_jvp_cast_f32_bf16(t, stream=stream)
+        res.append(_req(t, n, torch.bfloat16))
+    shape = tuple(res[0].shape)
+    if len(shape) != 4:
+        raise ValueError("q must be [B, H, N, d]")
+    for n, t in zip(("k", "v", "q_t", "k_t", "v_t"), res[1:]):
+        if tuple(t.shape) != shape:
+            raise ValueError("%s must have q's shape %s (got %s)" % (n, shape, tuple(t.shape)))
+    return res
+
+
+def _outputs(shape, device, out, out_t, lse, mu, need_rows):
+    B, H, N, d = shape
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=torch.float32, device=device)
+    if out_t is None:
+        out_t = torch.empty((B, H, N, d), dtype=torch.float32, device=device)
+    if lse is None and need_rows:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    if mu is None and need_rows:
+        mu = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    _req(out, "out", torch.float32, shape)
+    _req(out_t, "out_t", torch.float32, shape)
+    if lse is not None:
+        _req(lse, "lse", torch.float32, (B, H, N))
+    if mu is not None:
+        _req(mu, "mu", torch.float32, (B, H, N))
+    return out, out_t, lse, mu
+
+
+def attn_jvp_fwd(q, k, v, q_t, k_t, v_t, scale=None, out=None, out_t=None, lse=None, mu=None,
+                 want_rows=True, stream=None):
+    """(O, Ot, LSE, mu) of softmax attention and its JVP; inputs [B, H, N, d] bf16 (or fp32)."""
+    q, k, v, q_t, k_t, v_t = _bf16_inputs((q, k, v, q_t, k_t, v_t), stream)
+    B, H, N, d = q.shape
+    scale = d ** -0.5 if scale is None else float(scale)
+    out, out_t, lse, mu = _outputs(q.shape, q.device, out, out_t, lse, mu, want_rows)
+    rc = load().attn_jvp_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(q_t), _ptr(k_t), _ptr(v_t),
+                             _ptr(out), _ptr(out_t), _ptr(lse), _ptr(mu), B, H, N, d,
+                             ctypes.c_float(scale), _stream(stream))
+    _check("attn_jvp_fwd", rc)
+    return out, out_t, lse, mu
+
+
+def attn_jvp_fwd_chunk(q, k, v, q_t, k_t, v_t, kv_start, kv_len, scale=None, out=None, out_t=None,
+                       lse=None, mu=None, stream=None):
+    """Partials (O_c, Ot_c, LSE_c, mu_c) over keys [kv_start, kv_start + kv_len)."""
+    q, k, v, q_t, k_t, v_t = _bf16_inputs((q, k, v, q_t, k_t, v_t), stream)
+    B, H, N, d = q.shape
+    scale = d ** -0.5 if scale is None else float(scale)
+    out, out_t, lse, mu = _outputs(q.shape, q.device, out, out_t, lse, mu, True)
+    rc = load().attn_jvp_fwd_chunk(_ptr(q), _ptr(k), _ptr(v), _ptr(q_t), _ptr(k_t), _ptr(v_t),
+                                   _ptr(out), _ptr(out_t), _ptr(lse), _ptr(mu), B, H, N, d,
+                                   ctypes.c_float(scale), int(kv_start), int(kv_len), _stream(stream))
+    _check("attn_jvp_fwd_chunk", rc)
+    return out, out_t, lse, mu
+
+
+def attn_jvp_merge(o_c, ot_c, lse_c, mu_c, out=None, out_t=None, lse=None, mu=None, stream=None):
+    """Exact merge of chunk partials o_c/ot_c [C, B, H, N, d], lse_c/mu_c [C, B, H, N]."""
+    _req(o_c, "o_c", torch.float32)
+    C, B, H, N, d = o_c.shape
+    _req(ot_c, "ot_c", torch.float32, o_c.shape)
+    _req(lse_c, "lse_c", torch.float32, (C, B, H, N))
+    _req(mu_c, "mu_c", torch.float32, (C, B, H, N))
+    out, out_t, lse, mu = _outputs((B, H, N, d), o_c.device, out, out_t, lse, mu, True)
+    rc = load().attn_jvp_merge(_ptr(o_c), _ptr(ot_c), _ptr(lse_c), _ptr(mu_c), C, _ptr(out), _ptr(out_t),
+                               _ptr(lse), _ptr(mu), B, H, N, d, _stream(stream))
+    _check("attn_jvp_merge", rc)
+    return out, out_t, lse, mu
+
+
+def chunk_bounds(N, n_chunks):
+    """Key ranges [(start, len), ...] splitting N keys into n_chunks near-equal chunks."""
+    edges = [(N * c) // n_chunks for c in range(n_chunks + 1)]
+    return [(a, b - a) for a, b in zip(edges[:-1], edges[1:])]
+
+
+def attn_jvp_split(q, k, v, q_t, k_t, v_t, n_chunks, scale=None, workspace=None, out=None, out_t=None,
+                   lse=None, mu=None, stream=None):
+    """Split-KV path: one chunk launch per key range, then the exact merge.
+
+    ``workspace``: optional (o_c, ot_c, lse_c, mu_c) partial buffers to reuse.
+    """
+    q, k, v, q_t, k_t, v_t = _bf16_inputs((q, k, v, q_t, k_t, v_t), stream)
+    B, H, N, d = q.shape
+    if workspace is None:
+        workspace = split_workspace(q.shape, n_chunks, q.device)
+    o_c, ot_c, lse_c, mu_c = workspace
+    for c, (a, n) in enumerate(chunk_bounds(N, n_chunks)):
+        attn_jvp_fwd_chunk(q, k, v, q_t, k_t, v_t, a, n, scale=scale, out=o_c[c], out_t=ot_c[c],
+                           lse=lse_c[c], mu=mu_c[c], stream=stream)
+    return attn_jvp_merge(o_c, ot_c, lse_c, mu_c, out=out, out_t=out_t, lse=lse, mu=mu, stream=stream)
+
+
+def split_workspace(shape, n_chunks, device):
+    B, H, N, d = shape
+    return (torch.empty((n_chunks, B, H, N, d), dtype=torch.float32, device=device),
+            torch.empty((n_chunks, B, H, N, d), dtype=torch.float32, device=device),
+            torch.empty((n_chunks, B, H, N), dtype=torch.float32, device=device),
+            torch.empty((n_chunks, B, H, N), dtype=torch.float32, device=device))
+
+
+def trigflow_coeffs(t, tau=1000.0):
+    """(c_skip, c_out, c_in, c_noise) in FP64 (host function of the library)."""
+    c = (ctypes.c_double * 4)()
+    _check("trigflow_coeffs", load().trigflow_coeffs(float(t), float(tau), c))
+    return tuple(c)
+
+
+def trigflow_tangent(x0, eps, t, out=None, stream=None):
+    """dx_t/dt = -sin t x0 + cos t eps; x0/eps fp32 [B, ...], t FP64 [B] on the device."""
+    _req(x0, "x0", torch.float32)
+    _req(eps, "eps", torch.float32, x0.shape)
+    B = x0.shape[0]
+    _req(t, "t", torch.float64, (B,))
+    if out is None:
+        out = torch.empty_like(x0)
+    _req(out, "out", torch.float32, x0.shape)
+    per = x0.numel() // B
+    _check("trigflow_tangent", load().trigflow_tangent(_ptr(x0), _ptr(eps), _ptr(t), _ptr(out), B, per,
+                                                       _stream(stream)))
+    return out
+
+
+def attn_jvp_status(clear=True):
+    """0 if no kernel reported a problem; raises AttnJvpError(ETIMEOUT) otherwise."""
+    _check("attn_jvp_status", load().attn_jvp_status(1 if clear else 0))
+    return 0
+
+
+def attn_jvp_version():
+    return load().attn_jvp_version().decode()

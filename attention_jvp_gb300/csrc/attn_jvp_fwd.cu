@@ -1,0 +1,469 @@
+// Fused attention forward + forward-mode JVP for sm_103a (tcgen05 / TMEM / TMA).
+//
+// What it computes (page "带分数正则的一致性蒸馏", gitcode.csdn.net, section
+// 注意力 (attention), the streaming JVP paragraph, and section 前向 (forward)):
+// per query row, stream the keys in tiles while carrying a running max m, the
+// exponential sum l, r = rowsum(P~ (.) St) and two accumulators
+//     O~ = sum P~ V              T~ = sum P~ Vt + sum (P~ (.) St) V
+// (the page's A + B in one accumulator, since only their sum is used), where
+// P~ = exp(S - m) is the unnormalised softmax and every accumulator is
+// rescaled by exp(m_old - m_new) when the running max grows.  At the end
+//     O = O~ / l,  mu = r / l,  Ot = T~ / l - mu O,  LSE = m + ln l.
+//
+// GB300 mapping (one CTA = 128 query rows of one (batch, head)):
+//   warp 0      TMA producer for Q, Qt (once) and the K/Kt ring
+//   warp 1      TMEM allocator and the single-thread tcgen05.mma issuer
+//   warp 2      TMA producer for the V/Vt ring
+//   warps 4-7   softmax + JVP weights + lazy rescale + epilogue; thread t of
+//               warp 4+w owns query row 32w+t, which is TMEM lane 32w+t, so
+//               every row reduction is thread-local (no shuffles).
+// Per 64-key tile j (tensor-core work, fp32 accumulation in TMEM):
+//   S_b  = Q K_j^T                         (d-deep, N = 64)
+//   St_b = [Qt Q] [K_j Kt_j]^T             (one 2d-deep chain, N = 64)
+//   softmax warps: P~ = 2^(S*s*log2e - m), H~ = P~ (.) St * s, row sums in fp32,
+//                  P~ and H~ rounded to bf16 and written back into S_b's columns
+//   O += P~ V_j,  T += P~ Vt_j,  T += H~ V_j   (A operand read from TMEM)
+// S/St live in NB ping-pong TMEM buffers so the next tile's score MMAs overlap
+// the current tile's softmax.  Only MMAs of identical shape chain into one
+// accumulator, the ordering tcgen05 guarantees without extra waits.
+//
+// Lazy rescale: a row keeps its reference max until a tile's max exceeds it by
+// more than 8 (log2 units); only then are O, T, l, r rescaled.  All four share
+// the same reference, so the final normalisation is exact.
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "internal.h"
+#include "sm103_ptx.cuh"
+
+namespace attnjvp {
+namespace {
+
+using namespace ptx;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kBM = 128;                  // query rows per CTA (= TMEM lanes)
+  static constexpr int kBN = 64;                   // keys per tile
+  static constexpr int kDC = D / 64;               // 64-element (128-byte) d-chunks
+  static constexpr int kNB = (D == 128) ? 2 : 3;   // S/St TMEM buffers
+  static constexpr int kKS = (D == 128) ? 2 : 3;   // K/Kt ring stages
+  static constexpr int kVS = (D == 128) ? 2 : 3;   // V/Vt ring stages
+  static constexpr int kChunkQ = kBM * 128;        // one d-chunk of a Q tile (bytes)
+  static constexpr int kChunkK = kBN * 128;        // one d-chunk of a key tile (bytes)
+  static constexpr int kQBytes = kDC * kChunkQ;    // Q (or Qt) tile
+  static constexpr int kKStage = 2 * kDC * kChunkK;  // K chunks, then Kt chunks
+  static constexpr int kVStage = 2 * kDC * kChunkK;  // V chunks, then Vt chunks
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffQt = kQBytes;
+  static constexpr int kOffK = 2 * kQBytes;
+  static constexpr int kOffV = kOffK + kKS * kKStage;
+  static constexpr int kOffBar = kOffV + kVS * kVStage;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
+  // TMEM columns (fp32 each): O [0,D), T [D,2D), buffer b: S [2D+128b, +64), St [+64, +128)
+  static constexpr uint32_t kColO = 0;
+  static constexpr uint32_t kColT = D;
+  static constexpr uint32_t kColBuf = 2 * D;
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kColBuf + 128 * kNB <= kTmemCols, "TMEM budget");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+constexpr int kThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale once P~ could exceed 2^8
+
+struct FwdMaps {
+  CUtensorMap q, qt, k, kt, v, vt;
+};
+
+struct Barriers {
+  uint64_t q_full;
+  uint64_t k_full[3], k_empty[3];
+  uint64_t v_full[3], v_empty[3];
+  uint64_t s_full[3], p_full[3], pv_done[3];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_jvp_fwd_kernel(const __grid_constant__ FwdMaps maps, float* __restrict__ out, float* __restrict__ out_t,
+                        float* __restrict__ lse_out, float* __restrict__ mu_out, int N, int n_qtiles, int kv_start,
+                        int kv_len, float scale, int* status) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Barriers* bars = reinterpret_cast<Barriers*>(smem + C::kOffBar);
+  volatile int* abort_flag = &bars->abort_flag;
+
+  // Another CTA already hit a wait timeout: the whole CTA does nothing (read once, decided uniformly).
+  if (threadIdx.x == 0) bars->abort_flag = (*reinterpret_cast<volatile int*>(status) & kStatusTimeout) ? 1 : 0;
+  __syncthreads();
+  if (bars->abort_flag) return;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.x / n_qtiles;
+  const int q0 = (blockIdx.x % n_qtiles) * C::kBM;
+  const int n_tiles = (kv_len + C::kBN - 1) / C::kBN;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < 3; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->p_full[s], 128);
+      mbar_init(&bars->pv_done[s], 1);
+    }
+    mbar_init(&bars->drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ---------------- TMA producer: Q, Qt and the K/Kt ring ----------------
+    if (lane == 0) {
+      prefetch_tensormap(&maps.q);
+      prefetch_tensormap(&maps.qt);
+      prefetch_tensormap(&maps.k);
+      prefetch_tensormap(&maps.kt);
+      mbar_arrive_expect_tx(&bars->q_full, 2 * C::kQBytes);
+      for (int c = 0; c < C::kDC; ++c) {
+        tma_load_3d(smem + C::kOffQ + c * C::kChunkQ, &maps.q, &bars->q_full, c * 64, q0, bh);
+        tma_load_3d(smem + C::kOffQt + c * C::kChunkQ, &maps.qt, &bars->q_full, c * 64, q0, bh);
+      }
+      int issued = 0;
+      bool ok = true;
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        const int s = t % C::kKS;
+        ok = mbar_wait(&bars->k_empty[s], ((t / C::kKS) & 1) ^ 1, abort_flag, status, kStatusTimeout);
+        if (!ok) break;
+        uint8_t* st = smem + C::kOffK + s * C::kKStage;
+        const int key0 = kv_start + t * C::kBN;
+        mbar_arrive_expect_tx(&bars->k_full[s], C::kKStage);
+        for (int c = 0; c < C::kDC; ++c) {
+          tma_load_3d(st + c * C::kChunkK, &maps.k, &bars->k_full[s], c * 64, key0, bh);
+          tma_load_3d(st + (C::kDC + c) * C::kChunkK, &maps.kt, &bars->k_full[s], c * 64, key0, bh);
+        }
+        issued = t + 1;
+      }
+      if (!ok) {
+        // Let copies still in flight land before the CTA's shared memory goes away.
+        volatile int no_abort = 0;
+        mbar_wait(&bars->q_full, 0, &no_abort, nullptr, 0);
+        for (int t = issued - C::kKS; t < issued; ++t)
+          if (t >= 0) mbar_wait(&bars->k_full[t % C::kKS], (t / C::kKS) & 1, &no_abort, nullptr, 0);
+      }
+    }
+  } else if (warp == 2) {
+    // ---------------- TMA producer: the V/Vt ring ----------------
+    if (lane == 0) {
+      prefetch_tensormap(&maps.v);
+      prefetch_tensormap(&maps.vt);
+      int issued = 0;
+      bool ok = true;
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        const int s = t % C::kVS;
+        ok = mbar_wait(&bars->v_empty[s], ((t / C::kVS) & 1) ^ 1, abort_flag, status, kStatusTimeout);
+        if (!ok) break;
+        uint8_t* st = smem + C::kOffV + s * C::kVStage;
+        const int key0 = kv_start + t * C::kBN;
+        mbar_arrive_expect_tx(&bars->v_full[s], C::kVStage);
+        for (int c = 0; c < C::kDC; ++c) {
+          tma_load_3d(st + c * C::kChunkK, &maps.v, &bars->v_full[s], c * 64, key0, bh);
+          tma_load_3d(st + (C::kDC + c) * C::kChunkK, &maps.vt, &bars->v_full[s], c * 64, key0, bh);
+        }
+        issued = t + 1;
+      }
+      if (!ok) {
+        volatile int no_abort = 0;
+        for (int t = issued - C::kVS; t < issued; ++t)
+          if (t >= 0) mbar_wait(&bars->v_full[t % C::kVS], (t / C::kVS) & 1, &no_abort, nullptr, 0);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- tcgen05.mma issuer (one thread) ----------------
+    if (lane == 0) {
+      constexpr uint32_t kIdS = make_idesc_bf16_f32(128, C::kBN, false, false);  // Q K^T, both K-major
+      constexpr uint32_t kIdPV = make_idesc_bf16_f32(128, D, false, true);      // P~ V, V is N-major
+      const uint32_t sQ = smem_u32(smem + C::kOffQ);
+      const uint32_t sQt = smem_u32(smem + C::kOffQt);
+
+      auto issue_scores = [&](int t) -> bool {
+        const int b = t % C::kNB;
+        const int s = t % C::kKS;
+        if (!mbar_wait(&bars->k_full[s], (t / C::kKS) & 1, abort_flag, status, kStatusTimeout)) return false;
+        if (t >= C::kNB) {
+          // P~/H~ of tile t-NB sit in this buffer's S columns: wait until that tile's PV MMAs are done.
+          if (!mbar_wait(&bars->pv_done[b], ((t - C::kNB) / C::kNB) & 1, abort_flag, status, kStatusTimeout))
+            return false;
+        }
+        tc_fence_after_sync();
+        const uint32_t sK = smem_u32(smem + C::kOffK + s * C::kKStage);
+        const uint32_t dS = tmem + C::kColBuf + 128u * b;
+        const uint32_t dSt = dS + 64u;
+        // S = Q K^T
+#pragma unroll
+        for (int c = 0; c < C::kDC; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t a = make_smem_desc_sw128(sQ + c * C::kChunkQ + kk * 32, 16, 1024);
+            const uint64_t bd = make_smem_desc_sw128(sK + c * C::kChunkK + kk * 32, 16, 1024);
+            mma_ss(dS, a, bd, kIdS, (c | kk) != 0);
+          }
+        // St = [Qt Q] [K Kt]^T : one accumulator, 2d deep
+#pragma unroll
+        for (int c = 0; c < C::kDC; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t a = make_smem_desc_sw128(sQt + c * C::kChunkQ + kk * 32, 16, 1024);
+            const uint64_t bd = make_smem_desc_sw128(sK + c * C::kChunkK + kk * 32, 16, 1024);
+            mma_ss(dSt, a, bd, kIdS, (c | kk) != 0);
+          }
+#pragma unroll
+        for (int c = 0; c < C::kDC; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t a = make_smem_desc_sw128(sQ + c * C::kChunkQ + kk * 32, 16, 1024);
+            const uint64_t bd = make_smem_desc_sw128(sK + (C::kDC + c) * C::kChunkK + kk * 32, 16, 1024);
+            mma_ss(dSt, a, bd, kIdS, 1);
+          }
+        mma_commit(&bars->k_empty[s]);
+        mma_commit(&bars->s_full[b]);
+        return true;
+      };
+
+      bool ok = mbar_wait(&bars->q_full, 0, abort_flag, status, kStatusTimeout);
+      for (int t = 0; ok && t < C::kNB && t < n_tiles; ++t) ok = issue_scores(t);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int b = j % C::kNB;
+        const int s = j % C::kVS;
+        ok = mbar_wait(&bars->p_full[b], (j / C::kNB) & 1, abort_flag, status, kStatusTimeout) &&
+             mbar_wait(&bars->v_full[s], (j / C::kVS) & 1, abort_flag, status, kStatusTimeout);
+        if (!ok) break;
+        tc_fence_after_sync();
+        const uint32_t sV = smem_u32(smem + C::kOffV + s * C::kVStage);
+        const uint32_t sVt = sV + C::kDC * C::kChunkK;
+        const uint32_t aP = tmem + C::kColBuf + 128u * b;  // P~ packed bf16: 32 columns
+        const uint32_t aH = aP + 32u;                       // H~ packed bf16: 32 columns
+#pragma unroll
+        for (int kk = 0; kk < C::kBN / 16; ++kk) {
+          const uint64_t bV = make_smem_desc_sw128(sV + kk * 2048, C::kChunkK, 1024);
+          const uint64_t bVt = make_smem_desc_sw128(sVt + kk * 2048, C::kChunkK, 1024);
+          const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+          mma_ts(tmem + C::kColO, aP + kk * 8, bV, kIdPV, acc);   // O += P~ V
+          mma_ts(tmem + C::kColT, aP + kk * 8, bVt, kIdPV, acc);  // T += P~ Vt
+          mma_ts(tmem + C::kColT, aH + kk * 8, bV, kIdPV, 1u);    // T += H~ V
+        }
+        mma_commit(&bars->v_empty[s]);
+        mma_commit(&bars->pv_done[b]);
+        if (j + C::kNB < n_tiles) ok = issue_scores(j + C::kNB);
+      }
+      // Nothing may still be reading shared memory or TMEM when the CTA tears down.
+      mma_commit(&bars->drain);
+      volatile int no_abort = 0;
+      mbar_wait(&bars->drain, 0, &no_abort, nullptr, 0);
+    }
+  } else if (warp >= 4) {
+    // ---------------- softmax / JVP / epilogue: one query row per thread ----------------
+    const int quarter = warp - 4;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float c2 = scale * kLog2e;
+    float m = -INFINITY;  // reference max, log2 units of the scaled scores
+    float l = 0.f, r = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int b = j % C::kNB;
+      ok = mbar_wait(&bars->s_full[b], (j / C::kNB) & 1, abort_flag, status, kStatusTimeout);
+      ok = __all_sync(0xffffffffu, ok);  // keep the warp converged for the .sync.aligned TMEM ops
+      if (!ok) break;
+      tc_fence_after_sync();
+      const uint32_t cS = lane_addr + C::kColBuf + 128u * b;
+      const int valid = min(C::kBN, kv_len - j * C::kBN);
+      uint32_t sr[64];
+      tmem_ld32_wait(cS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32_wait(cS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      float x[64];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        x[i] = (i < valid) ? __uint_as_float(sr[i]) * c2 : -INFINITY;
+        mx = fmaxf(mx, x[i]);
+      }
+      float alpha = 1.f;
+      bool rescale = false;
+      if (j == 0) {
+        m = mx;
+      } else if (mx > m + kRescaleThreshold) {
+        alpha = ex2_approx(m - mx);
+        m = mx;
+        rescale = true;
+      }
+      float ls = 0.f;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        x[i] = ex2_approx(x[i] - m);
+        ls += x[i];
+      }
+      l = l * alpha + ls;
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
+      // H~ = P~ (.) St * s, row sum in fp32 before rounding.
+      uint32_t hk[32];
+      float rs = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t tr[32];
+        tmem_ld32_wait(cS + 64 + 32 * h, tr);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float h0 = x[32 * h + i] * (__uint_as_float(tr[i]) * scale);
+          const float h1 = x[32 * h + i + 1] * (__uint_as_float(tr[i + 1]) * scale);
+          rs += h0 + h1;
+          hk[16 * h + i / 2] = pack_bf16x2(h0, h1);
+        }
+      }
+      r = r * alpha + rs;
+      if (__any_sync(0xffffffffu, rescale)) {
+        // O and T may only be touched once the previous tile's PV MMAs are done.
+        ok = mbar_wait(&bars->pv_done[(j - 1) % C::kNB], ((j - 1) / C::kNB) & 1, abort_flag, status,
+                       kStatusTimeout);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after_sync();
+#pragma unroll 1
+        for (int c0 = 0; c0 < 2 * D; c0 += 32) {
+          uint32_t acc[32];
+          tmem_ld32_wait(lane_addr + C::kColO + c0, acc);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[i] = __float_as_uint(__uint_as_float(acc[i]) * alpha);
+          tmem_st32(lane_addr + C::kColO + c0, acc);
+        }
+      }
+      tmem_st32(cS, pk);
+      tmem_st32(cS + 32, hk);
+      tmem_wait_st();
+      tc_fence_before_sync();
+      mbar_arrive(&bars->p_full[b]);
+    }
+    // ---------------- epilogue ----------------
+    if (ok) ok = mbar_wait(&bars->pv_done[(n_tiles - 1) % C::kNB], ((n_tiles - 1) / C::kNB) & 1, abort_flag, status,
+                           kStatusTimeout);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      tc_fence_after_sync();
+      const int qrow = q0 + row;
+      const float inv_l = 1.f / l;
+      const float mu = r * inv_l;
+      const int64_t obase = (static_cast<int64_t>(bh) * N + qrow) * D;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t ov[32], tv[32];
+        tmem_ld32_wait(lane_addr + C::kColO + c0, ov);
+        tmem_ld32_wait(lane_addr + C::kColT + c0, tv);
+        if (qrow < N) {
+          float4* o4 = reinterpret_cast<float4*>(out + obase + c0);
+          float4* t4 = reinterpret_cast<float4*>(out_t + obase + c0);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float4 o, t;
+            o.x = __uint_as_float(ov[4 * i + 0]) * inv_l;
+            o.y = __uint_as_float(ov[4 * i + 1]) * inv_l;
+            o.z = __uint_as_float(ov[4 * i + 2]) * inv_l;
+            o.w = __uint_as_float(ov[4 * i + 3]) * inv_l;
+            t.x = __uint_as_float(tv[4 * i + 0]) * inv_l - mu * o.x;
+            t.y = __uint_as_float(tv[4 * i + 1]) * inv_l - mu * o.y;
+            t.z = __uint_as_float(tv[4 * i + 2]) * inv_l - mu * o.z;
+            t.w = __uint_as_float(tv[4 * i + 3]) * inv_l - mu * o.w;
+            o4[i] = o;
+            t4[i] = t;
+          }
+        }
+      }
+      if (qrow < N) {
+        const int64_t ridx = static_cast<int64_t>(bh) * N + qrow;
+        if (lse_out) lse_out[ridx] = (m + __log2f(l)) * kLn2;
+        if (mu_out) mu_out[ridx] = mu;
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+cudaError_t make_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t N, int64_t d, int box_rows) {
+  TensorMapEncodeFn enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int D>
+cudaError_t launch_d(const FwdArgs& a, const char** msg) {
+  using C = FwdCfg<D>;
+  FwdMaps maps;
+  cudaError_t e = cudaSuccess;
+  const void* ptrs[6] = {a.q, a.q_t, a.k, a.k_t, a.v, a.v_t};
+  CUtensorMap* dst[6] = {&maps.q, &maps.qt, &maps.k, &maps.kt, &maps.v, &maps.vt};
+  for (int i = 0; i < 6 && e == cudaSuccess; ++i)
+    e = make_map(dst[i], ptrs[i], a.BH, a.N, D, i < 2 ? C::kBM : C::kBN);
+  if (e != cudaSuccess) {
+    *msg = "cuTensorMapEncodeTiled rejected a tensor (alignment or size)";
+    return e;
+  }
+  static bool attr_set[2] = {false, false};
+  auto kern = attn_jvp_fwd_kernel<D>;
+  if (!attr_set[D == 128]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) {
+      *msg = "cudaFuncSetAttribute(max dynamic shared memory) failed";
+      return e;
+    }
+    attr_set[D == 128] = true;
+  }
+  const int n_qtiles = static_cast<int>((a.N + C::kBM - 1) / C::kBM);
+  const int64_t grid = static_cast<int64_t>(n_qtiles) * a.BH;
+  kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, a.stream>>>(
+      maps, a.out, a.out_t, a.lse, a.mu, static_cast<int>(a.N), n_qtiles, static_cast<int>(a.kv_start),
+      static_cast<int>(a.kv_len), a.scale, a.status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) *msg = "attention-JVP kernel launch failed";
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_attn_jvp_fwd(const FwdArgs& a, const char** msg) {
+  if (a.d == 128) return launch_d<128>(a, msg);
+  if (a.d == 64) return launch_d<64>(a, msg);
+  *msg = "unsupported head dimension";
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace attnjvp

@@ -1,0 +1,252 @@
+// C-ABI entry points: argument validation, per-device status word, error
+// strings, tensor-map encoder lookup, and the host-side TrigFlow coefficients.
+// Every check that needs no GPU runs before the first CUDA call, so invalid
+// arguments are reported identically on machines without a device.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include "../../include/attnjvp.h"
+#include "internal.h"
+
+namespace attnjvp {
+
+// Per-device status word (kStatusTimeout bit set by a kernel whose bounded wait ran out).
+__device__ int g_status_word;
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int ok() {
+  g_last_error[0] = '\0';
+  return ATTNJVP_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_status_ptr[kMaxDevices] = {};
+
+// Device address of the current device's status word (nullptr on failure).
+int* status_word(const char** why) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    *why = cudaGetErrorString(e);
+    return nullptr;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    *why = "device ordinal out of range";
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess) {
+      *why = cudaGetErrorString(e);
+      return nullptr;
+    }
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+int check_attn_args(const void* q, const void* k, const void* v, const void* q_t, const void* k_t, const void* v_t,
+                    const float* out, const float* out_t, const float* lse, const float* mu, int64_t B, int64_t H,
+                    int64_t N, int64_t d, float scale) {
+  const void* in[6] = {q, k, v, q_t, k_t, v_t};
+  const char* names[6] = {"q", "k", "v", "q_t", "k_t", "v_t"};
+  for (int i = 0; i < 6; ++i) {
+    if (!in[i]) return fail(ATTNJVP_EINVAL, "%s is NULL", names[i]);
+    if (!aligned(in[i], 16)) return fail(ATTNJVP_EINVAL, "%s is not 16-byte aligned (TMA base address)", names[i]);
+  }
+  if (!out || !out_t) return fail(ATTNJVP_EINVAL, "out/out_t is NULL");
+  if (!aligned(out, 16) || !aligned(out_t, 16)) return fail(ATTNJVP_EINVAL, "out/out_t is not 16-byte aligned");
+  if ((lse && !aligned(lse, 4)) || (mu && !aligned(mu, 4))) return fail(ATTNJVP_EINVAL, "lse/mu misaligned");
+  if (B < 1 || H < 1 || N < 1) return fail(ATTNJVP_EINVAL, "B, H, N must be >= 1 (got %lld, %lld, %lld)",
+                                           (long long)B, (long long)H, (long long)N);
+  if (B * H >= (int64_t(1) << 31) || N >= (int64_t(1) << 31))
+    return fail(ATTNJVP_EINVAL, "B*H and N must be < 2^31");
+  if (!std::isfinite(scale) || !(scale > 0.f)) return fail(ATTNJVP_EINVAL, "scale must be finite and > 0");
+  if (d != 64 && d != 128)
+    return fail(ATTNJVP_EUNSUPPORTED, "head dim %lld not supported (this build: 64, 128)", (long long)d);
+  const int64_t n_qtiles = (N + 127) / 128;
+  if (n_qtiles * B * H >= (int64_t(1) << 31)) return fail(ATTNJVP_EINVAL, "too many query tiles");
+  return ATTNJVP_OK;
+}
+
+int run_fwd(const void* q, const void* k, const void* v, const void* q_t, const void* k_t, const void* v_t,
+            float* out, float* out_t, float* lse, float* mu, int64_t B, int64_t H, int64_t N, int64_t d, float scale,
+            int64_t kv_start, int64_t kv_len, void* stream) {
+  const char* why = "";
+  int* st = status_word(&why);
+  if (!st) return fail(ATTNJVP_ECUDA, "no CUDA device / status word: %s", why);
+  FwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.q_t = q_t;
+  a.k_t = k_t;
+  a.v_t = v_t;
+  a.out = out;
+  a.out_t = out_t;
+  a.lse = lse;
+  a.mu = mu;
+  a.BH = B * H;
+  a.N = N;
+  a.d = d;
+  a.scale = scale;
+  a.kv_start = kv_start;
+  a.kv_len = kv_len;
+  a.status = st;
+  a.stream = static_cast<cudaStream_t>(stream);
+  const char* msg = "";
+  cudaError_t e = launch_attn_jvp_fwd(a, &msg);
+  if (e != cudaSuccess) return fail(ATTNJVP_ECUDA, "%s: %s", msg, cudaGetErrorString(e));
+  return ok();
+}
+
+}  // namespace
+
+TensorMapEncodeFn tensor_map_encoder() {
+  static TensorMapEncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<TensorMapEncodeFn>(p);
+  });
+  return fn;
+}
+
+}  // namespace attnjvp
+
+using namespace attnjvp;
+
+extern "C" {
+
+int attn_jvp_fwd(const void* q, const void* k, const void* v, const void* q_t, const void* k_t, const void* v_t,
+                 float* out, float* out_t, float* lse, float* mu, int64_t B, int64_t H, int64_t N, int64_t d,
+                 float scale, void* stream) {
+  int rc = check_attn_args(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, d, scale);
+  if (rc != ATTNJVP_OK) return rc;
+  return run_fwd(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, d, scale, 0, N, stream);
+}
+
+int attn_jvp_fwd_chunk(const void* q, const void* k, const void* v, const void* q_t, const void* k_t,
+                       const void* v_t, float* out, float* out_t, float* lse, float* mu, int64_t B, int64_t H,
+                       int64_t N, int64_t d, float scale, int64_t kv_start, int64_t kv_len, void* stream) {
+  int rc = check_attn_args(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, d, scale);
+  if (rc != ATTNJVP_OK) return rc;
+  if (!lse || !mu) return fail(ATTNJVP_EINVAL, "chunk mode needs lse and mu (the merge consumes them)");
+  if (kv_start < 0 || kv_len < 1 || kv_start + kv_len > N)
+    return fail(ATTNJVP_EINVAL, "key range [%lld, %lld) outside [0, %lld) or empty", (long long)kv_start,
+                (long long)(kv_start + kv_len), (long long)N);
+  return run_fwd(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, d, scale, kv_start, kv_len, stream);
+}
+
+int attn_jvp_merge(const float* o_c, const float* ot_c, const float* lse_c, const float* mu_c, int64_t n_chunks,
+                   float* out, float* out_t, float* lse, float* mu, int64_t B, int64_t H, int64_t N, int64_t d,
+                   void* stream) {
+  if (!o_c || !ot_c || !lse_c || !mu_c || !out || !out_t) return fail(ATTNJVP_EINVAL, "NULL tensor");
+  if (!aligned(o_c, 16) || !aligned(ot_c, 16) || !aligned(out, 16) || !aligned(out_t, 16))
+    return fail(ATTNJVP_EINVAL, "o_c/ot_c/out/out_t must be 16-byte aligned");
+  if (!aligned(lse_c, 4) || !aligned(mu_c, 4) || (lse && !aligned(lse, 4)) || (mu && !aligned(mu, 4)))
+    return fail(ATTNJVP_EINVAL, "per-row tensor misaligned");
+  if (n_chunks < 1 || n_chunks > (1 << 20)) return fail(ATTNJVP_EINVAL, "n_chunks must be in [1, 2^20]");
+  if (B < 1 || H < 1 || N < 1) return fail(ATTNJVP_EINVAL, "B, H, N must be >= 1");
+  if (d < 4 || d > 256 || (d % 4) != 0) return fail(ATTNJVP_EINVAL, "d must be a multiple of 4 in [4, 256]");
+  const int64_t rows = B * H * N;
+  if (rows * (d / 4) / 256 >= (int64_t(1) << 31)) return fail(ATTNJVP_EINVAL, "too many rows");
+  int dev;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(ATTNJVP_ECUDA, "no CUDA device: %s", cudaGetErrorString(e));
+  e = launch_merge(o_c, ot_c, lse_c, mu_c, n_chunks, out, out_t, lse, mu, rows, d, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(ATTNJVP_ECUDA, "merge launch failed: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+int attn_jvp_cast_f32_bf16(const float* in, void* out, int64_t n, void* stream) {
+  if (n < 0) return fail(ATTNJVP_EINVAL, "n must be >= 0");
+  if (n == 0) return ok();
+  if (!in || !out) return fail(ATTNJVP_EINVAL, "NULL tensor");
+  if (!aligned(in, 16) || !aligned(out, 16)) return fail(ATTNJVP_EINVAL, "in/out must be 16-byte aligned");
+  int dev;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(ATTNJVP_ECUDA, "no CUDA device: %s", cudaGetErrorString(e));
+  e = launch_cast_f32_bf16(in, out, n, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(ATTNJVP_ECUDA, "cast launch failed: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+int trigflow_coeffs(double t, double tau, double* c) {
+  if (!c) return fail(ATTNJVP_EINVAL, "c is NULL");
+  if (!std::isfinite(t) || !std::isfinite(tau)) return fail(ATTNJVP_EINVAL, "t and tau must be finite");
+  const double s = std::sin(t), co = std::cos(t);
+  const double den = co + s;
+  if (!(den > 0.0)) return fail(ATTNJVP_EINVAL, "cos t + sin t <= 0: t outside (-pi/4, 3pi/4)");
+  const double inv = 1.0 / den;
+  c[0] = inv;
+  c[1] = -s * inv;
+  c[2] = inv;
+  c[3] = tau * s * inv;
+  return ok();
+}
+
+int trigflow_tangent(const float* x0, const float* eps, const double* t, float* out, int64_t B, int64_t per_sample,
+                     void* stream) {
+  if (!x0 || !eps || !t || !out) return fail(ATTNJVP_EINVAL, "NULL tensor");
+  if (!aligned(x0, 16) || !aligned(eps, 16) || !aligned(out, 16) || !aligned(t, 8))
+    return fail(ATTNJVP_EINVAL, "x0/eps/out must be 16-byte aligned and t 8-byte aligned");
+  if (B < 1 || B > 65535) return fail(ATTNJVP_EINVAL, "B must be in [1, 65535]");
+  if (per_sample < 1) return fail(ATTNJVP_EINVAL, "per_sample must be >= 1");
+  int dev;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(ATTNJVP_ECUDA, "no CUDA device: %s", cudaGetErrorString(e));
+  e = launch_trigflow_tangent(x0, eps, t, out, B, per_sample, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(ATTNJVP_ECUDA, "trigflow_tangent launch failed: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+int attn_jvp_status(int clear) {
+  const char* why = "";
+  int* st = status_word(&why);
+  if (!st) return fail(ATTNJVP_ECUDA, "no CUDA device / status word: %s", why);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail(ATTNJVP_ECUDA, "synchronize failed: %s", cudaGetErrorString(e));
+  int word = 0;
+  e = cudaMemcpy(&word, st, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(ATTNJVP_ECUDA, "status read failed: %s", cudaGetErrorString(e));
+  if (clear) {
+    const int zero = 0;
+    e = cudaMemcpy(st, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return fail(ATTNJVP_ECUDA, "status clear failed: %s", cudaGetErrorString(e));
+  }
+  if (word & kStatusTimeout) return fail(ATTNJVP_ETIMEOUT, "a kernel's bounded wait ran out (status 0x%x)", word);
+  return ok();
+}
+
+const char* attn_jvp_last_error(void) { return g_last_error; }
+
+const char* attn_jvp_version(void) { return "0.1.0"; }
+
+}  // extern "C"

@@ -1,0 +1,42 @@
+// Internal launch interface between the C-ABI layer (capi.cu) and the kernel
+// translation units.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace attnjvp {
+
+// Status bits a kernel ORs into the per-device status word.
+constexpr int kStatusTimeout = 1;
+
+struct FwdArgs {
+  const void *q, *k, *v, *q_t, *k_t, *v_t;  // bf16 [BH, N, d]
+  float *out, *out_t, *lse, *mu;            // fp32; lse/mu may be null
+  int64_t BH, N, d;
+  float scale;
+  int64_t kv_start, kv_len;
+  int* status;                               // device status word
+  cudaStream_t stream;
+};
+
+// Returns cudaSuccess or the failing CUDA error; ``*msg`` gets a static message.
+cudaError_t launch_attn_jvp_fwd(const FwdArgs& a, const char** msg);
+
+cudaError_t launch_merge(const float* o_c, const float* ot_c, const float* lse_c, const float* mu_c,
+                         int64_t n_chunks, float* out, float* out_t, float* lse, float* mu, int64_t rows,
+                         int64_t d, cudaStream_t stream);
+
+cudaError_t launch_cast_f32_bf16(const float* in, void* out, int64_t n, cudaStream_t stream);
+
+cudaError_t launch_trigflow_tangent(const float* x0, const float* eps, const double* t, float* out, int64_t B,
+                                    int64_t per_sample, cudaStream_t stream);
+
+// cuTensorMapEncodeTiled obtained through the runtime (no link-time libcuda dependency).
+typedef CUresult (*TensorMapEncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                      const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                      CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+TensorMapEncodeFn tensor_map_encoder();
+
+}  // namespace attnjvp

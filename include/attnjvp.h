@@ -1,0 +1,145 @@
+/*
+ * attnjvp.h — C ABI of the GB300 (sm_103a) forward-mode attention-JVP library.
+ *
+ * Operation (page "带分数正则的一致性蒸馏", gitcode.csdn.net, section 注意力
+ * (attention) and section 前向 (forward)): for every batch b, head h and query
+ * row i, with s the softmax scale,
+ *     S_ij  = s q_i . k_j                      P_i = softmax_j(S_ij)
+ *     St_ij = s (qt_i . k_j + q_i . kt_j)      (tangent of the scores, t_s)
+ *     O_i   = sum_j P_ij v_j                   LSE_i = ln sum_j exp(S_ij)
+ *     mu_i  = sum_j P_ij St_ij
+ *     Ot_i  = sum_j P_ij vt_j + sum_j P_ij (St_ij - mu_i) v_j
+ * i.e. the JVP t_o = P t_v + t_p V with t_p = P (.) t_s - (P t_s^T) P.  The
+ * output tangent is a stop-gradient value: nothing here builds a graph.
+ * Attention is non-causal and unmasked, with as many keys as queries.
+ *
+ * Conventions for every entry point:
+ *   - Tensors are DEVICE pointers (unless stated otherwise), row-major and
+ *     contiguous.  Attention tensors are [B, H, N, d]; per-row outputs are
+ *     [B, H, N].  The caller allocates and owns every buffer; the library keeps
+ *     no pointer after a call returns.
+ *   - ``stream`` is a cudaStream_t (NULL = legacy default stream).  Work is
+ *     enqueued asynchronously on it; a return value of 0 means "validated and
+ *     launched", not "finished".
+ *   - Return value: 0 on success or a negative ATTNJVP_E* code; the matching
+ *     human-readable message is available from attn_jvp_last_error() on the
+ *     same host thread.  No entry point aborts, throws or falls back to the CPU.
+ *   - Kernels wait on on-chip barriers with a bounded budget (one second per
+ *     wait).  A wait that runs out records ATTNJVP_ETIMEOUT in a per-device
+ *     status word, the kernel releases what it holds and returns early; read
+ *     the word with attn_jvp_status() after synchronising the stream.
+ */
+#ifndef ATTNJVP_H
+#define ATTNJVP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ATTNJVP_OK 0
+#define ATTNJVP_EINVAL (-1)       /* bad argument: null / misaligned pointer, bad size, bad scale */
+#define ATTNJVP_EUNSUPPORTED (-2) /* valid request this build does not implement (e.g. head dim) */
+#define ATTNJVP_ECUDA (-3)        /* a CUDA runtime or driver call failed */
+#define ATTNJVP_ETIMEOUT (-4)     /* a kernel's bounded wait ran out (see attn_jvp_status) */
+
+/*
+ * Fused attention forward + JVP (the operation above) over all N keys.
+ *   q, k, v, q_t, k_t, v_t : bf16 [B, H, N, d]; each base 16-byte aligned.
+ *                            Tangents have exactly the primals' shape and layout
+ *                            (the page's host wrapper asserts equal shape and stride).
+ *   out, out_t             : fp32 [B, H, N, d] — O and Ot; 16-byte aligned.
+ *   lse, mu                : fp32 [B, H, N] — natural-log LSE and mu; either may be
+ *                            NULL when not wanted.
+ *   B, H, N                : >= 1 each; B*H < 2^31 and N < 2^31.
+ *   d                      : head dimension; 64 or 128 in this build
+ *                            (others: ATTNJVP_EUNSUPPORTED).
+ *   scale                  : softmax scale s, finite and > 0 (the page's default is d^-1/2).
+ */
+int attn_jvp_fwd(const void* q, const void* k, const void* v,
+                 const void* q_t, const void* k_t, const void* v_t,
+                 float* out, float* out_t, float* lse, float* mu,
+                 int64_t B, int64_t H, int64_t N, int64_t d,
+                 float scale, void* stream);
+
+/*
+ * Same operation restricted to the key range [kv_start, kv_start + kv_len):
+ * every query row attends only to those keys.  The outputs are the chunk's
+ * own normalised partials (O_c, Ot_c, LSE_c, mu_c); attn_jvp_merge combines
+ * chunks exactly.  Arguments as attn_jvp_fwd, plus:
+ *   lse, mu   : required (not NULL) — the merge needs them.
+ *   kv_start  : >= 0;  kv_len >= 1;  kv_start + kv_len <= N.
+ * (The page has no key split; chunking is exact algebra on the definitions above.)
+ */
+int attn_jvp_fwd_chunk(const void* q, const void* k, const void* v,
+                       const void* q_t, const void* k_t, const void* v_t,
+                       float* out, float* out_t, float* lse, float* mu,
+                       int64_t B, int64_t H, int64_t N, int64_t d,
+                       float scale, int64_t kv_start, int64_t kv_len, void* stream);
+
+/*
+ * Exact merge of C key-chunk partials into the full-row result:
+ *   LSE = ln sum_c e^{LSE_c},  w_c = e^{LSE_c - LSE},
+ *   O = sum_c w_c O_c,  mu = sum_c w_c mu_c,  Ot = sum_c w_c (Ot_c + mu_c O_c) - mu O.
+ *   o_c, ot_c   : fp32 [C, B, H, N, d] (chunk-major), 16-byte aligned.
+ *   lse_c, mu_c : fp32 [C, B, H, N].
+ *   out, out_t  : fp32 [B, H, N, d], 16-byte aligned;  lse, mu : fp32 [B, H, N] or NULL.
+ *   n_chunks    : C >= 1.  d: a multiple of 4, 4 <= d <= 256.
+ * Outputs must not alias inputs.
+ */
+int attn_jvp_merge(const float* o_c, const float* ot_c, const float* lse_c, const float* mu_c,
+                   int64_t n_chunks, float* out, float* out_t, float* lse, float* mu,
+                   int64_t B, int64_t H, int64_t N, int64_t d, void* stream);
+
+/*
+ * Round fp32 to bf16 (nearest-even) element-wise on the device, so fp32 inputs
+ * can be fed to the bf16 kernels.  in: fp32 [n]; out: bf16 [n]; n >= 0.
+ * Both 16-byte aligned.
+ */
+int attn_jvp_cast_f32_bf16(const float* in, void* out, int64_t n, void* stream);
+
+/*
+ * TrigFlow-to-rectified-flow preconditioning coefficients in FP64 (page
+ * "带分数正则的一致性蒸馏", section 时间步转换 (timestep conversion),
+ * RectifiedFlow_TrigFlowWrapper with sigma_data = 1):
+ *   c[0] = c_skip  = 1 / (cos t + sin t)
+ *   c[1] = c_out   = -sin t / (cos t + sin t)
+ *   c[2] = c_in    = 1 / (cos t + sin t)
+ *   c[3] = c_noise = tau * sin t / (cos t + sin t)      (the page's config uses tau = 1000)
+ * Host function; c is a HOST array of 4 doubles.  Returns ATTNJVP_EINVAL when
+ * c is NULL, t or tau is not finite, or cos t + sin t <= 0 (t outside
+ * (-pi/4, 3pi/4); the documented domain is [0, pi/2]).
+ */
+int trigflow_coeffs(double t, double tau, double* c);
+
+/*
+ * Time derivative of the TrigFlow forward process x_t = cos t x0 + sin t eps
+ * (same page and section; also the velocity F of the section's wrapper):
+ *   out[b, i] = -sin(t[b]) x0[b, i] + cos(t[b]) eps[b, i]
+ *   x0, eps, out : fp32 [B, per_sample] (device), 16-byte aligned.
+ *   t            : FP64 [B] (device); sin/cos are taken in FP64 once per sample.
+ *   B >= 1, per_sample >= 1.  out may alias x0 or eps.
+ */
+int trigflow_tangent(const float* x0, const float* eps, const double* t, float* out,
+                     int64_t B, int64_t per_sample, void* stream);
+
+/*
+ * Reads (and, if ``clear`` is non-zero, resets) the status word of the current
+ * device after a device-wide synchronisation.  Returns 0 when no kernel has
+ * reported a problem since the last clear, ATTNJVP_ETIMEOUT when a bounded
+ * wait ran out, ATTNJVP_ECUDA when the word cannot be read.
+ */
+int attn_jvp_status(int clear);
+
+/* Message for the last non-zero return on the calling host thread ("" if none). */
+const char* attn_jvp_last_error(void);
+
+/* Library version, e.g. "0.1.0". */
+const char* attn_jvp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTNJVP_H */

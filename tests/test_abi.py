@@ -1,0 +1,117 @@
+"""CPU-side checks of the C ABI: the library loads, exports every declared
+symbol, validates arguments before touching CUDA, and its host-side TrigFlow
+coefficients match the oracle to 1e-12."""
+import ctypes
+import math
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+import oracle
+from attention_jvp_gb300 import _build, binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attnjvp.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("defined",)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for expected in ("attn_jvp_fwd", "attn_jvp_fwd_chunk", "attn_jvp_merge", "attn_jvp_cast_f32_bf16",
+                     "trigflow_coeffs", "trigflow_tangent", "attn_jvp_status", "attn_jvp_last_error",
+                     "attn_jvp_version"):
+        assert expected in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if line.strip())
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_library_targets_sm103a_only():
+    out = subprocess.run(["cuobjdump", "--list-elf", binding.LIB_PATH], capture_output=True, text=True).stdout
+    arches = set(re.findall(r"sm_\d+a?", out))
+    assert arches == {"sm_103a"}, arches
+
+
+def _fwd(lib, ptrs=None, B=1, H=1, N=128, d=128, scale=0.1, chunk=None):
+    p = [ctypes.c_void_p(256)] * 10 if ptrs is None else ptrs
+    if chunk is None:
+        return lib.attn_jvp_fwd(*p, B, H, N, d, ctypes.c_float(scale), None)
+    return lib.attn_jvp_fwd_chunk(*p, B, H, N, d, ctypes.c_float(scale), chunk[0], chunk[1], None)
+
+
+def test_argument_validation_needs_no_gpu(lib):
+    E = binding
+    null = [ctypes.c_void_p(0)] + [ctypes.c_void_p(256)] * 9
+    assert _fwd(lib, null) == E.ATTNJVP_EINVAL
+    assert b"q is NULL" in lib.attn_jvp_last_error()
+    mis = [ctypes.c_void_p(256)] * 3 + [ctypes.c_void_p(258)] + [ctypes.c_void_p(256)] * 6
+    assert _fwd(lib, mis) == E.ATTNJVP_EINVAL
+    assert b"16-byte" in lib.attn_jvp_last_error()
+    assert _fwd(lib, N=0) == E.ATTNJVP_EINVAL
+    assert _fwd(lib, B=0) == E.ATTNJVP_EINVAL
+    assert _fwd(lib, scale=float("nan")) == E.ATTNJVP_EINVAL
+    assert _fwd(lib, scale=-1.0) == E.ATTNJVP_EINVAL
+    assert _fwd(lib, scale=float("inf")) == E.ATTNJVP_EINVAL
+    assert _fwd(lib, d=96) == E.ATTNJVP_EUNSUPPORTED
+    assert _fwd(lib, d=256) == E.ATTNJVP_EUNSUPPORTED
+    assert _fwd(lib, chunk=(0, 0)) == E.ATTNJVP_EINVAL
+    assert _fwd(lib, chunk=(100, 29)) == E.ATTNJVP_EINVAL
+    assert _fwd(lib, chunk=(-1, 10)) == E.ATTNJVP_EINVAL
+    no_rows = [ctypes.c_void_p(256)] * 8 + [ctypes.c_void_p(0)] * 2
+    assert _fwd(lib, no_rows, chunk=(0, 64)) == E.ATTNJVP_EINVAL
+    vp = ctypes.c_void_p(256)
+    assert lib.attn_jvp_merge(vp, vp, vp, vp, 0, vp, vp, None, None, 1, 1, 8, 128, None) == E.ATTNJVP_EINVAL
+    assert lib.attn_jvp_merge(vp, vp, vp, vp, 2, vp, vp, None, None, 1, 1, 8, 130, None) == E.ATTNJVP_EINVAL
+    assert lib.attn_jvp_cast_f32_bf16(vp, vp, -1, None) == E.ATTNJVP_EINVAL
+    assert lib.attn_jvp_cast_f32_bf16(vp, vp, 0, None) == E.ATTNJVP_OK
+    assert lib.trigflow_tangent(vp, vp, vp, vp, 0, 10, None) == E.ATTNJVP_EINVAL
+    assert lib.trigflow_tangent(vp, vp, vp, vp, 2, 0, None) == E.ATTNJVP_EINVAL
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_valid_call_without_device_reports_cuda_error(lib):
+    assert _fwd(lib) == binding.ATTNJVP_ECUDA
+    assert len(lib.attn_jvp_last_error()) > 0
+
+
+@pytest.mark.parametrize("t", [0.0, 1e-3, 0.3, math.pi / 4, 1.0, 1.4, 1.5, math.atan(80.0), math.pi / 2])
+def test_trigflow_coeffs_match_oracle(lib, t):
+    got = binding.trigflow_coeffs(t, 1000.0)
+    ref = oracle.trigflow_coeffs(t, 1000.0)
+    for g, r in zip(got, ref):
+        assert abs(g - r) <= 1e-12 * max(abs(r), 1e-300) or abs(g - r) <= 1e-15
+    assert lib.attn_jvp_last_error() == b""
+
+
+def test_trigflow_coeffs_domain(lib):
+    with pytest.raises(binding.AttnJvpError) as e:
+        binding.trigflow_coeffs(-math.pi / 2)
+    assert e.value.code == binding.ATTNJVP_EINVAL
+    with pytest.raises(binding.AttnJvpError):
+        binding.trigflow_coeffs(float("nan"))
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(binding, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        binding.load(str(tmp_path / "libattnjvp.so"))
