@@ -199,55 +199,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdS = make_idesc_bf16_f32(128, C::kBN, false, false);  // Q K^T, both K-major
       constexpr uint32_t kIdPV = make_idesc_bf16_f32(128, D, false, true);      // P~ V, V is N-major
-      const uint32_t sQ = smem_u32(smem + C::kOffQ);
-      const uint32_t sQt = smem_u32(smem + C::kOffQt);
+      // Descriptors are built once; an operand step adds its byte offset / 16 to the
+      // start-address field (every offset here stays inside one CTA's shared memory).
+      const uint64_t dQ = make_smem_desc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
+      const uint64_t dQt = make_smem_desc_sw128(smem_u32(smem + C::kOffQt), 16, 1024);
+      const uint64_t dK0 = make_smem_desc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
+      const uint64_t dV0 = make_smem_desc_sw128(smem_u32(smem + C::kOffV), C::kChunkK, 1024);
+      auto off = [](uint64_t desc, uint32_t bytes) { return desc + static_cast<uint64_t>(bytes >> 4); };
 
-      auto issue_scores = [&](int t) -> bool {
-        const int b = t % C::kNB;
+      // St_t = [Qt Q] [K_t Kt_t]^T into buffer t % NB.  PV of the buffer's previous
+      // tile reads only the P~/H~ columns (the S half), so this may be issued
+      // before that PV has completed.
+      auto issue_st = [&](int t) -> bool {
         const int s = t % C::kKS;
         if (!mbar_wait(&bars->k_full[s], (t / C::kKS) & 1, abort_flag, status, kStatusTimeout)) return false;
-        if (t >= C::kNB) {
-          // P~/H~ of tile t-NB sit in this buffer's S columns: wait until that tile's PV MMAs are done.
-          if (!mbar_wait(&bars->pv_done[b], ((t - C::kNB) / C::kNB) & 1, abort_flag, status, kStatusTimeout))
-            return false;
-        }
         tc_fence_after_sync();
-        const uint32_t sK = smem_u32(smem + C::kOffK + s * C::kKStage);
+        const uint64_t dK = off(dK0, s * C::kKStage);
+        const uint32_t dSt = tmem + C::kColBuf + 128u * (t % C::kNB) + 64u;
+#pragma unroll
+        for (int c = 0; c < C::kDC; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(dSt, off(dQt, c * C::kChunkQ + kk * 32), off(dK, c * C::kChunkK + kk * 32), kIdS,
+                   (c | kk) != 0);
+#pragma unroll
+        for (int c = 0; c < C::kDC; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(dSt, off(dQ, c * C::kChunkQ + kk * 32), off(dK, (C::kDC + c) * C::kChunkK + kk * 32), kIdS, 1);
+        return true;
+      };
+      // S_t = Q K_t^T into the S half of buffer t % NB, which holds P~/H~ of tile
+      // t - NB until that tile's PV MMAs complete.
+      auto issue_s = [&](int t) -> bool {
+        const int b = t % C::kNB;
+        const int s = t % C::kKS;
+        if (t >= C::kNB &&
+            !mbar_wait(&bars->pv_done[b], ((t - C::kNB) / C::kNB) & 1, abort_flag, status, kStatusTimeout))
+          return false;
+        tc_fence_after_sync();
+        const uint64_t dK = off(dK0, s * C::kKStage);
         const uint32_t dS = tmem + C::kColBuf + 128u * b;
-        const uint32_t dSt = dS + 64u;
-        // S = Q K^T
 #pragma unroll
         for (int c = 0; c < C::kDC; ++c)
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t a = make_smem_desc_sw128(sQ + c * C::kChunkQ + kk * 32, 16, 1024);
-            const uint64_t bd = make_smem_desc_sw128(sK + c * C::kChunkK + kk * 32, 16, 1024);
-            mma_ss(dS, a, bd, kIdS, (c | kk) != 0);
-          }
-        // St = [Qt Q] [K Kt]^T : one accumulator, 2d deep
-#pragma unroll
-        for (int c = 0; c < C::kDC; ++c)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t a = make_smem_desc_sw128(sQt + c * C::kChunkQ + kk * 32, 16, 1024);
-            const uint64_t bd = make_smem_desc_sw128(sK + c * C::kChunkK + kk * 32, 16, 1024);
-            mma_ss(dSt, a, bd, kIdS, (c | kk) != 0);
-          }
-#pragma unroll
-        for (int c = 0; c < C::kDC; ++c)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t a = make_smem_desc_sw128(sQ + c * C::kChunkQ + kk * 32, 16, 1024);
-            const uint64_t bd = make_smem_desc_sw128(sK + (C::kDC + c) * C::kChunkK + kk * 32, 16, 1024);
-            mma_ss(dSt, a, bd, kIdS, 1);
-          }
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(dS, off(dQ, c * C::kChunkQ + kk * 32), off(dK, c * C::kChunkK + kk * 32), kIdS, (c | kk) != 0);
         mma_commit(&bars->k_empty[s]);
         mma_commit(&bars->s_full[b]);
         return true;
       };
 
       bool ok = mbar_wait(&bars->q_full, 0, abort_flag, status, kStatusTimeout);
-      for (int t = 0; ok && t < C::kNB && t < n_tiles; ++t) ok = issue_scores(t);
+      for (int t = 0; ok && t < C::kNB && t < n_tiles; ++t) ok = issue_st(t) && issue_s(t);
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int b = j % C::kNB;
         const int s = j % C::kVS;
@@ -255,14 +259,13 @@ __global__ void __launch_bounds__(kThreads, 1)
              mbar_wait(&bars->v_full[s], (j / C::kVS) & 1, abort_flag, status, kStatusTimeout);
         if (!ok) break;
         tc_fence_after_sync();
-        const uint32_t sV = smem_u32(smem + C::kOffV + s * C::kVStage);
-        const uint32_t sVt = sV + C::kDC * C::kChunkK;
+        const uint64_t dV = off(dV0, s * C::kVStage);
         const uint32_t aP = tmem + C::kColBuf + 128u * b;  // P~ packed bf16: 32 columns
         const uint32_t aH = aP + 32u;                       // H~ packed bf16: 32 columns
 #pragma unroll
         for (int kk = 0; kk < C::kBN / 16; ++kk) {
-          const uint64_t bV = make_smem_desc_sw128(sV + kk * 2048, C::kChunkK, 1024);
-          const uint64_t bVt = make_smem_desc_sw128(sVt + kk * 2048, C::kChunkK, 1024);
+          const uint64_t bV = off(dV, kk * 2048);
+          const uint64_t bVt = off(dV, C::kDC * C::kChunkK + kk * 2048);
           const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
           mma_ts(tmem + C::kColO, aP + kk * 8, bV, kIdPV, acc);   // O += P~ V
           mma_ts(tmem + C::kColT, aP + kk * 8, bVt, kIdPV, acc);  // T += P~ Vt
@@ -270,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(&bars->v_empty[s]);
         mma_commit(&bars->pv_done[b]);
-        if (j + C::kNB < n_tiles) ok = issue_scores(j + C::kNB);
+        if (j + C::kNB < n_tiles) ok = issue_st(j + C::kNB) && issue_s(j + C::kNB);
       }
       // Nothing may still be reading shared memory or TMEM when the CTA tears down.
       mma_commit(&bars->drain);
@@ -294,16 +297,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const uint32_t cS = lane_addr + C::kColBuf + 128u * b;
       const int valid = min(C::kBN, kv_len - j * C::kBN);
-      uint32_t sr[64];
-      tmem_ld32_wait(cS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32_wait(cS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      float x[64];
-      float mx = -INFINITY;
+      // One load brings the row's 64 raw scores (columns 0-63) and 64 raw score
+      // tangents (columns 64-127) of this buffer.
+      uint32_t raw[128];
+      tmem_ld128_wait(cS, raw);
+      if (valid < C::kBN) {
+        // Tail tile: keys past the range get score -inf (weight 0) and tangent 0.
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        x[i] = (i < valid) ? __uint_as_float(sr[i]) * c2 : -INFINITY;
-        mx = fmaxf(mx, x[i]);
+        for (int i = 0; i < 64; ++i)
+          if (i >= valid) {
+            raw[i] = __float_as_uint(-INFINITY);
+            raw[64 + i] = 0u;
+          }
       }
+      // Row max of the raw scores (the scale is positive, so it keeps the order);
+      // eight independent chains keep the dependency depth short.
+      float mx8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx8[k] = __uint_as_float(raw[k]);
+#pragma unroll
+      for (int i = 8; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(raw[i]));
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * c2;
       float alpha = 1.f;
       bool rescale = false;
       if (j == 0) {
@@ -313,32 +328,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         m = mx;
         rescale = true;
       }
-      float ls = 0.f;
+      // P~ = 2^(S s log2e - m): one FFMA and one MUFU ex2 per score.
+      float p[64];
+      float ls8[8];
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
-        x[i] = ex2_approx(x[i] - m);
-        ls += x[i];
+        p[i] = ex2_approx(fmaf(__uint_as_float(raw[i]), c2, -m));
+        ls8[i & 7] = (i < 8) ? p[i] : ls8[i & 7] + p[i];
       }
-      l = l * alpha + ls;
+      l = l * alpha + (((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7])));
       uint32_t pk[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
-      // H~ = P~ (.) St * s, row sum in fp32 before rounding.
+      for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
+      // H~ = P~ (.) St s; its row sum is taken in fp32 before rounding to bf16.
       uint32_t hk[32];
-      float rs = 0.f;
+      float rs8[8];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t tr[32];
-        tmem_ld32_wait(cS + 64 + 32 * h, tr);
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float h0 = x[32 * h + i] * (__uint_as_float(tr[i]) * scale);
-          const float h1 = x[32 * h + i + 1] * (__uint_as_float(tr[i + 1]) * scale);
-          rs += h0 + h1;
-          hk[16 * h + i / 2] = pack_bf16x2(h0, h1);
-        }
+      for (int i = 0; i < 64; i += 2) {
+        const float h0 = p[i] * (__uint_as_float(raw[64 + i]) * scale);
+        const float h1 = p[i + 1] * (__uint_as_float(raw[65 + i]) * scale);
+        const int k = (i >> 1) & 7;
+        rs8[k] = (i < 16) ? (h0 + h1) : rs8[k] + (h0 + h1);
+        hk[i >> 1] = pack_bf16x2(h0, h1);
       }
-      r = r * alpha + rs;
+      r = r * alpha + (((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7])));
       if (__any_sync(0xffffffffu, rescale)) {
         // O and T may only be touched once the previous tile's PV MMAs are done.
         ok = mbar_wait(&bars->pv_done[(j - 1) % C::kNB], ((j - 1) / C::kNB) & 1, abort_flag, status,

@@ -120,6 +120,27 @@ def workload_inputs(name, device="cpu", **overrides):
     return make_inputs(**spec, device=device)
 
 
+def latent_for(name_or_spec, device="cpu", seed=None):
+    """Latent batch (x0, eps, t) for the TrigFlow steps of a workload.
+
+    Each attention token stands for a 2x2 patch of a 16-channel latent, so a
+    sample holds 64 * N values (video: 16 ch x 21 frames x 60x104 for N=32760).
+    TrigFlow times follow the page's sCM time sampler (section 训练设置, training
+    setup): ln sigma ~ N(-0.8, 1.6^2), t = arctan(sigma), one t per sample, FP64.
+    """
+    spec = dict(WORKLOADS[name_or_spec]) if isinstance(name_or_spec, str) else dict(name_or_spec)
+    B, N = spec["B"], spec["N"]
+    seed = spec["seed"] + 1000 if seed is None else seed
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    x0 = torch.randn((B, 64 * N), generator=gen, device=device, dtype=torch.float32)
+    eps = torch.randn((B, 64 * N), generator=gen, device=device, dtype=torch.float32)
+    log_sigma = torch.randn((B,), generator=gen, device=device, dtype=torch.float64) * 1.6 - 0.8
+    t = torch.atan(torch.exp(log_sigma))
+    return x0, eps, t
+
+
 def sample_rows(N, count, seed):
     """``count`` distinct query-row indices in [0, N), seeded, always including 0 and N-1."""
     gen = torch.Generator(device="cpu")

@@ -1,0 +1,464 @@
+#!/usr/bin/env python
+"""Benchmark of the attention-JVP hot path on GB300; prints ONE JSON line.
+
+A step is one pass of the whole path over one batch of synthetic inputs:
+the FP64 TrigFlow coefficients of the batch's times (host), the TrigFlow
+tangent of the latent batch (GPU), and the fused attention forward + JVP
+(GPU; split into key chunks + exact merge for the long-video workload).
+The metric counts the attention's 12*B*H*N^2*d flops per step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the FP64 CPU oracle on host cores
+
+Multi-GPU: launched by torchrun, each rank runs an independent replica of the
+workload on its own GPU (the path shards into independent heads; no data
+collective); timing is the max over ranks, value is the whole-job throughput.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention-JVP TFLOPS (12·B·H·N²·d) and % of GB300 BF16 tensor peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "video_dit"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCE = os.path.join(ROOT, "attention_jvp_gb300", "csrc", "attn_jvp_fwd.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=30)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    p.add_argument("--heads", type=int, default=None, help="override H (profiling on a smaller case)")
+    p.add_argument("--skip-e2e", action="store_true")
+    p.add_argument("--skip-cpu", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# host-side helpers (no GPU needed; covered by tests/test_bench_host.py)
+# ---------------------------------------------------------------------------
+def workload_spec(name, heads=None):
+    from attention_jvp_gb300 import inputs
+    spec = dict(inputs.WORKLOADS[name])
+    if heads is not None:
+        spec["H"] = int(heads)
+    return spec
+
+
+def attention_flops(spec, kv_len=None):
+    """Algorithmic flops of one attention JVP pass: 12 d per (query, key) pair.
+
+    2d for S, 4d for St (two d-deep products), 2d each for P~V, P~Vt and H~V.
+    """
+    kv = spec["N"] if kv_len is None else kv_len
+    return 12.0 * spec["B"] * spec["H"] * spec["N"] * kv * spec["d"]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            peaks = json.load(f)
+        return peaks, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha():
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_per_launch(kernel, workload, heads):
+    """DRAM bytes per launch from the committed ncu summary, or None if absent or stale."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            table = json.load(f)
+    except (OSError, ValueError):
+        return None
+    rec = table.get(kernel, {}).get(workload)
+    if not rec or rec.get("source_sha") != kernel_source_sha():
+        return None
+    # counters scale with the number of heads processed (each head is independent)
+    return float(rec["dram_bytes_per_launch"]) * heads / float(rec["heads"])
+
+
+def aggregate(local_ms, local_units, world, reduce_max=None, reduce_sum=None):
+    """Whole-job numbers from per-rank timings: max time over ranks, total units."""
+    t = reduce_max(local_ms) if (world > 1 and reduce_max) else local_ms
+    u = reduce_sum(local_units) if (world > 1 and reduce_sum) else local_units
+    return t, u
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    @classmethod
+    def summarize(cls, lines):
+        sm, mx, reasons = [], [], set()
+        for ln in lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(cls.REASONS, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU legs: the oracle on a bounded sample of the workload
+# ---------------------------------------------------------------------------
+def oracle_rows_for(spec, x_host_head, target_s, seed=0):
+    """Number of query rows the FP64 oracle evaluates in about ``target_s`` seconds."""
+    import oracle
+    from attention_jvp_gb300 import inputs
+
+    cores = oracle.default_threads()
+    q, k, v, qt, kt, vt = x_host_head
+    rows = inputs.sample_rows(spec["N"], max(cores, 8), seed).numpy()
+    t0 = time.perf_counter()
+    oracle.attn_jvp(q, k, v, qt, kt, vt, spec["scale"], rows=rows, nthreads=cores)
+    per_row = (time.perf_counter() - t0) / len(rows)
+    return int(max(len(rows), min(spec["N"], target_s / max(per_row, 1e-9))))
+
+
+def oracle_sample(spec, x_host_head, n_rows, seed=0):
+    """Time the FP64 oracle on ``n_rows`` query rows of one head against all N keys.
+
+    Returns (tflops, cores, rows, seconds); flops are the same 12 d per
+    (query, key) pair the GPU metric counts.
+    """
+    import oracle
+    from attention_jvp_gb300 import inputs
+
+    cores = oracle.default_threads()
+    q, k, v, qt, kt, vt = x_host_head
+    N, d = spec["N"], spec["d"]
+    rows = inputs.sample_rows(N, n_rows, seed + 1).numpy()
+    t0 = time.perf_counter()
+    oracle.attn_jvp(q, k, v, qt, kt, vt, spec["scale"], rows=rows, nthreads=cores)
+    dt = time.perf_counter() - t0
+    return 12.0 * len(rows) * N * d / dt / 1e12, cores, len(rows), dt
+
+
+def host_head(x, h=0):
+    """FP64 host copies of one head's six inputs (the values the GPU sees)."""
+    B, H, N, d = x["q"].shape
+    return tuple(x[n].reshape(B * H, N, d)[h].to("cpu").double().numpy()
+                 for n in ("q", "k", "v", "q_t", "k_t", "v_t"))
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import torch
+
+    from attention_jvp_gb300 import inputs
+    spec = workload_spec(args.workload, args.heads)
+    spec["scale"] = inputs.default_scale(spec["d"])
+    # one head's inputs, drawn on the CPU with the workload's recipe
+    one = dict(spec, B=1, H=1)
+    x = inputs.make_inputs(**one, device="cpu")
+    xh = host_head(x)
+    total = args.steps + args.warmup
+    per_step = max(0.5, min(10.0, 150.0 / max(total, 1)))
+    import oracle
+    cores = oracle.default_threads()
+    n_rows = oracle_rows_for(spec, xh, per_step)
+    rates = []
+    for s in range(total):
+        tf, cores, rows_used, dt = oracle_sample(spec, xh, n_rows, seed=s)
+        if s >= args.warmup:
+            rates.append(tf)
+    value = statistics.median(rates) if rates else None
+    full = attention_flops(spec)
+    rec = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": (full / (value * 1e12) * 1e3) if value else None,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "B": spec["B"], "H": spec["H"], "N": spec["N"], "d": spec["d"]},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "%d query rows of one head vs all %d keys per step; ms_per_step "
+                                   "extrapolated to the full workload" % (rows_used, spec["N"])},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(rec))
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    from attention_jvp_gb300 import _build, binding, inputs
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    binding.load()
+
+    spec = workload_spec(args.workload, args.heads)
+    B, H, N, d = spec["B"], spec["H"], spec["N"], spec["d"]
+    x = inputs.make_inputs(**spec, device=dev)
+    scale = x["scale"]
+    x0, eps, t = inputs.latent_for(spec, device=dev)
+    t_host = t.cpu().tolist()
+    dxdt = torch.empty_like(x0)
+    out = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+    out_t = torch.empty_like(out)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    mu = torch.empty_like(lse)
+    n_chunks = spec.get("kv_chunks", 1)
+    ws = binding.split_workspace((B, H, N, d), n_chunks, dev) if n_chunks > 1 else None
+    bounds = binding.chunk_bounds(N, n_chunks)
+    stream = torch.cuda.current_stream()
+    attn_events = []  # (start, end, kv_len) per attention-kernel launch in the timed region
+
+    def attention(q, k, v, q_t, k_t, v_t, record):
+        if n_chunks == 1:
+            e0 = torch.cuda.Event(enable_timing=True) if record else None
+            e1 = torch.cuda.Event(enable_timing=True) if record else None
+            if record:
+                e0.record(stream)
+            binding.attn_jvp_fwd(q, k, v, q_t, k_t, v_t, scale=scale, out=out, out_t=out_t, lse=lse, mu=mu,
+                                 stream=stream)
+            if record:
+                e1.record(stream)
+                attn_events.append((e0, e1, N))
+        else:
+            for c, (a, n) in enumerate(bounds):
+                e0 = torch.cuda.Event(enable_timing=True) if record else None
+                e1 = torch.cuda.Event(enable_timing=True) if record else None
+                if record:
+                    e0.record(stream)
+                binding.attn_jvp_fwd_chunk(q, k, v, q_t, k_t, v_t, a, n, scale=scale, out=ws[0][c],
+                                           out_t=ws[1][c], lse=ws[2][c], mu=ws[3][c], stream=stream)
+                if record:
+                    e1.record(stream)
+                    attn_events.append((e0, e1, n))
+            binding.attn_jvp_merge(*ws, out=out, out_t=out_t, lse=lse, mu=mu, stream=stream)
+
+    def step(record=False, xin=x):
+        coeffs = [binding.trigflow_coeffs(tt) for tt in t_host]  # FP64, host
+        binding.trigflow_tangent(x0, eps, t, out=dxdt, stream=stream)
+        attention(xin["q"], xin["k"], xin["v"], xin["q_t"], xin["k_t"], xin["v_t"], record)
+        return coeffs
+
+    launches_per_step = 1 + (1 if n_chunks == 1 else n_chunks + 1)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    binding.attn_jvp_status()
+
+    gpu_index = local
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local < len(ids) and ids[local].isdigit():
+            gpu_index = int(ids[local])
+    sampler = ClockSampler(gpu_index)
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)  # let the sampler take a first idle-to-load sample
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    sampler.stop()
+    binding.attn_jvp_status()
+    local_ms = ev0.elapsed_time(ev1)
+    attn_ms = [a.elapsed_time(b) for a, b, _ in attn_events]
+    attn_kv = [kv for _, _, kv in attn_events]
+
+    flops_step = attention_flops(spec)
+
+    def rmax(v):
+        tt = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        return float(tt.item())
+
+    def rsum(v):
+        tt = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.SUM)
+        return float(tt.item())
+
+    job_ms, job_flops = aggregate(local_ms, flops_step * args.steps, world, rmax, rsum)
+    value = job_flops / (job_ms * 1e-3) / 1e12
+
+    # ---- roofline of the dominant kernel (the fused attention-JVP kernel) ----
+    peaks, peak_src = load_peaks()
+    mean_launch_ms = sum(attn_ms) / len(attn_ms)
+    flops_launch = sum(attention_flops(spec, kv) for kv in attn_kv) / len(attn_kv)
+    achieved = flops_launch / (mean_launch_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops_sustained"])
+    kname = "attn_jvp_fwd_kernel<%d>" % d
+    traffic = traffic_per_launch(kname, args.workload, H * B)
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": UNIT,
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_source": "%s bf16_tflops_sustained (kernel timed inside a long step)" % peak_src,
+                "frac_of_burst_peak": round(achieved / float(peaks["bf16_tflops"]), 4),
+                "kernel": kname, "launch_ms": round(mean_launch_ms, 4),
+                "flops_per_launch": flops_launch}
+
+    # ---- end to end through the C ABI with host buffers ----
+    e2e = None
+    if not args.skip_e2e:
+        host_in = {n: torch.empty(x[n].shape, dtype=x[n].dtype, pin_memory=True) for n in inputs.NAMES}
+        for n in inputs.NAMES:
+            host_in[n].copy_(x[n])
+        dev_in = {n: torch.empty_like(x[n]) for n in inputs.NAMES}
+        host_out = [torch.empty(tt.shape, dtype=tt.dtype, pin_memory=True) for tt in (out, out_t, lse, mu)]
+        h2d = sum(host_in[n].numel() * host_in[n].element_size() for n in inputs.NAMES)
+        d2h = sum(tt.numel() * tt.element_size() for tt in host_out)
+
+        def e2e_step():
+            for n in inputs.NAMES:
+                dev_in[n].copy_(host_in[n], non_blocking=True)
+            step(xin=dev_in)
+            for hdst, src in zip(host_out, (out, out_t, lse, mu)):
+                hdst.copy_(src, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms, e_flops = aggregate(e0.elapsed_time(e1), flops_step * args.e2e_steps, world, rmax, rsum)
+        e2e = {"value": round(e_flops / (e_ms * 1e-3) / 1e12, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+               "ms_per_step": round(e_ms / args.e2e_steps, 3)}
+        binding.attn_jvp_status()
+        del host_in, dev_in, host_out
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only) ----
+    cpu = None
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        spec_s = dict(spec, scale=scale)
+        xh = host_head(x)
+        tf, cores, nrows, dt = oracle_sample(spec_s, xh, oracle_rows_for(spec_s, xh, args.cpu_seconds))
+        cpu = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": "%d query rows of head 0 vs all %d keys (%.1f s FP64 on %d host threads)"
+                         % (nrows, N, dt, cores)}
+
+    if rank == 0:
+        clocks = ClockSampler.summarize(sampler.lines)
+        total_bytes = sum(x[n].numel() * x[n].element_size() for n in inputs.NAMES)
+        rec = {
+            "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(job_ms / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "B": B, "H": H, "N": N, "d": d, "kv_chunks": n_chunks,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "inputs larger than L2 (%.2f GB of bf16 inputs per step vs 129 MB L2)"
+                             % (total_bytes / 1e9)},
+            "pct_of_peak": {"bf16_sustained_%.0f" % float(peaks["bf16_tflops_sustained"]):
+                            round(100 * value / world / float(peaks["bf16_tflops_sustained"]), 2),
+                            "bf16_burst_%.0f" % float(peaks["bf16_tflops"]):
+                            round(100 * value / world / float(peaks["bf16_tflops"]), 2)},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(rec))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,125 @@
+"""Host-side logic of bench.py (no GPU): flop counting, clock parsing, the
+traffic record, the reference arm's JSON line, and the multi-rank aggregation
+(max time over ranks, summed work) on two gloo ranks."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_attention_flops_counts_twelve_d_per_pair():
+    spec = dict(B=1, H=40, N=32760, d=128)
+    assert bench.attention_flops(spec) == 12.0 * 40 * 32760 ** 2 * 128
+    assert bench.attention_flops(spec, kv_len=18900) == 12.0 * 40 * 32760 * 18900 * 128
+
+
+def test_clock_summary_parses_reasons():
+    lines = [
+        "0, 1995, 2070, 850.1, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "0, 2070, 2070, 1200.5, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 2040, 2070, 1300.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "garbage",
+    ]
+    s = bench.ClockSampler.summarize(lines)
+    assert s["sm_mhz"] == 2040 and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 3
+    assert bench.ClockSampler.summarize([])["sm_mhz"] is None
+
+
+def test_traffic_record_tracks_kernel_source(tmp_path, monkeypatch):
+    rec = {"k": {"w": {"source_sha": bench.kernel_source_sha(), "heads": 4, "dram_bytes_per_launch": 400.0}}}
+    path = tmp_path / "traffic.json"
+    path.write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(path))
+    assert bench.traffic_per_launch("k", "w", 40) == 4000.0
+    rec["k"]["w"]["source_sha"] = "stale"
+    path.write_text(json.dumps(rec))
+    assert bench.traffic_per_launch("k", "w", 40) is None
+    assert bench.traffic_per_launch("other", "w", 40) is None
+
+
+def test_committed_traffic_record_is_well_formed():
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        table = json.load(f)
+    for kernel, per_workload in table.items():
+        for workload, rec in per_workload.items():
+            assert rec["dram_bytes_per_launch"] > 0 and rec["heads"] >= 1
+            assert len(rec["source_sha"]) == 16
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, local_ms, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+
+    def rmax(v):
+        t = torch.tensor([v], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def rsum(v):
+        t = torch.tensor([v], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        return float(t.item())
+
+    dist.barrier()
+    t, u = bench.aggregate(local_ms[rank], 1.0e12, world, rmax, rsum)
+    q.put((rank, t, u))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_aggregate_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    local_ms = [41.0, 57.5]
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, local_ms, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, t, u in res:
+        assert t == 57.5          # the slowest rank's time
+        assert u == 2.0e12        # work of both replicas
+
+
+def test_aggregate_single_rank_is_identity():
+    assert bench.aggregate(12.5, 3.0, 1) == (12.5, 3.0)
+
+
+def test_reference_arm_prints_one_json_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "tiny",
+                          "--steps", "2", "--warmup", "1"], capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["unit"] == "TFLOP/s" and rec["value"] > 0
+    assert rec["cpu_baseline"]["kind"] == "oracle" and rec["cpu_baseline"]["cores"] >= 1
+    assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["e2e"]["d2h_bytes_per_step"] == 0
+    assert rec["metric"] == bench.METRIC
+
+
+def test_reference_arm_nonzero_rank_exits_quietly():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "tiny"],
+                         capture_output=True, text=True, timeout=120, cwd=ROOT, env=env)
+    assert out.returncode == 0 and out.stdout.strip() == ""
