@@ -43,12 +43,14 @@ def load(path=None):
     lib.attn_jvp_fwd_chunk.argtypes = [vp] * 6 + [fp] * 4 + [i64] * 4 + [ctypes.c_float, i64, i64, vp]
     lib.attn_jvp_merge.argtypes = [vp] * 4 + [i64] + [vp] * 4 + [i64] * 4 + [vp]
     lib.attn_jvp_cast_f32_bf16.argtypes = [vp, vp, i64, vp]
+    lib.attn_jvp_fwd_split_noalloc.argtypes = [vp] * 6 + [fp] * 4 + [i64] * 4 + [ctypes.c_float, i64, vp]
     lib.trigflow_coeffs.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.POINTER(ctypes.c_double)]
     lib.trigflow_tangent.argtypes = [vp, vp, vp, vp, i64, i64, vp]
     lib.attn_jvp_status.argtypes = [ctypes.c_int]
     lib.attn_jvp_last_error.restype = ctypes.c_char_p
     lib.attn_jvp_version.restype = ctypes.c_char_p
     for name in ("attn_jvp_fwd", "attn_jvp_fwd_chunk", "attn_jvp_merge", "attn_jvp_cast_f32_bf16",
+                 "attn_jvp_fwd_split_noalloc",
                  "trigflow_coeffs", "trigflow_tangent", "attn_jvp_status"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
@@ -191,6 +193,28 @@ def attn_jvp_split(q, k, v, q_t, k_t, v_t, n_chunks, scale=None, workspace=None,
         attn_jvp_fwd_chunk(q, k, v, q_t, k_t, v_t, a, n, scale=scale, out=o_c[c], out_t=ot_c[c],
                            lse=lse_c[c], mu=mu_c[c], stream=stream)
     return attn_jvp_merge(o_c, ot_c, lse_c, mu_c, out=out, out_t=out_t, lse=lse, mu=mu, stream=stream)
+
+
+def attn_jvp_fwd_split_noalloc(q, k, v, q_t, k_t, v_t, n_chunks, out, out_t, lse=None, mu=None, scale=None,
+                               stream=None):
+    """Split-KV path whose chunk partials live in the library's built-in
+    scratch array, for callers that cannot allocate device memory.  All
+    outputs are caller-provided; this wrapper allocates nothing either."""
+    for n, t in zip(("q", "k", "v", "q_t", "k_t", "v_t"), (q, k, v, q_t, k_t, v_t)):
+        _req(t, n, torch.bfloat16, q.shape)
+    B, H, N, d = q.shape
+    _req(out, "out", torch.float32, q.shape)
+    _req(out_t, "out_t", torch.float32, q.shape)
+    if lse is not None:
+        _req(lse, "lse", torch.float32, (B, H, N))
+    if mu is not None:
+        _req(mu, "mu", torch.float32, (B, H, N))
+    scale = d ** -0.5 if scale is None else float(scale)
+    rc = load().attn_jvp_fwd_split_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(q_t), _ptr(k_t), _ptr(v_t),
+                                           _ptr(out), _ptr(out_t), _ptr(lse), _ptr(mu), B, H, N, d,
+                                           ctypes.c_float(scale), int(n_chunks), _stream(stream))
+    _check("attn_jvp_fwd_split_noalloc", rc)
+    return out, out_t, lse, mu
 
 
 def split_workspace(shape, n_chunks, device):

@@ -124,6 +124,8 @@ int run_fwd(const void* q, const void* k, const void* v, const void* q_t, const 
 
 }  // namespace
 
+void set_last_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg ? msg : ""); }
+
 TensorMapEncodeFn tensor_map_encoder() {
   static TensorMapEncodeFn fn = nullptr;
   static std::once_flag once;

@@ -33,6 +33,9 @@ cudaError_t launch_cast_f32_bf16(const float* in, void* out, int64_t n, cudaStre
 cudaError_t launch_trigflow_tangent(const float* x0, const float* eps, const double* t, float* out, int64_t B,
                                     int64_t per_sample, cudaStream_t stream);
 
+// Sets the calling thread's message returned by attn_jvp_last_error().
+void set_last_error(const char* msg);
+
 // cuTensorMapEncodeTiled obtained through the runtime (no link-time libcuda dependency).
 typedef CUresult (*TensorMapEncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                       const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,

@@ -93,6 +93,32 @@ int attn_jvp_merge(const float* o_c, const float* ot_c, const float* lse_c, cons
                    int64_t B, int64_t H, int64_t N, int64_t d, void* stream);
 
 /*
+ * Split-KV attention JVP (the same result as attn_jvp_fwd_chunk over
+ * n_chunks near-equal key ranges followed by attn_jvp_merge) for callers that
+ * may not allocate device memory: for example code that runs inside a host
+ * framework which owns all device memory and passes in only an operation's
+ * tensors, or a loop where the implicit device synchronisation of
+ * cudaMalloc/cudaFree is not allowed.  The pages have no counterpart; this is
+ * an interface convenience around the split path above.
+ *   Arguments as attn_jvp_fwd, plus n_chunks in [1, N]; lse and mu may be NULL.
+ *   The chunk partials live in a 16 MiB array built into the library (one per
+ *   device that loads it, held until the process exits), so
+ *   n_chunks * B * H * N * (2d + 2) * 4 bytes must not exceed 16 MiB;
+ *   larger requests return ATTNJVP_EINVAL with the sizes in the message.
+ *   No allocator is called.  The first call on a device looks up the array's
+ *   device address (cudaGetSymbolAddress); make that first call before any
+ *   stream capture.  Every call on a device uses the same array: calls that
+ *   can overlap on the GPU (unordered streams, concurrent host threads) race
+ *   and must be serialised by the caller.  Each call writes every partial
+ *   before reading it, so nothing from an earlier call leaks into a result.
+ */
+int attn_jvp_fwd_split_noalloc(const void* q, const void* k, const void* v,
+                               const void* q_t, const void* k_t, const void* v_t,
+                               float* out, float* out_t, float* lse, float* mu,
+                               int64_t B, int64_t H, int64_t N, int64_t d,
+                               float scale, int64_t n_chunks, void* stream);
+
+/*
  * Round fp32 to bf16 (nearest-even) element-wise on the device, so fp32 inputs
  * can be fed to the bf16 kernels.  in: fp32 [n]; out: bf16 [n]; n >= 0.
  * Both 16-byte aligned.
