@@ -12,8 +12,10 @@
 //
 // GB300 mapping (one CTA = 128 query rows of one (batch, head)):
 //   warp 0      TMA producer for Q, Qt (once) and the K/Kt ring
-//   warp 1      TMEM allocator and the single-thread tcgen05.mma issuer
+//   warp 1      TMEM allocator and the tcgen05.mma issuer of the value MMAs
 //   warp 2      TMA producer for the V/Vt ring
+//   warp 3      tcgen05.mma issuer of the score MMAs (a second issuing thread
+//               keeps the tensor pipe fed while the other waits on a barrier)
 //   warps 4-7   softmax + JVP weights + lazy rescale + epilogue; thread t of
 //               warp 4+w owns query row 32w+t, which is TMEM lane 32w+t, so
 //               every row reduction is thread-local (no shuffles).
@@ -83,10 +85,143 @@ struct Barriers {
   uint64_t k_full[3], k_empty[3];
   uint64_t v_full[3], v_empty[3];
   uint64_t s_full[3], p_full[3], pv_done[3];
-  uint64_t drain;
+  uint64_t drain, drain_s;
   uint32_t tmem_base;
   int abort_flag;
 };
+
+// Online-softmax state of one query row (log2 units of the scaled scores).
+struct RowState {
+  float m = -INFINITY;  // reference max
+  float l = 0.f;        // sum of P~
+  float r = 0.f;        // sum of P~ (.) St s
+};
+
+// Softmax + JVP weights of one 64-key tile for the calling thread's query row.
+// ``cS`` is the row's TMEM address of the tile's buffer (raw S in columns 0-63,
+// raw St in 64-127).  On return P~ and H~ (bf16 pairs) sit in columns 0-31 and
+// 32-63 of that buffer, their stores have completed and the tcgen05 fence that
+// precedes the hand-off to the MMA thread has been executed.  When the row max
+// grows by more than the threshold the accumulators O and T (columns 0-2D) are
+// rescaled after ``wait_prev_pv()`` confirms the previous tile's value MMAs are
+// done.  Returns false (warp-uniformly) when a wait gave up.
+template <int D, class WaitPrevPv>
+__device__ __forceinline__ bool softmax_tile(uint32_t lane_addr, uint32_t cS, int valid, bool first, float c2,
+                                             float scale, RowState& st, WaitPrevPv wait_prev_pv) {
+  // One load brings the row's 64 raw scores and 64 raw score tangents.
+  uint32_t raw[128];
+  tmem_ld128_wait(cS, raw);
+  if (valid < 64) {
+    // Tail tile: keys past the range get score -inf (weight 0) and tangent 0.
+#pragma unroll
+    for (int i = 0; i < 64; ++i)
+      if (i >= valid) {
+        raw[i] = __float_as_uint(-INFINITY);
+        raw[64 + i] = 0u;
+      }
+  }
+  // Row max of the raw scores (the scale is positive, so it keeps the order);
+  // eight independent chains keep the dependency depth short.
+  float mx8[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) mx8[k] = __uint_as_float(raw[k]);
+#pragma unroll
+  for (int i = 8; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(raw[i]));
+  const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * c2;
+  float alpha = 1.f;
+  bool rescale = false;
+  if (first) {
+    st.m = mx;
+  } else if (mx > st.m + kRescaleThreshold) {
+    alpha = ex2_approx(st.m - mx);
+    st.m = mx;
+    rescale = true;
+  }
+  // P~ = 2^(S s log2e - m): one FFMA and one MUFU ex2 per score.
+  float p[64];
+  float ls8[8];
+#pragma unroll
+  for (int i = 0; i < 64; ++i) {
+    p[i] = ex2_approx(fmaf(__uint_as_float(raw[i]), c2, -st.m));
+    ls8[i & 7] = (i < 8) ? p[i] : ls8[i & 7] + p[i];
+  }
+  st.l = st.l * alpha + (((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7])));
+  uint32_t pk[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
+  // H~ = P~ (.) St s; its row sum is taken in fp32 before rounding to bf16.
+  uint32_t hk[32];
+  float rs8[8];
+#pragma unroll
+  for (int i = 0; i < 64; i += 2) {
+    const float h0 = p[i] * (__uint_as_float(raw[64 + i]) * scale);
+    const float h1 = p[i + 1] * (__uint_as_float(raw[65 + i]) * scale);
+    const int k = (i >> 1) & 7;
+    rs8[k] = (i < 16) ? (h0 + h1) : rs8[k] + (h0 + h1);
+    hk[i >> 1] = pack_bf16x2(h0, h1);
+  }
+  st.r = st.r * alpha + (((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7])));
+  if (__any_sync(0xffffffffu, rescale)) {
+    // O and T may only be touched once the previous tile's value MMAs are done.
+    const bool ok = __all_sync(0xffffffffu, wait_prev_pv());
+    if (!ok) return false;
+    tc_fence_after_sync();
+#pragma unroll 1
+    for (int c0 = 0; c0 < 2 * D; c0 += 32) {
+      uint32_t acc[32];
+      tmem_ld32_wait(lane_addr + c0, acc);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc[i] = __float_as_uint(__uint_as_float(acc[i]) * alpha);
+      tmem_st32(lane_addr + c0, acc);
+    }
+  }
+  tmem_st32(cS, pk);
+  tmem_st32(cS + 32, hk);
+  tmem_wait_st();
+  tc_fence_before_sync();
+  return true;
+}
+
+// Epilogue of the calling thread's row: O = O~/l, mu = r/l, Ot = T~/l - mu O and
+// LSE = (m + log2 l) ln 2, read from TMEM (O~ in columns 0-D, T~ in D-2D).
+template <int D>
+__device__ __forceinline__ void write_row(uint32_t lane_addr, const RowState& st, int64_t bh, int N, int qrow,
+                                          float* __restrict__ out, float* __restrict__ out_t,
+                                          float* __restrict__ lse_out, float* __restrict__ mu_out) {
+  const float inv_l = 1.f / st.l;
+  const float mu = st.r * inv_l;
+  const int64_t obase = (bh * N + qrow) * D;
+#pragma unroll 1
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    uint32_t ov[32], tv[32];
+    tmem_ld32_wait(lane_addr + c0, ov);
+    tmem_ld32_wait(lane_addr + D + c0, tv);
+    if (qrow < N) {
+      float4* o4 = reinterpret_cast<float4*>(out + obase + c0);
+      float4* t4 = reinterpret_cast<float4*>(out_t + obase + c0);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float4 o, t;
+        o.x = __uint_as_float(ov[4 * i + 0]) * inv_l;
+        o.y = __uint_as_float(ov[4 * i + 1]) * inv_l;
+        o.z = __uint_as_float(ov[4 * i + 2]) * inv_l;
+        o.w = __uint_as_float(ov[4 * i + 3]) * inv_l;
+        t.x = __uint_as_float(tv[4 * i + 0]) * inv_l - mu * o.x;
+        t.y = __uint_as_float(tv[4 * i + 1]) * inv_l - mu * o.y;
+        t.z = __uint_as_float(tv[4 * i + 2]) * inv_l - mu * o.z;
+        t.w = __uint_as_float(tv[4 * i + 3]) * inv_l - mu * o.w;
+        o4[i] = o;
+        t4[i] = t;
+      }
+    }
+  }
+  if (qrow < N) {
+    const int64_t ridx = bh * N + qrow;
+    if (lse_out) lse_out[ridx] = (st.m + __log2f(st.l)) * kLn2;
+    if (mu_out) mu_out[ridx] = mu;
+  }
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -122,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->pv_done[s], 1);
     }
     mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain_s, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -194,8 +330,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (t >= 0) mbar_wait(&bars->v_full[t % C::kVS], (t / C::kVS) & 1, &no_abort, nullptr, 0);
       }
     }
-  } else if (warp == 1) {
-    // ---------------- tcgen05.mma issuer (one thread) ----------------
+  } else if (warp == 1 || warp == 3) {
+    // ---------------- tcgen05.mma issuers: warp 3 the score MMAs, warp 1 the value MMAs ----------------
+    // Two independent issuing threads keep the tensor pipe fed while either of
+    // them waits on a barrier; they meet only through the mbarriers below.
     if (lane == 0) {
       constexpr uint32_t kIdS = make_idesc_bf16_f32(128, C::kBN, false, false);  // Q K^T, both K-major
       constexpr uint32_t kIdPV = make_idesc_bf16_f32(128, D, false, true);      // P~ V, V is N-major
@@ -206,79 +344,80 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dK0 = make_smem_desc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
       const uint64_t dV0 = make_smem_desc_sw128(smem_u32(smem + C::kOffV), C::kChunkK, 1024);
       auto off = [](uint64_t desc, uint32_t bytes) { return desc + static_cast<uint64_t>(bytes >> 4); };
-
-      // St_t = [Qt Q] [K_t Kt_t]^T into buffer t % NB.  PV of the buffer's previous
-      // tile reads only the P~/H~ columns (the S half), so this may be issued
-      // before that PV has completed.
-      auto issue_st = [&](int t) -> bool {
-        const int s = t % C::kKS;
-        if (!mbar_wait(&bars->k_full[s], (t / C::kKS) & 1, abort_flag, status, kStatusTimeout)) return false;
-        tc_fence_after_sync();
-        const uint64_t dK = off(dK0, s * C::kKStage);
-        const uint32_t dSt = tmem + C::kColBuf + 128u * (t % C::kNB) + 64u;
-#pragma unroll
-        for (int c = 0; c < C::kDC; ++c)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ss(dSt, off(dQt, c * C::kChunkQ + kk * 32), off(dK, c * C::kChunkK + kk * 32), kIdS,
-                   (c | kk) != 0);
-#pragma unroll
-        for (int c = 0; c < C::kDC; ++c)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ss(dSt, off(dQ, c * C::kChunkQ + kk * 32), off(dK, (C::kDC + c) * C::kChunkK + kk * 32), kIdS, 1);
-        return true;
-      };
-      // S_t = Q K_t^T into the S half of buffer t % NB, which holds P~/H~ of tile
-      // t - NB until that tile's PV MMAs complete.
-      auto issue_s = [&](int t) -> bool {
-        const int b = t % C::kNB;
-        const int s = t % C::kKS;
-        if (t >= C::kNB &&
-            !mbar_wait(&bars->pv_done[b], ((t - C::kNB) / C::kNB) & 1, abort_flag, status, kStatusTimeout))
-          return false;
-        tc_fence_after_sync();
-        const uint64_t dK = off(dK0, s * C::kKStage);
-        const uint32_t dS = tmem + C::kColBuf + 128u * b;
-#pragma unroll
-        for (int c = 0; c < C::kDC; ++c)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ss(dS, off(dQ, c * C::kChunkQ + kk * 32), off(dK, c * C::kChunkK + kk * 32), kIdS, (c | kk) != 0);
-        mma_commit(&bars->k_empty[s]);
-        mma_commit(&bars->s_full[b]);
-        return true;
-      };
-
-      bool ok = mbar_wait(&bars->q_full, 0, abort_flag, status, kStatusTimeout);
-      for (int t = 0; ok && t < C::kNB && t < n_tiles; ++t) ok = issue_st(t) && issue_s(t);
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int b = j % C::kNB;
-        const int s = j % C::kVS;
-        ok = mbar_wait(&bars->p_full[b], (j / C::kNB) & 1, abort_flag, status, kStatusTimeout) &&
-             mbar_wait(&bars->v_full[s], (j / C::kVS) & 1, abort_flag, status, kStatusTimeout);
-        if (!ok) break;
-        tc_fence_after_sync();
-        const uint64_t dV = off(dV0, s * C::kVStage);
-        const uint32_t aP = tmem + C::kColBuf + 128u * b;  // P~ packed bf16: 32 columns
-        const uint32_t aH = aP + 32u;                       // H~ packed bf16: 32 columns
-#pragma unroll
-        for (int kk = 0; kk < C::kBN / 16; ++kk) {
-          const uint64_t bV = off(dV, kk * 2048);
-          const uint64_t bVt = off(dV, C::kDC * C::kChunkK + kk * 2048);
-          const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
-          mma_ts(tmem + C::kColO, aP + kk * 8, bV, kIdPV, acc);   // O += P~ V
-          mma_ts(tmem + C::kColT, aP + kk * 8, bVt, kIdPV, acc);  // T += P~ Vt
-          mma_ts(tmem + C::kColT, aH + kk * 8, bV, kIdPV, 1u);    // T += H~ V
-        }
-        mma_commit(&bars->v_empty[s]);
-        mma_commit(&bars->pv_done[b]);
-        if (j + C::kNB < n_tiles) ok = issue_st(j + C::kNB) && issue_s(j + C::kNB);
-      }
-      // Nothing may still be reading shared memory or TMEM when the CTA tears down.
-      mma_commit(&bars->drain);
       volatile int no_abort = 0;
-      mbar_wait(&bars->drain, 0, &no_abort, nullptr, 0);
+      if (warp == 3) {
+        bool ok = mbar_wait(&bars->q_full, 0, abort_flag, status, kStatusTimeout);
+        for (int t = 0; ok && t < n_tiles; ++t) {
+          const int b = t % C::kNB;
+          const int s = t % C::kKS;
+          ok = mbar_wait(&bars->k_full[s], (t / C::kKS) & 1, abort_flag, status, kStatusTimeout);
+          // The buffer's St half is free once the softmax has finished tile t - NB.
+          if (ok && t >= C::kNB)
+            ok = mbar_wait(&bars->p_full[b], ((t - C::kNB) / C::kNB) & 1, abort_flag, status, kStatusTimeout);
+          if (!ok) break;
+          tc_fence_after_sync();
+          const uint64_t dK = off(dK0, s * C::kKStage);
+          const uint32_t dS = tmem + C::kColBuf + 128u * b;
+          const uint32_t dSt = dS + 64u;
+          // St_t = [Qt Q] [K_t Kt_t]^T : one accumulator, 2d deep
+#pragma unroll
+          for (int c = 0; c < C::kDC; ++c)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(dSt, off(dQt, c * C::kChunkQ + kk * 32), off(dK, c * C::kChunkK + kk * 32), kIdS,
+                     (c | kk) != 0);
+#pragma unroll
+          for (int c = 0; c < C::kDC; ++c)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(dSt, off(dQ, c * C::kChunkQ + kk * 32), off(dK, (C::kDC + c) * C::kChunkK + kk * 32), kIdS,
+                     1);
+          // The S half holds P~/H~ of tile t - NB until that tile's value MMAs are done.
+          if (t >= C::kNB) {
+            ok = mbar_wait(&bars->pv_done[b], ((t - C::kNB) / C::kNB) & 1, abort_flag, status, kStatusTimeout);
+            if (!ok) break;
+            tc_fence_after_sync();
+          }
+          // S_t = Q K_t^T
+#pragma unroll
+          for (int c = 0; c < C::kDC; ++c)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(dS, off(dQ, c * C::kChunkQ + kk * 32), off(dK, c * C::kChunkK + kk * 32), kIdS,
+                     (c | kk) != 0);
+          mma_commit(&bars->k_empty[s]);
+          mma_commit(&bars->s_full[b]);
+        }
+        // Nothing may still be reading shared memory or TMEM when the CTA tears down.
+        mma_commit(&bars->drain_s);
+        mbar_wait(&bars->drain_s, 0, &no_abort, nullptr, 0);
+      } else {
+        bool ok = true;
+        for (int j = 0; ok && j < n_tiles; ++j) {
+          const int b = j % C::kNB;
+          const int s = j % C::kVS;
+          ok = mbar_wait(&bars->p_full[b], (j / C::kNB) & 1, abort_flag, status, kStatusTimeout) &&
+               mbar_wait(&bars->v_full[s], (j / C::kVS) & 1, abort_flag, status, kStatusTimeout);
+          if (!ok) break;
+          tc_fence_after_sync();
+          const uint64_t dV = off(dV0, s * C::kVStage);
+          const uint32_t aP = tmem + C::kColBuf + 128u * b;  // P~ packed bf16: 32 columns
+          const uint32_t aH = aP + 32u;                       // H~ packed bf16: 32 columns
+#pragma unroll
+          for (int kk = 0; kk < C::kBN / 16; ++kk) {
+            const uint64_t bV = off(dV, kk * 2048);
+            const uint64_t bVt = off(dV, C::kDC * C::kChunkK + kk * 2048);
+            const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+            mma_ts(tmem + C::kColO, aP + kk * 8, bV, kIdPV, acc);   // O += P~ V
+            mma_ts(tmem + C::kColT, aP + kk * 8, bVt, kIdPV, acc);  // T += P~ Vt
+            mma_ts(tmem + C::kColT, aH + kk * 8, bV, kIdPV, 1u);    // T += H~ V
+          }
+          mma_commit(&bars->v_empty[s]);
+          mma_commit(&bars->pv_done[b]);
+        }
+        mma_commit(&bars->drain);
+        mbar_wait(&bars->drain, 0, &no_abort, nullptr, 0);
+      }
     }
   } else if (warp >= 4) {
     // ---------------- softmax / JVP / epilogue: one query row per thread ----------------
@@ -286,8 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float c2 = scale * kLog2e;
-    float m = -INFINITY;  // reference max, log2 units of the scaled scores
-    float l = 0.f, r = 0.f;
+    RowState st;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
       const int b = j % C::kNB;
@@ -297,81 +435,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const uint32_t cS = lane_addr + C::kColBuf + 128u * b;
       const int valid = min(C::kBN, kv_len - j * C::kBN);
-      // One load brings the row's 64 raw scores (columns 0-63) and 64 raw score
-      // tangents (columns 64-127) of this buffer.
-      uint32_t raw[128];
-      tmem_ld128_wait(cS, raw);
-      if (valid < C::kBN) {
-        // Tail tile: keys past the range get score -inf (weight 0) and tangent 0.
-#pragma unroll
-        for (int i = 0; i < 64; ++i)
-          if (i >= valid) {
-            raw[i] = __float_as_uint(-INFINITY);
-            raw[64 + i] = 0u;
-          }
-      }
-      // Row max of the raw scores (the scale is positive, so it keeps the order);
-      // eight independent chains keep the dependency depth short.
-      float mx8[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = __uint_as_float(raw[k]);
-#pragma unroll
-      for (int i = 8; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(raw[i]));
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * c2;
-      float alpha = 1.f;
-      bool rescale = false;
-      if (j == 0) {
-        m = mx;
-      } else if (mx > m + kRescaleThreshold) {
-        alpha = ex2_approx(m - mx);
-        m = mx;
-        rescale = true;
-      }
-      // P~ = 2^(S s log2e - m): one FFMA and one MUFU ex2 per score.
-      float p[64];
-      float ls8[8];
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        p[i] = ex2_approx(fmaf(__uint_as_float(raw[i]), c2, -m));
-        ls8[i & 7] = (i < 8) ? p[i] : ls8[i & 7] + p[i];
-      }
-      l = l * alpha + (((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7])));
-      uint32_t pk[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
-      // H~ = P~ (.) St s; its row sum is taken in fp32 before rounding to bf16.
-      uint32_t hk[32];
-      float rs8[8];
-#pragma unroll
-      for (int i = 0; i < 64; i += 2) {
-        const float h0 = p[i] * (__uint_as_float(raw[64 + i]) * scale);
-        const float h1 = p[i + 1] * (__uint_as_float(raw[65 + i]) * scale);
-        const int k = (i >> 1) & 7;
-        rs8[k] = (i < 16) ? (h0 + h1) : rs8[k] + (h0 + h1);
-        hk[i >> 1] = pack_bf16x2(h0, h1);
-      }
-      r = r * alpha + (((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7])));
-      if (__any_sync(0xffffffffu, rescale)) {
-        // O and T may only be touched once the previous tile's PV MMAs are done.
-        ok = mbar_wait(&bars->pv_done[(j - 1) % C::kNB], ((j - 1) / C::kNB) & 1, abort_flag, status,
-                       kStatusTimeout);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after_sync();
-#pragma unroll 1
-        for (int c0 = 0; c0 < 2 * D; c0 += 32) {
-          uint32_t acc[32];
-          tmem_ld32_wait(lane_addr + C::kColO + c0, acc);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) acc[i] = __float_as_uint(__uint_as_float(acc[i]) * alpha);
-          tmem_st32(lane_addr + C::kColO + c0, acc);
-        }
-      }
-      tmem_st32(cS, pk);
-      tmem_st32(cS + 32, hk);
-      tmem_wait_st();
-      tc_fence_before_sync();
+      ok = softmax_tile<D>(lane_addr, cS, valid, j == 0, c2, scale, st, [&]() {
+        return mbar_wait(&bars->pv_done[(j - 1) % C::kNB], ((j - 1) / C::kNB) & 1, abort_flag, status,
+                         kStatusTimeout);
+      });
+      if (!ok) break;
       mbar_arrive(&bars->p_full[b]);
     }
     // ---------------- epilogue ----------------
@@ -380,39 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       tc_fence_after_sync();
-      const int qrow = q0 + row;
-      const float inv_l = 1.f / l;
-      const float mu = r * inv_l;
-      const int64_t obase = (static_cast<int64_t>(bh) * N + qrow) * D;
-#pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t ov[32], tv[32];
-        tmem_ld32_wait(lane_addr + C::kColO + c0, ov);
-        tmem_ld32_wait(lane_addr + C::kColT + c0, tv);
-        if (qrow < N) {
-          float4* o4 = reinterpret_cast<float4*>(out + obase + c0);
-          float4* t4 = reinterpret_cast<float4*>(out_t + obase + c0);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            float4 o, t;
-            o.x = __uint_as_float(ov[4 * i + 0]) * inv_l;
-            o.y = __uint_as_float(ov[4 * i + 1]) * inv_l;
-            o.z = __uint_as_float(ov[4 * i + 2]) * inv_l;
-            o.w = __uint_as_float(ov[4 * i + 3]) * inv_l;
-            t.x = __uint_as_float(tv[4 * i + 0]) * inv_l - mu * o.x;
-            t.y = __uint_as_float(tv[4 * i + 1]) * inv_l - mu * o.y;
-            t.z = __uint_as_float(tv[4 * i + 2]) * inv_l - mu * o.z;
-            t.w = __uint_as_float(tv[4 * i + 3]) * inv_l - mu * o.w;
-            o4[i] = o;
-            t4[i] = t;
-          }
-        }
-      }
-      if (qrow < N) {
-        const int64_t ridx = static_cast<int64_t>(bh) * N + qrow;
-        if (lse_out) lse_out[ridx] = (m + __log2f(l)) * kLn2;
-        if (mu_out) mu_out[ridx] = mu;
-      }
+      write_row<D>(lane_addr, st, bh, N, q0 + row, out, out_t, lse_out, mu_out);
     }
   }
 
@@ -421,6 +457,286 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ===========================================================================
+// CTA-pair kernel (d = 128): two CTAs on two SMs form one 256-row query tile.
+// Every MMA is a tcgen05 cta_group::2 MMA issued by the even CTA: M = 256 (each
+// CTA's 128 rows stay in its own shared and tensor memory) and each operand B
+// is split in halves between the two CTAs, so each CTA loads only half of every
+// key tile (32 of 64 keys for the score MMAs; 64 of 128 value columns for the
+// value MMAs).  Per SM that halves the B-operand shared-memory reads and the
+// TMA writes of the single-CTA kernel, the two costs that bound it.
+// Barrier placement: TMA completions and softmax hand-offs are counted on the
+// even CTA's barriers (what the MMA thread waits for); MMA completions are
+// multicast to the barriers of both CTAs (what producers and softmax wait for).
+// ===========================================================================
+struct PairCfg {
+  static constexpr int D = 128;
+  static constexpr int kBM = 128;                   // query rows per CTA (256 per pair)
+  static constexpr int kBN = 64;                    // keys per tile (per pair)
+  static constexpr int kDC = 2;                     // 64-element d-chunks
+  static constexpr int kNB = 2;                     // S/St TMEM buffers
+  static constexpr int kKS = 4;                     // K/Kt ring stages
+  static constexpr int kVS = 4;                     // V/Vt ring stages
+  static constexpr int kChunkQ = kBM * 128;         // one d-chunk of this CTA's Q rows
+  static constexpr int kHalfK = (kBN / 2) * 128;    // one d-chunk of this CTA's 32 keys
+  static constexpr int kQBytes = kDC * kChunkQ;
+  static constexpr int kKStage = 2 * kDC * kHalfK;  // K chunks, then Kt chunks (this CTA's keys)
+  static constexpr int kVHalf = kBN * 128;          // this CTA's 64 value columns of a tile
+  static constexpr int kVStage = 2 * kVHalf;        // V, then Vt
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffQt = kQBytes;
+  static constexpr int kOffK = 2 * kQBytes;
+  static constexpr int kOffV = kOffK + kKS * kKStage;
+  static constexpr int kOffBar = kOffV + kVS * kVStage;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;
+  static constexpr uint32_t kColO = 0, kColT = D, kColBuf = 2 * D, kTmemCols = 512;
+  static_assert(kColBuf + 128 * kNB <= kTmemCols, "TMEM budget");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+struct PairBarriers {
+  uint64_t q_full;
+  uint64_t k_full[PairCfg::kKS], k_empty[PairCfg::kKS];
+  uint64_t v_full[PairCfg::kVS], v_empty[PairCfg::kVS];
+  uint64_t s_full[PairCfg::kNB], p_full[PairCfg::kNB], pv_done[PairCfg::kNB];
+  uint64_t drain, drain_s;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// Spin for ``ns`` nanoseconds (lets copies already in flight land before teardown).
+__device__ __forceinline__ void settle_ns(uint64_t ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < ns) {
+  }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    attn_jvp_fwd_pair_kernel(const __grid_constant__ FwdMaps maps, float* __restrict__ out,
+                             float* __restrict__ out_t, float* __restrict__ lse_out, float* __restrict__ mu_out,
+                             int N, int n_pairs, int kv_start, int kv_len, float scale, int* status) {
+  using C = PairCfg;
+  constexpr int D = C::D;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  PairBarriers* bars = reinterpret_cast<PairBarriers*>(smem + C::kOffBar);
+  volatile int* abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cid = blockIdx.x >> 1;
+  const int bh = cid / n_pairs;
+  const int q0 = ((cid % n_pairs) * 2 + static_cast<int>(rank)) * C::kBM;
+  const int n_tiles = (kv_len + C::kBN - 1) / C::kBN;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < C::kKS; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < C::kVS; ++s) {
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    for (int b = 0; b < C::kNB; ++b) {
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->p_full[b], 2 * 128);  // every softmax thread of both CTAs
+      mbar_init(&bars->pv_done[b], 1);
+    }
+    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain_s, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&bars->tmem_base, C::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before_sync();
+  cluster_sync();  // both CTAs' barriers exist before any remote access
+  tc_fence_after_sync();
+  const uint32_t tmem = bars->tmem_base;
+  auto lead = [](uint64_t* bar) { return mapa_shared(smem_u32(bar), 0); };
+
+  if (warp == 0) {
+    // ---------------- TMA producer: this CTA's Q, Qt and its half of each K/Kt tile ----------------
+    if (lane == 0) {
+      prefetch_tensormap(&maps.q);
+      prefetch_tensormap(&maps.qt);
+      prefetch_tensormap(&maps.k);
+      prefetch_tensormap(&maps.kt);
+      if (leader) mbar_arrive_expect_tx(&bars->q_full, 2 * 2 * C::kQBytes);
+      const uint32_t qf = lead(&bars->q_full);
+      for (int c = 0; c < C::kDC; ++c) {
+        tma_load_3d_pair(smem + C::kOffQ + c * C::kChunkQ, &maps.q, qf, c * 64, q0, bh);
+        tma_load_3d_pair(smem + C::kOffQt + c * C::kChunkQ, &maps.qt, qf, c * 64, q0, bh);
+      }
+      bool ok = true;
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        const int s = t % C::kKS;
+        ok = mbar_wait_cluster(&bars->k_empty[s], ((t / C::kKS) & 1) ^ 1, abort_flag, status, kStatusTimeout);
+        if (!ok) break;
+        uint8_t* st = smem + C::kOffK + s * C::kKStage;
+        const uint32_t kf = lead(&bars->k_full[s]);
+        if (leader) mbar_arrive_expect_tx(&bars->k_full[s], 2 * C::kKStage);
+        const int key0 = kv_start + t * C::kBN + static_cast<int>(rank) * (C::kBN / 2);
+        for (int c = 0; c < C::kDC; ++c) {
+          tma_load_3d_pair(st + c * C::kHalfK, &maps.k, kf, c * 64, key0, bh);
+          tma_load_3d_pair(st + (C::kDC + c) * C::kHalfK, &maps.kt, kf, c * 64, key0, bh);
+        }
+      }
+      if (!ok) settle_ns(50000);
+    }
+  } else if (warp == 2) {
+    // ---------------- TMA producer: this CTA's value columns of each V/Vt tile ----------------
+    if (lane == 0) {
+      prefetch_tensormap(&maps.v);
+      prefetch_tensormap(&maps.vt);
+      bool ok = true;
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        const int s = t % C::kVS;
+        ok = mbar_wait_cluster(&bars->v_empty[s], ((t / C::kVS) & 1) ^ 1, abort_flag, status, kStatusTimeout);
+        if (!ok) break;
+        uint8_t* st = smem + C::kOffV + s * C::kVStage;
+        const uint32_t vf = lead(&bars->v_full[s]);
+        if (leader) mbar_arrive_expect_tx(&bars->v_full[s], 2 * C::kVStage);
+        const int key0 = kv_start + t * C::kBN;
+        tma_load_3d_pair(st, &maps.v, vf, static_cast<int>(rank) * 64, key0, bh);
+        tma_load_3d_pair(st + C::kVHalf, &maps.vt, vf, static_cast<int>(rank) * 64, key0, bh);
+      }
+      if (!ok) settle_ns(50000);
+    }
+  } else if (warp == 1 || warp == 3) {
+    // ---------------- pair MMA issuers (even CTA): warp 3 the scores, warp 1 the values ----------------
+    if (lane == 0 && leader) {
+      constexpr uint32_t kIdS = make_idesc_bf16_f32(256, C::kBN, false, false);
+      constexpr uint32_t kIdPV = make_idesc_bf16_f32(256, D, false, true);
+      const uint64_t dQ = make_smem_desc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
+      const uint64_t dQt = make_smem_desc_sw128(smem_u32(smem + C::kOffQt), 16, 1024);
+      const uint64_t dK0 = make_smem_desc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
+      const uint64_t dV0 = make_smem_desc_sw128(smem_u32(smem + C::kOffV), C::kVHalf, 1024);
+      auto off = [](uint64_t desc, uint32_t bytes) { return desc + static_cast<uint64_t>(bytes >> 4); };
+      constexpr uint16_t kBoth = 0x3;
+      volatile int no_abort = 0;
+      if (warp == 3) {
+        bool ok = mbar_wait_cluster(&bars->q_full, 0, abort_flag, status, kStatusTimeout);
+        for (int t = 0; ok && t < n_tiles; ++t) {
+          const int b = t % C::kNB;
+          const int s = t % C::kKS;
+          ok = mbar_wait_cluster(&bars->k_full[s], (t / C::kKS) & 1, abort_flag, status, kStatusTimeout);
+          // The buffer's St half is free once both CTAs' softmax finished tile t - NB.
+          if (ok && t >= C::kNB)
+            ok = mbar_wait_cluster(&bars->p_full[b], ((t - C::kNB) / C::kNB) & 1, abort_flag, status,
+                                   kStatusTimeout);
+          if (!ok) break;
+          tc_fence_after_sync();
+          const uint64_t dK = off(dK0, s * C::kKStage);
+          const uint32_t dS = tmem + C::kColBuf + 128u * b;
+          const uint32_t dSt = dS + 64u;
+#pragma unroll
+          for (int c = 0; c < C::kDC; ++c)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss_pair(dSt, off(dQt, c * C::kChunkQ + kk * 32), off(dK, c * C::kHalfK + kk * 32), kIdS,
+                          (c | kk) != 0);
+#pragma unroll
+          for (int c = 0; c < C::kDC; ++c)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss_pair(dSt, off(dQ, c * C::kChunkQ + kk * 32), off(dK, (C::kDC + c) * C::kHalfK + kk * 32),
+                          kIdS, 1);
+          // The S half holds P~/H~ of tile t - NB until that tile's value MMAs are done.
+          if (t >= C::kNB) {
+            ok = mbar_wait_cluster(&bars->pv_done[b], ((t - C::kNB) / C::kNB) & 1, abort_flag, status,
+                                   kStatusTimeout);
+            if (!ok) break;
+            tc_fence_after_sync();
+          }
+#pragma unroll
+          for (int c = 0; c < C::kDC; ++c)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss_pair(dS, off(dQ, c * C::kChunkQ + kk * 32), off(dK, c * C::kHalfK + kk * 32), kIdS,
+                          (c | kk) != 0);
+          mma_commit_pair(&bars->k_empty[s], kBoth);
+          mma_commit_pair(&bars->s_full[b], kBoth);
+        }
+        // Nothing may still read either CTA's shared or tensor memory at teardown.
+        mma_commit_pair(&bars->drain_s, 0x1);
+        mbar_wait(&bars->drain_s, 0, &no_abort, nullptr, 0);
+      } else {
+        bool ok = true;
+        for (int j = 0; ok && j < n_tiles; ++j) {
+          const int b = j % C::kNB;
+          const int s = j % C::kVS;
+          ok = mbar_wait_cluster(&bars->p_full[b], (j / C::kNB) & 1, abort_flag, status, kStatusTimeout) &&
+               mbar_wait_cluster(&bars->v_full[s], (j / C::kVS) & 1, abort_flag, status, kStatusTimeout);
+          if (!ok) break;
+          tc_fence_after_sync();
+          const uint64_t dV = off(dV0, s * C::kVStage);
+          const uint32_t aP = tmem + C::kColBuf + 128u * b;
+          const uint32_t aH = aP + 32u;
+#pragma unroll
+          for (int kk = 0; kk < C::kBN / 16; ++kk) {
+            const uint64_t bV = off(dV, kk * 2048);
+            const uint64_t bVt = off(dV, C::kVHalf + kk * 2048);
+            const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+            mma_ts_pair(tmem + C::kColO, aP + kk * 8, bV, kIdPV, acc);   // O += P~ V
+            mma_ts_pair(tmem + C::kColT, aP + kk * 8, bVt, kIdPV, acc);  // T += P~ Vt
+            mma_ts_pair(tmem + C::kColT, aH + kk * 8, bV, kIdPV, 1u);    // T += H~ V
+          }
+          mma_commit_pair(&bars->v_empty[s], kBoth);
+          mma_commit_pair(&bars->pv_done[b], kBoth);
+        }
+        mma_commit_pair(&bars->drain, 0x1);
+        mbar_wait(&bars->drain, 0, &no_abort, nullptr, 0);
+      }
+    }
+  } else if (warp >= 4) {
+    // ---------------- softmax / JVP / epilogue: this CTA's 128 rows ----------------
+    const int quarter = warp - 4;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float c2 = scale * kLog2e;
+    RowState st;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int b = j % C::kNB;
+      ok = mbar_wait_cluster(&bars->s_full[b], (j / C::kNB) & 1, abort_flag, status, kStatusTimeout);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const uint32_t cS = lane_addr + C::kColBuf + 128u * b;
+      const int valid = min(C::kBN, kv_len - j * C::kBN);
+      ok = softmax_tile<D>(lane_addr, cS, valid, j == 0, c2, scale, st, [&]() {
+        return mbar_wait_cluster(&bars->pv_done[(j - 1) % C::kNB], ((j - 1) / C::kNB) & 1, abort_flag, status,
+                                 kStatusTimeout);
+      });
+      if (!ok) break;
+      mbar_arrive_cluster(lead(&bars->p_full[b]));
+    }
+    if (ok)
+      ok = mbar_wait_cluster(&bars->pv_done[(n_tiles - 1) % C::kNB], ((n_tiles - 1) / C::kNB) & 1, abort_flag,
+                             status, kStatusTimeout);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      tc_fence_after_sync();
+      write_row<D>(lane_addr, st, bh, N, q0 + row, out, out_t, lse_out, mu_out);
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before_sync();
+  cluster_sync();  // the peer may still be reading this CTA's memory until here
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem, C::kTmemCols);
   }
 }
 
@@ -470,10 +786,38 @@ cudaError_t launch_d(const FwdArgs& a, const char** msg) {
   return e;
 }
 
+cudaError_t launch_pair(const FwdArgs& a, const char** msg) {
+  using C = PairCfg;
+  FwdMaps maps;
+  cudaError_t e = cudaSuccess;
+  const void* ptrs[6] = {a.q, a.q_t, a.k, a.k_t, a.v, a.v_t};
+  CUtensorMap* dst[6] = {&maps.q, &maps.qt, &maps.k, &maps.kt, &maps.v, &maps.vt};
+  const int rows[6] = {C::kBM, C::kBM, C::kBN / 2, C::kBN / 2, C::kBN, C::kBN};
+  for (int i = 0; i < 6 && e == cudaSuccess; ++i) e = make_map(dst[i], ptrs[i], a.BH, a.N, C::D, rows[i]);
+  if (e != cudaSuccess) {
+    *msg = "cuTensorMapEncodeTiled rejected a tensor (alignment or size)";
+    return e;
+  }
+  e = cudaFuncSetAttribute(attn_jvp_fwd_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) {
+    *msg = "cudaFuncSetAttribute(max dynamic shared memory) failed";
+    return e;
+  }
+  const int n_qtiles = static_cast<int>((a.N + C::kBM - 1) / C::kBM);
+  const int n_pairs = (n_qtiles + 1) / 2;
+  const int64_t grid = 2 * static_cast<int64_t>(n_pairs) * a.BH;
+  attn_jvp_fwd_pair_kernel<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, a.stream>>>(
+      maps, a.out, a.out_t, a.lse, a.mu, static_cast<int>(a.N), n_pairs, static_cast<int>(a.kv_start),
+      static_cast<int>(a.kv_len), a.scale, a.status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) *msg = "attention-JVP pair kernel launch failed";
+  return e;
+}
+
 }  // namespace
 
 cudaError_t launch_attn_jvp_fwd(const FwdArgs& a, const char** msg) {
-  if (a.d == 128) return launch_d<128>(a, msg);
+  if (a.d == 128) return launch_pair(a, msg);
   if (a.d == 64) return launch_d<64>(a, msg);
   *msg = "unsupported head dimension";
   return cudaErrorInvalidValue;
