@@ -84,7 +84,7 @@ struct Barriers {
   uint64_t q_full;
   uint64_t k_full[3], k_empty[3];
   uint64_t v_full[3], v_empty[3];
-  uint64_t s_full[3], p_full[3], pv_done[3];
+  uint64_t s_full[3], p_full[3], pv_done[3], st_free[3];
   uint64_t drain, drain_s;
   uint32_t tmem_base;
   int abort_flag;
@@ -99,18 +99,23 @@ struct RowState {
 
 // Softmax + JVP weights of one 64-key tile for the calling thread's query row.
 // ``cS`` is the row's TMEM address of the tile's buffer (raw S in columns 0-63,
-// raw St in 64-127).  On return P~ and H~ (bf16 pairs) sit in columns 0-31 and
+// raw St in 64-127).  ``on_loaded()`` runs once both are in registers (the St
+// half is then free for the next tile's score MMAs).  On return P~ and H~ (bf16 pairs) sit in columns 0-31 and
 // 32-63 of that buffer, their stores have completed and the tcgen05 fence that
 // precedes the hand-off to the MMA thread has been executed.  When the row max
 // grows by more than the threshold the accumulators O and T (columns 0-2D) are
 // rescaled after ``wait_prev_pv()`` confirms the previous tile's value MMAs are
 // done.  Returns false (warp-uniformly) when a wait gave up.
-template <int D, class WaitPrevPv>
+template <int D, class OnLoaded, class WaitPrevPv>
 __device__ __forceinline__ bool softmax_tile(uint32_t lane_addr, uint32_t cS, int valid, bool first, float c2,
-                                             float scale, RowState& st, WaitPrevPv wait_prev_pv) {
-  // One load brings the row's 64 raw scores and 64 raw score tangents.
+                                             float scale, RowState& st, OnLoaded on_loaded,
+                                             WaitPrevPv wait_prev_pv) {
+  // One load brings the row's 64 raw scores and 64 raw score tangents; from
+  // then on the buffer's St columns may be overwritten (``on_loaded``).
   uint32_t raw[128];
   tmem_ld128_wait(cS, raw);
+  tc_fence_before_sync();
+  on_loaded();
   if (valid < 64) {
     // Tail tile: keys past the range get score -inf (weight 0) and tangent 0.
 #pragma unroll
@@ -253,8 +258,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
       mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->p_full[s], 128);
+      mbar_init(&bars->p_full[s], 4);  // one arrival per softmax warp
       mbar_init(&bars->pv_done[s], 1);
+      mbar_init(&bars->st_free[s], 4);
     }
     mbar_init(&bars->drain, 1);
     mbar_init(&bars->drain_s, 1);
@@ -351,9 +357,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int b = t % C::kNB;
           const int s = t % C::kKS;
           ok = mbar_wait(&bars->k_full[s], (t / C::kKS) & 1, abort_flag, status, kStatusTimeout);
-          // The buffer's St half is free once the softmax has finished tile t - NB.
+          // The buffer's St half is free once the softmax has loaded tile t - NB.
           if (ok && t >= C::kNB)
-            ok = mbar_wait(&bars->p_full[b], ((t - C::kNB) / C::kNB) & 1, abort_flag, status, kStatusTimeout);
+            ok = mbar_wait(&bars->st_free[b], ((t - C::kNB) / C::kNB) & 1, abort_flag, status, kStatusTimeout);
           if (!ok) break;
           tc_fence_after_sync();
           const uint64_t dK = off(dK0, s * C::kKStage);
@@ -435,12 +441,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const uint32_t cS = lane_addr + C::kColBuf + 128u * b;
       const int valid = min(C::kBN, kv_len - j * C::kBN);
-      ok = softmax_tile<D>(lane_addr, cS, valid, j == 0, c2, scale, st, [&]() {
-        return mbar_wait(&bars->pv_done[(j - 1) % C::kNB], ((j - 1) / C::kNB) & 1, abort_flag, status,
-                         kStatusTimeout);
-      });
+      // Hand-offs arrive once per warp: every lane has fenced its own TMEM
+      // accesses, __syncwarp orders them before lane 0's arrival.
+      ok = softmax_tile<D>(
+          lane_addr, cS, valid, j == 0, c2, scale, st,
+          [&]() {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->st_free[b]);
+          },
+          [&]() {
+            return mbar_wait(&bars->pv_done[(j - 1) % C::kNB], ((j - 1) / C::kNB) & 1, abort_flag, status,
+                             kStatusTimeout);
+          });
       if (!ok) break;
-      mbar_arrive(&bars->p_full[b]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full[b]);
     }
     // ---------------- epilogue ----------------
     if (ok) ok = mbar_wait(&bars->pv_done[(n_tiles - 1) % C::kNB], ((n_tiles - 1) / C::kNB) & 1, abort_flag, status,
@@ -457,286 +472,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, C::kTmemCols);
-  }
-}
-
-// ===========================================================================
-// CTA-pair kernel (d = 128): two CTAs on two SMs form one 256-row query tile.
-// Every MMA is a tcgen05 cta_group::2 MMA issued by the even CTA: M = 256 (each
-// CTA's 128 rows stay in its own shared and tensor memory) and each operand B
-// is split in halves between the two CTAs, so each CTA loads only half of every
-// key tile (32 of 64 keys for the score MMAs; 64 of 128 value columns for the
-// value MMAs).  Per SM that halves the B-operand shared-memory reads and the
-// TMA writes of the single-CTA kernel, the two costs that bound it.
-// Barrier placement: TMA completions and softmax hand-offs are counted on the
-// even CTA's barriers (what the MMA thread waits for); MMA completions are
-// multicast to the barriers of both CTAs (what producers and softmax wait for).
-// ===========================================================================
-struct PairCfg {
-  static constexpr int D = 128;
-  static constexpr int kBM = 128;                   // query rows per CTA (256 per pair)
-  static constexpr int kBN = 64;                    // keys per tile (per pair)
-  static constexpr int kDC = 2;                     // 64-element d-chunks
-  static constexpr int kNB = 2;                     // S/St TMEM buffers
-  static constexpr int kKS = 4;                     // K/Kt ring stages
-  static constexpr int kVS = 4;                     // V/Vt ring stages
-  static constexpr int kChunkQ = kBM * 128;         // one d-chunk of this CTA's Q rows
-  static constexpr int kHalfK = (kBN / 2) * 128;    // one d-chunk of this CTA's 32 keys
-  static constexpr int kQBytes = kDC * kChunkQ;
-  static constexpr int kKStage = 2 * kDC * kHalfK;  // K chunks, then Kt chunks (this CTA's keys)
-  static constexpr int kVHalf = kBN * 128;          // this CTA's 64 value columns of a tile
-  static constexpr int kVStage = 2 * kVHalf;        // V, then Vt
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffQt = kQBytes;
-  static constexpr int kOffK = 2 * kQBytes;
-  static constexpr int kOffV = kOffK + kKS * kKStage;
-  static constexpr int kOffBar = kOffV + kVS * kVStage;
-  static constexpr int kSmemBytes = kOffBar + 256 + 1024;
-  static constexpr uint32_t kColO = 0, kColT = D, kColBuf = 2 * D, kTmemCols = 512;
-  static_assert(kColBuf + 128 * kNB <= kTmemCols, "TMEM budget");
-  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-};
-
-struct PairBarriers {
-  uint64_t q_full;
-  uint64_t k_full[PairCfg::kKS], k_empty[PairCfg::kKS];
-  uint64_t v_full[PairCfg::kVS], v_empty[PairCfg::kVS];
-  uint64_t s_full[PairCfg::kNB], p_full[PairCfg::kNB], pv_done[PairCfg::kNB];
-  uint64_t drain, drain_s;
-  uint32_t tmem_base;
-  int abort_flag;
-};
-
-// Spin for ``ns`` nanoseconds (lets copies already in flight land before teardown).
-__device__ __forceinline__ void settle_ns(uint64_t ns) {
-  const uint64_t t0 = globaltimer_ns();
-  while (globaltimer_ns() - t0 < ns) {
-  }
-}
-
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    attn_jvp_fwd_pair_kernel(const __grid_constant__ FwdMaps maps, float* __restrict__ out,
-                             float* __restrict__ out_t, float* __restrict__ lse_out, float* __restrict__ mu_out,
-                             int N, int n_pairs, int kv_start, int kv_len, float scale, int* status) {
-  using C = PairCfg;
-  constexpr int D = C::D;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  PairBarriers* bars = reinterpret_cast<PairBarriers*>(smem + C::kOffBar);
-  volatile int* abort_flag = &bars->abort_flag;
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  const bool leader = rank == 0;
-  const int cid = blockIdx.x >> 1;
-  const int bh = cid / n_pairs;
-  const int q0 = ((cid % n_pairs) * 2 + static_cast<int>(rank)) * C::kBM;
-  const int n_tiles = (kv_len + C::kBN - 1) / C::kBN;
-
-  if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
-    for (int s = 0; s < C::kKS; ++s) {
-      mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_empty[s], 1);
-    }
-    for (int s = 0; s < C::kVS; ++s) {
-      mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->v_empty[s], 1);
-    }
-    for (int b = 0; b < C::kNB; ++b) {
-      mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->p_full[b], 2 * 128);  // every softmax thread of both CTAs
-      mbar_init(&bars->pv_done[b], 1);
-    }
-    mbar_init(&bars->drain, 1);
-    mbar_init(&bars->drain_s, 1);
-    bars->abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) {
-    tmem_alloc_pair(&bars->tmem_base, C::kTmemCols);
-    tmem_relinquish_pair();
-  }
-  tc_fence_before_sync();
-  cluster_sync();  // both CTAs' barriers exist before any remote access
-  tc_fence_after_sync();
-  const uint32_t tmem = bars->tmem_base;
-  auto lead = [](uint64_t* bar) { return mapa_shared(smem_u32(bar), 0); };
-
-  if (warp == 0) {
-    // ---------------- TMA producer: this CTA's Q, Qt and its half of each K/Kt tile ----------------
-    if (lane == 0) {
-      prefetch_tensormap(&maps.q);
-      prefetch_tensormap(&maps.qt);
-      prefetch_tensormap(&maps.k);
-      prefetch_tensormap(&maps.kt);
-      if (leader) mbar_arrive_expect_tx(&bars->q_full, 2 * 2 * C::kQBytes);
-      const uint32_t qf = lead(&bars->q_full);
-      for (int c = 0; c < C::kDC; ++c) {
-        tma_load_3d_pair(smem + C::kOffQ + c * C::kChunkQ, &maps.q, qf, c * 64, q0, bh);
-        tma_load_3d_pair(smem + C::kOffQt + c * C::kChunkQ, &maps.qt, qf, c * 64, q0, bh);
-      }
-      bool ok = true;
-      for (int t = 0; t < n_tiles && ok; ++t) {
-        const int s = t % C::kKS;
-        ok = mbar_wait_cluster(&bars->k_empty[s], ((t / C::kKS) & 1) ^ 1, abort_flag, status, kStatusTimeout);
-        if (!ok) break;
-        uint8_t* st = smem + C::kOffK + s * C::kKStage;
-        const uint32_t kf = lead(&bars->k_full[s]);
-        if (leader) mbar_arrive_expect_tx(&bars->k_full[s], 2 * C::kKStage);
-        const int key0 = kv_start + t * C::kBN + static_cast<int>(rank) * (C::kBN / 2);
-        for (int c = 0; c < C::kDC; ++c) {
-          tma_load_3d_pair(st + c * C::kHalfK, &maps.k, kf, c * 64, key0, bh);
-          tma_load_3d_pair(st + (C::kDC + c) * C::kHalfK, &maps.kt, kf, c * 64, key0, bh);
-        }
-      }
-      if (!ok) settle_ns(50000);
-    }
-  } else if (warp == 2) {
-    // ---------------- TMA producer: this CTA's value columns of each V/Vt tile ----------------
-    if (lane == 0) {
-      prefetch_tensormap(&maps.v);
-      prefetch_tensormap(&maps.vt);
-      bool ok = true;
-      for (int t = 0; t < n_tiles && ok; ++t) {
-        const int s = t % C::kVS;
-        ok = mbar_wait_cluster(&bars->v_empty[s], ((t / C::kVS) & 1) ^ 1, abort_flag, status, kStatusTimeout);
-        if (!ok) break;
-        uint8_t* st = smem + C::kOffV + s * C::kVStage;
-        const uint32_t vf = lead(&bars->v_full[s]);
-        if (leader) mbar_arrive_expect_tx(&bars->v_full[s], 2 * C::kVStage);
-        const int key0 = kv_start + t * C::kBN;
-        tma_load_3d_pair(st, &maps.v, vf, static_cast<int>(rank) * 64, key0, bh);
-        tma_load_3d_pair(st + C::kVHalf, &maps.vt, vf, static_cast<int>(rank) * 64, key0, bh);
-      }
-      if (!ok) settle_ns(50000);
-    }
-  } else if (warp == 1 || warp == 3) {
-    // ---------------- pair MMA issuers (even CTA): warp 3 the scores, warp 1 the values ----------------
-    if (lane == 0 && leader) {
-      constexpr uint32_t kIdS = make_idesc_bf16_f32(256, C::kBN, false, false);
-      constexpr uint32_t kIdPV = make_idesc_bf16_f32(256, D, false, true);
-      const uint64_t dQ = make_smem_desc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
-      const uint64_t dQt = make_smem_desc_sw128(smem_u32(smem + C::kOffQt), 16, 1024);
-      const uint64_t dK0 = make_smem_desc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
-      const uint64_t dV0 = make_smem_desc_sw128(smem_u32(smem + C::kOffV), C::kVHalf, 1024);
-      auto off = [](uint64_t desc, uint32_t bytes) { return desc + static_cast<uint64_t>(bytes >> 4); };
-      constexpr uint16_t kBoth = 0x3;
-      volatile int no_abort = 0;
-      if (warp == 3) {
-        bool ok = mbar_wait_cluster(&bars->q_full, 0, abort_flag, status, kStatusTimeout);
-        for (int t = 0; ok && t < n_tiles; ++t) {
-          const int b = t % C::kNB;
-          const int s = t % C::kKS;
-          ok = mbar_wait_cluster(&bars->k_full[s], (t / C::kKS) & 1, abort_flag, status, kStatusTimeout);
-          // The buffer's St half is free once both CTAs' softmax finished tile t - NB.
-          if (ok && t >= C::kNB)
-            ok = mbar_wait_cluster(&bars->p_full[b], ((t - C::kNB) / C::kNB) & 1, abort_flag, status,
-                                   kStatusTimeout);
-          if (!ok) break;
-          tc_fence_after_sync();
-          const uint64_t dK = off(dK0, s * C::kKStage);
-          const uint32_t dS = tmem + C::kColBuf + 128u * b;
-          const uint32_t dSt = dS + 64u;
-#pragma unroll
-          for (int c = 0; c < C::kDC; ++c)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ss_pair(dSt, off(dQt, c * C::kChunkQ + kk * 32), off(dK, c * C::kHalfK + kk * 32), kIdS,
-                          (c | kk) != 0);
-#pragma unroll
-          for (int c = 0; c < C::kDC; ++c)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ss_pair(dSt, off(dQ, c * C::kChunkQ + kk * 32), off(dK, (C::kDC + c) * C::kHalfK + kk * 32),
-                          kIdS, 1);
-          // The S half holds P~/H~ of tile t - NB until that tile's value MMAs are done.
-          if (t >= C::kNB) {
-            ok = mbar_wait_cluster(&bars->pv_done[b], ((t - C::kNB) / C::kNB) & 1, abort_flag, status,
-                                   kStatusTimeout);
-            if (!ok) break;
-            tc_fence_after_sync();
-          }
-#pragma unroll
-          for (int c = 0; c < C::kDC; ++c)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ss_pair(dS, off(dQ, c * C::kChunkQ + kk * 32), off(dK, c * C::kHalfK + kk * 32), kIdS,
-                          (c | kk) != 0);
-          mma_commit_pair(&bars->k_empty[s], kBoth);
-          mma_commit_pair(&bars->s_full[b], kBoth);
-        }
-        // Nothing may still read either CTA's shared or tensor memory at teardown.
-        mma_commit_pair(&bars->drain_s, 0x1);
-        mbar_wait(&bars->drain_s, 0, &no_abort, nullptr, 0);
-      } else {
-        bool ok = true;
-        for (int j = 0; ok && j < n_tiles; ++j) {
-          const int b = j % C::kNB;
-          const int s = j % C::kVS;
-          ok = mbar_wait_cluster(&bars->p_full[b], (j / C::kNB) & 1, abort_flag, status, kStatusTimeout) &&
-               mbar_wait_cluster(&bars->v_full[s], (j / C::kVS) & 1, abort_flag, status, kStatusTimeout);
-          if (!ok) break;
-          tc_fence_after_sync();
-          const uint64_t dV = off(dV0, s * C::kVStage);
-          const uint32_t aP = tmem + C::kColBuf + 128u * b;
-          const uint32_t aH = aP + 32u;
-#pragma unroll
-          for (int kk = 0; kk < C::kBN / 16; ++kk) {
-            const uint64_t bV = off(dV, kk * 2048);
-            const uint64_t bVt = off(dV, C::kVHalf + kk * 2048);
-            const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
-            mma_ts_pair(tmem + C::kColO, aP + kk * 8, bV, kIdPV, acc);   // O += P~ V
-            mma_ts_pair(tmem + C::kColT, aP + kk * 8, bVt, kIdPV, acc);  // T += P~ Vt
-            mma_ts_pair(tmem + C::kColT, aH + kk * 8, bV, kIdPV, 1u);    // T += H~ V
-          }
-          mma_commit_pair(&bars->v_empty[s], kBoth);
-          mma_commit_pair(&bars->pv_done[b], kBoth);
-        }
-        mma_commit_pair(&bars->drain, 0x1);
-        mbar_wait(&bars->drain, 0, &no_abort, nullptr, 0);
-      }
-    }
-  } else if (warp >= 4) {
-    // ---------------- softmax / JVP / epilogue: this CTA's 128 rows ----------------
-    const int quarter = warp - 4;
-    const int row = quarter * 32 + lane;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const float c2 = scale * kLog2e;
-    RowState st;
-    bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int b = j % C::kNB;
-      ok = mbar_wait_cluster(&bars->s_full[b], (j / C::kNB) & 1, abort_flag, status, kStatusTimeout);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after_sync();
-      const uint32_t cS = lane_addr + C::kColBuf + 128u * b;
-      const int valid = min(C::kBN, kv_len - j * C::kBN);
-      ok = softmax_tile<D>(lane_addr, cS, valid, j == 0, c2, scale, st, [&]() {
-        return mbar_wait_cluster(&bars->pv_done[(j - 1) % C::kNB], ((j - 1) / C::kNB) & 1, abort_flag, status,
-                                 kStatusTimeout);
-      });
-      if (!ok) break;
-      mbar_arrive_cluster(lead(&bars->p_full[b]));
-    }
-    if (ok)
-      ok = mbar_wait_cluster(&bars->pv_done[(n_tiles - 1) % C::kNB], ((n_tiles - 1) / C::kNB) & 1, abort_flag,
-                             status, kStatusTimeout);
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
-      tc_fence_after_sync();
-      write_row<D>(lane_addr, st, bh, N, q0 + row, out, out_t, lse_out, mu_out);
-    }
-  }
-
-  __syncwarp();
-  tc_fence_before_sync();
-  cluster_sync();  // the peer may still be reading this CTA's memory until here
-  if (warp == 1) {
-    tc_fence_after_sync();
-    tmem_dealloc_pair(tmem, C::kTmemCols);
   }
 }
 
@@ -786,38 +521,10 @@ cudaError_t launch_d(const FwdArgs& a, const char** msg) {
   return e;
 }
 
-cudaError_t launch_pair(const FwdArgs& a, const char** msg) {
-  using C = PairCfg;
-  FwdMaps maps;
-  cudaError_t e = cudaSuccess;
-  const void* ptrs[6] = {a.q, a.q_t, a.k, a.k_t, a.v, a.v_t};
-  CUtensorMap* dst[6] = {&maps.q, &maps.qt, &maps.k, &maps.kt, &maps.v, &maps.vt};
-  const int rows[6] = {C::kBM, C::kBM, C::kBN / 2, C::kBN / 2, C::kBN, C::kBN};
-  for (int i = 0; i < 6 && e == cudaSuccess; ++i) e = make_map(dst[i], ptrs[i], a.BH, a.N, C::D, rows[i]);
-  if (e != cudaSuccess) {
-    *msg = "cuTensorMapEncodeTiled rejected a tensor (alignment or size)";
-    return e;
-  }
-  e = cudaFuncSetAttribute(attn_jvp_fwd_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-  if (e != cudaSuccess) {
-    *msg = "cudaFuncSetAttribute(max dynamic shared memory) failed";
-    return e;
-  }
-  const int n_qtiles = static_cast<int>((a.N + C::kBM - 1) / C::kBM);
-  const int n_pairs = (n_qtiles + 1) / 2;
-  const int64_t grid = 2 * static_cast<int64_t>(n_pairs) * a.BH;
-  attn_jvp_fwd_pair_kernel<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, a.stream>>>(
-      maps, a.out, a.out_t, a.lse, a.mu, static_cast<int>(a.N), n_pairs, static_cast<int>(a.kv_start),
-      static_cast<int>(a.kv_len), a.scale, a.status);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) *msg = "attention-JVP pair kernel launch failed";
-  return e;
-}
-
 }  // namespace
 
 cudaError_t launch_attn_jvp_fwd(const FwdArgs& a, const char** msg) {
-  if (a.d == 128) return launch_pair(a, msg);
+  if (a.d == 128) return launch_d<128>(a, msg);
   if (a.d == 64) return launch_d<64>(a, msg);
   *msg = "unsupported head dimension";
   return cudaErrorInvalidValue;
