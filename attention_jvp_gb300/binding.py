@@ -47,11 +47,12 @@ def load(path=None):
     lib.trigflow_coeffs.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.POINTER(ctypes.c_double)]
     lib.trigflow_tangent.argtypes = [vp, vp, vp, vp, i64, i64, vp]
     lib.attn_jvp_status.argtypes = [ctypes.c_int]
+    lib.attn_jvp_selftest_wait.argtypes = [i64, vp]
     lib.attn_jvp_last_error.restype = ctypes.c_char_p
     lib.attn_jvp_version.restype = ctypes.c_char_p
     for name in ("attn_jvp_fwd", "attn_jvp_fwd_chunk", "attn_jvp_merge", "attn_jvp_cast_f32_bf16",
                  "attn_jvp_fwd_split_noalloc",
-                 "trigflow_coeffs", "trigflow_tangent", "attn_jvp_status"):
+                 "trigflow_coeffs", "trigflow_tangent", "attn_jvp_status", "attn_jvp_selftest_wait"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -251,6 +252,11 @@ def attn_jvp_status(clear=True):
     """0 if no kernel reported a problem; raises AttnJvpError(ETIMEOUT) otherwise."""
     _check("attn_jvp_status", load().attn_jvp_status(1 if clear else 0))
     return 0
+
+
+def attn_jvp_selftest_wait(limit_ns, stream=None):
+    """Launch the bounded-wait self-test kernel (see include/attnjvp.h)."""
+    _check("attn_jvp_selftest_wait", load().attn_jvp_selftest_wait(int(limit_ns), _stream(stream)))
 
 
 def attn_jvp_version():

@@ -9,6 +9,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "sm103_ptx.cuh"
 
 namespace attnjvp {
 namespace {
@@ -125,6 +126,24 @@ __global__ void __launch_bounds__(256) trigflow_tangent_kernel(const float* x0, 
   for (int64_t i = (n4 << 2) + tid0; i < per_sample; i += stride) ob[i] = fmaf(c, eb[i], -s * xb[i]);
 }
 
+// ---------------------------------------------------------------------------
+// Failure-path self-test: one thread waits, with the kernels' own bounded-wait
+// routine, on an mbarrier that nothing will ever complete.  The wait must give
+// up after ``limit_ns`` and record the timeout in the status word; the kernel
+// then returns normally, leaving the context usable.
+// ---------------------------------------------------------------------------
+__global__ void wait_selftest_kernel(int* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);  // expects one arrival that never comes
+    abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) ptx::mbar_wait(&bar, 0, &abort_flag, status, kStatusTimeout, limit_ns);
+}
+
 int sm_count() {
   static int cached = 0;
   if (cached == 0) {
@@ -157,6 +176,11 @@ cudaError_t launch_cast_f32_bf16(const float* in, void* out, int64_t n, cudaStre
   const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
   const int64_t blocks = want < 1 ? 1 : (want < cap ? want : cap);
   cast_f32_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(in, static_cast<__nv_bfloat16*>(out), n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
   return cudaGetLastError();
 }
 

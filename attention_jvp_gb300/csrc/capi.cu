@@ -229,6 +229,16 @@ int trigflow_tangent(const float* x0, const float* eps, const double* t, float* 
   return ok();
 }
 
+int attn_jvp_selftest_wait(int64_t limit_ns, void* stream) {
+  if (limit_ns < 1000 || limit_ns > 2000000000) return fail(ATTNJVP_EINVAL, "limit_ns must be in [1e3, 2e9]");
+  const char* why = "";
+  int* st = status_word(&why);
+  if (!st) return fail(ATTNJVP_ECUDA, "no CUDA device / status word: %s", why);
+  cudaError_t e = launch_wait_selftest(st, static_cast<uint64_t>(limit_ns), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(ATTNJVP_ECUDA, "self-test launch failed: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 int attn_jvp_status(int clear) {
   const char* why = "";
   int* st = status_word(&why);

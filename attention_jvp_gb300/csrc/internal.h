@@ -33,6 +33,8 @@ cudaError_t launch_cast_f32_bf16(const float* in, void* out, int64_t n, cudaStre
 cudaError_t launch_trigflow_tangent(const float* x0, const float* eps, const double* t, float* out, int64_t B,
                                     int64_t per_sample, cudaStream_t stream);
 
+cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t stream);
+
 // Sets the calling thread's message returned by attn_jvp_last_error().
 void set_last_error(const char* msg);
 

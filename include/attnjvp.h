@@ -151,6 +151,18 @@ int trigflow_tangent(const float* x0, const float* eps, const double* t, float* 
                      int64_t B, int64_t per_sample, void* stream);
 
 /*
+ * Failure-path self-test.  Launches one tiny kernel on ``stream`` that waits,
+ * with the same bounded-wait routine the attention kernels use, on an
+ * on-chip barrier nothing ever completes; the wait gives up after
+ * ``limit_ns`` nanoseconds (1e3 .. 2e9) and records ATTNJVP_ETIMEOUT in the
+ * device's status word, exactly as a stuck attention kernel would, without
+ * faulting or hanging the GPU.  Afterwards attn_jvp_status() reports
+ * ATTNJVP_ETIMEOUT (and clears the word when asked).  While the word is set,
+ * attention kernels skip their work, so clear it before further launches.
+ */
+int attn_jvp_selftest_wait(int64_t limit_ns, void* stream);
+
+/*
  * Reads (and, if ``clear`` is non-zero, resets) the status word of the current
  * device after a device-wide synchronisation.  Returns 0 when no kernel has
  * reported a problem since the last clear, ATTNJVP_ETIMEOUT when a bounded

@@ -34,7 +34,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for expected in ("attn_jvp_fwd", "attn_jvp_fwd_chunk", "attn_jvp_merge", "attn_jvp_cast_f32_bf16",
                      "trigflow_coeffs", "trigflow_tangent", "attn_jvp_status", "attn_jvp_last_error",
-                     "attn_jvp_version"):
+                     "attn_jvp_version", "attn_jvp_selftest_wait", "attn_jvp_fwd_split_noalloc"):
         assert expected in names
 
 
@@ -85,6 +85,10 @@ def test_argument_validation_needs_no_gpu(lib):
     assert lib.attn_jvp_cast_f32_bf16(vp, vp, -1, None) == E.ATTNJVP_EINVAL
     assert lib.attn_jvp_cast_f32_bf16(vp, vp, 0, None) == E.ATTNJVP_OK
     assert lib.trigflow_tangent(vp, vp, vp, vp, 0, 10, None) == E.ATTNJVP_EINVAL
+    assert lib.attn_jvp_selftest_wait(10, None) == E.ATTNJVP_EINVAL
+    assert lib.attn_jvp_selftest_wait(5_000_000_000, None) == E.ATTNJVP_EINVAL
+    assert lib.attn_jvp_fwd_split_noalloc(*[ctypes.c_void_p(256)] * 10, 1, 1, 64, 128, ctypes.c_float(0.1), 0,
+                                          None) == E.ATTNJVP_EINVAL
     assert lib.trigflow_tangent(vp, vp, vp, vp, 2, 0, None) == E.ATTNJVP_EINVAL
 
 
