@@ -14,19 +14,26 @@
 //   warp 0      TMA producer for Q, Qt (once) and the K/Kt ring
 //   warp 1      TMEM allocator and the tcgen05.mma issuer of the value MMAs
 //   warp 2      TMA producer for the V/Vt ring
-//   warp 3      tcgen05.mma issuer of the score MMAs (a second issuing thread
-//               keeps the tensor pipe fed while the other waits on a barrier)
+//   warp 3      tcgen05.mma issuer of the score-tangent MMAs (St)
 //   warps 4-7   softmax + JVP weights + lazy rescale + epilogue; thread t of
 //               warp 4+w owns query row 32w+t, which is TMEM lane 32w+t, so
 //               every row reduction is thread-local (no shuffles).
+//   warp 8      tcgen05.mma issuer of the score MMAs (S)
+// Three issuing threads keep the tensor pipe fed while any one of them waits
+// on a barrier, and the short S chain (which gates the softmax of the next
+// tile) never queues behind the long St chain of the same thread.
 // Per 64-key tile j (tensor-core work, fp32 accumulation in TMEM):
 //   S_b  = Q K_j^T                         (d-deep, N = 64)
-//   St_b = [Qt Q] [K_j Kt_j]^T             (one 2d-deep chain, N = 64)
+//   St_c = [Qt Q] [K_j Kt_j]^T             (one 2d-deep chain, N = 64)
 //   softmax warps: P~ = 2^(S*s*log2e - m), H~ = P~ (.) St * s, row sums in fp32,
-//                  P~ and H~ rounded to bf16 and written back into S_b's columns
+//                  P~ and H~ rounded to bf16 and written back into St_c's columns
 //   O += P~ V_j,  T += P~ Vt_j,  T += H~ V_j   (A operand read from TMEM)
-// S/St live in NB ping-pong TMEM buffers so the next tile's score MMAs overlap
-// the current tile's softmax.  Only MMAs of identical shape chain into one
+// S buffers and St buffers are two separate TMEM rings.  An St buffer stays
+// busy until the value MMAs have read the P~/H~ written into it, an S buffer
+// only until the softmax has loaded it.  The long 2d-deep St chain therefore
+// gets the deeper ring and is issued first, as soon as the value MMAs of tile
+// j - NSt are done; the short S chain waits only for the softmax to have
+// loaded tile j - NS.  Only MMAs of identical shape chain into one
 // accumulator, the ordering tcgen05 guarantees without extra waits.
 //
 // Lazy rescale: a row keeps its reference max until a tile's max exceeds it by
@@ -48,7 +55,8 @@ struct FwdCfg {
   static constexpr int kBM = 128;                  // query rows per CTA (= TMEM lanes)
   static constexpr int kBN = 64;                   // keys per tile
   static constexpr int kDC = D / 64;               // 64-element (128-byte) d-chunks
-  static constexpr int kNB = (D == 128) ? 2 : 3;   // S/St TMEM buffers
+  static constexpr int kNS = (D == 128) ? 1 : 3;   // S TMEM buffers
+  static constexpr int kNSt = 3;                   // St (then P~/H~) TMEM buffers
   static constexpr int kKS = (D == 128) ? 2 : 3;   // K/Kt ring stages
   static constexpr int kVS = (D == 128) ? 2 : 3;   // V/Vt ring stages
   static constexpr int kChunkQ = kBM * 128;        // one d-chunk of a Q tile (bytes)
@@ -62,16 +70,19 @@ struct FwdCfg {
   static constexpr int kOffV = kOffK + kKS * kKStage;
   static constexpr int kOffBar = kOffV + kVS * kVStage;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
-  // TMEM columns (fp32 each): O [0,D), T [D,2D), buffer b: S [2D+128b, +64), St [+64, +128)
+  // TMEM columns (fp32 each): O [0,D), T [D,2D), S buffer b [2D+64b, +64),
+  // St buffer c [2D+64NS+64c, +64)
   static constexpr uint32_t kColO = 0;
   static constexpr uint32_t kColT = D;
-  static constexpr uint32_t kColBuf = 2 * D;
+  static constexpr uint32_t kColS = 2 * D;
+  static constexpr uint32_t kColSt = 2 * D + 64 * kNS;
   static constexpr uint32_t kTmemCols = 512;
-  static_assert(kColBuf + 128 * kNB <= kTmemCols, "TMEM budget");
+  static_assert(kColSt + 64 * kNSt <= kTmemCols, "TMEM budget");
+  static_assert(kNS <= 3 && kNSt <= 3 && kKS <= 3 && kVS <= 3, "barrier arrays");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 288;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale once P~ could exceed 2^8
@@ -84,8 +95,8 @@ struct Barriers {
   uint64_t q_full;
   uint64_t k_full[3], k_empty[3];
   uint64_t v_full[3], v_empty[3];
-  uint64_t s_full[3], p_full[3], pv_done[3], st_free[3];
-  uint64_t drain, drain_s;
+  uint64_t s_full[3], st_full[3], s_free[3], p_full[3], pv_done[3];
+  uint64_t drain, drain_s, drain_st;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -98,22 +109,24 @@ struct RowState {
 };
 
 // Softmax + JVP weights of one 64-key tile for the calling thread's query row.
-// ``cS`` is the row's TMEM address of the tile's buffer (raw S in columns 0-63,
-// raw St in 64-127).  ``on_loaded()`` runs once both are in registers (the St
-// half is then free for the next tile's score MMAs).  On return P~ and H~ (bf16 pairs) sit in columns 0-31 and
-// 32-63 of that buffer, their stores have completed and the tcgen05 fence that
+// ``cS`` / ``cSt`` are the row's TMEM addresses of the tile's raw S and raw St
+// (64 columns each).  ``on_loaded()`` runs once both are in registers (the S
+// buffer is then free for a later tile's score MMAs).  On return P~ and H~ (bf16
+// pairs) sit in columns 0-31 and 32-63 of the St buffer, their stores have
+// completed and the tcgen05 fence that
 // precedes the hand-off to the MMA thread has been executed.  When the row max
 // grows by more than the threshold the accumulators O and T (columns 0-2D) are
 // rescaled after ``wait_prev_pv()`` confirms the previous tile's value MMAs are
 // done.  Returns false (warp-uniformly) when a wait gave up.
 template <int D, class OnLoaded, class WaitPrevPv>
-__device__ __forceinline__ bool softmax_tile(uint32_t lane_addr, uint32_t cS, int valid, bool first, float c2,
+__device__ __forceinline__ bool softmax_tile(uint32_t lane_addr, uint32_t cS, uint32_t cSt, int valid, bool first,
+                                             float c2,
                                              float scale, RowState& st, OnLoaded on_loaded,
                                              WaitPrevPv wait_prev_pv) {
-  // One load brings the row's 64 raw scores and 64 raw score tangents; from
-  // then on the buffer's St columns may be overwritten (``on_loaded``).
+  // The row's 64 raw scores and 64 raw score tangents; from then on the S
+  // buffer may be overwritten (``on_loaded``).
   uint32_t raw[128];
-  tmem_ld128_wait(cS, raw);
+  tmem_ld64x2_wait(cS, cSt, raw);
   tc_fence_before_sync();
   on_loaded();
   if (valid < 64) {
@@ -126,14 +139,18 @@ __device__ __forceinline__ bool softmax_tile(uint32_t lane_addr, uint32_t cS, in
       }
   }
   // Row max of the raw scores (the scale is positive, so it keeps the order);
-  // eight independent chains keep the dependency depth short.
+  // eight independent chains of three-input maxima keep the dependency depth short.
+  auto f = [&](int i) { return __uint_as_float(raw[i]); };
   float mx8[8];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) mx8[k] = __uint_as_float(raw[k]);
+  for (int k = 0; k < 8; ++k) mx8[k] = fmax3(f(k), f(8 + k), f(16 + k));
 #pragma unroll
-  for (int i = 8; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(raw[i]));
-  const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * c2;
+  for (int i = 24; i < 56; i += 16)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mx8[k] = fmax3(mx8[k], f(i + k), f(i + 8 + k));
+#pragma unroll
+  for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], f(56 + k));
+  const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7])) * c2;
   float alpha = 1.f;
   bool rescale = false;
   if (first) {
@@ -143,30 +160,44 @@ __device__ __forceinline__ bool softmax_tile(uint32_t lane_addr, uint32_t cS, in
     st.m = mx;
     rescale = true;
   }
-  // P~ = 2^(S s log2e - m): one FFMA and one MUFU ex2 per score.
+  // P~ = 2^(S s log2e - m): one paired FFMA per two scores, one MUFU ex2 per score.
+  // Row sums run in four paired chains (eight fp32 lanes).
+  const uint64_t c2x2 = f2_pack(c2, c2);
+  const uint64_t negm2 = f2_pack(-st.m, -st.m);
   float p[64];
-  float ls8[8];
+  uint64_t l4[4];
 #pragma unroll
-  for (int i = 0; i < 64; ++i) {
-    p[i] = ex2_approx(fmaf(__uint_as_float(raw[i]), c2, -st.m));
-    ls8[i & 7] = (i < 8) ? p[i] : ls8[i & 7] + p[i];
+  for (int i = 0; i < 64; i += 2) {
+    float x0, x1;
+    f2_unpack(f2_fma(f2_pack(f(i), f(i + 1)), c2x2, negm2), x0, x1);
+    p[i] = ex2_approx(x0);
+    p[i + 1] = ex2_approx(x1);
+    const uint64_t pp = f2_pack(p[i], p[i + 1]);
+    const int k = (i >> 1) & 3;
+    l4[k] = (i < 8) ? pp : f2_add(l4[k], pp);
   }
-  st.l = st.l * alpha + (((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7])));
+  float la, lb;
+  f2_unpack(f2_add(f2_add(l4[0], l4[1]), f2_add(l4[2], l4[3])), la, lb);
+  st.l = st.l * alpha + (la + lb);
   uint32_t pk[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
   // H~ = P~ (.) St s; its row sum is taken in fp32 before rounding to bf16.
+  const uint64_t s2 = f2_pack(scale, scale);
   uint32_t hk[32];
-  float rs8[8];
+  uint64_t r4[4];
 #pragma unroll
   for (int i = 0; i < 64; i += 2) {
-    const float h0 = p[i] * (__uint_as_float(raw[64 + i]) * scale);
-    const float h1 = p[i + 1] * (__uint_as_float(raw[65 + i]) * scale);
-    const int k = (i >> 1) & 7;
-    rs8[k] = (i < 16) ? (h0 + h1) : rs8[k] + (h0 + h1);
+    const uint64_t hh = f2_mul(f2_pack(p[i], p[i + 1]), f2_mul(f2_pack(f(64 + i), f(65 + i)), s2));
+    float h0, h1;
+    f2_unpack(hh, h0, h1);
     hk[i >> 1] = pack_bf16x2(h0, h1);
+    const int k = (i >> 1) & 3;
+    r4[k] = (i < 8) ? hh : f2_add(r4[k], hh);
   }
-  st.r = st.r * alpha + (((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7])));
+  float ra, rb;
+  f2_unpack(f2_add(f2_add(r4[0], r4[1]), f2_add(r4[2], r4[3])), ra, rb);
+  st.r = st.r * alpha + (ra + rb);
   if (__any_sync(0xffffffffu, rescale)) {
     // O and T may only be touched once the previous tile's value MMAs are done.
     const bool ok = __all_sync(0xffffffffu, wait_prev_pv());
@@ -181,8 +212,8 @@ __device__ __forceinline__ bool softmax_tile(uint32_t lane_addr, uint32_t cS, in
       tmem_st32(lane_addr + c0, acc);
     }
   }
-  tmem_st32(cS, pk);
-  tmem_st32(cS + 32, hk);
+  tmem_st32(cSt, pk);
+  tmem_st32(cSt + 32, hk);
   tmem_wait_st();
   tc_fence_before_sync();
   return true;
@@ -254,16 +285,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < 3; ++s) {
       mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->k_empty[s], 2);  // one commit from each score issuer
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
       mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->st_full[s], 1);
       mbar_init(&bars->p_full[s], 4);  // one arrival per softmax warp
       mbar_init(&bars->pv_done[s], 1);
-      mbar_init(&bars->st_free[s], 4);
+      mbar_init(&bars->s_free[s], 4);
     }
     mbar_init(&bars->drain, 1);
     mbar_init(&bars->drain_s, 1);
+    mbar_init(&bars->drain_st, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -336,10 +369,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (t >= 0) mbar_wait(&bars->v_full[t % C::kVS], (t / C::kVS) & 1, &no_abort, nullptr, 0);
       }
     }
-  } else if (warp == 1 || warp == 3) {
-    // ---------------- tcgen05.mma issuers: warp 3 the score MMAs, warp 1 the value MMAs ----------------
-    // Two independent issuing threads keep the tensor pipe fed while either of
-    // them waits on a barrier; they meet only through the mbarriers below.
+  } else if (warp == 1 || warp == 3 || warp == 8) {
+    // ---------------- tcgen05.mma issuers: warp 8 S, warp 3 St, warp 1 the value MMAs ----------------
+    // Independent issuing threads; they meet only through the mbarriers below.
     if (lane == 0) {
       constexpr uint32_t kIdS = make_idesc_bf16_f32(128, C::kBN, false, false);  // Q K^T, both K-major
       constexpr uint32_t kIdPV = make_idesc_bf16_f32(128, D, false, true);      // P~ V, V is N-major
@@ -351,39 +383,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dV0 = make_smem_desc_sw128(smem_u32(smem + C::kOffV), C::kChunkK, 1024);
       auto off = [](uint64_t desc, uint32_t bytes) { return desc + static_cast<uint64_t>(bytes >> 4); };
       volatile int no_abort = 0;
-      if (warp == 3) {
+      if (warp == 8) {
         bool ok = mbar_wait(&bars->q_full, 0, abort_flag, status, kStatusTimeout);
         for (int t = 0; ok && t < n_tiles; ++t) {
-          const int b = t % C::kNB;
+          const int b = t % C::kNS;
           const int s = t % C::kKS;
           ok = mbar_wait(&bars->k_full[s], (t / C::kKS) & 1, abort_flag, status, kStatusTimeout);
-          // The buffer's St half is free once the softmax has loaded tile t - NB.
-          if (ok && t >= C::kNB)
-            ok = mbar_wait(&bars->st_free[b], ((t - C::kNB) / C::kNB) & 1, abort_flag, status, kStatusTimeout);
+          // The S buffer is free once the softmax has loaded tile t - NS.
+          if (ok && t >= C::kNS)
+            ok = mbar_wait(&bars->s_free[b], ((t - C::kNS) / C::kNS) & 1, abort_flag, status, kStatusTimeout);
           if (!ok) break;
           tc_fence_after_sync();
           const uint64_t dK = off(dK0, s * C::kKStage);
-          const uint32_t dS = tmem + C::kColBuf + 128u * b;
-          const uint32_t dSt = dS + 64u;
-          // St_t = [Qt Q] [K_t Kt_t]^T : one accumulator, 2d deep
-#pragma unroll
-          for (int c = 0; c < C::kDC; ++c)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ss(dSt, off(dQt, c * C::kChunkQ + kk * 32), off(dK, c * C::kChunkK + kk * 32), kIdS,
-                     (c | kk) != 0);
-#pragma unroll
-          for (int c = 0; c < C::kDC; ++c)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ss(dSt, off(dQ, c * C::kChunkQ + kk * 32), off(dK, (C::kDC + c) * C::kChunkK + kk * 32), kIdS,
-                     1);
-          // The S half holds P~/H~ of tile t - NB until that tile's value MMAs are done.
-          if (t >= C::kNB) {
-            ok = mbar_wait(&bars->pv_done[b], ((t - C::kNB) / C::kNB) & 1, abort_flag, status, kStatusTimeout);
-            if (!ok) break;
-            tc_fence_after_sync();
-          }
+          const uint32_t dS = tmem + C::kColS + 64u * b;
           // S_t = Q K_t^T
 #pragma unroll
           for (int c = 0; c < C::kDC; ++c)
@@ -397,17 +409,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Nothing may still be reading shared memory or TMEM when the CTA tears down.
         mma_commit(&bars->drain_s);
         mbar_wait(&bars->drain_s, 0, &no_abort, nullptr, 0);
+      } else if (warp == 3) {
+        bool ok = mbar_wait(&bars->q_full, 0, abort_flag, status, kStatusTimeout);
+        for (int t = 0; ok && t < n_tiles; ++t) {
+          const int bt = t % C::kNSt;
+          const int s = t % C::kKS;
+          ok = mbar_wait(&bars->k_full[s], (t / C::kKS) & 1, abort_flag, status, kStatusTimeout);
+          // The St buffer holds P~/H~ of tile t - NSt until that tile's value MMAs are done.
+          if (ok && t >= C::kNSt)
+            ok = mbar_wait(&bars->pv_done[bt], ((t - C::kNSt) / C::kNSt) & 1, abort_flag, status, kStatusTimeout);
+          if (!ok) break;
+          tc_fence_after_sync();
+          const uint64_t dK = off(dK0, s * C::kKStage);
+          const uint32_t dSt = tmem + C::kColSt + 64u * bt;
+          // St_t = [Qt Q] [K_t Kt_t]^T : one accumulator, 2d deep
+#pragma unroll
+          for (int c = 0; c < C::kDC; ++c)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(dSt, off(dQt, c * C::kChunkQ + kk * 32), off(dK, c * C::kChunkK + kk * 32), kIdS,
+                     (c | kk) != 0);
+#pragma unroll
+          for (int c = 0; c < C::kDC; ++c)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(dSt, off(dQ, c * C::kChunkQ + kk * 32), off(dK, (C::kDC + c) * C::kChunkK + kk * 32), kIdS,
+                     1);
+          mma_commit(&bars->k_empty[s]);
+          mma_commit(&bars->st_full[bt]);
+        }
+        mma_commit(&bars->drain_st);
+        mbar_wait(&bars->drain_st, 0, &no_abort, nullptr, 0);
       } else {
         bool ok = true;
         for (int j = 0; ok && j < n_tiles; ++j) {
-          const int b = j % C::kNB;
+          const int bt = j % C::kNSt;
           const int s = j % C::kVS;
-          ok = mbar_wait(&bars->p_full[b], (j / C::kNB) & 1, abort_flag, status, kStatusTimeout) &&
+          ok = mbar_wait(&bars->p_full[bt], (j / C::kNSt) & 1, abort_flag, status, kStatusTimeout) &&
                mbar_wait(&bars->v_full[s], (j / C::kVS) & 1, abort_flag, status, kStatusTimeout);
           if (!ok) break;
           tc_fence_after_sync();
           const uint64_t dV = off(dV0, s * C::kVStage);
-          const uint32_t aP = tmem + C::kColBuf + 128u * b;  // P~ packed bf16: 32 columns
+          const uint32_t aP = tmem + C::kColSt + 64u * bt;  // P~ packed bf16: 32 columns
           const uint32_t aH = aP + 32u;                       // H~ packed bf16: 32 columns
 #pragma unroll
           for (int kk = 0; kk < C::kBN / 16; ++kk) {
@@ -419,13 +462,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ts(tmem + C::kColT, aH + kk * 8, bV, kIdPV, 1u);    // T += H~ V
           }
           mma_commit(&bars->v_empty[s]);
-          mma_commit(&bars->pv_done[b]);
+          mma_commit(&bars->pv_done[bt]);
         }
         mma_commit(&bars->drain);
         mbar_wait(&bars->drain, 0, &no_abort, nullptr, 0);
       }
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 8) {
     // ---------------- softmax / JVP / epilogue: one query row per thread ----------------
     const int quarter = warp - 4;
     const int row = quarter * 32 + lane;
@@ -434,31 +477,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     RowState st;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-      const int b = j % C::kNB;
-      ok = mbar_wait(&bars->s_full[b], (j / C::kNB) & 1, abort_flag, status, kStatusTimeout);
+      const int b = j % C::kNS;
+      const int bt = j % C::kNSt;
+      ok = mbar_wait(&bars->s_full[b], (j / C::kNS) & 1, abort_flag, status, kStatusTimeout) &&
+           mbar_wait(&bars->st_full[bt], (j / C::kNSt) & 1, abort_flag, status, kStatusTimeout);
       ok = __all_sync(0xffffffffu, ok);  // keep the warp converged for the .sync.aligned TMEM ops
       if (!ok) break;
       tc_fence_after_sync();
-      const uint32_t cS = lane_addr + C::kColBuf + 128u * b;
+      const uint32_t cS = lane_addr + C::kColS + 64u * b;
+      const uint32_t cSt = lane_addr + C::kColSt + 64u * bt;
       const int valid = min(C::kBN, kv_len - j * C::kBN);
       // Hand-offs arrive once per warp: every lane has fenced its own TMEM
       // accesses, __syncwarp orders them before lane 0's arrival.
       ok = softmax_tile<D>(
-          lane_addr, cS, valid, j == 0, c2, scale, st,
+          lane_addr, cS, cSt, valid, j == 0, c2, scale, st,
           [&]() {
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->st_free[b]);
+            if (lane == 0) mbar_arrive(&bars->s_free[b]);
           },
           [&]() {
-            return mbar_wait(&bars->pv_done[(j - 1) % C::kNB], ((j - 1) / C::kNB) & 1, abort_flag, status,
+            return mbar_wait(&bars->pv_done[(j - 1) % C::kNSt], ((j - 1) / C::kNSt) & 1, abort_flag, status,
                              kStatusTimeout);
           });
       if (!ok) break;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[b]);
+      if (lane == 0) mbar_arrive(&bars->p_full[bt]);
     }
     // ---------------- epilogue ----------------
-    if (ok) ok = mbar_wait(&bars->pv_done[(n_tiles - 1) % C::kNB], ((n_tiles - 1) / C::kNB) & 1, abort_flag, status,
+    if (ok) ok = mbar_wait(&bars->pv_done[(n_tiles - 1) % C::kNSt], ((n_tiles - 1) / C::kNSt) & 1, abort_flag, status,
                            kStatusTimeout);
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
