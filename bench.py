@@ -32,7 +32,8 @@ METRIC = "attention-JVP TFLOPS (12·B·H·N²·d) and % of GB300 BF16 tensor pea
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "video_dit"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCE = os.path.join(ROOT, "attention_jvp_gb300", "csrc", "attn_jvp_fwd.cu")
+# Sources whose change invalidates a recorded DRAM-traffic capture of the fused kernel.
+KERNEL_SOURCES = tuple(os.path.join(ROOT, "attention_jvp_gb300", "csrc", n) for n in ("attn_jvp_fwd.cu", "sm103_ptx.cuh"))
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -82,8 +83,11 @@ def load_peaks():
 
 
 def kernel_source_sha():
-    with open(KERNEL_SOURCE, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for path in KERNEL_SOURCES:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def traffic_per_launch(kernel, workload, heads):
