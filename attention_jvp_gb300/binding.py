@@ -44,6 +44,9 @@ def load(path=None):
     lib.attn_jvp_merge.argtypes = [vp] * 4 + [i64] + [vp] * 4 + [i64] * 4 + [vp]
     lib.attn_jvp_cast_f32_bf16.argtypes = [vp, vp, i64, vp]
     lib.attn_jvp_fwd_split_noalloc.argtypes = [vp] * 6 + [fp] * 4 + [i64] * 4 + [ctypes.c_float, i64, vp]
+    lib.attn_jvp_fwd_host.argtypes = [vp] * 6 + [fp] * 4 + [i64] * 4 + [ctypes.c_float, i64, i64, vp, i64, vp]
+    lib.attn_jvp_fwd_host_workspace_bytes.argtypes = [i64] * 6
+    lib.attn_jvp_fwd_host_workspace_bytes.restype = i64
     lib.trigflow_coeffs.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.POINTER(ctypes.c_double)]
     lib.trigflow_tangent.argtypes = [vp, vp, vp, vp, i64, i64, vp]
     lib.attn_jvp_status.argtypes = [ctypes.c_int]
@@ -51,7 +54,7 @@ def load(path=None):
     lib.attn_jvp_last_error.restype = ctypes.c_char_p
     lib.attn_jvp_version.restype = ctypes.c_char_p
     for name in ("attn_jvp_fwd", "attn_jvp_fwd_chunk", "attn_jvp_merge", "attn_jvp_cast_f32_bf16",
-                 "attn_jvp_fwd_split_noalloc",
+                 "attn_jvp_fwd_split_noalloc", "attn_jvp_fwd_host",
                  "trigflow_coeffs", "trigflow_tangent", "attn_jvp_status", "attn_jvp_selftest_wait"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
@@ -215,6 +218,63 @@ def attn_jvp_fwd_split_noalloc(q, k, v, q_t, k_t, v_t, n_chunks, out, out_t, lse
                                            _ptr(out), _ptr(out_t), _ptr(lse), _ptr(mu), B, H, N, d,
                                            ctypes.c_float(scale), int(n_chunks), _stream(stream))
     _check("attn_jvp_fwd_split_noalloc", rc)
+    return out, out_t, lse, mu
+
+
+def _host(t, name, dtype, shape=None):
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+        raise ValueError("%s must be a host (CPU) tensor" % name)
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s (got %s)" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s (got %s)" % (name, tuple(shape), tuple(t.shape)))
+    return t
+
+
+def attn_jvp_fwd_host_workspace_bytes(shape, n_chunks=1, group_heads=0):
+    """Device workspace bytes attn_jvp_fwd_host needs for inputs of ``shape`` [B, H, N, d]."""
+    B, H, N, d = shape
+    n = load().attn_jvp_fwd_host_workspace_bytes(B, H, N, d, int(n_chunks), int(group_heads))
+    if n < 0:
+        _check("attn_jvp_fwd_host_workspace_bytes", int(n))
+    return int(n)
+
+
+def host_workspace(shape, n_chunks=1, group_heads=0, device=None):
+    """A device buffer sized for attn_jvp_fwd_host (torch's allocator aligns it to 256 bytes or more)."""
+    n = attn_jvp_fwd_host_workspace_bytes(shape, n_chunks, group_heads)
+    return torch.empty(n, dtype=torch.uint8, device=device or torch.device("cuda"))
+
+
+def attn_jvp_fwd_host(q, k, v, q_t, k_t, v_t, out, out_t, lse=None, mu=None, scale=None, n_chunks=1,
+                      group_heads=0, workspace=None, stream=None):
+    """The attention JVP on host tensors (bf16 [B, H, N, d] in; fp32 out), with the
+    library overlapping the transfers with compute.  Use pinned host tensors for
+    overlap.  Outputs are complete once ``stream`` has been synchronised."""
+    shape = tuple(q.shape)
+    if len(shape) != 4:
+        raise ValueError("q must be [B, H, N, d]")
+    for n, t in zip(("q", "k", "v", "q_t", "k_t", "v_t"), (q, k, v, q_t, k_t, v_t)):
+        _host(t, n, torch.bfloat16, shape)
+    B, H, N, d = shape
+    _host(out, "out", torch.float32, shape)
+    _host(out_t, "out_t", torch.float32, shape)
+    if lse is not None:
+        _host(lse, "lse", torch.float32, (B, H, N))
+    if mu is not None:
+        _host(mu, "mu", torch.float32, (B, H, N))
+    if workspace is None:
+        workspace = host_workspace(shape, n_chunks, group_heads)
+    if not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor")
+    scale = d ** -0.5 if scale is None else float(scale)
+    rc = load().attn_jvp_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(q_t), _ptr(k_t), _ptr(v_t),
+                                  _ptr(out), _ptr(out_t), _ptr(lse), _ptr(mu), B, H, N, d,
+                                  ctypes.c_float(scale), int(n_chunks), int(group_heads), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("attn_jvp_fwd_host", rc)
     return out, out_t, lse, mu
 
 

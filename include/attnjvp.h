@@ -151,6 +151,51 @@ int trigflow_tangent(const float* x0, const float* eps, const double* t, float* 
                      int64_t B, int64_t per_sample, void* stream);
 
 /*
+ * Attention JVP on HOST-resident tensors: the same operation and result as
+ * attn_jvp_fwd (n_chunks == 1) or the split path (n_chunks > 1), with the
+ * host<->device transfers done by the library and overlapped with compute.
+ * The pages have no counterpart; it serves callers whose tensors live in host
+ * memory and who would otherwise pay copy-in + compute + copy-out in series.
+ *   q .. v_t            : HOST bf16 [B, H, N, d] (pinned memory for overlap;
+ *                         pageable memory works but serialises the copies).
+ *   out, out_t          : HOST fp32 [B, H, N, d];  lse, mu: HOST fp32 [B, H, N]
+ *                         or NULL.
+ *   B, H, N, d, scale   : as attn_jvp_fwd.
+ *   n_chunks            : 1, or the number of key chunks of the split path (<= N).
+ *   group_heads         : heads per pipelined item (>= 1), or 0 for automatic
+ *                         (about 608 CTAs per item: four waves on a 152-SM GB300).
+ *   workspace           : DEVICE buffer, 256-byte aligned, of at least
+ *                         attn_jvp_fwd_host_workspace_bytes(B, H, N, d, n_chunks,
+ *                         group_heads) bytes (three slots of group_heads heads);
+ *                         owned by the caller.
+ * Items of at most group_heads heads of one batch entry rotate through three
+ * workspace slots, each computed on its own library-owned stream; item i+1 is
+ * copied in and item i-1 copied out on two more library-owned streams while
+ * item i computes, and consecutive items' kernels may overlap on the GPU.  The
+ * first and last items are cut to a quarter group to shorten the exposed
+ * first copy-in and last copy-out.
+ * On return the work is enqueued; once ``stream`` has been synchronised every
+ * output is in host memory.  Inputs must stay unchanged, and outputs unread,
+ * until then.  Calls that share a workspace must be ordered on one stream.
+ * Each item runs the device entry points on a [group, N, d] slice, so the
+ * results equal a device-resident call bit for bit.
+ */
+int attn_jvp_fwd_host(const void* q, const void* k, const void* v,
+                      const void* q_t, const void* k_t, const void* v_t,
+                      float* out, float* out_t, float* lse, float* mu,
+                      int64_t B, int64_t H, int64_t N, int64_t d, float scale,
+                      int64_t n_chunks, int64_t group_heads,
+                      void* workspace, int64_t workspace_bytes, void* stream);
+
+/*
+ * Device workspace, in bytes, that attn_jvp_fwd_host needs for these sizes,
+ * or a negative ATTNJVP_E* code for arguments attn_jvp_fwd_host would reject.
+ * Needs no GPU.
+ */
+int64_t attn_jvp_fwd_host_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d,
+                                          int64_t n_chunks, int64_t group_heads);
+
+/*
  * Failure-path self-test.  Launches one tiny kernel on ``stream`` that waits,
  * with the same bounded-wait routine the attention kernels use, on an
  * on-chip barrier nothing ever completes; the wait gives up after

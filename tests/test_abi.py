@@ -34,7 +34,8 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for expected in ("attn_jvp_fwd", "attn_jvp_fwd_chunk", "attn_jvp_merge", "attn_jvp_cast_f32_bf16",
                      "trigflow_coeffs", "trigflow_tangent", "attn_jvp_status", "attn_jvp_last_error",
-                     "attn_jvp_version", "attn_jvp_selftest_wait", "attn_jvp_fwd_split_noalloc"):
+                     "attn_jvp_version", "attn_jvp_selftest_wait", "attn_jvp_fwd_split_noalloc",
+                     "attn_jvp_fwd_host", "attn_jvp_fwd_host_workspace_bytes"):
         assert expected in names
 
 
@@ -113,6 +114,45 @@ def test_trigflow_coeffs_domain(lib):
     assert e.value.code == binding.ATTNJVP_EINVAL
     with pytest.raises(binding.AttnJvpError):
         binding.trigflow_coeffs(float("nan"))
+
+
+def _host_call(lib, ws=256, ws_bytes=1 << 40, d=128, n_chunks=1, group=0, first=256):
+    vp = ctypes.c_void_p
+    ins = [vp(first)] + [vp(256)] * 5
+    return lib.attn_jvp_fwd_host(*ins, vp(256), vp(256), None, None, 1, 4, 300, d, ctypes.c_float(0.1),
+                                 n_chunks, group, vp(ws) if ws else None, ws_bytes, None)
+
+
+def test_host_entry_validation_needs_no_gpu(lib):
+    E = binding
+    assert _host_call(lib, first=0) == E.ATTNJVP_EINVAL
+    assert _host_call(lib, d=96) == E.ATTNJVP_EUNSUPPORTED
+    assert _host_call(lib, ws=0) == E.ATTNJVP_EINVAL
+    assert b"workspace" in lib.attn_jvp_last_error()
+    assert _host_call(lib, ws=512 + 16) == E.ATTNJVP_EINVAL
+    assert b"256-byte" in lib.attn_jvp_last_error()
+    assert _host_call(lib, ws_bytes=1024) == E.ATTNJVP_EINVAL
+    assert b"needs" in lib.attn_jvp_last_error()
+    assert _host_call(lib, n_chunks=0) == E.ATTNJVP_EINVAL
+    assert _host_call(lib, n_chunks=301) == E.ATTNJVP_EINVAL
+    assert _host_call(lib, group=-1) == E.ATTNJVP_EINVAL
+
+
+def test_host_workspace_size(lib):
+    size = lambda *a: lib.attn_jvp_fwd_host_workspace_bytes(*a)
+    B, H, N, d = 1, 40, 32760, 128
+    auto = size(B, H, N, d, 1, 0)
+    # automatic grouping: ceil(608 / ceil(N / 128)) = 3 heads per item, three slots
+    per_head = 6 * N * d * 2 + 2 * N * d * 4 + 2 * N * 4
+    assert auto >= 3 * 3 * per_head and auto < 3 * 3 * per_head + 3 * 10 * 256
+    assert size(B, H, N, d, 1, 3) == auto
+    assert size(B, H, N, d, 1, 1) < auto < size(B, H, N, d, 1, 40)
+    assert size(B, H, N, d, 1, 400) == size(B, H, N, d, 1, 40)  # clamped to H
+    assert size(B, H, N, d, 4, 3) > auto  # chunk partials
+    assert size(B, H, N, 96, 1, 0) == binding.ATTNJVP_EUNSUPPORTED
+    assert size(0, H, N, d, 1, 0) == binding.ATTNJVP_EINVAL
+    with pytest.raises(binding.AttnJvpError):
+        binding.attn_jvp_fwd_host_workspace_bytes((1, 2, 64, 96))
 
 
 def test_missing_library_fails_loudly(tmp_path, monkeypatch):
