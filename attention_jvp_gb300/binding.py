@@ -45,6 +45,8 @@ def load(path=None):
     lib.attn_jvp_cast_f32_bf16.argtypes = [vp, vp, i64, vp]
     lib.attn_jvp_fwd_split_noalloc.argtypes = [vp] * 6 + [fp] * 4 + [i64] * 4 + [ctypes.c_float, i64, vp]
     lib.attn_jvp_fwd_host.argtypes = [vp] * 6 + [fp] * 4 + [i64] * 4 + [ctypes.c_float, i64, i64, vp, i64, vp]
+    lib.attn_jvp_fwd_strided.argtypes = [vp] * 6 + [fp] * 4 + [i64] * 5 + [ctypes.POINTER(i64), ctypes.c_float,
+                                                                          i64, i64, vp]
     lib.attn_jvp_fwd_host_workspace_bytes.argtypes = [i64] * 6
     lib.attn_jvp_fwd_host_workspace_bytes.restype = i64
     lib.trigflow_coeffs.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.POINTER(ctypes.c_double)]
@@ -54,7 +56,7 @@ def load(path=None):
     lib.attn_jvp_last_error.restype = ctypes.c_char_p
     lib.attn_jvp_version.restype = ctypes.c_char_p
     for name in ("attn_jvp_fwd", "attn_jvp_fwd_chunk", "attn_jvp_merge", "attn_jvp_cast_f32_bf16",
-                 "attn_jvp_fwd_split_noalloc", "attn_jvp_fwd_host",
+                 "attn_jvp_fwd_split_noalloc", "attn_jvp_fwd_host", "attn_jvp_fwd_strided",
                  "trigflow_coeffs", "trigflow_tangent", "attn_jvp_status", "attn_jvp_selftest_wait"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
@@ -159,6 +161,73 @@ def attn_jvp_fwd_chunk(q, k, v, q_t, k_t, v_t, kv_start, kv_len, scale=None, out
                                    _ptr(out), _ptr(out_t), _ptr(lse), _ptr(mu), B, H, N, d,
                                    ctypes.c_float(scale), int(kv_start), int(kv_len), _stream(stream))
     _check("attn_jvp_fwd_chunk", rc)
+    return out, out_t, lse, mu
+
+
+_LAYOUTS = {
+    # layout -> (index of B, S, H, D in the tensor's shape)
+    "bhsd": (0, 2, 1, 3),
+    "bshd": (0, 1, 2, 3),
+}
+
+
+def _layout_view(t, name, layout):
+    """(B, S, H, D) and element strides (batch, seq, head) of a bf16 CUDA tensor in ``layout``."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != torch.bfloat16:
+        raise ValueError("%s must be torch.bfloat16 (got %s)" % (name, t.dtype))
+    if t.dim() != 4 or t.stride(3) != 1:
+        raise ValueError("%s must be 4-D with a unit stride in the head dimension" % name)
+    ib, isq, ih, _ = _LAYOUTS[layout]
+    dims = (t.shape[ib], t.shape[isq], t.shape[ih], t.shape[3])
+    return dims, (t.stride(ib), t.stride(isq), t.stride(ih))
+
+
+def attn_jvp_fwd_strided(q, k, v, q_t, k_t, v_t, layout="bhsd", scale=None, out=None, out_t=None, lse=None,
+                         mu=None, kv_start=0, kv_len=None, want_rows=True, stream=None):
+    """Strided / cross-attention form.  ``layout`` names the dimension order of every
+    tensor's shape: "bhsd" ([B, H, S, D]) or "bshd" ([B, S, H, D], the page's).  Any
+    strides are accepted as long as the head dimension is unit-stride; tangents must
+    share their primal's strides.  Outputs O, Ot default to a new contiguous tensor in
+    ``layout``; lse, mu are [B, H, N_q].  ``kv_start``/``kv_len`` select a key range."""
+    if layout not in _LAYOUTS:
+        raise ValueError("layout must be one of %s" % sorted(_LAYOUTS))
+    (B, Nq, H, d), qs = _layout_view(q, "q", layout)
+    (Bk, Nkv, Hk, dk), ks = _layout_view(k, "k", layout)
+    if (Bk, Hk, dk) != (B, H, d):
+        raise ValueError("k must match q in batch, heads and head dim")
+    for n, t, ref in (("q_t", q_t, q), ("v", v, k), ("k_t", k_t, k), ("v_t", v_t, k)):
+        _layout_view(t, n, layout)
+        if tuple(t.shape) != tuple(ref.shape) or t.stride() != ref.stride():
+            raise ValueError("%s must have the shape and strides of %s" % (n, "q" if ref is q else "k"))
+    shape_q = tuple(q.shape)
+    if out is None:
+        out = torch.empty(shape_q, dtype=torch.float32, device=q.device)
+    if out_t is None:
+        out_t = torch.empty(shape_q, dtype=torch.float32, device=q.device)
+    for n, t in (("out", out), ("out_t", out_t)):
+        if not t.is_cuda or t.dtype != torch.float32 or tuple(t.shape) != shape_q or t.stride(3) != 1:
+            raise ValueError("%s must be a float32 CUDA tensor of q's shape with a unit last stride" % n)
+    if out_t.stride() != out.stride():
+        raise ValueError("out_t must have out's strides")
+    ib, isq, ih, _ = _LAYOUTS[layout]
+    os_ = (out.stride(ib), out.stride(isq), out.stride(ih))
+    if lse is None and want_rows:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if mu is None and want_rows:
+        mu = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _req(lse, "lse", torch.float32, (B, H, Nq))
+    if mu is not None:
+        _req(mu, "mu", torch.float32, (B, H, Nq))
+    kv_len = Nkv - kv_start if kv_len is None else int(kv_len)
+    scale = d ** -0.5 if scale is None else float(scale)
+    strides = (ctypes.c_int64 * 9)(*qs, *ks, *os_)
+    rc = load().attn_jvp_fwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(q_t), _ptr(k_t), _ptr(v_t),
+                                     _ptr(out), _ptr(out_t), _ptr(lse), _ptr(mu), B, H, Nq, Nkv, d, strides,
+                                     ctypes.c_float(scale), int(kv_start), kv_len, _stream(stream))
+    _check("attn_jvp_fwd_strided", rc)
     return out, out_t, lse, mu
 
 

@@ -91,6 +91,17 @@ struct FwdMaps {
   CUtensorMap q, qt, k, kt, v, vt;
 };
 
+// The tensor maps are 4-D over (head-dimension column, sequence row, head,
+// batch), each dimension with the tensor's own stride, so any strided layout
+// with a unit head-dimension stride ([B, H, S, D], [B, S, H, D], slices of a
+// packed QKV tensor, ...) is read in place.
+struct FwdGeom {
+  int H, Nq, n_qtiles, kv_start, kv_len;
+  int d;                    // real head dimension; columns d..D-1 of every tile are zero (TMA fill)
+  float scale;
+  int64_t o_stride[3];      // output element strides: batch, sequence, head
+};
+
 struct Barriers {
   uint64_t q_full;
   uint64_t k_full[3], k_empty[3];
@@ -220,24 +231,29 @@ __device__ __forceinline__ bool softmax_tile(uint32_t lane_addr, uint32_t cS, ui
 }
 
 // Epilogue of the calling thread's row: O = O~/l, mu = r/l, Ot = T~/l - mu O and
-// LSE = (m + log2 l) ln 2, read from TMEM (O~ in columns 0-D, T~ in D-2D).
+// LSE = (m + log2 l) ln 2, read from TMEM (O~ in columns 0-D, T~ in D-2D).  The
+// first d columns are written, at element offset ``obase`` of out / out_t.
 template <int D>
-__device__ __forceinline__ void write_row(uint32_t lane_addr, const RowState& st, int64_t bh, int N, int qrow,
-                                          float* __restrict__ out, float* __restrict__ out_t,
-                                          float* __restrict__ lse_out, float* __restrict__ mu_out) {
+__device__ __forceinline__ void write_row(uint32_t lane_addr, const RowState& st, int64_t ridx, int64_t obase,
+                                          bool valid_row, int d, float* __restrict__ out,
+                                          float* __restrict__ out_t, float* __restrict__ lse_out,
+                                          float* __restrict__ mu_out) {
   const float inv_l = 1.f / st.l;
   const float mu = st.r * inv_l;
-  const int64_t obase = (bh * N + qrow) * D;
+  // d == D except for the 16/32-wide heads run by the D = 64 instantiation.
+  const int ncols = D == 128 ? D : d;
 #pragma unroll 1
-  for (int c0 = 0; c0 < D; c0 += 32) {
+  for (int c0 = 0; c0 < ncols; c0 += 32) {
     uint32_t ov[32], tv[32];
     tmem_ld32_wait(lane_addr + c0, ov);
     tmem_ld32_wait(lane_addr + D + c0, tv);
-    if (qrow < N) {
+    if (valid_row) {
       float4* o4 = reinterpret_cast<float4*>(out + obase + c0);
       float4* t4 = reinterpret_cast<float4*>(out_t + obase + c0);
+      const int n4 = D == 128 ? 8 : min(8, (ncols - c0) >> 2);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
+        if (D != 128 && i >= n4) break;
         float4 o, t;
         o.x = __uint_as_float(ov[4 * i + 0]) * inv_l;
         o.y = __uint_as_float(ov[4 * i + 1]) * inv_l;
@@ -252,8 +268,7 @@ __device__ __forceinline__ void write_row(uint32_t lane_addr, const RowState& st
       }
     }
   }
-  if (qrow < N) {
-    const int64_t ridx = bh * N + qrow;
+  if (valid_row) {
     if (lse_out) lse_out[ridx] = (st.m + __log2f(st.l)) * kLn2;
     if (mu_out) mu_out[ridx] = mu;
   }
@@ -261,9 +276,9 @@ __device__ __forceinline__ void write_row(uint32_t lane_addr, const RowState& st
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_jvp_fwd_kernel(const __grid_constant__ FwdMaps maps, float* __restrict__ out, float* __restrict__ out_t,
-                        float* __restrict__ lse_out, float* __restrict__ mu_out, int N, int n_qtiles, int kv_start,
-                        int kv_len, float scale, int* status) {
+    attn_jvp_fwd_kernel(const __grid_constant__ FwdMaps maps, const __grid_constant__ FwdGeom geom,
+                        float* __restrict__ out, float* __restrict__ out_t, float* __restrict__ lse_out,
+                        float* __restrict__ mu_out, int* status) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -277,9 +292,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int n_qtiles = geom.n_qtiles, kv_start = geom.kv_start, kv_len = geom.kv_len;
+  const float scale = geom.scale;
   const int bh = blockIdx.x / n_qtiles;
+  const int hh = bh % geom.H, bb = bh / geom.H;
   const int q0 = (blockIdx.x % n_qtiles) * C::kBM;
   const int n_tiles = (kv_len + C::kBN - 1) / C::kBN;
+
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -317,8 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&maps.kt);
       mbar_arrive_expect_tx(&bars->q_full, 2 * C::kQBytes);
       for (int c = 0; c < C::kDC; ++c) {
-        tma_load_3d(smem + C::kOffQ + c * C::kChunkQ, &maps.q, &bars->q_full, c * 64, q0, bh);
-        tma_load_3d(smem + C::kOffQt + c * C::kChunkQ, &maps.qt, &bars->q_full, c * 64, q0, bh);
+        tma_load_4d(smem + C::kOffQ + c * C::kChunkQ, &maps.q, &bars->q_full, c * 64, q0, hh, bb);
+        tma_load_4d(smem + C::kOffQt + c * C::kChunkQ, &maps.qt, &bars->q_full, c * 64, q0, hh, bb);
       }
       int issued = 0;
       bool ok = true;
@@ -330,8 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int key0 = kv_start + t * C::kBN;
         mbar_arrive_expect_tx(&bars->k_full[s], C::kKStage);
         for (int c = 0; c < C::kDC; ++c) {
-          tma_load_3d(st + c * C::kChunkK, &maps.k, &bars->k_full[s], c * 64, key0, bh);
-          tma_load_3d(st + (C::kDC + c) * C::kChunkK, &maps.kt, &bars->k_full[s], c * 64, key0, bh);
+          tma_load_4d(st + c * C::kChunkK, &maps.k, &bars->k_full[s], c * 64, key0, hh, bb);
+          tma_load_4d(st + (C::kDC + c) * C::kChunkK, &maps.kt, &bars->k_full[s], c * 64, key0, hh, bb);
         }
         issued = t + 1;
       }
@@ -358,8 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int key0 = kv_start + t * C::kBN;
         mbar_arrive_expect_tx(&bars->v_full[s], C::kVStage);
         for (int c = 0; c < C::kDC; ++c) {
-          tma_load_3d(st + c * C::kChunkK, &maps.v, &bars->v_full[s], c * 64, key0, bh);
-          tma_load_3d(st + (C::kDC + c) * C::kChunkK, &maps.vt, &bars->v_full[s], c * 64, key0, bh);
+          tma_load_4d(st + c * C::kChunkK, &maps.v, &bars->v_full[s], c * 64, key0, hh, bb);
+          tma_load_4d(st + (C::kDC + c) * C::kChunkK, &maps.vt, &bars->v_full[s], c * 64, key0, hh, bb);
         }
         issued = t + 1;
       }
@@ -509,7 +528,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       tc_fence_after_sync();
-      write_row<D>(lane_addr, st, bh, N, q0 + row, out, out_t, lse_out, mu_out);
+      const int qrow = q0 + row;
+      const int64_t obase = static_cast<int64_t>(bb) * geom.o_stride[0] +
+                            static_cast<int64_t>(qrow) * geom.o_stride[1] +
+                            static_cast<int64_t>(hh) * geom.o_stride[2];
+      write_row<D>(lane_addr, st, static_cast<int64_t>(bh) * geom.Nq + qrow, obase, qrow < geom.Nq, geom.d, out,
+                   out_t, lse_out, mu_out);
     }
   }
 
@@ -521,14 +545,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-cudaError_t make_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t N, int64_t d, int box_rows) {
+// 4-D map over (column, sequence row, head, batch) with the tensor's strides
+// (elements; the column stride is 1).  A dimension of extent 1 is never
+// stepped, so its stride is replaced by the tensor's span to keep it a valid
+// TMA stride whatever the caller passed.  Columns past ``d`` (d < 64) and rows
+// past ``rows`` read as zero.
+cudaError_t make_map(CUtensorMap* map, const void* ptr, int64_t d, int64_t rows, int64_t H, int64_t B,
+                     const int64_t stride[3], int box_rows) {
   TensorMapEncodeFn enc = tensor_map_encoder();
   if (!enc) return cudaErrorNotSupported;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+  const int64_t extent[3] = {rows, H, B};
+  int64_t st[3] = {stride[1], stride[2], stride[0]};  // sequence, head, batch
+  int64_t span = d;
+  for (int i = 0; i < 3; ++i)
+    if (extent[i] > 1 && extent[i] * st[i] > span) span = extent[i] * st[i];
+  for (int i = 0; i < 3; ++i)
+    if (extent[i] == 1) st[i] = (span + 7) / 8 * 8;
+  cuuint64_t gdim[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t gstr[3] = {static_cast<cuuint64_t>(st[0]) * 2, static_cast<cuuint64_t>(st[1]) * 2,
+                        static_cast<cuuint64_t>(st[2]) * 2};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), gdim, gstr, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -538,13 +577,17 @@ template <int D>
 cudaError_t launch_d(const FwdArgs& a, const char** msg) {
   using C = FwdCfg<D>;
   FwdMaps maps;
+  FwdGeom geom;
   cudaError_t e = cudaSuccess;
   const void* ptrs[6] = {a.q, a.q_t, a.k, a.k_t, a.v, a.v_t};
   CUtensorMap* dst[6] = {&maps.q, &maps.qt, &maps.k, &maps.kt, &maps.v, &maps.vt};
-  for (int i = 0; i < 6 && e == cudaSuccess; ++i)
-    e = make_map(dst[i], ptrs[i], a.BH, a.N, D, i < 2 ? C::kBM : C::kBN);
+  for (int i = 0; i < 6 && e == cudaSuccess; ++i) {
+    const bool query = i < 2;
+    e = make_map(dst[i], ptrs[i], a.d, query ? a.Nq : a.Nkv, a.H, a.B, query ? a.q_stride : a.kv_stride,
+                 query ? C::kBM : C::kBN);
+  }
   if (e != cudaSuccess) {
-    *msg = "cuTensorMapEncodeTiled rejected a tensor (alignment or size)";
+    *msg = "cuTensorMapEncodeTiled rejected a tensor (alignment, stride or size)";
     return e;
   }
   static bool attr_set[2] = {false, false};
@@ -557,11 +600,18 @@ cudaError_t launch_d(const FwdArgs& a, const char** msg) {
     }
     attr_set[D == 128] = true;
   }
-  const int n_qtiles = static_cast<int>((a.N + C::kBM - 1) / C::kBM);
-  const int64_t grid = static_cast<int64_t>(n_qtiles) * a.BH;
-  kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, a.stream>>>(
-      maps, a.out, a.out_t, a.lse, a.mu, static_cast<int>(a.N), n_qtiles, static_cast<int>(a.kv_start),
-      static_cast<int>(a.kv_len), a.scale, a.status);
+  const int n_qtiles = static_cast<int>((a.Nq + C::kBM - 1) / C::kBM);
+  geom.H = static_cast<int>(a.H);
+  geom.Nq = static_cast<int>(a.Nq);
+  geom.n_qtiles = n_qtiles;
+  geom.kv_start = static_cast<int>(a.kv_start);
+  geom.kv_len = static_cast<int>(a.kv_len);
+  geom.d = static_cast<int>(a.d);
+  geom.scale = a.scale;
+  for (int i = 0; i < 3; ++i) geom.o_stride[i] = a.o_stride[i];
+  const int64_t grid = static_cast<int64_t>(n_qtiles) * a.B * a.H;
+  kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, a.stream>>>(maps, geom, a.out, a.out_t, a.lse, a.mu,
+                                                                           a.status);
   e = cudaGetLastError();
   if (e != cudaSuccess) *msg = "attention-JVP kernel launch failed";
   return e;
@@ -571,7 +621,7 @@ cudaError_t launch_d(const FwdArgs& a, const char** msg) {
 
 cudaError_t launch_attn_jvp_fwd(const FwdArgs& a, const char** msg) {
   if (a.d == 128) return launch_d<128>(a, msg);
-  if (a.d == 64) return launch_d<64>(a, msg);
+  if (a.d == 16 || a.d == 32 || a.d == 64) return launch_d<64>(a, msg);
   *msg = "unsupported head dimension";
   return cudaErrorInvalidValue;
 }

@@ -67,6 +67,15 @@ int* status_word(const char** why) {
   return g_status_ptr[dev];
 }
 
+int check_head_dim(int64_t d) {
+  if (d == 16 || d == 32 || d == 64 || d == 128) return ATTNJVP_OK;
+  if (d == 256)
+    return fail(ATTNJVP_EUNSUPPORTED,
+                "head dim 256 not supported: the fp32 O and Ot accumulators of 128 query rows would fill all 512 "
+                "tensor-memory columns, leaving none for the scores");
+  return fail(ATTNJVP_EUNSUPPORTED, "head dim %lld not supported (this build: 16, 32, 64, 128)", (long long)d);
+}
+
 int check_attn_args(const void* q, const void* k, const void* v, const void* q_t, const void* k_t, const void* v_t,
                     const float* out, const float* out_t, const float* lse, const float* mu, int64_t B, int64_t H,
                     int64_t N, int64_t d, float scale) {
@@ -84,16 +93,23 @@ int check_attn_args(const void* q, const void* k, const void* v, const void* q_t
   if (B * H >= (int64_t(1) << 31) || N >= (int64_t(1) << 31))
     return fail(ATTNJVP_EINVAL, "B*H and N must be < 2^31");
   if (!std::isfinite(scale) || !(scale > 0.f)) return fail(ATTNJVP_EINVAL, "scale must be finite and > 0");
-  if (d != 64 && d != 128)
-    return fail(ATTNJVP_EUNSUPPORTED, "head dim %lld not supported (this build: 64, 128)", (long long)d);
+  int rc = check_head_dim(d);
+  if (rc != ATTNJVP_OK) return rc;
   const int64_t n_qtiles = (N + 127) / 128;
   if (n_qtiles * B * H >= (int64_t(1) << 31)) return fail(ATTNJVP_EINVAL, "too many query tiles");
   return ATTNJVP_OK;
 }
 
+// Element strides (batch, sequence, head) of a contiguous [B, H, N, d] tensor.
+void contiguous_strides(int64_t H, int64_t N, int64_t d, int64_t st[3]) {
+  st[0] = H * N * d;
+  st[1] = d;
+  st[2] = N * d;
+}
+
 int run_fwd(const void* q, const void* k, const void* v, const void* q_t, const void* k_t, const void* v_t,
-            float* out, float* out_t, float* lse, float* mu, int64_t B, int64_t H, int64_t N, int64_t d, float scale,
-            int64_t kv_start, int64_t kv_len, void* stream) {
+            float* out, float* out_t, float* lse, float* mu, int64_t B, int64_t H, int64_t Nq, int64_t Nkv,
+            int64_t d, const int64_t* strides, float scale, int64_t kv_start, int64_t kv_len, void* stream) {
   const char* why = "";
   int* st = status_word(&why);
   if (!st) return fail(ATTNJVP_ECUDA, "no CUDA device / status word: %s", why);
@@ -108,9 +124,22 @@ int run_fwd(const void* q, const void* k, const void* v, const void* q_t, const 
   a.out_t = out_t;
   a.lse = lse;
   a.mu = mu;
-  a.BH = B * H;
-  a.N = N;
+  a.B = B;
+  a.H = H;
+  a.Nq = Nq;
+  a.Nkv = Nkv;
   a.d = d;
+  if (strides) {
+    for (int i = 0; i < 3; ++i) {
+      a.q_stride[i] = strides[i];
+      a.kv_stride[i] = strides[3 + i];
+      a.o_stride[i] = strides[6 + i];
+    }
+  } else {
+    contiguous_strides(H, Nq, d, a.q_stride);
+    contiguous_strides(H, Nkv, d, a.kv_stride);
+    contiguous_strides(H, Nq, d, a.o_stride);
+  }
   a.scale = scale;
   a.kv_start = kv_start;
   a.kv_len = kv_len;
@@ -151,7 +180,7 @@ int attn_jvp_fwd(const void* q, const void* k, const void* v, const void* q_t, c
                  float scale, void* stream) {
   int rc = check_attn_args(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, d, scale);
   if (rc != ATTNJVP_OK) return rc;
-  return run_fwd(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, d, scale, 0, N, stream);
+  return run_fwd(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, N, d, nullptr, scale, 0, N, stream);
 }
 
 int attn_jvp_fwd_chunk(const void* q, const void* k, const void* v, const void* q_t, const void* k_t,
@@ -163,7 +192,35 @@ int attn_jvp_fwd_chunk(const void* q, const void* k, const void* v, const void* 
   if (kv_start < 0 || kv_len < 1 || kv_start + kv_len > N)
     return fail(ATTNJVP_EINVAL, "key range [%lld, %lld) outside [0, %lld) or empty", (long long)kv_start,
                 (long long)(kv_start + kv_len), (long long)N);
-  return run_fwd(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, d, scale, kv_start, kv_len, stream);
+  return run_fwd(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, N, d, nullptr, scale, kv_start, kv_len,
+                 stream);
+}
+
+int attn_jvp_fwd_strided(const void* q, const void* k, const void* v, const void* q_t, const void* k_t,
+                         const void* v_t, float* out, float* out_t, float* lse, float* mu, int64_t B, int64_t H,
+                         int64_t Nq, int64_t Nkv, int64_t d, const int64_t* strides, float scale, int64_t kv_start,
+                         int64_t kv_len, void* stream) {
+  int rc = check_attn_args(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, Nq, d, scale);
+  if (rc != ATTNJVP_OK) return rc;
+  if (Nkv < 1 || Nkv >= (int64_t(1) << 31)) return fail(ATTNJVP_EINVAL, "N_kv must be in [1, 2^31)");
+  if (kv_start < 0 || kv_len < 1 || kv_start + kv_len > Nkv)
+    return fail(ATTNJVP_EINVAL, "key range [%lld, %lld) outside [0, %lld) or empty", (long long)kv_start,
+                (long long)(kv_start + kv_len), (long long)Nkv);
+  if (strides) {
+    const char* what[3] = {"q", "kv", "out"};
+    for (int g = 0; g < 3; ++g) {
+      // bf16 inputs: TMA strides are multiples of 16 bytes; fp32 outputs: float4 stores.
+      const int64_t unit = g < 2 ? 8 : 4;
+      for (int i = 0; i < 3; ++i) {
+        const int64_t x = strides[3 * g + i];
+        if (x < 0 || x % unit != 0 || x >= (int64_t(1) << 38))
+          return fail(ATTNJVP_EINVAL, "%s stride %d is %lld: must be a non-negative multiple of %lld elements",
+                      what[g], i, (long long)x, (long long)unit);
+      }
+    }
+  }
+  return run_fwd(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, Nq, Nkv, d, strides, scale, kv_start, kv_len,
+                 stream);
 }
 
 int attn_jvp_merge(const float* o_c, const float* ot_c, const float* lse_c, const float* mu_c, int64_t n_chunks,

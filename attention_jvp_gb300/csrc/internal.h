@@ -12,9 +12,10 @@ namespace attnjvp {
 constexpr int kStatusTimeout = 1;
 
 struct FwdArgs {
-  const void *q, *k, *v, *q_t, *k_t, *v_t;  // bf16 [BH, N, d]
-  float *out, *out_t, *lse, *mu;            // fp32; lse/mu may be null
-  int64_t BH, N, d;
+  const void *q, *k, *v, *q_t, *k_t, *v_t;  // bf16; element (b, s, h, c) at b*st[0] + s*st[1] + h*st[2] + c
+  float *out, *out_t, *lse, *mu;            // fp32 O, Ot at the output strides; lse/mu [B, H, Nq] or null
+  int64_t B, H, Nq, Nkv, d;                 // d: the real head dimension (16, 32, 64 or 128)
+  int64_t q_stride[3], kv_stride[3], o_stride[3];  // element strides (batch, seq, head); head-dim stride 1
   float scale;
   int64_t kv_start, kv_len;
   int* status;                               // device status word

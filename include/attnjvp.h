@@ -11,7 +11,8 @@
  *     Ot_i  = sum_j P_ij vt_j + sum_j P_ij (St_ij - mu_i) v_j
  * i.e. the JVP t_o = P t_v + t_p V with t_p = P (.) t_s - (P t_s^T) P.  The
  * output tangent is a stop-gradient value: nothing here builds a graph.
- * Attention is non-causal and unmasked, with as many keys as queries.
+ * Attention is non-causal and unmasked; attn_jvp_fwd_strided allows a different
+ * number of keys than queries.
  *
  * Conventions for every entry point:
  *   - Tensors are DEVICE pointers (unless stated otherwise), row-major and
@@ -53,8 +54,8 @@ extern "C" {
  *   lse, mu                : fp32 [B, H, N] — natural-log LSE and mu; either may be
  *                            NULL when not wanted.
  *   B, H, N                : >= 1 each; B*H < 2^31 and N < 2^31.
- *   d                      : head dimension; 64 or 128 in this build
- *                            (others: ATTNJVP_EUNSUPPORTED).
+ *   d                      : head dimension; 16, 32, 64 or 128 in this build (others,
+ *                            including the page's 256: ATTNJVP_EUNSUPPORTED).
  *   scale                  : softmax scale s, finite and > 0 (the page's default is d^-1/2).
  */
 int attn_jvp_fwd(const void* q, const void* k, const void* v,
@@ -77,6 +78,42 @@ int attn_jvp_fwd_chunk(const void* q, const void* k, const void* v,
                        float* out, float* out_t, float* lse, float* mu,
                        int64_t B, int64_t H, int64_t N, int64_t d,
                        float scale, int64_t kv_start, int64_t kv_len, void* stream);
+
+/*
+ * General form: strided layouts, as many or as few keys as queries, and an
+ * optional key range.  Element (b, s, h, c) of a tensor is at
+ *     b * stride_batch + s * stride_seq + h * stride_head + c
+ * elements from its base (the head-dimension stride is 1), so [B, H, S, d],
+ * the page's [B, S, H, d], and views such as q/k/v slices of a packed
+ * [B, S, 3, H, d] tensor are all accepted without copies.
+ *   q, q_t              : bf16, N_q query rows; share the query strides.
+ *   k, k_t, v, v_t      : bf16, N_kv key rows; share the key strides (the page's
+ *                         wrapper requires tangents to have the primals' strides).
+ *   out, out_t          : fp32 O and Ot at the output strides; 16-byte aligned.
+ *   lse, mu             : fp32 [B, H, N_q] contiguous, or NULL.
+ *   B, H, N_q, N_kv     : >= 1 each (cross-attention when N_q != N_kv).
+ *   d                   : 16, 32, 64 or 128.
+ *   strides             : HOST array of 9 element strides — query (batch, seq,
+ *                         head), key (batch, seq, head), output (batch, seq,
+ *                         head) — or NULL for contiguous [B, H, N, d] everywhere.
+ *                         Input strides must be non-negative multiples of 8
+ *                         elements (16 bytes, a TMA rule), output strides
+ *                         multiples of 4; a stride is ignored when its extent is 1.
+ *                         Layouts in which output elements overlap give
+ *                         unspecified results.
+ *   kv_start, kv_len    : key range [kv_start, kv_start + kv_len) within [0, N_kv);
+ *                         the whole range gives the full result, a sub-range the
+ *                         chunk partials of attn_jvp_fwd_chunk.
+ * (The page's host wrapper hands [B, S, H, D] tensors to its kernel as
+ * transposed views together with their strides; its section 前向 (forward)
+ * allows seqlen_q != seqlen_kv and head dims {16, 32, 64, 128, 256}.)
+ */
+int attn_jvp_fwd_strided(const void* q, const void* k, const void* v,
+                         const void* q_t, const void* k_t, const void* v_t,
+                         float* out, float* out_t, float* lse, float* mu,
+                         int64_t B, int64_t H, int64_t N_q, int64_t N_kv, int64_t d,
+                         const int64_t* strides, float scale,
+                         int64_t kv_start, int64_t kv_len, void* stream);
 
 /*
  * Exact merge of C key-chunk partials into the full-row result:

@@ -35,7 +35,7 @@ def test_header_declares_the_boundary():
     for expected in ("attn_jvp_fwd", "attn_jvp_fwd_chunk", "attn_jvp_merge", "attn_jvp_cast_f32_bf16",
                      "trigflow_coeffs", "trigflow_tangent", "attn_jvp_status", "attn_jvp_last_error",
                      "attn_jvp_version", "attn_jvp_selftest_wait", "attn_jvp_fwd_split_noalloc",
-                     "attn_jvp_fwd_host", "attn_jvp_fwd_host_workspace_bytes"):
+                     "attn_jvp_fwd_host", "attn_jvp_fwd_host_workspace_bytes", "attn_jvp_fwd_strided"):
         assert expected in names
 
 
@@ -114,6 +114,42 @@ def test_trigflow_coeffs_domain(lib):
     assert e.value.code == binding.ATTNJVP_EINVAL
     with pytest.raises(binding.AttnJvpError):
         binding.trigflow_coeffs(float("nan"))
+
+
+def _strided(lib, strides=None, d=64, nq=100, nkv=300, kv=(0, 300), scale=0.1):
+    vp = ctypes.c_void_p
+    st = None if strides is None else (ctypes.c_int64 * 9)(*strides)
+    return lib.attn_jvp_fwd_strided(*[vp(256)] * 6, vp(256), vp(256), None, None, 2, 3, nq, nkv, d, st,
+                                    ctypes.c_float(scale), kv[0], kv[1], None)
+
+
+def test_strided_entry_validation_needs_no_gpu(lib):
+    E = binding
+    bshd = [nq * 3 * 64 for nq in (100,)] + [3 * 64, 64] + [300 * 3 * 64, 3 * 64, 64] + [100 * 3 * 64, 3 * 64, 64]
+    assert _strided(lib, d=256) == E.ATTNJVP_EUNSUPPORTED
+    assert b"tensor-memory" in lib.attn_jvp_last_error()
+    assert _strided(lib, d=48) == E.ATTNJVP_EUNSUPPORTED
+    assert _strided(lib, nkv=0, kv=(0, 1)) == E.ATTNJVP_EINVAL
+    assert _strided(lib, kv=(250, 51)) == E.ATTNJVP_EINVAL
+    assert _strided(lib, kv=(0, 0)) == E.ATTNJVP_EINVAL
+    bad = list(bshd)
+    bad[1] = 3 * 64 + 4  # query sequence stride: not a multiple of 8 elements (16 bytes)
+    assert _strided(lib, bad) == E.ATTNJVP_EINVAL
+    assert b"q stride 1" in lib.attn_jvp_last_error()
+    bad = list(bshd)
+    bad[5] = -64
+    assert _strided(lib, bad) == E.ATTNJVP_EINVAL
+    bad = list(bshd)
+    bad[7] = 3 * 64 + 2  # output stride: not a multiple of 4 (float4 stores)
+    assert _strided(lib, bad) == E.ATTNJVP_EINVAL
+    assert b"out stride 1" in lib.attn_jvp_last_error()
+    assert _strided(lib, scale=0.0) == E.ATTNJVP_EINVAL
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_valid_strided_call_without_device_reports_cuda_error(lib):
+    bshd = [100 * 3 * 16, 3 * 16, 16, 300 * 3 * 16, 3 * 16, 16, 100 * 3 * 16, 3 * 16, 16]
+    assert _strided(lib, bshd, d=16) == binding.ATTNJVP_ECUDA
 
 
 def _host_call(lib, ws=256, ws_bytes=1 << 40, d=128, n_chunks=1, group=0, first=256):

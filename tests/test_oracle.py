@@ -191,6 +191,26 @@ def test_query_and_key_counts_may_differ():
     assert o.shape == (1, 2, 9, 16) and _rel(o, ref) < 1e-12
 
 
+@pytest.mark.parametrize("nq,nk,d", [(9, 21, 32), (40, 7, 16)])
+def test_cross_attention_tangent_matches_autodiff_jvp(nq, nk, d):
+    # Fewer or more keys than queries and the small head dims of the page's
+    # supported set: library autodiff of naive FP64 attention.
+    q, _, _, qt, _, _ = _case(B=2, H=2, N=nq, d=d, seed=41)
+    _, k, v, _, kt, vt = _case(B=2, H=2, N=nk, d=d, seed=43)
+    s = d ** -0.5
+
+    def attn(q_, k_, v_):
+        return torch.matmul(torch.softmax(torch.matmul(q_, k_.transpose(-1, -2)) * s, dim=-1), v_)
+
+    prim = tuple(torch.from_numpy(x) for x in (q, k, v))
+    tang = tuple(torch.from_numpy(x) for x in (qt, kt, vt))
+    ref_o, ref_ot = torch.func.jvp(attn, prim, tang)
+    o, ot, _, _ = oracle.attn_jvp(q, k, v, qt, kt, vt, s)
+    assert o.shape == (2, 2, nq, d)
+    assert _rel(o, ref_o.numpy()) < 1e-12
+    assert _rel(ot, ref_ot.numpy()) < 1e-12
+
+
 @pytest.mark.parametrize("chunks", [1, 2, 4, 5])
 def test_key_chunk_merge_equals_unsplit(chunks):
     q, k, v, qt, kt, vt = _case(N=61, seed=37)
