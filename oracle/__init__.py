@@ -11,7 +11,9 @@ t_o = P t_v + t_p V, t_p = P (.) t_s - (P t_s^T) P, t_s = (t_q K^T + Q t_k^T) s;
 section 前向 (forward) for the natural-log LSE; section 时间步转换 (timestep
 conversion) for the TrigFlow wrapper coefficients and x_t = cos t x0 + sin t eps.
 The key-chunk merge is exact algebra on those definitions (the pages have no
-key split).
+key split).  The output side of a consistency step (coefficient JVP, the JVP of
+_process_output, the tangent target with its NaN masks and normalisation, the
+sCM loss) follows section 一致性模型 (consistency model), its 蒸馏代码 listing.
 
 Parity pins for every function here are in tests/test_oracle.py; none is unpinned.
 """
@@ -40,6 +42,13 @@ def _load():
         lib.oracle_trigflow_coeffs.restype = ctypes.c_int
         lib.oracle_trigflow_tangent.argtypes = [dp, dp, dp, i64, i64, dp]
         lib.oracle_trigflow_tangent.restype = ctypes.c_int
+        lib.oracle_trigflow_coeffs_jvp.argtypes = [ctypes.c_double] * 3 + [dp]
+        lib.oracle_trigflow_coeffs_jvp.restype = ctypes.c_int
+        lib.oracle_process_output_jvp.argtypes = [dp] * 6 + [i64] * 4 + [dp] * 2
+        lib.oracle_process_output_jvp.restype = ctypes.c_int
+        ip = ctypes.POINTER(ctypes.c_int)
+        lib.oracle_scm_tangent_loss.argtypes = [dp] * 6 + [ctypes.c_double] + [i64] * 4 + [dp] * 3 + [ip] * 2
+        lib.oracle_scm_tangent_loss.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -143,3 +152,65 @@ def trigflow_tangent(x0, eps, t):
     if rc != 0:
         raise RuntimeError("oracle_trigflow_tangent failed")
     return out
+
+
+def trigflow_coeffs_jvp(t, v, tau=1000.0):
+    """((c_skip, c_out, c_in, c_noise), v * d/dt of each) in FP64 at scalar time t."""
+    lib = _load()
+    out = np.empty(8)
+    rc = lib.oracle_trigflow_coeffs_jvp(float(t), float(v), float(tau), _ptr(out))
+    if rc != 0:
+        raise ValueError("trigflow_coeffs_jvp: cos t + sin t <= 0")
+    return tuple(float(x) for x in out[:4]), tuple(float(x) for x in out[4:])
+
+
+def _bcthw(x):
+    """[B, C, T, ...] -> FP64 array and its (B, C, T, HW)."""
+    x = _f64(x)
+    B, C, T = x.shape[:3]
+    HW = int(np.prod(x.shape[3:])) if x.ndim > 3 else 1
+    return x, (B, C, T, HW)
+
+
+def process_output_jvp(x, n, tx, tn, t, tt):
+    """F and its tangent from the network output: x, n (network output) and their
+    tangents tx, tn are [B, C, T, ...]; the time t and its tangent tt are [B, T]."""
+    lib = _load()
+    x, dims = _bcthw(x)
+    n, tx, tn = (_bcthw(a)[0] for a in (n, tx, tn))
+    t, tt = _f64(t), _f64(tt)
+    if not (n.shape == tx.shape == tn.shape == x.shape and t.shape == tt.shape == dims[:1] + dims[2:3]):
+        raise ValueError("process_output_jvp: inconsistent shapes")
+    F = np.empty_like(x)
+    tF = np.empty_like(x)
+    rc = lib.oracle_process_output_jvp(_ptr(x), _ptr(n), _ptr(tx), _ptr(tn), _ptr(t), _ptr(tt), *dims,
+                                       _ptr(F), _ptr(tF))
+    if rc != 0:
+        raise ValueError("process_output_jvp: bad time (need cos t + sin t > 0 and sin t != 0)")
+    return F, tF
+
+
+def scm_tangent_loss(F_theta, F_sg, F_teacher, x, tF, t, r):
+    """Tangent target and sCM loss: returns (g_n, df_dt, loss [B], nan_g [B], nan_F [B]).
+
+    Tensors are [B, C, T, ...] FP64; t is [B, T]; r is the warm-up ratio."""
+    lib = _load()
+    F_theta, dims = _bcthw(F_theta)
+    F_sg, F_teacher, x, tF = (_bcthw(a)[0] for a in (F_sg, F_teacher, x, tF))
+    t = _f64(t)
+    if not (F_sg.shape == F_teacher.shape == x.shape == tF.shape == F_theta.shape
+            and t.shape == dims[:1] + dims[2:3]):
+        raise ValueError("scm_tangent_loss: inconsistent shapes")
+    g = np.empty_like(F_theta)
+    dfdt = np.empty_like(F_theta)
+    B = dims[0]
+    loss = np.empty(B)
+    ng = np.zeros(B, dtype=np.int32)
+    nf = np.zeros(B, dtype=np.int32)
+    ip = ctypes.POINTER(ctypes.c_int)
+    rc = lib.oracle_scm_tangent_loss(_ptr(F_theta), _ptr(F_sg), _ptr(F_teacher), _ptr(x), _ptr(tF), _ptr(t),
+                                     float(r), *dims, _ptr(g), _ptr(dfdt), _ptr(loss), ng.ctypes.data_as(ip),
+                                     nf.ctypes.data_as(ip))
+    if rc != 0:
+        raise RuntimeError("oracle_scm_tangent_loss failed")
+    return g, dfdt, loss, ng.astype(bool), nf.astype(bool)

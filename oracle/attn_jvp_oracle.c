@@ -16,6 +16,9 @@
  *     of the scaled scores, one float per query row.
  *   - section 时间步转换 (timestep conversion): the RectifiedFlow_TrigFlowWrapper
  *     coefficients and the TrigFlow forward process x_t = cos t x0 + sin t eps.
+ *   - section 一致性模型 (consistency model), its 蒸馏代码 listing: the JVP of
+ *     the wrapper coefficients and of _process_output, the tangent target g
+ *     with its warm-up, NaN masks and normalisation, and the sCM loss.
  *
  * Every step below is the plain definition, computed in the order written on
  * the page: two passes over the keys for the softmax (max, then exponentials),
@@ -25,6 +28,10 @@
  * central finite differences of O and LSE, torch.func.jvp autodiff, linearity,
  * zero tangents, constant-V rows, one-key and two-key closed forms, the
  * mu shift identity, and for TrigFlow the values printed on the page.
+ * The output-side functions (tests/test_epilogue_oracle.py): finite
+ * differences, torch.func.jvp of the page's _process_output, the TrigFlow
+ * velocity of a perfect network, and closed forms of each term of the
+ * tangent target, of its normalisation, of the loss and of the NaN masks.
  */
 #include <math.h>
 #include <pthread.h>
@@ -239,6 +246,137 @@ int oracle_trigflow_tangent(const double *x0, const double *eps, const double *t
         const double s = sin(t[b]), c = cos(t[b]);
         for (int64_t i = 0; i < M; ++i)
             out[b * M + i] = -s * x0[b * M + i] + c * eps[b * M + i];
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Output side of one consistency step (section 一致性模型, consistency      */
+/* model, its 蒸馏代码 listing: student_F_withT, _process_output, the tangent */
+/* target g, its NaN masks and normalisation, and the sCM loss).             */
+/* Tensors are [B, C, T, HW] (the page's B_C_T_H_W with H and W merged); the  */
+/* time t and its tangent are given per (b, frame) as [B, T].                */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The wrapper coefficients and their tangents (the page's
+ * torch.func.jvp(self.scaling, (t,), (v,))):
+ *   out[0..3] = c_skip, c_out, c_in, c_noise at t;
+ *   out[4..7] = v * d/dt of each.
+ * With D = cos t + sin t: c_skip = c_in = 1/D, c_out = -sin t / D,
+ * c_noise = tau sin t / D, so d(1/D)/dt = -(cos t - sin t) / D^2,
+ * d(-sin t / D)/dt = -(cos t D - sin t (cos t - sin t)) / D^2 = -1 / D^2 and
+ * d(tau sin t / D)/dt = tau / D^2.
+ */
+int oracle_trigflow_coeffs_jvp(double t, double v, double tau, double *out)
+{
+    if (!out) return -1;
+    const double c = cos(t), s = sin(t);
+    const double den = c + s;
+    if (!(den > 0.0)) return -1;
+    const double den2 = den * den;
+    out[0] = 1.0 / den;
+    out[1] = -s / den;
+    out[2] = 1.0 / den;
+    out[3] = tau * s / den;
+    out[4] = v * (-(c - s) / den2);
+    out[5] = v * (-1.0 / den2);
+    out[6] = v * (-(c - s) / den2);
+    out[7] = v * (tau / den2);
+    return 0;
+}
+
+/*
+ * _process_output and its JVP, elementwise:
+ *   x0 = c_skip x + c_out n,   F = (cos t x - x0) / sin t,
+ * differentiated along (t_x, t_n, t_c_skip, t_c_out, t_t) where the
+ * coefficient tangents come from oracle_trigflow_coeffs_jvp(t, t_t):
+ *   t_x0 = t_c_skip x + c_skip t_x + t_c_out n + c_out t_n
+ *   t_F  = ((-sin t t_t x + cos t t_x - t_x0) sin t - (cos t x - x0) cos t t_t) / sin^2 t.
+ * sin t must be non-zero for every (b, frame) (t in (0, pi/2]).
+ */
+int oracle_process_output_jvp(const double *x, const double *n, const double *tx, const double *tn,
+                              const double *t, const double *tt, int64_t B, int64_t C, int64_t T,
+                              int64_t HW, double *F, double *tF)
+{
+    if (!x || !n || !tx || !tn || !t || !tt || !F || !tF || B < 0 || C < 0 || T < 0 || HW < 0) return -1;
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t f = 0; f < T; ++f) {
+            const double tm = t[b * T + f], vt = tt[b * T + f];
+            double k[8];
+            if (oracle_trigflow_coeffs_jvp(tm, vt, 1.0, k) != 0) return -1;
+            const double c = cos(tm), s = sin(tm);
+            if (s == 0.0) return -1;
+            for (int64_t ch = 0; ch < C; ++ch) {
+                const int64_t base = ((b * C + ch) * T + f) * HW;
+                for (int64_t i = 0; i < HW; ++i) {
+                    const int64_t e = base + i;
+                    const double x0 = k[0] * x[e] + k[1] * n[e];
+                    const double tx0 = k[4] * x[e] + k[0] * tx[e] + k[5] * n[e] + k[1] * tn[e];
+                    const double num = c * x[e] - x0;
+                    F[e] = num / s;
+                    tF[e] = ((-s * vt * x[e] + c * tx[e] - tx0) * s - num * c * vt) / (s * s);
+                }
+            }
+        }
+    return 0;
+}
+
+/*
+ * Tangent target, NaN masks, normalisation and the sCM loss, in the page's order:
+ *   g     = -cos t sqrt(1 - r^2 sin^2 t) (F_sg - F_teacher) - (r cos t sin t x + t_F)
+ *   df_dt = -cos t (F_sg - F_teacher) - (sin t x + t_F)                (not masked)
+ *   nan_g[b] = any element of g[b] is NaN;  nan_F[b] = any element of F_theta[b] is NaN
+ *   for a masked sample (nan_g or nan_F) g, F_theta and F_sg are taken as 0
+ *   g_n   = g / (||g[b]||_2 + 0.1)
+ *   loss[b] = sum over the sample of (F_theta - F_sg - g_n)^2
+ * r is the warm-up ratio min(1, iteration / tangent_warmup).
+ */
+int oracle_scm_tangent_loss(const double *F_theta, const double *F_sg, const double *F_teacher,
+                            const double *x, const double *tF, const double *t, double r, int64_t B,
+                            int64_t C, int64_t T, int64_t HW, double *g_n, double *dfdt, double *loss,
+                            int *nan_g, int *nan_F)
+{
+    if (!F_theta || !F_sg || !F_teacher || !x || !tF || !t || !g_n || !dfdt || !loss || !nan_g || !nan_F ||
+        B < 0 || C < 0 || T < 0 || HW < 0)
+        return -1;
+    const int64_t per = C * T * HW;
+    for (int64_t b = 0; b < B; ++b) {
+        int ng = 0, nf = 0;
+        /* g and df_dt */
+        for (int64_t ch = 0; ch < C; ++ch)
+            for (int64_t f = 0; f < T; ++f) {
+                const double tm = t[b * T + f];
+                const double c = cos(tm), s = sin(tm);
+                const double w = sqrt(1.0 - r * r * s * s);
+                const int64_t base = ((b * C + ch) * T + f) * HW;
+                for (int64_t i = 0; i < HW; ++i) {
+                    const int64_t e = base + i;
+                    const double dF = F_sg[e] - F_teacher[e];
+                    g_n[e] = -c * w * dF - (r * c * s * x[e] + tF[e]);
+                    dfdt[e] = -c * dF - (s * x[e] + tF[e]);
+                    if (isnan(g_n[e])) ng = 1;
+                    if (isnan(F_theta[e])) nf = 1;
+                }
+            }
+        nan_g[b] = ng;
+        nan_F[b] = nf;
+        const int masked = ng || nf;
+        /* norm over the sample */
+        double ss = 0.0;
+        for (int64_t e = b * per; e < (b + 1) * per; ++e) {
+            if (masked) g_n[e] = 0.0;
+            ss += g_n[e] * g_n[e];
+        }
+        const double den = sqrt(ss) + 0.1;
+        double l = 0.0;
+        for (int64_t e = b * per; e < (b + 1) * per; ++e) {
+            g_n[e] = g_n[e] / den;
+            const double a = masked ? 0.0 : F_theta[e] - F_sg[e];
+            const double d = a - g_n[e];
+            l += d * d;
+        }
+        loss[b] = l;
     }
     return 0;
 }
