@@ -49,6 +49,11 @@ def load(path=None):
                                                                           i64, i64, vp]
     lib.attn_jvp_fwd_host_workspace_bytes.argtypes = [i64] * 6
     lib.attn_jvp_fwd_host_workspace_bytes.restype = i64
+    lib.trigflow_coeffs_jvp.argtypes = [ctypes.c_double] * 3 + [ctypes.POINTER(ctypes.c_double)]
+    lib.trigflow_output_jvp.argtypes = [vp] * 8 + [i64] * 4 + [vp]
+    lib.scm_tangent_loss.argtypes = [vp] * 6 + [ctypes.c_double] + [vp] * 5 + [i64] * 4 + [vp, i64, vp]
+    lib.scm_tangent_loss_workspace_bytes.argtypes = [i64] * 4
+    lib.scm_tangent_loss_workspace_bytes.restype = i64
     lib.trigflow_coeffs.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.POINTER(ctypes.c_double)]
     lib.trigflow_tangent.argtypes = [vp, vp, vp, vp, i64, i64, vp]
     lib.attn_jvp_status.argtypes = [ctypes.c_int]
@@ -57,6 +62,7 @@ def load(path=None):
     lib.attn_jvp_version.restype = ctypes.c_char_p
     for name in ("attn_jvp_fwd", "attn_jvp_fwd_chunk", "attn_jvp_merge", "attn_jvp_cast_f32_bf16",
                  "attn_jvp_fwd_split_noalloc", "attn_jvp_fwd_host", "attn_jvp_fwd_strided",
+                 "trigflow_coeffs_jvp", "trigflow_output_jvp", "scm_tangent_loss",
                  "trigflow_coeffs", "trigflow_tangent", "attn_jvp_status", "attn_jvp_selftest_wait"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
@@ -390,3 +396,79 @@ def attn_jvp_selftest_wait(limit_ns, stream=None):
 
 def attn_jvp_version():
     return load().attn_jvp_version().decode()
+
+
+# ---- output side of one consistency step ----
+
+def trigflow_coeffs_jvp(t, v, tau=1000.0):
+    """((c_skip, c_out, c_in, c_noise), v * d/dt of each) in FP64 (host function of the library)."""
+    out = (ctypes.c_double * 8)()
+    _check("trigflow_coeffs_jvp", load().trigflow_coeffs_jvp(float(t), float(v), float(tau), out))
+    return tuple(out[:4]), tuple(out[4:])
+
+
+def _latent(t, name, shape=None):
+    _req(t, name, torch.float32, shape)
+    if t.dim() < 3:
+        raise ValueError("%s must be [B, C, T, ...]" % name)
+    return t
+
+
+def _bcthw_dims(x):
+    B, C, T = x.shape[:3]
+    HW = 1
+    for s_ in x.shape[3:]:
+        HW *= s_
+    return B, C, T, HW
+
+
+def trigflow_output_jvp(x, n, x_t, n_t, t, t_t, out=None, out_t=None, stream=None):
+    """F = (cos t x - (c_skip x + c_out n)) / sin t and its tangent; x, n, x_t, n_t are
+    fp32 [B, C, T, ...] on the GPU, t and t_t FP64 [B, T]."""
+    _latent(x, "x")
+    for nm, a in (("n", n), ("x_t", x_t), ("n_t", n_t)):
+        _latent(a, nm, x.shape)
+    B, C, T, HW = _bcthw_dims(x)
+    _req(t, "t", torch.float64, (B, T))
+    _req(t_t, "t_t", torch.float64, (B, T))
+    out = torch.empty_like(x) if out is None else _latent(out, "out", x.shape)
+    out_t = torch.empty_like(x) if out_t is None else _latent(out_t, "out_t", x.shape)
+    rc = load().trigflow_output_jvp(_ptr(x), _ptr(n), _ptr(x_t), _ptr(n_t), _ptr(t), _ptr(t_t), _ptr(out),
+                                    _ptr(out_t), B, C, T, HW, _stream(stream))
+    _check("trigflow_output_jvp", rc)
+    return out, out_t
+
+
+def scm_workspace(shape, device=None):
+    B, C, T = shape[:3]
+    HW = 1
+    for s_ in shape[3:]:
+        HW *= s_
+    n = load().scm_tangent_loss_workspace_bytes(B, C, T, HW)
+    if n < 0:
+        _check("scm_tangent_loss_workspace_bytes", int(n))
+    return torch.empty((n + 7) // 8, dtype=torch.float64, device=device or torch.device("cuda"))
+
+
+def scm_tangent_loss(F_theta, F_sg, F_teacher, x, F_t, t, r, workspace=None, stream=None):
+    """Tangent target, its NaN masks and normalisation, and the sCM loss.
+
+    Returns (g_n fp32, df_dt fp32, loss FP64 [B], nan_g bool [B], nan_F bool [B])."""
+    _latent(F_theta, "F_theta")
+    for nm, a in (("F_sg", F_sg), ("F_teacher", F_teacher), ("x", x), ("F_t", F_t)):
+        _latent(a, nm, F_theta.shape)
+    B, C, T, HW = _bcthw_dims(F_theta)
+    _req(t, "t", torch.float64, (B, T))
+    dev = F_theta.device
+    g_n = torch.empty_like(F_theta)
+    dfdt = torch.empty_like(F_theta)
+    loss = torch.empty(B, dtype=torch.float64, device=dev)
+    nan_g = torch.empty(B, dtype=torch.int32, device=dev)
+    nan_F = torch.empty(B, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = scm_workspace(tuple(F_theta.shape), dev)
+    rc = load().scm_tangent_loss(_ptr(F_theta), _ptr(F_sg), _ptr(F_teacher), _ptr(x), _ptr(F_t), _ptr(t),
+                                 float(r), _ptr(g_n), _ptr(dfdt), _ptr(loss), _ptr(nan_g), _ptr(nan_F), B, C, T,
+                                 HW, _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("scm_tangent_loss", rc)
+    return g_n, dfdt, loss, nan_g.bool(), nan_F.bool()

@@ -286,6 +286,86 @@ int trigflow_tangent(const float* x0, const float* eps, const double* t, float* 
   return ok();
 }
 
+int trigflow_coeffs_jvp(double t, double v, double tau, double* out) {
+  if (!out) return fail(ATTNJVP_EINVAL, "out is NULL");
+  if (!std::isfinite(t) || !std::isfinite(v) || !std::isfinite(tau))
+    return fail(ATTNJVP_EINVAL, "t, v and tau must be finite");
+  const double c = std::cos(t), s = std::sin(t), den = c + s;
+  if (!(den > 0.0)) return fail(ATTNJVP_EINVAL, "cos t + sin t must be > 0 (t in (-pi/4, 3pi/4))");
+  const double den2 = den * den;
+  out[0] = 1.0 / den;
+  out[1] = -s / den;
+  out[2] = 1.0 / den;
+  out[3] = tau * s / den;
+  out[4] = v * (-(c - s) / den2);
+  out[5] = v * (-1.0 / den2);
+  out[6] = v * (-(c - s) / den2);
+  out[7] = v * (tau / den2);
+  return ok();
+}
+
+namespace {
+int check_epilogue_shape(int64_t B, int64_t C, int64_t T, int64_t HW) {
+  if (B < 1 || C < 1 || T < 1 || HW < 1) return fail(ATTNJVP_EINVAL, "B, C, T, HW must be >= 1");
+  const int64_t lim = int64_t(1) << 31;
+  if (B >= lim || C >= lim || T >= lim || HW >= (int64_t(1) << 40) || B * C >= lim || B * C * T >= lim)
+    return fail(ATTNJVP_EINVAL, "B * C * T must be < 2^31 and HW < 2^40");
+  if ((B * C * T) > (int64_t(1) << 46) / HW) return fail(ATTNJVP_EINVAL, "tensor too large");
+  if (epilogue_items(B, C, T, 1) * ((HW + 2047) / 2048) >= lim) return fail(ATTNJVP_EINVAL, "tensor too large");
+  return ATTNJVP_OK;
+}
+}  // namespace
+
+int trigflow_output_jvp(const float* x, const float* n, const float* x_t, const float* n_t, const double* t,
+                        const double* t_t, float* F, float* F_t, int64_t B, int64_t C, int64_t T, int64_t HW,
+                        void* stream) {
+  const void* ptrs[8] = {x, n, x_t, n_t, t, t_t, F, F_t};
+  for (const void* p : ptrs)
+    if (!p) return fail(ATTNJVP_EINVAL, "NULL tensor");
+  for (int i = 0; i < 8; ++i)
+    if (!aligned(ptrs[i], (i == 4 || i == 5) ? 8 : 4)) return fail(ATTNJVP_EINVAL, "misaligned tensor");
+  int rc = check_epilogue_shape(B, C, T, HW);
+  if (rc != ATTNJVP_OK) return rc;
+  int dev;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(ATTNJVP_ECUDA, "no CUDA device: %s", cudaGetErrorString(e));
+  e = launch_output_jvp(x, n, x_t, n_t, t, t_t, F, F_t, B, C, T, HW, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(ATTNJVP_ECUDA, "output-JVP launch failed: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+int64_t scm_tangent_loss_workspace_bytes(int64_t B, int64_t C, int64_t T, int64_t HW) {
+  int rc = check_epilogue_shape(B, C, T, HW);
+  if (rc != ATTNJVP_OK) return rc;
+  ok();
+  return scm_workspace_doubles(B, C, T, HW) * 8;
+}
+
+int scm_tangent_loss(const float* F_theta, const float* F_sg, const float* F_teacher, const float* x,
+                     const float* F_t, const double* t, double r, float* g_n, float* df_dt, double* loss,
+                     int32_t* nan_g, int32_t* nan_F, int64_t B, int64_t C, int64_t T, int64_t HW, void* workspace,
+                     int64_t workspace_bytes, void* stream) {
+  const void* ptrs[12] = {F_theta, F_sg, F_teacher, x, F_t, t, g_n, df_dt, loss, nan_g, nan_F, workspace};
+  for (const void* p : ptrs)
+    if (!p) return fail(ATTNJVP_EINVAL, "NULL tensor or workspace");
+  for (int i = 0; i < 12; ++i)
+    if (!aligned(ptrs[i], (i == 5 || i == 8 || i == 11) ? 8 : 4)) return fail(ATTNJVP_EINVAL, "misaligned tensor");
+  if (!std::isfinite(r) || r < 0.0 || r > 1.0) return fail(ATTNJVP_EINVAL, "warm-up ratio r must be in [0, 1]");
+  int rc = check_epilogue_shape(B, C, T, HW);
+  if (rc != ATTNJVP_OK) return rc;
+  const int64_t need = scm_workspace_doubles(B, C, T, HW) * 8;
+  if (workspace_bytes < need)
+    return fail(ATTNJVP_EINVAL, "workspace holds %lld bytes, needs %lld", (long long)workspace_bytes,
+                (long long)need);
+  int dev;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(ATTNJVP_ECUDA, "no CUDA device: %s", cudaGetErrorString(e));
+  e = launch_scm_tangent_loss(F_theta, F_sg, F_teacher, x, F_t, t, r, g_n, df_dt, loss, nan_g, nan_F, B, C, T, HW,
+                              static_cast<double*>(workspace), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(ATTNJVP_ECUDA, "sCM tangent/loss launch failed: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 int attn_jvp_selftest_wait(int64_t limit_ns, void* stream) {
   if (limit_ns < 1000 || limit_ns > 2000000000) return fail(ATTNJVP_EINVAL, "limit_ns must be in [1e3, 2e9]");
   const char* why = "";

@@ -36,6 +36,17 @@ cudaError_t launch_trigflow_tangent(const float* x0, const float* eps, const dou
 
 cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t stream);
 
+// Output side of a consistency step (epilogue.cu).
+int64_t epilogue_items(int64_t B, int64_t C, int64_t T, int64_t HW);  // launch blocks
+int64_t scm_workspace_doubles(int64_t B, int64_t C, int64_t T, int64_t HW);
+cudaError_t launch_output_jvp(const float* x, const float* n, const float* tx, const float* tn, const double* t,
+                              const double* tt, float* F, float* tF, int64_t B, int64_t C, int64_t T, int64_t HW,
+                              cudaStream_t stream);
+cudaError_t launch_scm_tangent_loss(const float* F_theta, const float* F_sg, const float* F_tc, const float* x,
+                                    const float* tF, const double* t, double r, float* g_n, float* dfdt,
+                                    double* loss, int* nan_g, int* nan_F, int64_t B, int64_t C, int64_t T, int64_t HW,
+                                    double* ws, cudaStream_t stream);
+
 // Sets the calling thread's message returned by attn_jvp_last_error().
 void set_last_error(const char* msg);
 

@@ -47,6 +47,7 @@ def parse_args(argv=None):
     p.add_argument("--heads", type=int, default=None, help="override H (profiling on a smaller case)")
     p.add_argument("--skip-e2e", action="store_true")
     p.add_argument("--skip-cpu", action="store_true")
+    p.add_argument("--skip-epilogue", action="store_true", help="skip the output-side kernels' bandwidth line")
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     return p.parse_args(argv)
@@ -80,6 +81,64 @@ def load_peaks():
         return peaks, "measured"
     except (OSError, ValueError):
         return dict(FALLBACK_PEAKS), "fallback"
+
+
+def epilogue_shape(spec, min_elems=64 << 20):
+    """[B, C, T, H*W] of a latent batch with at least ``min_elems`` elements (more than
+    L2 holds in fp32): 16 channels and 21 frames when the tokens split into 21
+    frames, else one frame; a sample holds 64 * N values."""
+    per = 64 * spec["N"]
+    T = 21 if (4 * spec["N"]) % 21 == 0 else 1
+    HW = per // (16 * T)
+    B = max(1, -(-min_elems // per))
+    return B, 16, T, HW
+
+
+def measure_epilogue(spec, dev, stream, peaks, reps=10, warmup=3):
+    """Achieved bandwidth of the two output-side kernels on a latent batch larger than L2.
+
+    Algorithmic bytes per element: trigflow_output_jvp reads x, n and their tangents and
+    writes F and its tangent (24 B); scm_tangent_loss reads F_theta, F_sg, F_teacher, x and
+    F_t and writes g_n and df_dt (28 B); its second pass over g, F_theta and F_sg (16 B
+    more) is an implementation cost the figure does not credit."""
+    import torch
+    from attention_jvp_gb300 import binding
+
+    B, C, T, HW = epilogue_shape(spec)
+    shape = (B, C, T, HW)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(int(spec["seed"]) + 4242)
+    make = lambda: torch.randn(shape, generator=gen, device=dev, dtype=torch.float32)
+    x, n, xt, nt = make(), make(), make(), make()
+    t = torch.rand((B, T), generator=gen, device=dev, dtype=torch.float64) * 1.3 + 0.2
+    tt = torch.rand((B, T), generator=gen, device=dev, dtype=torch.float64)
+    F, Ft = torch.empty_like(x), torch.empty_like(x)
+    ws = binding.scm_workspace(shape, dev)
+    elems = B * C * T * HW
+    res = {"shape": [B, C, T, HW], "elements": elems}
+    ops = {
+        "trigflow_output_jvp": (24, lambda: binding.trigflow_output_jvp(x, n, xt, nt, t, tt, out=F, out_t=Ft,
+                                                                         stream=stream)),
+        "scm_tangent_loss": (28, lambda: binding.scm_tangent_loss(F, x, n, xt, nt, t, 0.5, workspace=ws,
+                                                                  stream=stream)),
+    }
+    peak = float(peaks["hbm_gbs"])
+    for name, (bpe, fn) in ops.items():
+        for _ in range(warmup):
+            fn()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        gbs = bpe * elems / (ms * 1e-3) / 1e9
+        res[name] = {"bound": "hbm", "algorithmic_bytes_per_elem": bpe, "ms": round(ms, 4),
+                     "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4)}
+    binding.attn_jvp_status()
+    return res
 
 
 def kernel_source_sha():
@@ -433,6 +492,11 @@ def run_gpu(args):
         binding.attn_jvp_status()
         del host_in, host_out, lat_in, lat_dev, lat_out, ws_host
 
+    # ---- output-side kernels (not part of the timed step): bandwidth on a batch above L2 ----
+    epi = None
+    if not args.skip_epilogue and rank == 0:
+        epi = measure_epilogue(spec, dev, stream, peaks)
+
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only) ----
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu:
@@ -462,6 +526,7 @@ def run_gpu(args):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
+            "epilogue": epi,
             "clocks": clocks,
         }
         print(json.dumps(rec))

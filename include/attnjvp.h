@@ -233,6 +233,66 @@ int64_t attn_jvp_fwd_host_workspace_bytes(int64_t B, int64_t H, int64_t N, int64
                                           int64_t n_chunks, int64_t group_heads);
 
 /*
+ * ---- Output side of one consistency step (page "带分数正则的一致性蒸馏",
+ * section 一致性模型 (consistency model), its 蒸馏代码 listing). ----
+ * Latent tensors are fp32 [B, C, T, HW] (the page's B_C_T_H_W with H and W
+ * merged), contiguous, 4-byte aligned; the time t is FP64 [B, T] (one value
+ * per batch entry and frame, broadcast over channels and pixels).
+ */
+
+/*
+ * The wrapper coefficients at time t and their tangents (the page's
+ * torch.func.jvp of its scaling function along v): out[0..3] = c_skip, c_out,
+ * c_in, c_noise (as trigflow_coeffs); out[4..7] = v * d/dt of each.  Host
+ * function, FP64.  EINVAL unless cos t + sin t > 0 and t, v, tau are finite.
+ */
+int trigflow_coeffs_jvp(double t, double v, double tau, double* out);
+
+/*
+ * The student prediction F from the network output and its tangent (the JVP
+ * of the page's _process_output):
+ *   x0 = c_skip(t) x + c_out(t) n,   F = (cos t x - x0) / sin t,
+ *   F_t = d F along (x_t, n_t, t_t), the coefficients differentiated through t.
+ *   x, n, x_t, n_t : DEVICE fp32 [B, C, T, HW]  (x = x_t of the process, n = the
+ *                    network output, and their tangents).
+ *   t, t_t         : DEVICE FP64 [B, T]; sin t must be non-zero.
+ *   F, F_t         : DEVICE fp32 [B, C, T, HW].
+ *   B * C * T < 2^31.  Coefficients are formed per frame in FP64, the
+ *   elementwise arithmetic is fp32.
+ */
+int trigflow_output_jvp(const float* x, const float* n, const float* x_t, const float* n_t,
+                        const double* t, const double* t_t, float* F, float* F_t,
+                        int64_t B, int64_t C, int64_t T, int64_t HW, void* stream);
+
+/*
+ * Tangent target and sCM loss:
+ *   g     = -cos t sqrt(1 - r^2 sin^2 t) (F_sg - F_teacher) - (r cos t sin t x + F_t)
+ *   df_dt = -cos t (F_sg - F_teacher) - (sin t x + F_t)          (never masked)
+ *   nan_g[b] / nan_F[b] = 1 when any element of sample b of g / F_theta is NaN;
+ *   a flagged sample has g, F_theta and F_sg taken as 0;
+ *   g_n   = g / (||g[b]||_2 + 0.1)                                (norm in FP64)
+ *   loss[b] = sum over sample b of (F_theta - F_sg - g_n)^2       (FP64)
+ *   F_theta, F_sg, F_teacher, x, F_t : DEVICE fp32 [B, C, T, HW] (student output,
+ *                    its stop-gradient copy, teacher output, x_t, student tangent).
+ *   t              : DEVICE FP64 [B, T].   r: warm-up ratio in [0, 1].
+ *   g_n, df_dt     : DEVICE fp32 [B, C, T, HW] outputs (g_n rounded from FP64).
+ *   loss           : DEVICE FP64 [B];  nan_g, nan_F: DEVICE int32 [B].
+ *   workspace      : DEVICE, 8-byte aligned, scm_tangent_loss_workspace_bytes()
+ *                    bytes.  Per-sample sums are reduced in a fixed order, so
+ *                    results are reproducible run to run.  The loss is formed
+ *                    as sum a^2 - 2 s sum a g + s^2 sum g^2 (a = F_theta - F_sg,
+ *                    s = 1 / (||g|| + 0.1)), exact algebra on the sum above.
+ */
+int scm_tangent_loss(const float* F_theta, const float* F_sg, const float* F_teacher,
+                     const float* x, const float* F_t, const double* t, double r,
+                     float* g_n, float* df_dt, double* loss, int32_t* nan_g, int32_t* nan_F,
+                     int64_t B, int64_t C, int64_t T, int64_t HW,
+                     void* workspace, int64_t workspace_bytes, void* stream);
+
+/* Workspace bytes scm_tangent_loss needs, or a negative ATTNJVP_E* code.  Needs no GPU. */
+int64_t scm_tangent_loss_workspace_bytes(int64_t B, int64_t C, int64_t T, int64_t HW);
+
+/*
  * Failure-path self-test.  Launches one tiny kernel on ``stream`` that waits,
  * with the same bounded-wait routine the attention kernels use, on an
  * on-chip barrier nothing ever completes; the wait gives up after

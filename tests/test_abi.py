@@ -35,7 +35,9 @@ def test_header_declares_the_boundary():
     for expected in ("attn_jvp_fwd", "attn_jvp_fwd_chunk", "attn_jvp_merge", "attn_jvp_cast_f32_bf16",
                      "trigflow_coeffs", "trigflow_tangent", "attn_jvp_status", "attn_jvp_last_error",
                      "attn_jvp_version", "attn_jvp_selftest_wait", "attn_jvp_fwd_split_noalloc",
-                     "attn_jvp_fwd_host", "attn_jvp_fwd_host_workspace_bytes", "attn_jvp_fwd_strided"):
+                     "attn_jvp_fwd_host", "attn_jvp_fwd_host_workspace_bytes", "attn_jvp_fwd_strided",
+                     "trigflow_coeffs_jvp", "trigflow_output_jvp", "scm_tangent_loss",
+                     "scm_tangent_loss_workspace_bytes"):
         assert expected in names
 
 
@@ -106,6 +108,38 @@ def test_trigflow_coeffs_match_oracle(lib, t):
     for g, r in zip(got, ref):
         assert abs(g - r) <= 1e-12 * max(abs(r), 1e-300) or abs(g - r) <= 1e-15
     assert lib.attn_jvp_last_error() == b""
+
+
+@pytest.mark.parametrize("t", [0.0, 0.2, math.pi / 4, 1.3, math.pi / 2])
+def test_trigflow_coeffs_jvp_match_oracle(lib, t):
+    vals, tans = binding.trigflow_coeffs_jvp(t, -0.7, 1000.0)
+    rv, rt = oracle.trigflow_coeffs_jvp(t, -0.7, 1000.0)
+    for g, r in zip(vals + tans, rv + rt):
+        assert abs(g - r) <= 1e-12 * max(abs(r), 1.0)
+    with pytest.raises(binding.AttnJvpError):
+        binding.trigflow_coeffs_jvp(-math.pi / 2, 1.0)
+
+
+def test_epilogue_validation_needs_no_gpu(lib):
+    E = binding
+    vp = ctypes.c_void_p
+    p4, p8 = vp(256), vp(256)
+    out8 = [p4] * 4 + [p8, p8] + [p4, p4]
+    assert lib.trigflow_output_jvp(None, *out8[1:], 2, 3, 4, 5, None) == E.ATTNJVP_EINVAL
+    assert lib.trigflow_output_jvp(*out8, 1 << 20, 1 << 10, 1 << 10, 5, None) == E.ATTNJVP_EINVAL
+    assert lib.trigflow_output_jvp(*out8, 2, 3, 4, 1 << 41, None) == E.ATTNJVP_EINVAL
+    assert lib.trigflow_output_jvp(*out8, 2, 0, 4, 5, None) == E.ATTNJVP_EINVAL
+    misaligned = [p4] * 4 + [vp(260), p8] + [p4, p4]  # t must be 8-byte aligned
+    assert lib.trigflow_output_jvp(*misaligned, 2, 3, 4, 5, None) == E.ATTNJVP_EINVAL
+    need = lib.scm_tangent_loss_workspace_bytes(2, 3, 4, 5)
+    assert need > 0 and need % 8 == 0
+    assert lib.scm_tangent_loss_workspace_bytes(2, 3, 4, 0) == E.ATTNJVP_EINVAL
+    scm = lambda r, ws, nbytes: lib.scm_tangent_loss(*[p4] * 5, p8, ctypes.c_double(r), p4, p4, p8, p4, p4,
+                                                     2, 3, 4, 5, ws, nbytes, None)
+    assert scm(1.5, p8, need) == E.ATTNJVP_EINVAL
+    assert b"warm-up" in lib.attn_jvp_last_error()
+    assert scm(0.5, p8, need - 8) == E.ATTNJVP_EINVAL
+    assert scm(0.5, None, need) == E.ATTNJVP_EINVAL
 
 
 def test_trigflow_coeffs_domain(lib):
