@@ -14,6 +14,7 @@ The key-chunk merge is exact algebra on those definitions (the pages have no
 key split).  The output side of a consistency step (coefficient JVP, the JVP of
 _process_output, the tangent target with its NaN masks and normalisation, the
 sCM loss) follows section 一致性模型 (consistency model), its 蒸馏代码 listing.
+The primal backward (dQ, dK, dV) follows section 反向 (backward).
 
 Parity pins for every function here are in tests/test_oracle.py; none is unpinned.
 """
@@ -49,6 +50,8 @@ def _load():
         ip = ctypes.POINTER(ctypes.c_int)
         lib.oracle_scm_tangent_loss.argtypes = [dp] * 6 + [ctypes.c_double] + [i64] * 4 + [dp] * 3 + [ip] * 2
         lib.oracle_scm_tangent_loss.restype = ctypes.c_int
+        lib.oracle_attn_bwd_head.argtypes = [dp] * 4 + [i64] * 3 + [ctypes.c_double] + [dp] * 3
+        lib.oracle_attn_bwd_head.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -214,3 +217,28 @@ def scm_tangent_loss(F_theta, F_sg, F_teacher, x, tF, t, r):
     if rc != 0:
         raise RuntimeError("oracle_scm_tangent_loss failed")
     return g, dfdt, loss, ng.astype(bool), nf.astype(bool)
+
+
+def attn_bwd(q, k, v, dO, scale):
+    """Primal attention backward in FP64: (dQ, dK, dV) for upstream gradient dO.
+
+    q, dO: [..., Nq, d]; k, v: [..., Nk, d] with the same leading dims (one head each)."""
+    lib = _load()
+    q, k, v, dO = (_f64(x) for x in (q, k, v, dO))
+    lead = q.shape[:-2]
+    Nq, d = q.shape[-2:]
+    Nk = k.shape[-2]
+    if not (k.shape[:-2] == v.shape[:-2] == lead and dO.shape == q.shape and k.shape[-1] == d
+            and v.shape == k.shape):
+        raise ValueError("oracle.attn_bwd: inconsistent shapes")
+    heads = int(np.prod(lead)) if lead else 1
+    qf, dOf = q.reshape(heads, Nq, d), dO.reshape(heads, Nq, d)
+    kf, vf = k.reshape(heads, Nk, d), v.reshape(heads, Nk, d)
+    dq, dk, dv = np.empty((heads, Nq, d)), np.empty((heads, Nk, d)), np.empty((heads, Nk, d))
+    for h in range(heads):
+        args = [np.ascontiguousarray(x[h]) for x in (qf, kf, vf, dOf)]
+        outs = [dq[h], dk[h], dv[h]]
+        rc = lib.oracle_attn_bwd_head(*[_ptr(a) for a in args], Nq, Nk, d, float(scale), *[_ptr(a) for a in outs])
+        if rc != 0:
+            raise RuntimeError("oracle_attn_bwd_head failed (%d)" % rc)
+    return dq.reshape(q.shape), dk.reshape(k.shape), dv.reshape(v.shape)

@@ -19,6 +19,8 @@
  *   - section 一致性模型 (consistency model), its 蒸馏代码 listing: the JVP of
  *     the wrapper coefficients and of _process_output, the tangent target g
  *     with its warm-up, NaN masks and normalisation, and the sCM loss.
+ *   - section 反向 (backward): dV = P^T dO, dP = dO V^T,
+ *     dS = P (.) (dP - rowsum(dP (.) P)), dQ = s dS K, dK = s dS^T Q.
  *
  * Every step below is the plain definition, computed in the order written on
  * the page: two passes over the keys for the softmax (max, then exponentials),
@@ -32,6 +34,9 @@
  * differences, torch.func.jvp of the page's _process_output, the TrigFlow
  * velocity of a perfect network, and closed forms of each term of the
  * tangent target, of its normalisation, of the loss and of the NaN masks.
+ * The backward (tests/test_bwd_oracle.py): torch.autograd, a central
+ * difference of <O, dO>, one key, key-shift invariance, and the rowsum
+ * identity rowsum(dP (.) P) = rowsum(dO (.) O).
  */
 #include <math.h>
 #include <pthread.h>
@@ -378,5 +383,70 @@ int oracle_scm_tangent_loss(const double *F_theta, const double *F_sg, const dou
         }
         loss[b] = l;
     }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Primal attention backward (section 反向, backward): given the upstream     */
+/* gradient dO of O = P V with P = softmax(S), S = s Q K^T,                   */
+/*   dV = P^T dO,  dP = dO V^T,  dS = P (.) (dP - rowsum(dP (.) P)),          */
+/*   dQ = s dS K,  dK = s dS^T Q.                                             */
+/* One head; q, dO [Nq, d]; k, v [Nk, d].  P is formed from S by the plain    */
+/* two-pass softmax (the page's kernel reuses the forward's LSE instead; the  */
+/* probabilities are the same).                                               */
+/* ------------------------------------------------------------------------ */
+int oracle_attn_bwd_head(const double *q, const double *k, const double *v, const double *dO, int64_t Nq,
+                         int64_t Nk, int64_t d, double scale, double *dq, double *dk, double *dv)
+{
+    if (!q || !k || !v || !dO || !dq || !dk || !dv || Nq < 1 || Nk < 1 || d < 1) return -1;
+    double *P = (double *)malloc(sizeof(double) * (size_t)(Nq * Nk));
+    double *dS = (double *)malloc(sizeof(double) * (size_t)(Nq * Nk));
+    if (!P || !dS) {
+        free(P);
+        free(dS);
+        return -2;
+    }
+    for (int64_t i = 0; i < Nq; ++i) {
+        double m = -INFINITY;
+        for (int64_t j = 0; j < Nk; ++j) {
+            double s = 0.0;
+            for (int64_t c = 0; c < d; ++c) s += q[i * d + c] * k[j * d + c];
+            P[i * Nk + j] = s * scale;
+            if (P[i * Nk + j] > m) m = P[i * Nk + j];
+        }
+        double l = 0.0;
+        for (int64_t j = 0; j < Nk; ++j) {
+            P[i * Nk + j] = exp(P[i * Nk + j] - m);
+            l += P[i * Nk + j];
+        }
+        for (int64_t j = 0; j < Nk; ++j) P[i * Nk + j] /= l;
+        /* dP_ij = dO_i . v_j, then dS = P (.) (dP - rowsum(dP (.) P)) */
+        double rs = 0.0;
+        for (int64_t j = 0; j < Nk; ++j) {
+            double dp = 0.0;
+            for (int64_t c = 0; c < d; ++c) dp += dO[i * d + c] * v[j * d + c];
+            dS[i * Nk + j] = dp;
+            rs += dp * P[i * Nk + j];
+        }
+        for (int64_t j = 0; j < Nk; ++j) dS[i * Nk + j] = P[i * Nk + j] * (dS[i * Nk + j] - rs);
+    }
+    for (int64_t i = 0; i < Nq; ++i)
+        for (int64_t c = 0; c < d; ++c) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < Nk; ++j) acc += dS[i * Nk + j] * k[j * d + c];
+            dq[i * d + c] = scale * acc;
+        }
+    for (int64_t j = 0; j < Nk; ++j)
+        for (int64_t c = 0; c < d; ++c) {
+            double ak = 0.0, av = 0.0;
+            for (int64_t i = 0; i < Nq; ++i) {
+                ak += dS[i * Nk + j] * q[i * d + c];
+                av += P[i * Nk + j] * dO[i * d + c];
+            }
+            dk[j * d + c] = scale * ak;
+            dv[j * d + c] = av;
+        }
+    free(P);
+    free(dS);
     return 0;
 }
