@@ -54,6 +54,9 @@ def load(path=None):
     lib.scm_tangent_loss.argtypes = [vp] * 6 + [ctypes.c_double] + [vp] * 5 + [i64] * 4 + [vp, i64, vp]
     lib.scm_tangent_loss_workspace_bytes.argtypes = [i64] * 4
     lib.scm_tangent_loss_workspace_bytes.restype = i64
+    lib.attn_bwd.argtypes = [vp] * 9 + [i64] * 5 + [ctypes.c_float, vp, i64, vp]
+    lib.attn_bwd_workspace_bytes.argtypes = [i64] * 3
+    lib.attn_bwd_workspace_bytes.restype = i64
     lib.trigflow_coeffs.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.POINTER(ctypes.c_double)]
     lib.trigflow_tangent.argtypes = [vp, vp, vp, vp, i64, i64, vp]
     lib.attn_jvp_status.argtypes = [ctypes.c_int]
@@ -62,7 +65,7 @@ def load(path=None):
     lib.attn_jvp_version.restype = ctypes.c_char_p
     for name in ("attn_jvp_fwd", "attn_jvp_fwd_chunk", "attn_jvp_merge", "attn_jvp_cast_f32_bf16",
                  "attn_jvp_fwd_split_noalloc", "attn_jvp_fwd_host", "attn_jvp_fwd_strided",
-                 "trigflow_coeffs_jvp", "trigflow_output_jvp", "scm_tangent_loss",
+                 "trigflow_coeffs_jvp", "trigflow_output_jvp", "scm_tangent_loss", "attn_bwd",
                  "trigflow_coeffs", "trigflow_tangent", "attn_jvp_status", "attn_jvp_selftest_wait"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
@@ -472,3 +475,43 @@ def scm_tangent_loss(F_theta, F_sg, F_teacher, x, F_t, t, r, workspace=None, str
                                  HW, _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     _check("scm_tangent_loss", rc)
     return g_n, dfdt, loss, nan_g.bool(), nan_F.bool()
+
+
+# ---- primal attention backward ----
+
+def attn_bwd(q, k, v, dout, out, lse, scale=None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """(dQ, dK, dV) of attention for the upstream gradient ``dout``.
+
+    q, dout bf16 [B, H, N_q, d]; k, v bf16 [B, H, N_kv, d]; ``out`` (fp32 O) and ``lse``
+    are the forward's outputs for the same q, k, v and scale.  fp32 dout is rounded to
+    bf16 by the library's cast kernel."""
+    if isinstance(dout, torch.Tensor) and dout.dtype == torch.float32:
+        _req(dout, "dout", torch.float32)
+        dout = attn_jvp_cast_f32_bf16(dout, stream=stream)
+    _req(q, "q", torch.bfloat16)
+    B, H, Nq, d = q.shape
+    _req(k, "k", torch.bfloat16)
+    Nkv = k.shape[2]
+    if tuple(k.shape) != (B, H, Nkv, d):
+        raise ValueError("k must be [B, H, N_kv, d] with q's B, H, d")
+    _req(v, "v", torch.bfloat16, k.shape)
+    _req(dout, "dout", torch.bfloat16, q.shape)
+    _req(out, "out", torch.float32, q.shape)
+    _req(lse, "lse", torch.float32, (B, H, Nq))
+    dq = torch.empty(q.shape, dtype=torch.float32, device=q.device) if dq is None else _req(dq, "dq", torch.float32,
+                                                                                             q.shape)
+    dk = torch.empty(k.shape, dtype=torch.float32, device=q.device) if dk is None else _req(dk, "dk", torch.float32,
+                                                                                             k.shape)
+    dv = torch.empty(k.shape, dtype=torch.float32, device=q.device) if dv is None else _req(dv, "dv", torch.float32,
+                                                                                             k.shape)
+    if workspace is None:
+        n = load().attn_bwd_workspace_bytes(B, H, Nq)
+        if n < 0:
+            _check("attn_bwd_workspace_bytes", int(n))
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+    scale = d ** -0.5 if scale is None else float(scale)
+    rc = load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(out), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                         B, H, Nq, Nkv, d, ctypes.c_float(scale), _ptr(workspace),
+                         workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("attn_bwd", rc)
+    return dq, dk, dv

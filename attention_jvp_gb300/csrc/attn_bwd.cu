@@ -1,0 +1,562 @@
+// Primal attention backward for sm_103a (tcgen05 / TMEM / TMA).
+//
+// What it computes (page "带分数正则的一致性蒸馏", section 反向 (backward)): with
+// the upstream gradient dO of O = P V, P = softmax(S), S = s Q K^T,
+//     dV = P^T dO,  dP = dO V^T,  dS = P (.) (dP - rowsum(dP (.) P)),
+//     dQ = s dS K,  dK = s dS^T Q.
+// P is rebuilt exactly from the forward's LSE (P = exp(s q.k - LSE)), and
+// rowsum(dP (.) P) is taken as rowsum(dO (.) O), the same number by
+// O = P V, computed once per query row by bwd_prep_kernel together with
+// -LSE log2 e.
+//
+// Two passes, each one CTA per 128 resident rows of one (batch, head), each
+// streaming 64-row tiles of the other side, with the same warp roles and
+// hand-offs as the forward kernel:
+//   dQ pass   (resident Q, dO; streamed K, V):  S1 = Q K^T, S2 = dO V^T,
+//             dS = P (.) (S2 - D) per query row, dQ += dS K.
+//   dK/dV pass (resident K, V; streamed Q, dO and the per-query -LSE log2 e
+//             and -D):  S1 = K Q^T, S2 = V dO^T (both transposed: TMEM lane =
+//             key), P^T and dS^T per key row, dV += P^T dO, dK += dS^T Q.
+// Warps: 0 resident loads + score-tile ring, 1 TMEM + value MMAs, 2 value-tile
+// ring, 3 S2 MMAs, 4-7 elementwise + epilogue (thread = resident row = TMEM
+// lane), 8 S1 MMAs.  The two passes recompute S and dP (14 d flops per
+// (query, key) pair instead of 10) but need no atomics, so results are
+// deterministic.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "internal.h"
+#include "sm103_ptx.cuh"
+
+namespace attnjvp {
+namespace {
+
+using namespace ptx;
+
+constexpr int kModeDQ = 0;
+constexpr int kModeDKDV = 1;
+
+template <int D, int kMode>
+struct BwdCfg {
+  static constexpr bool kDKDV = kMode == kModeDKDV;
+  static constexpr int kBM = 128;                  // resident rows per CTA (= TMEM lanes)
+  static constexpr int kBN = 64;                   // streamed rows per tile
+  static constexpr int kDC = D / 64;               // 64-element (128-byte) d-chunks
+  static constexpr int kNS = (kDKDV && D == 128) ? 1 : 3;  // S1 TMEM buffers
+  static constexpr int kNSt = 3;                   // S2 (then packed operands) TMEM buffers
+  static constexpr int kKS = (D == 128) ? 2 : 3;   // score-tile ring stages
+  static constexpr int kVS = (D == 128) ? (kDKDV ? 2 : 3) : 3;  // value-tile ring stages
+  static constexpr int kChunkR = kBM * 128;        // one d-chunk of a resident tile (bytes)
+  static constexpr int kChunkX = kBN * 128;        // one d-chunk of a streamed tile (bytes)
+  static constexpr int kRBytes = kDC * kChunkR;
+  static constexpr int kVecBytes = kDKDV ? 1024 : 0;            // per-query -LSE log2e and -D (64 + 64 floats), padded
+  static constexpr int kKStage = 2 * kDC * kChunkX;              // X1 chunks, X2 chunks
+  static constexpr int kVTensors = kDKDV ? 2 : 1;
+  // dK/dV: dO, Q, then the streamed queries' vectors (they stay until the tile's
+  // value MMAs are done, i.e. after the elementwise warps used them); dQ: K
+  static constexpr int kVStage = kVTensors * kDC * kChunkX + kVecBytes;
+  static constexpr int kOffR1 = 0;
+  static constexpr int kOffR2 = kRBytes;
+  static constexpr int kOffK = 2 * kRBytes;
+  static constexpr int kOffV = kOffK + kKS * kKStage;
+  static constexpr int kOffBar = kOffV + kVS * kVStage;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;
+  // TMEM: ACC1 [0, D) (dQ or dV), ACC2 [D, 2D) (dK), S1 buffers, S2 buffers (64 columns each)
+  static constexpr uint32_t kColAcc1 = 0;
+  static constexpr uint32_t kColAcc2 = D;
+  static constexpr uint32_t kColS = (kDKDV ? 2 : 1) * D;
+  static constexpr uint32_t kColSt = kColS + 64 * kNS;
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kColSt + 64 * kNSt <= kTmemCols, "TMEM budget");
+  static_assert(kNS <= 3 && kNSt <= 3 && kKS <= 3 && kVS <= 3, "barrier arrays");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(kKStage % 1024 == 0, "stage alignment (128-byte swizzle atoms)");
+};
+
+constexpr int kThreads = 288;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct BwdMaps {
+  CUtensorMap r1, r2, x1, x2;  // resident and streamed bf16 tiles
+  CUtensorMap nl2, nd;         // dK/dV pass: per-query -LSE log2e and -D, fp32 [B*H, Nq]
+};
+
+struct BwdGeom {
+  int H, n_rtiles, n_res, n_str;  // resident / streamed row counts
+  int nq_pad;                     // row length of the per-query vectors (N_q rounded up to 4)
+  int d;
+  float scale;
+  const float* row_nl2;           // dQ pass: per resident row (query) -LSE log2e and -D
+  const float* row_nd;
+  float* out1;                    // dQ pass: dQ;  dK/dV pass: dV
+  float* out2;                    // dK/dV pass: dK
+};
+
+struct Barriers {
+  uint64_t r_full;
+  uint64_t k_full[3], k_empty[3];
+  uint64_t v_full[3], v_empty[3];
+  uint64_t s_full[3], st_full[3], s_free[3], p_full[3], pv_done[3];
+  uint64_t drain, drain_s, drain_st;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// Elementwise step of one 64-column tile for the calling thread's resident
+// row.  cS / cSt: the row's TMEM addresses of raw S1 and S2.  dQ pass: dS in
+// cSt columns 0-31 (bf16 pairs).  dK/dV pass: P^T in 0-31 and dS^T in 32-63.
+// ``nl2`` / ``nd``: -LSE log2e and -D, per row (dQ pass, in registers) or per
+// column (dK/dV pass, 64 values each in shared memory).  kMasked: only the
+// first ``valid`` columns are real.
+template <int kMode, bool kMasked>
+__device__ __forceinline__ void bwd_tile(uint32_t cS, uint32_t cSt, int valid, float c2, float row_nl2,
+                                         float row_nd, const float* col_nl2, const float* col_nd,
+                                         uint64_t* s_free, int lane) {
+  uint32_t raw[128];
+  tmem_ld64x2_wait(cS, cSt, raw);
+  tc_fence_before_sync();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(s_free);
+  if (kMasked) {
+#pragma unroll
+    for (int i = 0; i < 64; ++i)
+      if (i >= valid) raw[i] = __float_as_uint(-INFINITY);  // weight 0
+  }
+  auto f = [&](int i) { return __uint_as_float(raw[i]); };
+  const uint64_t c2x2 = f2_pack(c2, c2);
+  uint32_t pk[32], dk[32];
+#pragma unroll
+  for (int i = 0; i < 64; i += 2) {
+    uint64_t nl, nd;
+    if (kMode == kModeDQ) {
+      nl = f2_pack(row_nl2, row_nl2);
+      nd = f2_pack(row_nd, row_nd);
+    } else {
+      const float2 a = *reinterpret_cast<const float2*>(col_nl2 + i);
+      const float2 b = *reinterpret_cast<const float2*>(col_nd + i);
+      nl = f2_pack(a.x, a.y);
+      nd = f2_pack(b.x, b.y);
+    }
+    float x0, x1;
+    f2_unpack(f2_fma(f2_pack(f(i), f(i + 1)), c2x2, nl), x0, x1);
+    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+    float d0, d1;
+    f2_unpack(f2_mul(f2_pack(p0, p1), f2_add(f2_pack(f(64 + i), f(65 + i)), nd)), d0, d1);
+    if (kMode == kModeDKDV) pk[i >> 1] = pack_bf16x2(p0, p1);
+    dk[i >> 1] = pack_bf16x2(d0, d1);
+  }
+  if (kMode == kModeDKDV) {
+    tmem_st32(cSt, pk);
+    tmem_st32(cSt + 32, dk);
+  } else {
+    tmem_st32(cSt, dk);
+  }
+  tmem_wait_st();
+  tc_fence_before_sync();
+}
+
+template <int D, int kMode>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const __grid_constant__ BwdGeom geom, int* status) {
+  using C = BwdCfg<D, kMode>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Barriers* bars = reinterpret_cast<Barriers*>(smem + C::kOffBar);
+  volatile int* abort_flag = &bars->abort_flag;
+
+  if (threadIdx.x == 0) bars->abort_flag = (*reinterpret_cast<volatile int*>(status) & kStatusTimeout) ? 1 : 0;
+  __syncthreads();
+  if (bars->abort_flag) return;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.x / geom.n_rtiles;
+  const int hh = bh % geom.H, bb = bh / geom.H;
+  const int r0 = (blockIdx.x % geom.n_rtiles) * C::kBM;
+  const int n_tiles = (geom.n_str + C::kBN - 1) / C::kBN;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->r_full, 1);
+    for (int s = 0; s < 3; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 2);  // one commit from each score issuer
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->st_full[s], 1);
+      mbar_init(&bars->p_full[s], 4);  // one arrival per elementwise warp
+      mbar_init(&bars->pv_done[s], 1);
+      mbar_init(&bars->s_free[s], 4);
+    }
+    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain_s, 1);
+    mbar_init(&bars->drain_st, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ---------------- TMA producer: resident tiles and the score-tile ring ----------------
+    if (lane == 0) {
+      prefetch_tensormap(&maps.r1);
+      prefetch_tensormap(&maps.r2);
+      prefetch_tensormap(&maps.x1);
+      prefetch_tensormap(&maps.x2);
+      mbar_arrive_expect_tx(&bars->r_full, 2 * C::kRBytes);
+      for (int c = 0; c < C::kDC; ++c) {
+        tma_load_4d(smem + C::kOffR1 + c * C::kChunkR, &maps.r1, &bars->r_full, c * 64, r0, hh, bb);
+        tma_load_4d(smem + C::kOffR2 + c * C::kChunkR, &maps.r2, &bars->r_full, c * 64, r0, hh, bb);
+      }
+      int issued = 0;
+      bool ok = true;
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        const int s = t % C::kKS;
+        ok = mbar_wait(&bars->k_empty[s], ((t / C::kKS) & 1) ^ 1, abort_flag, status, kStatusTimeout);
+        if (!ok) break;
+        uint8_t* st = smem + C::kOffK + s * C::kKStage;
+        const int row0 = t * C::kBN;
+        mbar_arrive_expect_tx(&bars->k_full[s], C::kKStage);
+        for (int c = 0; c < C::kDC; ++c) {
+          tma_load_4d(st + c * C::kChunkX, &maps.x1, &bars->k_full[s], c * 64, row0, hh, bb);
+          tma_load_4d(st + (C::kDC + c) * C::kChunkX, &maps.x2, &bars->k_full[s], c * 64, row0, hh, bb);
+        }
+        issued = t + 1;
+      }
+      if (!ok) {
+        volatile int no_abort = 0;
+        mbar_wait(&bars->r_full, 0, &no_abort, nullptr, 0);
+        for (int t = issued - C::kKS; t < issued; ++t)
+          if (t >= 0) mbar_wait(&bars->k_full[t % C::kKS], (t / C::kKS) & 1, &no_abort, nullptr, 0);
+      }
+    }
+  } else if (warp == 2) {
+    // ---------------- TMA producer: the value-tile ring ----------------
+    if (lane == 0) {
+      int issued = 0;
+      bool ok = true;
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        const int s = t % C::kVS;
+        ok = mbar_wait(&bars->v_empty[s], ((t / C::kVS) & 1) ^ 1, abort_flag, status, kStatusTimeout);
+        if (!ok) break;
+        uint8_t* st = smem + C::kOffV + s * C::kVStage;
+        const int row0 = t * C::kBN;
+        mbar_arrive_expect_tx(&bars->v_full[s], C::kVStage - (C::kDKDV ? C::kVecBytes - 512 : 0));
+        for (int c = 0; c < C::kDC; ++c) {
+          if (C::kDKDV) {  // dO (for dV), then Q (for dK)
+            tma_load_4d(st + c * C::kChunkX, &maps.x2, &bars->v_full[s], c * 64, row0, hh, bb);
+            tma_load_4d(st + (C::kDC + c) * C::kChunkX, &maps.x1, &bars->v_full[s], c * 64, row0, hh, bb);
+          } else {  // K (for dQ)
+            tma_load_4d(st + c * C::kChunkX, &maps.x1, &bars->v_full[s], c * 64, row0, hh, bb);
+          }
+        }
+        if (C::kDKDV) {  // the streamed queries' -LSE log2e and -D (256 bytes each)
+          float* vec = reinterpret_cast<float*>(st + 2 * C::kDC * C::kChunkX);
+          tma_load_2d(vec, &maps.nl2, &bars->v_full[s], row0, bh);
+          tma_load_2d(vec + 64, &maps.nd, &bars->v_full[s], row0, bh);
+        }
+        issued = t + 1;
+      }
+      if (!ok) {
+        volatile int no_abort = 0;
+        for (int t = issued - C::kVS; t < issued; ++t)
+          if (t >= 0) mbar_wait(&bars->v_full[t % C::kVS], (t / C::kVS) & 1, &no_abort, nullptr, 0);
+      }
+    }
+  } else if (warp == 1 || warp == 3 || warp == 8) {
+    // ---------------- tcgen05.mma issuers: warp 8 S1, warp 3 S2, warp 1 the value MMAs ----------------
+    if (lane == 0) {
+      constexpr uint32_t kIdS = make_idesc_bf16_f32(128, C::kBN, false, false);  // both K-major
+      constexpr uint32_t kIdPV = make_idesc_bf16_f32(128, D, false, true);      // B N-major
+      const uint64_t dR1 = make_smem_desc_sw128(smem_u32(smem + C::kOffR1), 16, 1024);
+      const uint64_t dR2 = make_smem_desc_sw128(smem_u32(smem + C::kOffR2), 16, 1024);
+      const uint64_t dK0 = make_smem_desc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
+      const uint64_t dV0 = make_smem_desc_sw128(smem_u32(smem + C::kOffV), C::kChunkX, 1024);
+      auto off = [](uint64_t desc, uint32_t bytes) { return desc + static_cast<uint64_t>(bytes >> 4); };
+      volatile int no_abort = 0;
+      if (warp == 8 || warp == 3) {
+        // S1 = R1 X1^T (warp 8) or S2 = R2 X2^T (warp 3), d-deep, N = 64.
+        const bool first = warp == 8;
+        const uint64_t dA = first ? dR1 : dR2;
+        const uint32_t xoff = first ? 0u : static_cast<uint32_t>(C::kDC * C::kChunkX);
+        bool ok = mbar_wait(&bars->r_full, 0, abort_flag, status, kStatusTimeout);
+        for (int t = 0; ok && t < n_tiles; ++t) {
+          const int s = t % C::kKS;
+          const int b = first ? t % C::kNS : t % C::kNSt;
+          ok = mbar_wait(&bars->k_full[s], (t / C::kKS) & 1, abort_flag, status, kStatusTimeout);
+          // S1 buffers are free once the elementwise warps loaded tile t - NS; S2 buffers
+          // hold the packed operands of tile t - NSt until its value MMAs are done.
+          if (ok && first && t >= C::kNS)
+            ok = mbar_wait(&bars->s_free[b], ((t - C::kNS) / C::kNS) & 1, abort_flag, status, kStatusTimeout);
+          if (ok && !first && t >= C::kNSt)
+            ok = mbar_wait(&bars->pv_done[b], ((t - C::kNSt) / C::kNSt) & 1, abort_flag, status, kStatusTimeout);
+          if (!ok) break;
+          tc_fence_after_sync();
+          const uint64_t dX = off(dK0, s * C::kKStage + xoff);
+          const uint32_t dst = tmem + (first ? C::kColS : C::kColSt) + 64u * b;
+#pragma unroll
+          for (int c = 0; c < C::kDC; ++c)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(dst, off(dA, c * C::kChunkR + kk * 32), off(dX, c * C::kChunkX + kk * 32), kIdS,
+                     (c | kk) != 0);
+          mma_commit(&bars->k_empty[s]);
+          mma_commit(first ? &bars->s_full[b] : &bars->st_full[b]);
+        }
+        uint64_t* drain = first ? &bars->drain_s : &bars->drain_st;
+        mma_commit(drain);
+        mbar_wait(drain, 0, &no_abort, nullptr, 0);
+      } else {
+        bool ok = true;
+        for (int j = 0; ok && j < n_tiles; ++j) {
+          const int bt = j % C::kNSt;
+          const int s = j % C::kVS;
+          ok = mbar_wait(&bars->p_full[bt], (j / C::kNSt) & 1, abort_flag, status, kStatusTimeout) &&
+               mbar_wait(&bars->v_full[s], (j / C::kVS) & 1, abort_flag, status, kStatusTimeout);
+          if (!ok) break;
+          tc_fence_after_sync();
+          const uint64_t dV = off(dV0, s * C::kVStage);
+          const uint32_t a0 = tmem + C::kColSt + 64u * bt;  // dQ: dS;  dK/dV: P^T (then dS^T at +32)
+#pragma unroll
+          for (int kk = 0; kk < C::kBN / 16; ++kk) {
+            const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+            if (C::kDKDV) {
+              mma_ts(tmem + C::kColAcc1, a0 + kk * 8, off(dV, kk * 2048), kIdPV, acc);  // dV += P^T dO
+              mma_ts(tmem + C::kColAcc2, a0 + 32 + kk * 8, off(dV, C::kDC * C::kChunkX + kk * 2048), kIdPV,
+                     acc);  // dK += dS^T Q
+            } else {
+              mma_ts(tmem + C::kColAcc1, a0 + kk * 8, off(dV, kk * 2048), kIdPV, acc);  // dQ += dS K
+            }
+          }
+          mma_commit(&bars->v_empty[s]);
+          mma_commit(&bars->pv_done[bt]);
+        }
+        mma_commit(&bars->drain);
+        mbar_wait(&bars->drain, 0, &no_abort, nullptr, 0);
+      }
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------- elementwise + epilogue: one resident row per thread ----------------
+    const int quarter = warp - 4;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float c2 = geom.scale * kLog2e;
+    float row_nl2 = 0.f, row_nd = 0.f;
+    if (!C::kDKDV && r0 + row < geom.n_res) {
+      const int64_t ridx = static_cast<int64_t>(bh) * geom.nq_pad + r0 + row;
+      row_nl2 = geom.row_nl2[ridx];
+      row_nd = geom.row_nd[ridx];
+    }
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int b = j % C::kNS;
+      const int bt = j % C::kNSt;
+      ok = mbar_wait(&bars->s_full[b], (j / C::kNS) & 1, abort_flag, status, kStatusTimeout) &&
+           mbar_wait(&bars->st_full[bt], (j / C::kNSt) & 1, abort_flag, status, kStatusTimeout);
+      // dK/dV pass: the streamed queries' vectors arrive with the value tiles.
+      if (C::kDKDV && ok)
+        ok = mbar_wait(&bars->v_full[j % C::kVS], (j / C::kVS) & 1, abort_flag, status, kStatusTimeout);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const uint32_t cS = lane_addr + C::kColS + 64u * b;
+      const uint32_t cSt = lane_addr + C::kColSt + 64u * bt;
+      const int valid = min(C::kBN, geom.n_str - j * C::kBN);
+      const float* vec = reinterpret_cast<const float*>(smem + C::kOffV + (j % C::kVS) * C::kVStage +
+                                                        2 * C::kDC * C::kChunkX);
+      if (valid == C::kBN)
+        bwd_tile<kMode, false>(cS, cSt, valid, c2, row_nl2, row_nd, vec, vec + 64, &bars->s_free[b], lane);
+      else
+        bwd_tile<kMode, true>(cS, cSt, valid, c2, row_nl2, row_nd, vec, vec + 64, &bars->s_free[b], lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full[bt]);
+    }
+    // ---------------- epilogue ----------------
+    if (ok) ok = mbar_wait(&bars->pv_done[(n_tiles - 1) % C::kNSt], ((n_tiles - 1) / C::kNSt) & 1, abort_flag,
+                           status, kStatusTimeout);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      tc_fence_after_sync();
+      const int rrow = r0 + row;
+      const bool valid_row = rrow < geom.n_res;
+      const int64_t obase = (static_cast<int64_t>(bh) * geom.n_res + rrow) * geom.d;
+      // dQ pass: ACC1 = dS K, times s.  dK/dV pass: ACC1 = dV, ACC2 = dS^T Q, times s.
+#pragma unroll 1
+      for (int acc = 0; acc < (C::kDKDV ? 2 : 1); ++acc) {
+        float* out = (C::kDKDV && acc == 1) ? geom.out2 : geom.out1;
+        const float mul = (C::kDKDV && acc == 0) ? 1.f : geom.scale;
+        const uint32_t col = acc == 0 ? C::kColAcc1 : C::kColAcc2;
+        const int ncols = D == 128 ? D : geom.d;
+#pragma unroll 1
+        for (int c0 = 0; c0 < ncols; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32_wait(lane_addr + col + c0, v);
+          if (valid_row) {
+            float4* o4 = reinterpret_cast<float4*>(out + obase + c0);
+            const int n4 = D == 128 ? 8 : min(8, (ncols - c0) >> 2);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              if (D != 128 && i >= n4) break;
+              o4[i] = make_float4(__uint_as_float(v[4 * i]) * mul, __uint_as_float(v[4 * i + 1]) * mul,
+                                  __uint_as_float(v[4 * i + 2]) * mul, __uint_as_float(v[4 * i + 3]) * mul);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// -LSE log2e and -D = -rowsum(dO (.) O) per query row, one warp per row,
+// stored in rows of nq_pad floats per (b, h) (16-byte TMA strides).
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ dO,
+                                                       const float* __restrict__ O, const float* __restrict__ lse,
+                                                       float* __restrict__ nl2, float* __restrict__ nd, int64_t rows,
+                                                       int64_t nq, int64_t nq_pad, int d) {
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  float s = 0.f;
+  for (int c = lane; c < d; c += 32) s = fmaf(__bfloat162float(dO[r * d + c]), O[r * d + c], s);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
+  if (lane == 0) {
+    const int64_t w = (r / nq) * nq_pad + r % nq;
+    nl2[w] = -lse[r] * kLog2e;
+    nd[w] = -s;
+  }
+}
+
+cudaError_t make_map4(CUtensorMap* map, const void* ptr, int64_t d, int64_t rows, int64_t H, int64_t B,
+                      int box_rows) {
+  TensorMapEncodeFn enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  cuuint64_t gdim[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t gstr[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(rows * d) * 2,
+                        static_cast<cuuint64_t>(H * rows * d) * 2};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), gdim, gstr, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// fp32 [BH, rows] vector map (row stride ``pitch`` floats, a multiple of 4),
+// 64-element boxes; rows past the end read as zero.
+cudaError_t make_vec_map(CUtensorMap* map, const float* ptr, int64_t rows, int64_t pitch, int64_t BH) {
+  TensorMapEncodeFn enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  cuuint64_t gdim[2] = {static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
+  cuuint64_t gstr[1] = {static_cast<cuuint64_t>(pitch) * 4};
+  cuuint32_t box[2] = {64, 1};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), gdim, gstr, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int D, int kMode>
+cudaError_t launch_pass(const BwdArgs& a, const float* nl2, const float* nd, const char** msg) {
+  using C = BwdCfg<D, kMode>;
+  const bool dkdv = kMode == kModeDKDV;
+  BwdMaps maps;
+  BwdGeom geom;
+  const int64_t n_res = dkdv ? a.Nkv : a.Nq, n_str = dkdv ? a.Nq : a.Nkv;
+  // Resident: dQ pass Q, dO; dK/dV pass K, V.  Streamed: dQ pass K, V; dK/dV pass Q, dO.
+  const void* r1 = dkdv ? a.k : a.q;
+  const void* r2 = dkdv ? a.v : a.dout;
+  const void* x1 = dkdv ? a.q : a.k;
+  const void* x2 = dkdv ? a.dout : a.v;
+  cudaError_t e = make_map4(&maps.r1, r1, a.d, n_res, a.H, a.B, C::kBM);
+  if (e == cudaSuccess) e = make_map4(&maps.r2, r2, a.d, n_res, a.H, a.B, C::kBM);
+  if (e == cudaSuccess) e = make_map4(&maps.x1, x1, a.d, n_str, a.H, a.B, C::kBN);
+  if (e == cudaSuccess) e = make_map4(&maps.x2, x2, a.d, n_str, a.H, a.B, C::kBN);
+  const int64_t nq_pad = (a.Nq + 3) / 4 * 4;
+  if (e == cudaSuccess && dkdv) e = make_vec_map(&maps.nl2, nl2, a.Nq, nq_pad, a.B * a.H);
+  if (e == cudaSuccess && dkdv) e = make_vec_map(&maps.nd, nd, a.Nq, nq_pad, a.B * a.H);
+  if (e != cudaSuccess) {
+    *msg = "cuTensorMapEncodeTiled rejected a tensor (alignment or size)";
+    return e;
+  }
+  if (!dkdv) {
+    maps.nl2 = maps.r1;  // unused by the dQ pass
+    maps.nd = maps.r1;
+  }
+  static bool attr_set[2][2] = {{false, false}, {false, false}};
+  auto kern = attn_bwd_kernel<D, kMode>;
+  if (!attr_set[D == 128][kMode]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) {
+      *msg = "cudaFuncSetAttribute(max dynamic shared memory) failed";
+      return e;
+    }
+    attr_set[D == 128][kMode] = true;
+  }
+  const int n_rtiles = static_cast<int>((n_res + C::kBM - 1) / C::kBM);
+  geom.H = static_cast<int>(a.H);
+  geom.n_rtiles = n_rtiles;
+  geom.n_res = static_cast<int>(n_res);
+  geom.n_str = static_cast<int>(n_str);
+  geom.nq_pad = static_cast<int>(nq_pad);
+  geom.d = static_cast<int>(a.d);
+  geom.scale = a.scale;
+  geom.row_nl2 = nl2;
+  geom.row_nd = nd;
+  geom.out1 = dkdv ? a.dv : a.dq;
+  geom.out2 = dkdv ? a.dk : nullptr;
+  const int64_t grid = static_cast<int64_t>(n_rtiles) * a.B * a.H;
+  kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, a.stream>>>(maps, geom, a.status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) *msg = "attention-backward kernel launch failed";
+  return e;
+}
+
+int64_t vec_floats(int64_t B, int64_t H, int64_t Nq) { return ((B * H * ((Nq + 3) / 4 * 4)) + 63) / 64 * 64; }
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdArgs& a, const char** msg) {
+  const int64_t rows = a.B * a.H * a.Nq;
+  float* nl2 = a.ws;
+  float* nd = a.ws + vec_floats(a.B, a.H, a.Nq);
+  bwd_prep_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, a.stream>>>(
+      static_cast<const __nv_bfloat16*>(a.dout), a.out, a.lse, nl2, nd, rows, a.Nq, (a.Nq + 3) / 4 * 4,
+      static_cast<int>(a.d));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *msg = "backward preprocessing launch failed";
+    return e;
+  }
+  e = launch_pass<D, kModeDKDV>(a, nl2, nd, msg);
+  if (e == cudaSuccess) e = launch_pass<D, kModeDQ>(a, nl2, nd, msg);
+  return e;
+}
+
+}  // namespace
+
+int64_t attn_bwd_workspace_floats(int64_t B, int64_t H, int64_t Nq) { return 2 * vec_floats(B, H, Nq); }
+
+cudaError_t launch_attn_bwd(const BwdArgs& a, const char** msg) {
+  if (a.d == 128) return launch_bwd_d<128>(a, msg);
+  if (a.d == 16 || a.d == 32 || a.d == 64) return launch_bwd_d<64>(a, msg);
+  *msg = "unsupported head dimension";
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace attnjvp

@@ -286,6 +286,65 @@ int trigflow_tangent(const float* x0, const float* eps, const double* t, float* 
   return ok();
 }
 
+int64_t attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N_q) {
+  if (B < 1 || H < 1 || N_q < 1) return fail(ATTNJVP_EINVAL, "B, H, N_q must be >= 1");
+  if (B * H >= (int64_t(1) << 31) || N_q >= (int64_t(1) << 31)) return fail(ATTNJVP_EINVAL, "too large");
+  ok();
+  return attn_bwd_workspace_floats(B, H, N_q) * 4;
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* dout, const float* out, const float* lse,
+             float* dq, float* dk, float* dv, int64_t B, int64_t H, int64_t N_q, int64_t N_kv, int64_t d, float scale,
+             void* workspace, int64_t workspace_bytes, void* stream) {
+  const void* in16[4] = {q, k, v, dout};
+  const char* names[4] = {"q", "k", "v", "dout"};
+  for (int i = 0; i < 4; ++i) {
+    if (!in16[i]) return fail(ATTNJVP_EINVAL, "%s is NULL", names[i]);
+    if (!aligned(in16[i], 16)) return fail(ATTNJVP_EINVAL, "%s is not 16-byte aligned (TMA base address)", names[i]);
+  }
+  if (!out || !lse || !aligned(out, 4) || !aligned(lse, 4)) return fail(ATTNJVP_EINVAL, "out/lse NULL or misaligned");
+  if (!dq || !dk || !dv || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16))
+    return fail(ATTNJVP_EINVAL, "dq/dk/dv NULL or not 16-byte aligned");
+  if (!workspace || !aligned(workspace, 256)) return fail(ATTNJVP_EINVAL, "workspace NULL or not 256-byte aligned");
+  if (B < 1 || H < 1 || N_q < 1 || N_kv < 1) return fail(ATTNJVP_EINVAL, "B, H, N_q, N_kv must be >= 1");
+  if (B * H >= (int64_t(1) << 31) || N_q >= (int64_t(1) << 31) || N_kv >= (int64_t(1) << 31))
+    return fail(ATTNJVP_EINVAL, "B*H, N_q and N_kv must be < 2^31");
+  if (!std::isfinite(scale) || !(scale > 0.f)) return fail(ATTNJVP_EINVAL, "scale must be finite and > 0");
+  int rc = check_head_dim(d);
+  if (rc != ATTNJVP_OK) return rc;
+  if (((N_q + 127) / 128) * B * H >= (int64_t(1) << 31) || ((N_kv + 127) / 128) * B * H >= (int64_t(1) << 31))
+    return fail(ATTNJVP_EINVAL, "too many row tiles");
+  const int64_t need = attn_bwd_workspace_floats(B, H, N_q) * 4;
+  if (workspace_bytes < need)
+    return fail(ATTNJVP_EINVAL, "workspace holds %lld bytes, needs %lld", (long long)workspace_bytes, (long long)need);
+  const char* why = "";
+  int* st = status_word(&why);
+  if (!st) return fail(ATTNJVP_ECUDA, "no CUDA device / status word: %s", why);
+  BwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.dout = dout;
+  a.out = out;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.B = B;
+  a.H = H;
+  a.Nq = N_q;
+  a.Nkv = N_kv;
+  a.d = d;
+  a.scale = scale;
+  a.ws = static_cast<float*>(workspace);
+  a.status = st;
+  a.stream = static_cast<cudaStream_t>(stream);
+  const char* msg = "";
+  cudaError_t e = launch_attn_bwd(a, &msg);
+  if (e != cudaSuccess) return fail(ATTNJVP_ECUDA, "%s: %s", msg, cudaGetErrorString(e));
+  return ok();
+}
+
 int trigflow_coeffs_jvp(double t, double v, double tau, double* out) {
   if (!out) return fail(ATTNJVP_EINVAL, "out is NULL");
   if (!std::isfinite(t) || !std::isfinite(v) || !std::isfinite(tau))

@@ -25,7 +25,6 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kVecPerThread = 4;                            // float4 groups per thread per block
-constexpr int64_t kChunkVec = kThreads * kVecPerThread;     // float4 groups per block (vector path)
 constexpr int64_t kChunkScalar = kThreads * 8;              // elements per block (scalar path)
 // The target pass keeps fewer groups per thread (more blocks in flight per SM).
 constexpr int kTgtVecPerThread = 4;

@@ -36,6 +36,20 @@ cudaError_t launch_trigflow_tangent(const float* x0, const float* eps, const dou
 
 cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t stream);
 
+// Primal attention backward (attn_bwd.cu); contiguous [B, H, N, d] tensors.
+struct BwdArgs {
+  const void *q, *k, *v, *dout;  // bf16
+  const float *out, *lse;        // forward's O (fp32) and natural-log LSE
+  float *dq, *dk, *dv;           // fp32
+  int64_t B, H, Nq, Nkv, d;
+  float scale;
+  float* ws;                     // attn_bwd_workspace_floats() floats
+  int* status;
+  cudaStream_t stream;
+};
+int64_t attn_bwd_workspace_floats(int64_t B, int64_t H, int64_t Nq);
+cudaError_t launch_attn_bwd(const BwdArgs& a, const char** msg);
+
 // Output side of a consistency step (epilogue.cu).
 int64_t epilogue_items(int64_t B, int64_t C, int64_t T, int64_t HW);  // launch blocks
 int64_t scm_workspace_doubles(int64_t B, int64_t C, int64_t T, int64_t HW);

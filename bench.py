@@ -48,6 +48,7 @@ def parse_args(argv=None):
     p.add_argument("--skip-e2e", action="store_true")
     p.add_argument("--skip-cpu", action="store_true")
     p.add_argument("--skip-epilogue", action="store_true", help="skip the output-side kernels' bandwidth line")
+    p.add_argument("--skip-backward", action="store_true", help="skip the primal-backward line")
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     return p.parse_args(argv)
@@ -139,6 +140,45 @@ def measure_epilogue(spec, dev, stream, peaks, reps=10, warmup=3):
                      "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4)}
     binding.attn_jvp_status()
     return res
+
+
+def measure_backward(x, spec, o, lse, dev, stream, peaks, reps=5, warmup=2):
+    """Primal attention backward on the workload's Q, K, V with a random upstream gradient.
+
+    ``tflops`` counts 10 d flops per (query, key) pair (S, dP, dV, dQ, dK), the usual
+    figure for an attention backward; the two-pass kernels execute 14 d (they form S
+    and dP in both passes), reported as ``tflops_executed``."""
+    import torch
+    from attention_jvp_gb300 import binding
+
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(int(spec["seed"]) + 777)
+    q, k, v = x["q"], x["k"], x["v"]
+    dO = torch.randn(q.shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    dq, dk, dv = (torch.empty(t.shape, dtype=torch.float32, device=dev) for t in (q, k, v))
+    n = binding.load().attn_bwd_workspace_bytes(q.shape[0], q.shape[1], q.shape[2])
+    ws = torch.empty(n, dtype=torch.uint8, device=dev)
+
+    def run():
+        binding.attn_bwd(q, k, v, dO, o, lse, scale=x["scale"], dq=dq, dk=dk, dv=dv, workspace=ws, stream=stream)
+
+    for _ in range(warmup):
+        run()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    binding.attn_jvp_status()
+    ms = e0.elapsed_time(e1) / reps
+    B, H, N, d = q.shape
+    pairs = B * H * float(N) * N
+    return {"ms": round(ms, 4), "tflops": round(10 * d * pairs / (ms * 1e-3) / 1e12, 2),
+            "tflops_executed": round(14 * d * pairs / (ms * 1e-3) / 1e12, 2),
+            "frac_of_sustained_peak": round(14 * d * pairs / (ms * 1e-3) / 1e12 / float(peaks["bf16_tflops_sustained"]), 4),
+            "flops_convention": "10 d per (query, key) pair; executed 14 d (two passes)"}
 
 
 def kernel_source_sha():
@@ -497,6 +537,11 @@ def run_gpu(args):
     if not args.skip_epilogue and rank == 0:
         epi = measure_epilogue(spec, dev, stream, peaks)
 
+    # ---- primal attention backward (not part of the timed step) ----
+    bwd = None
+    if not args.skip_backward and rank == 0 and n_chunks == 1:
+        bwd = measure_backward(x, spec, out, lse, dev, stream, peaks)
+
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only) ----
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu:
@@ -527,6 +572,7 @@ def run_gpu(args):
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
             "epilogue": epi,
+            "backward": bwd,
             "clocks": clocks,
         }
         print(json.dumps(rec))

@@ -233,6 +233,30 @@ int64_t attn_jvp_fwd_host_workspace_bytes(int64_t B, int64_t H, int64_t N, int64
                                           int64_t n_chunks, int64_t group_heads);
 
 /*
+ * Primal attention backward (page section 反向 (backward)): for the upstream
+ * gradient dO of O = softmax(s Q K^T) V,
+ *   dV = P^T dO,  dP = dO V^T,  dS = P (.) (dP - rowsum(dP (.) P)),
+ *   dQ = s dS K,  dK = s dS^T Q.
+ *   q, dout        : bf16 [B, H, N_q, d];  k, v: bf16 [B, H, N_kv, d]; 16-byte aligned.
+ *   out, lse       : the forward's O (fp32 [B, H, N_q, d]) and natural-log LSE
+ *                    (fp32 [B, H, N_q]), as attn_jvp_fwd / attn_jvp_fwd_strided
+ *                    write them.  P is rebuilt from lse; rowsum(dP (.) P) is
+ *                    taken as rowsum(dO (.) O), equal since O = P V.
+ *   dq, dk, dv     : fp32, shaped like q, k, v; 16-byte aligned.
+ *   d              : 16, 32, 64 or 128;  scale: the forward's scale.
+ *   workspace      : DEVICE, 256-byte aligned, attn_bwd_workspace_bytes(B, H, N_q).
+ * Two passes (keys resident for dK/dV, queries resident for dQ) recompute the
+ * scores instead of accumulating dQ with atomics, so results are reproducible.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* dout,
+             const float* out, const float* lse, float* dq, float* dk, float* dv,
+             int64_t B, int64_t H, int64_t N_q, int64_t N_kv, int64_t d, float scale,
+             void* workspace, int64_t workspace_bytes, void* stream);
+
+/* Workspace bytes attn_bwd needs, or a negative ATTNJVP_E* code.  Needs no GPU. */
+int64_t attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N_q);
+
+/*
  * ---- Output side of one consistency step (page "带分数正则的一致性蒸馏",
  * section 一致性模型 (consistency model), its 蒸馏代码 listing). ----
  * Latent tensors are fp32 [B, C, T, HW] (the page's B_C_T_H_W with H and W

@@ -37,7 +37,7 @@ def test_header_declares_the_boundary():
                      "attn_jvp_version", "attn_jvp_selftest_wait", "attn_jvp_fwd_split_noalloc",
                      "attn_jvp_fwd_host", "attn_jvp_fwd_host_workspace_bytes", "attn_jvp_fwd_strided",
                      "trigflow_coeffs_jvp", "trigflow_output_jvp", "scm_tangent_loss",
-                     "scm_tangent_loss_workspace_bytes"):
+                     "scm_tangent_loss_workspace_bytes", "attn_bwd", "attn_bwd_workspace_bytes"):
         assert expected in names
 
 
@@ -140,6 +140,27 @@ def test_epilogue_validation_needs_no_gpu(lib):
     assert b"warm-up" in lib.attn_jvp_last_error()
     assert scm(0.5, p8, need - 8) == E.ATTNJVP_EINVAL
     assert scm(0.5, None, need) == E.ATTNJVP_EINVAL
+
+
+def test_backward_validation_needs_no_gpu(lib):
+    E = binding
+    vp = ctypes.c_void_p
+    p = vp(256)
+    assert lib.attn_bwd_workspace_bytes(2, 3, 517) >= 2 * 4 * 2 * 3 * 520
+    assert lib.attn_bwd_workspace_bytes(0, 3, 5) == E.ATTNJVP_EINVAL
+    need = lib.attn_bwd_workspace_bytes(2, 3, 300)  # the calls below use N_q = 300
+    assert need % 256 == 0
+    call = lambda ptrs, d=128, nq=300, nkv=700, ws=p, nbytes=need, scale=0.1: lib.attn_bwd(
+        *ptrs, 2, 3, nq, nkv, d, ctypes.c_float(scale), ws, nbytes, None)
+    good = [p] * 9
+    assert call([vp(0)] + good[1:]) == E.ATTNJVP_EINVAL
+    assert call(good[:3] + [vp(264)] + good[4:]) == E.ATTNJVP_EINVAL  # dout not 16-byte aligned
+    assert b"dout" in lib.attn_jvp_last_error()
+    assert call(good, d=256) == E.ATTNJVP_EUNSUPPORTED
+    assert call(good, nkv=0) == E.ATTNJVP_EINVAL
+    assert call(good, scale=float("nan")) == E.ATTNJVP_EINVAL
+    assert call(good, nbytes=need - 4) == E.ATTNJVP_EINVAL
+    assert call(good, ws=vp(0x1040)) == E.ATTNJVP_EINVAL  # workspace not 256-byte aligned
 
 
 def test_trigflow_coeffs_domain(lib):
