@@ -416,11 +416,12 @@ int scm_tangent_loss(const float* F_theta, const float* F_sg, const float* F_tea
   if (workspace_bytes < need)
     return fail(ATTNJVP_EINVAL, "workspace holds %lld bytes, needs %lld", (long long)workspace_bytes,
                 (long long)need);
-  int dev;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fail(ATTNJVP_ECUDA, "no CUDA device: %s", cudaGetErrorString(e));
-  e = launch_scm_tangent_loss(F_theta, F_sg, F_teacher, x, F_t, t, r, g_n, df_dt, loss, nan_g, nan_F, B, C, T, HW,
-                              static_cast<double*>(workspace), static_cast<cudaStream_t>(stream));
+  const char* why = "";
+  int* st = status_word(&why);
+  if (!st) return fail(ATTNJVP_ECUDA, "no CUDA device / status word: %s", why);
+  cudaError_t e = launch_scm_tangent_loss(F_theta, F_sg, F_teacher, x, F_t, t, r, g_n, df_dt, loss, nan_g, nan_F, B,
+                                          C, T, HW, static_cast<double*>(workspace), st,
+                                          static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(ATTNJVP_ECUDA, "sCM tangent/loss launch failed: %s", cudaGetErrorString(e));
   return ok();
 }

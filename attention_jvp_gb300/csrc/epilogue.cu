@@ -19,6 +19,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "sm103_ptx.cuh"
 
 namespace attnjvp {
 namespace {
@@ -26,8 +27,8 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kVecPerThread = 4;                            // float4 groups per thread per block
 constexpr int64_t kChunkScalar = kThreads * 8;              // elements per block (scalar path)
-// The target pass keeps fewer groups per thread (more blocks in flight per SM).
-constexpr int kTgtVecPerThread = 4;
+// The fused sCM pass: one item per row of a video latent (6240 pixels).
+constexpr int kTgtVecPerThread = 8;
 
 // Row segments: a work item is (row, chunk) with row = (b * C + c) * T + f.
 struct Rows {
@@ -141,6 +142,14 @@ struct PairSum {
     hi = s;
     lo += e + pe;
   }
+  // Adds another pair: the high parts by two-sum (exact), the rest in fp32.
+  __device__ __forceinline__ void add_pair(float h2, float l2) {
+    const float s = hi + h2;
+    const float bb = s - hi;
+    const float e = (hi - (s - bb)) + (h2 - bb);
+    hi = s;
+    lo += l2 + e;
+  }
   __device__ __forceinline__ double value() const { return static_cast<double>(hi) + static_cast<double>(lo); }
 };
 
@@ -164,6 +173,42 @@ __device__ __forceinline__ float tgt_one(const TgtCoef& c, float Ft, float Fs, f
   return g;
 }
 
+// Block-wide sums of the three pairs, all in fp32 pair arithmetic (a
+// shuffle tree per warp, then the warps in order); FP64 only for the block's
+// result.  GB300's FP64 pipe is narrow enough that an FP64 tree per block
+// would cost as much as the block's memory traffic.  Valid in thread 0.
+__device__ __forceinline__ void block_sum_pairs(Acc& acc, float* red, double& gg, double& aa, double& ag) {
+  PairSum* v[3] = {&acc.gg, &acc.aa, &acc.ag};
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      const float h2 = __shfl_down_sync(0xffffffffu, v[k]->hi, o);
+      const float l2 = __shfl_down_sync(0xffffffffu, v[k]->lo, o);
+      v[k]->add_pair(h2, l2);
+    }
+  }
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();  // red is free (a previous item may still be reading it)
+  if (lane == 0) {
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      red[6 * w + 2 * k] = v[k]->hi;
+      red[6 * w + 2 * k + 1] = v[k]->lo;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    PairSum t[3];
+    for (int i = 0; i < kThreads / 32; ++i)
+#pragma unroll
+      for (int k = 0; k < 3; ++k) t[k].add_pair(red[6 * i + 2 * k], red[6 * i + 2 * k + 1]);
+    gg = t[0].value();
+    aa = t[1].value();
+    ag = t[2].value();
+  }
+}
+
 __device__ __forceinline__ double block_sum(double v, double* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
@@ -177,34 +222,102 @@ __device__ __forceinline__ double block_sum(double v, double* red) {
   return s;  // valid in thread 0
 }
 
-// Pass 1: g (unnormalised, into g_out) and df/dt; per-item sums of g^2, a^2
-// and a g (pairs per thread, FP64 across the block); the samples' NaN flags.
-__global__ void __launch_bounds__(kThreads) target_kernel(const float* __restrict__ F_theta,
-                                                          const float* __restrict__ F_sg,
-                                                          const float* __restrict__ F_tc,
-                                                          const float* __restrict__ x,
-                                                          const float* __restrict__ tF,
-                                                          const double* __restrict__ t, double r,
-                                                          float* __restrict__ g_out, float* __restrict__ dfdt,
-                                                          double* __restrict__ part, int* __restrict__ nan_g,
-                                                          int* __restrict__ nan_F, Rows rows) {
-  __shared__ TgtCoef coef;
-  __shared__ double red[kThreads / 32];
-  const int64_t item = blockIdx.x;
+// Per-frame coefficients of the target (FP64, rounded once to fp32) and the
+// per-call state: NaN flags, per-sample completion counters and ready flags,
+// and the ticket counter of the fused pass, all zeroed here.
+__global__ void __launch_bounds__(kThreads) scm_prologue_kernel(const double* __restrict__ t, double r, int64_t BT,
+                                                                int64_t B, float* __restrict__ coef,
+                                                                int* __restrict__ nan_g, int* __restrict__ nan_F,
+                                                                unsigned long long* __restrict__ done,
+                                                                unsigned long long* __restrict__ ready,
+                                                                unsigned long long* __restrict__ ticket) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  if (i < BT) {
+    double s, c;
+    sincos(t[i], &s, &c);
+    coef[4 * i + 0] = static_cast<float>(c);
+    coef[4 * i + 1] = static_cast<float>(s);
+    coef[4 * i + 2] = static_cast<float>(c * sqrt(1.0 - r * r * s * s));
+    coef[4 * i + 3] = static_cast<float>(r * c * s);
+  }
+  if (i < B) {
+    nan_g[i] = 0;
+    nan_F[i] = 0;
+    done[i] = 0;
+    ready[i] = 0;
+  }
+  if (i == 0) *ticket = 0;
+}
+
+struct ScmArgs {
+  const float *F_theta, *F_sg, *F_tc, *x, *tF;
+  const float* coef;  // [B * T][4]
+  float *g, *dfdt;
+  double *part, *scale, *loss;
+  int *nan_g, *nan_F, *status;
+  unsigned long long *done, *ready, *ticket;
+  int64_t n;  // items per sample
+  int B;
+  Rows rows;
+};
+
+// Ticket order of the fused pass, with a lag of L = min(8, B) samples: the
+// target items of samples 0 .. L-1; then, for s = L .. B-1, the target items
+// of sample s followed by the normalisation items of sample s-L; last the
+// normalisation items of samples B-L .. B-1.  A normalisation item waits for
+// its sample's scale, which the last of that sample's target items publishes;
+// all of those hold earlier tickets, and a ticket is only ever taken by a
+// running block, so every wait ends.  The lag exceeds the items a full grid
+// holds at once (about a sample and a half of rows), so the waits are rare.
+// It also means g is re-read from HBM: the traffic of the items in flight
+// alone exceeds L2, so no order that waits for a whole sample could keep g
+// there.
+struct Unit {
+  bool normalise;
+  int b;
+  int64_t item;  // item index over the whole call: b * n + (index within the sample)
+};
+
+__device__ __forceinline__ Unit unit_of(unsigned long long j, int64_t n, int B) {
+  const int64_t q = static_cast<int64_t>(j / static_cast<unsigned long long>(n));
+  const int64_t r = static_cast<int64_t>(j) - q * n;
+  const int64_t L = B < 8 ? B : 8;
+  int b;
+  bool norm;
+  if (q < L) {
+    b = static_cast<int>(q), norm = false;
+  } else if (q < 2 * int64_t(B) - L) {
+    const int64_t k = q - L;
+    if (k & 1) b = static_cast<int>(k / 2), norm = true;
+    else b = static_cast<int>(L + k / 2), norm = false;
+  } else {
+    b = static_cast<int>(q - B), norm = true;
+  }
+  return {norm, b, b * n + r};
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// One target item: g (unnormalised, into g) and df/dt; the item's sums of
+// g^2, a^2 and a g (fp32 pairs per thread, FP64 across the block) into
+// part; the sample's NaN flags.  The block that completes its sample's last
+// item reduces the sample's sums in item order and publishes scale and loss.
+__device__ __forceinline__ void target_item(const ScmArgs& A, int b, int64_t item, float* pred, double* red,
+                                            int* s_last) {
+  const Rows& rows = A.rows;
   const int64_t row = item / rows.chunks;
   const int64_t chunk = item - row * rows.chunks;
-  const int b = static_cast<int>(row / rows.CT);
-  if (threadIdx.x == 0) {
-    const int f = static_cast<int>(row % rows.T);
-    double s, c;
-    sincos(t[static_cast<int64_t>(b) * rows.T + f], &s, &c);
-    coef.cos_t = static_cast<float>(c);
-    coef.sin_t = static_cast<float>(s);
-    coef.gap = static_cast<float>(c * sqrt(1.0 - r * r * s * s));
-    coef.xcoef = static_cast<float>(r * c * s);
-  }
-  __syncthreads();
-  const TgtCoef c = coef;
+  const int f = static_cast<int>(row % rows.T);
+  const float* cp = A.coef + 4 * (static_cast<int64_t>(b) * rows.T + f);
+  const TgtCoef c{__ldg(cp + 0), __ldg(cp + 1), __ldg(cp + 2), __ldg(cp + 3)};
   const int64_t base = row * rows.HW;
   const int64_t lo = chunk * rows.chunk_elems;
   const int64_t hi = min(lo + rows.chunk_elems, rows.HW);
@@ -215,88 +328,101 @@ __global__ void __launch_bounds__(kThreads) target_kernel(const float* __restric
       const int64_t i = lo + 4 * (k * kThreads + threadIdx.x);
       if (i >= hi) break;
       const int64_t e = base + i;
-      const float4 Ft = *reinterpret_cast<const float4*>(F_theta + e);
-      const float4 Fs = *reinterpret_cast<const float4*>(F_sg + e);
-      const float4 Fc = *reinterpret_cast<const float4*>(F_tc + e);
-      const float4 xv = *reinterpret_cast<const float4*>(x + e);
-      const float4 te = *reinterpret_cast<const float4*>(tF + e);
+      const float4 Ft = *reinterpret_cast<const float4*>(A.F_theta + e);
+      const float4 Fs = *reinterpret_cast<const float4*>(A.F_sg + e);
+      const float4 Fc = *reinterpret_cast<const float4*>(A.F_tc + e);
+      const float4 xv = *reinterpret_cast<const float4*>(A.x + e);
+      const float4 te = *reinterpret_cast<const float4*>(A.tF + e);
       float4 g, d;
       g.x = tgt_one(c, Ft.x, Fs.x, Fc.x, xv.x, te.x, d.x, acc);
       g.y = tgt_one(c, Ft.y, Fs.y, Fc.y, xv.y, te.y, d.y, acc);
       g.z = tgt_one(c, Ft.z, Fs.z, Fc.z, xv.z, te.z, d.z, acc);
       g.w = tgt_one(c, Ft.w, Fs.w, Fc.w, xv.w, te.w, d.w, acc);
-      *reinterpret_cast<float4*>(g_out + e) = g;
-      *reinterpret_cast<float4*>(dfdt + e) = d;
+      *reinterpret_cast<float4*>(A.g + e) = g;
+      *reinterpret_cast<float4*>(A.dfdt + e) = d;
     }
   } else {
     for (int64_t i = lo + threadIdx.x; i < hi; i += kThreads) {
       const int64_t e = base + i;
-      g_out[e] = tgt_one(c, F_theta[e], F_sg[e], F_tc[e], x[e], tF[e], dfdt[e], acc);
+      A.g[e] = tgt_one(c, A.F_theta[e], A.F_sg[e], A.F_tc[e], A.x[e], A.tF[e], A.dfdt[e], acc);
     }
   }
-  if (__any_sync(0xffffffffu, acc.bad_g) && (threadIdx.x & 31) == 0) atomicOr(&nan_g[b], 1);
-  if (__any_sync(0xffffffffu, acc.bad_F) && (threadIdx.x & 31) == 0) atomicOr(&nan_F[b], 1);
-  const double gg = block_sum(acc.gg.value(), red);
-  const double aa = block_sum(acc.aa.value(), red);
-  const double ag = block_sum(acc.ag.value(), red);
-  if (threadIdx.x == 0) {
-    part[3 * item + 0] = gg;
-    part[3 * item + 1] = aa;
-    part[3 * item + 2] = ag;
-  }
-}
-
-// Per sample, from the item sums in a fixed order: s = 1 / (||g|| + 0.1) and
-// loss = sum (a - s g)^2 = sum a^2 - 2 s sum a g + s^2 sum g^2 (exact algebra);
-// a masked sample gets s = 0 and loss = 0 (g, F_theta and F_sg taken as 0).
-__global__ void __launch_bounds__(kThreads) finish_kernel(const double* __restrict__ part, int64_t items_per_sample,
-                                                          const int* __restrict__ nan_g,
-                                                          const int* __restrict__ nan_F, double* __restrict__ scale,
-                                                          double* __restrict__ loss) {
-  __shared__ double red[kThreads / 32];
-  const int b = blockIdx.x;
+  if (__any_sync(0xffffffffu, acc.bad_g) && (threadIdx.x & 31) == 0) atomicOr(&A.nan_g[b], 1);
+  if (__any_sync(0xffffffffu, acc.bad_F) && (threadIdx.x & 31) == 0) atomicOr(&A.nan_F[b], 1);
   double gg = 0.0, aa = 0.0, ag = 0.0;
-  const double* p = part + 3 * static_cast<int64_t>(b) * items_per_sample;
-  for (int64_t i = threadIdx.x; i < items_per_sample; i += kThreads) {
-    gg += p[3 * i + 0];
-    aa += p[3 * i + 1];
-    ag += p[3 * i + 2];
-  }
-  gg = block_sum(gg, red);
-  aa = block_sum(aa, red);
-  ag = block_sum(ag, red);
+  block_sum_pairs(acc, pred, gg, aa, ag);
   if (threadIdx.x == 0) {
-    if (nan_g[b] | nan_F[b]) {
-      scale[b] = 0.0;
-      loss[b] = 0.0;
+    A.part[3 * item + 0] = gg;
+    A.part[3 * item + 1] = aa;
+    A.part[3 * item + 2] = ag;
+    __threadfence();  // the sums and the NaN flags before the count
+    const unsigned long long prev = atomicAdd(&A.done[b], 1ull);
+    *s_last = prev + 1 == static_cast<unsigned long long>(A.n);
+  }
+  __syncthreads();
+  if (!*s_last) return;
+  // This block finished the sample: reduce its item sums in item order.
+  __threadfence();
+  double sgg = 0.0, saa = 0.0, sag = 0.0;
+  const double* p = A.part + 3 * static_cast<int64_t>(b) * A.n;
+  for (int64_t i = threadIdx.x; i < A.n; i += kThreads) {
+    sgg += __ldcg(p + 3 * i + 0);
+    saa += __ldcg(p + 3 * i + 1);
+    sag += __ldcg(p + 3 * i + 2);
+  }
+  sgg = block_sum(sgg, red);
+  saa = block_sum(saa, red);
+  sag = block_sum(sag, red);
+  if (threadIdx.x == 0) {
+    const bool masked = (__ldcg(A.nan_g + b) | __ldcg(A.nan_F + b)) != 0;
+    if (masked) {
+      A.scale[b] = 0.0;
+      A.loss[b] = 0.0;
     } else {
-      const double s = 1.0 / (sqrt(gg) + 0.1);
-      scale[b] = s;
-      loss[b] = aa - 2.0 * s * ag + s * s * gg;
+      const double s = 1.0 / (sqrt(sgg) + 0.1);
+      A.scale[b] = s;
+      A.loss[b] = saa - 2.0 * s * sag + s * s * sgg;
     }
+    st_release(&A.ready[b], masked ? 2ull : 1ull);
   }
 }
 
-// Pass 2: g_n = g s (exactly 0 for a masked sample, whatever g held).
-__global__ void __launch_bounds__(kThreads) normalize_kernel(float* __restrict__ g, const double* __restrict__ scale,
-                                                             const int* __restrict__ nan_g,
-                                                             const int* __restrict__ nan_F, Rows rows) {
-  const int64_t item = blockIdx.x;
+// One normalisation item: g_n = g s (exactly 0 for a masked sample, whatever
+// g held), once the sample's scale is published.  g is read past L1: a cache
+// line may straddle two rows, one of them written after this SM last saw it.
+// Returns false when the wait ran out.
+__device__ __forceinline__ bool normalise_item(const ScmArgs& A, int b, int64_t item, float* s_scale,
+                                               int* s_state) {
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    unsigned long long st = ld_acquire(&A.ready[b]);
+    while (st == 0) {
+      __nanosleep(256);
+      if (ptx::globaltimer_ns() - t0 > ptx::kWaitLimitNs) break;
+      st = ld_acquire(&A.ready[b]);
+    }
+    if (st == 0) atomicOr(A.status, kStatusTimeout);
+    *s_state = static_cast<int>(st);
+    *s_scale = st == 1 ? static_cast<float>(__ldcg(A.scale + b)) : 0.f;
+  }
+  __syncthreads();
+  const int state = *s_state;
+  if (state == 0) return false;
+  const bool masked = state == 2;
+  const float s = *s_scale;
+  const Rows& rows = A.rows;
   const int64_t row = item / rows.chunks;
   const int64_t chunk = item - row * rows.chunks;
-  const int b = static_cast<int>(row / rows.CT);
-  const bool masked = (nan_g[b] | nan_F[b]) != 0;
-  const float s = static_cast<float>(scale[b]);
   const int64_t base = row * rows.HW;
   const int64_t lo = chunk * rows.chunk_elems;
   const int64_t hi = min(lo + rows.chunk_elems, rows.HW);
   if (rows.vec) {
 #pragma unroll
-    for (int k = 0; k < kVecPerThread; ++k) {
+    for (int k = 0; k < kTgtVecPerThread; ++k) {
       const int64_t i = lo + 4 * (k * kThreads + threadIdx.x);
       if (i >= hi) break;
-      float4* p = reinterpret_cast<float4*>(g + base + i);
-      float4 v = *p;
+      float4* p = reinterpret_cast<float4*>(A.g + base + i);
+      float4 v = __ldcg(p);
       if (masked) {
         v = make_float4(0.f, 0.f, 0.f, 0.f);
       } else {
@@ -309,8 +435,34 @@ __global__ void __launch_bounds__(kThreads) normalize_kernel(float* __restrict__
     }
   } else {
     for (int64_t i = lo + threadIdx.x; i < hi; i += kThreads) {
-      const int64_t e = base + i;
-      g[e] = masked ? 0.f : g[e] * s;
+      float* p = A.g + base + i;
+      *p = masked ? 0.f : __ldcg(p) * s;
+    }
+  }
+  return true;
+}
+
+// The fused target / reduce / normalise pass: a persistent grid that takes
+// items by ticket (see unit_of).  Capped at 40 registers a thread for six
+// blocks an SM: more loads in flight.
+__global__ void __launch_bounds__(kThreads, 6) scm_fused_kernel(ScmArgs A) {
+  __shared__ double red[kThreads / 32];
+  __shared__ float pred[6 * (kThreads / 32)];
+  __shared__ unsigned long long s_ticket;
+  __shared__ int s_last, s_state;
+  __shared__ float s_scale;
+  const unsigned long long total = 2ull * static_cast<unsigned long long>(A.B) * static_cast<unsigned long long>(A.n);
+  for (;;) {
+    if (threadIdx.x == 0) s_ticket = atomicAdd(A.ticket, 1ull);
+    __syncthreads();
+    const unsigned long long j = s_ticket;
+    __syncthreads();  // every thread has read the ticket before it is replaced
+    if (j >= total) return;
+    const Unit u = unit_of(j, A.n, A.B);
+    if (u.normalise) {
+      if (!normalise_item(A, u.b, u.item, &s_scale, &s_state)) return;
+    } else {
+      target_item(A, u.b, u.item, pred, red, &s_last);
     }
   }
 }
@@ -322,17 +474,32 @@ bool vec_ok(int64_t HW, std::initializer_list<const void*> ptrs) {
   return true;
 }
 
+// Workspace words (8 bytes each) of scm_tangent_loss, in this order.
+struct ScmLayout {
+  int64_t part, scale, coef, done, ready, ticket, words;
+};
+
+ScmLayout scm_layout(int64_t B, int64_t C, int64_t T, int64_t HW) {
+  // the larger (scalar-path) item count, 3 sums per item
+  const int64_t items = B * C * T * make_rows(C, T, HW, false).chunks;
+  ScmLayout l;
+  l.part = 0;
+  l.scale = l.part + 3 * items;
+  l.coef = l.scale + B;  // [B * T][4] fp32
+  l.done = l.coef + 2 * B * T;
+  l.ready = l.done + B;
+  l.ticket = l.ready + B;
+  l.words = l.ticket + 1;
+  return l;
+}
+
 }  // namespace
 
 int64_t epilogue_items(int64_t B, int64_t C, int64_t T, int64_t HW) {
   return B * C * T * make_rows(C, T, HW, HW % 4 == 0).chunks;
 }
 
-int64_t scm_workspace_doubles(int64_t B, int64_t C, int64_t T, int64_t HW) {
-  // the larger (scalar-path) item count, 3 sums per item, then the per-sample scale
-  const int64_t items = B * C * T * make_rows(C, T, HW, false).chunks;
-  return 3 * items + B;
-}
+int64_t scm_workspace_doubles(int64_t B, int64_t C, int64_t T, int64_t HW) { return scm_layout(B, C, T, HW).words; }
 
 cudaError_t launch_output_jvp(const float* x, const float* n, const float* tx, const float* tn, const double* t,
                               const double* tt, float* F, float* tF, int64_t B, int64_t C, int64_t T, int64_t HW,
@@ -346,22 +513,34 @@ cudaError_t launch_output_jvp(const float* x, const float* n, const float* tx, c
 cudaError_t launch_scm_tangent_loss(const float* F_theta, const float* F_sg, const float* F_tc, const float* x,
                                     const float* tF, const double* t, double r, float* g_n, float* dfdt,
                                     double* loss, int* nan_g, int* nan_F, int64_t B, int64_t C, int64_t T, int64_t HW,
-                                    double* ws, cudaStream_t stream) {
+                                    double* ws, int* status, cudaStream_t stream) {
   const bool vec = vec_ok(HW, {F_theta, F_sg, F_tc, x, tF, g_n, dfdt});
-  const Rows rows = make_rows(C, T, HW, vec, kTgtVecPerThread);
-  const Rows nrows = make_rows(C, T, HW, vec);
-  const int64_t items_per_sample = C * T * rows.chunks;
-  const int64_t items = B * items_per_sample;
-  double* part = ws;
-  double* scale = ws + 3 * items;
-  cudaError_t e = cudaMemsetAsync(nan_g, 0, B * sizeof(int), stream);
-  if (e == cudaSuccess) e = cudaMemsetAsync(nan_F, 0, B * sizeof(int), stream);
+  const ScmLayout lay = scm_layout(B, C, T, HW);
+  ScmArgs A;
+  A.F_theta = F_theta, A.F_sg = F_sg, A.F_tc = F_tc, A.x = x, A.tF = tF;
+  A.coef = reinterpret_cast<const float*>(ws + lay.coef);
+  A.g = g_n, A.dfdt = dfdt;
+  A.part = ws + lay.part, A.scale = ws + lay.scale, A.loss = loss;
+  A.nan_g = nan_g, A.nan_F = nan_F, A.status = status;
+  A.done = reinterpret_cast<unsigned long long*>(ws + lay.done);
+  A.ready = reinterpret_cast<unsigned long long*>(ws + lay.ready);
+  A.ticket = reinterpret_cast<unsigned long long*>(ws + lay.ticket);
+  A.rows = make_rows(C, T, HW, vec, kTgtVecPerThread);
+  A.n = C * T * A.rows.chunks;
+  A.B = static_cast<int>(B);
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, scm_fused_kernel, kThreads, 0);
   if (e != cudaSuccess) return e;
-  target_kernel<<<static_cast<unsigned>(items), kThreads, 0, stream>>>(F_theta, F_sg, F_tc, x, tF, t, r, g_n, dfdt,
-                                                                      part, nan_g, nan_F, rows);
-  finish_kernel<<<static_cast<unsigned>(B), kThreads, 0, stream>>>(part, items_per_sample, nan_g, nan_F, scale, loss);
-  normalize_kernel<<<static_cast<unsigned>(B * C * T * nrows.chunks), kThreads, 0, stream>>>(g_n, scale, nan_g,
-                                                                                             nan_F, nrows);
+  const int64_t BT = B * T;
+  const int64_t pro_threads = BT > B ? BT : B;
+  scm_prologue_kernel<<<static_cast<unsigned>((pro_threads + kThreads - 1) / kThreads), kThreads, 0, stream>>>(
+      t, r, BT, B, const_cast<float*>(A.coef), nan_g, nan_F, A.done, A.ready, A.ticket);
+  const int64_t units = 2 * B * A.n;
+  int64_t grid = static_cast<int64_t>(sms) * (per_sm > 0 ? per_sm : 1);
+  if (grid > units) grid = units;
+  scm_fused_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(A);
   return cudaGetLastError();
 }
 

@@ -59,7 +59,7 @@ cudaError_t launch_output_jvp(const float* x, const float* n, const float* tx, c
 cudaError_t launch_scm_tangent_loss(const float* F_theta, const float* F_sg, const float* F_tc, const float* x,
                                     const float* tF, const double* t, double r, float* g_n, float* dfdt,
                                     double* loss, int* nan_g, int* nan_F, int64_t B, int64_t C, int64_t T, int64_t HW,
-                                    double* ws, cudaStream_t stream);
+                                    double* ws, int* status, cudaStream_t stream);
 
 // Sets the calling thread's message returned by attn_jvp_last_error().
 void set_last_error(const char* msg);

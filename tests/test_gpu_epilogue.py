@@ -100,3 +100,23 @@ def test_scm_tangent_loss_is_reproducible(cuda_lib):
     b = binding.scm_tangent_loss(*args, t, 0.5)
     torch.cuda.synchronize()
     assert torch.equal(a[0], b[0]) and torch.equal(a[2], b[2])
+
+
+def test_scm_tangent_loss_with_a_dirty_reused_workspace(cuda_lib):
+    # Many small samples (one item each, so most normalisation items wait on
+    # their sample), a workspace holding garbage, and the same workspace twice.
+    shape = (9, 1, 2, 1, 4)
+    F, Fsg, Ftc, x, Ft = (_latent(shape, 60 + i) for i in range(5))
+    t = _times(9, 2, 65)
+    F[4, 0, 1, 0, 2] = float("nan")
+    ws = binding.scm_workspace(shape[:3] + (4,), torch.device("cuda"))
+    ws.fill_(float("nan"))
+    rg, rd, rl, rng, rnf = oracle.scm_tangent_loss(_np(F), _np(Fsg), _np(Ftc), _np(x), _np(Ft), _np(t), 0.25)
+    for _ in range(2):
+        g, dfdt, loss, ng, nf = binding.scm_tangent_loss(F, Fsg, Ftc, x, Ft, t, 0.25, workspace=ws)
+        torch.cuda.synchronize()
+        assert nf.cpu().tolist() == rnf.tolist() and not ng.any().item()
+        ok = [b for b in range(9) if b != 4]
+        assert _rel(_np(g)[ok], rg[ok]) < 1e-5
+        assert np.all(_np(g)[4] == 0) and _np(loss)[4] == 0.0
+        assert np.max(np.abs(_np(loss)[ok] - rl[ok]) / rl[ok]) < 2e-5
