@@ -17,10 +17,15 @@
 //   dK/dV pass (resident K, V; streamed Q, dO and the per-query -LSE log2 e
 //             and -D):  S1 = K Q^T, S2 = V dO^T (both transposed: TMEM lane =
 //             key), P^T and dS^T per key row, dV += P^T dO, dK += dS^T Q.
-// Warps: 0 resident loads + score-tile ring, 1 TMEM + value MMAs, 2 value-tile
-// ring, 3 S2 MMAs, 4-7 elementwise + epilogue (thread = resident row = TMEM
-// lane), 8 S1 MMAs.  The two passes recompute S and dP (14 d flops per
-// (query, key) pair instead of 10) but need no atomics, so results are
+// Warps: 0 TMA (resident tiles, then per streamed tile its score stage and its
+// value stage), 1 TMEM + value MMAs, 2 S2 MMAs, 3 S1 MMAs, and two groups of
+// elementwise warps (thread = resident row = TMEM lane): 4-7 take the even
+// tiles, 8-11 the odd ones.  One group's per-tile chain (barrier waits, TMEM
+// load, exp2 and packing, TMEM store, arrival) is about as long as the tile's
+// MMAs, so a single group left the tensor pipe idle half the time; with two,
+// one group's waits overlap the other's arithmetic.  The groups split the
+// epilogue by 32-column chunks.  The two passes recompute S and dP (14 d flops
+// per (query, key) pair instead of 10) but need no atomics, so results are
 // deterministic.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -44,23 +49,35 @@ struct BwdCfg {
   static constexpr int kBN = 64;                   // streamed rows per tile
   static constexpr int kDC = D / 64;               // 64-element (128-byte) d-chunks
   static constexpr int kNS = (kDKDV && D == 128) ? 1 : 3;  // S1 TMEM buffers
-  static constexpr int kNSt = 3;                   // S2 (then packed operands) TMEM buffers
+  static constexpr int kNSt = 3;                            // S2 (then packed operands) TMEM buffers
+  // Barrier slots of the S1 ring.  Tiles alternate between the two elementwise
+  // groups; with a single buffer, consecutive tiles on one barrier would belong
+  // to different groups, and a group could test a phase parity before the
+  // previous phase completed.  Two slots (by tile parity) give each group its
+  // own barrier.  With three buffers, the group reaching tile j + 3 has
+  // finished tile j + 1, so tile j's phase (issued earlier by the same thread)
+  // is complete.
+  static constexpr int kSBar = kNS == 1 ? 2 : kNS;
   static constexpr int kKS = (D == 128) ? 2 : 3;   // score-tile ring stages
   static constexpr int kVS = (D == 128) ? (kDKDV ? 2 : 3) : 3;  // value-tile ring stages
   static constexpr int kChunkR = kBM * 128;        // one d-chunk of a resident tile (bytes)
   static constexpr int kChunkX = kBN * 128;        // one d-chunk of a streamed tile (bytes)
   static constexpr int kRBytes = kDC * kChunkR;
-  static constexpr int kVecBytes = kDKDV ? 1024 : 0;            // per-query -LSE log2e and -D (64 + 64 floats), padded
   static constexpr int kKStage = 2 * kDC * kChunkX;              // X1 chunks, X2 chunks
   static constexpr int kVTensors = kDKDV ? 2 : 1;
-  // dK/dV: dO, Q, then the streamed queries' vectors (they stay until the tile's
-  // value MMAs are done, i.e. after the elementwise warps used them); dQ: K
-  static constexpr int kVStage = kVTensors * kDC * kChunkX + kVecBytes;
+  static constexpr int kVStage = kVTensors * kDC * kChunkX;      // dK/dV: dO, Q;  dQ: K
+  // dK/dV: the streamed queries' -LSE log2e and -D (64 + 64 floats) in a ring of
+  // their own, released by the elementwise warps once read (the value ring is
+  // released only by the value MMAs, two tiles later than they need it)
+  static constexpr int kVecS = 4;
+  static constexpr int kVecSlot = 512;
+  static constexpr int kVecRing = kDKDV ? kVecS * kVecSlot : 0;
   static constexpr int kOffR1 = 0;
   static constexpr int kOffR2 = kRBytes;
   static constexpr int kOffK = 2 * kRBytes;
   static constexpr int kOffV = kOffK + kKS * kKStage;
-  static constexpr int kOffBar = kOffV + kVS * kVStage;
+  static constexpr int kOffVec = kOffV + kVS * kVStage;
+  static constexpr int kOffBar = kOffVec + kVecRing;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;
   // TMEM: ACC1 [0, D) (dQ or dV), ACC2 [D, 2D) (dK), S1 buffers, S2 buffers (64 columns each)
   static constexpr uint32_t kColAcc1 = 0;
@@ -69,12 +86,12 @@ struct BwdCfg {
   static constexpr uint32_t kColSt = kColS + 64 * kNS;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kColSt + 64 * kNSt <= kTmemCols, "TMEM budget");
-  static_assert(kNS <= 3 && kNSt <= 3 && kKS <= 3 && kVS <= 3, "barrier arrays");
+  static_assert(kSBar <= 3 && kNSt <= 3 && kKS <= 3 && kVS <= 3, "barrier arrays");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static_assert(kKStage % 1024 == 0, "stage alignment (128-byte swizzle atoms)");
 };
 
-constexpr int kThreads = 288;
+constexpr int kThreads = 384;  // 12 warps
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct BwdMaps {
@@ -97,27 +114,43 @@ struct Barriers {
   uint64_t r_full;
   uint64_t k_full[3], k_empty[3];
   uint64_t v_full[3], v_empty[3];
+  uint64_t vec_full[4], vec_empty[4];
   uint64_t s_full[3], st_full[3], s_free[3], p_full[3], pv_done[3];
   uint64_t drain, drain_s, drain_st;
+  uint64_t acc_done;  // all value MMAs done (single use)
   uint32_t tmem_base;
   int abort_flag;
 };
 
+// 64 TMEM columns of the calling thread's lane into r[kOff .. kOff + 63].
+#define BWD_R8(o) "=r"(r[o + 0]), "=r"(r[o + 1]), "=r"(r[o + 2]), "=r"(r[o + 3]), \
+                  "=r"(r[o + 4]), "=r"(r[o + 5]), "=r"(r[o + 6]), "=r"(r[o + 7])
+template <int kOff>
+__device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, uint32_t (&r)[128]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,"
+      "%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,"
+      "%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : BWD_R8(kOff + 0), BWD_R8(kOff + 8), BWD_R8(kOff + 16), BWD_R8(kOff + 24), BWD_R8(kOff + 32),
+        BWD_R8(kOff + 40), BWD_R8(kOff + 48), BWD_R8(kOff + 56)
+      : "r"(taddr)
+      : "memory");
+}
+#undef BWD_R8
+
 // Elementwise step of one 64-column tile for the calling thread's resident
-// row.  cS / cSt: the row's TMEM addresses of raw S1 and S2.  dQ pass: dS in
-// cSt columns 0-31 (bf16 pairs).  dK/dV pass: P^T in 0-31 and dS^T in 32-63.
+// row, from raw S1 (raw[0..63]) and S2 (raw[64..127]) already loaded from
+// TMEM.  cSt: the row's TMEM address of the S2 buffer, which receives the
+// bf16 operands: dQ pass dS in columns 0-31 (bf16 pairs); dK/dV pass P^T in
+// 0-31 and dS^T in 32-63.
 // ``nl2`` / ``nd``: -LSE log2e and -D, per row (dQ pass, in registers) or per
 // column (dK/dV pass, 64 values each in shared memory).  kMasked: only the
 // first ``valid`` columns are real.
 template <int kMode, bool kMasked>
-__device__ __forceinline__ void bwd_tile(uint32_t cS, uint32_t cSt, int valid, float c2, float row_nl2,
-                                         float row_nd, const float* col_nl2, const float* col_nd,
-                                         uint64_t* s_free, int lane) {
-  uint32_t raw[128];
-  tmem_ld64x2_wait(cS, cSt, raw);
-  tc_fence_before_sync();
-  __syncwarp();
-  if (lane == 0) mbar_arrive(s_free);
+__device__ __forceinline__ void bwd_tile(uint32_t (&raw)[128], uint32_t cSt, int valid, float c2, float row_nl2,
+                                         float row_nd, const float* col_nl2, const float* col_nd) {
   if (kMasked) {
 #pragma unroll
     for (int i = 0; i < 64; ++i)
@@ -192,6 +225,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->drain, 1);
     mbar_init(&bars->drain_s, 1);
     mbar_init(&bars->drain_st, 1);
+    mbar_init(&bars->acc_done, 1);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&bars->vec_full[s], 1);
+      mbar_init(&bars->vec_empty[s], 4);  // one arrival per warp of the group that used the slot
+    }
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -204,7 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
 
   if (warp == 0) {
-    // ---------------- TMA producer: resident tiles and the score-tile ring ----------------
+    // ---------------- TMA producer: resident tiles, then the score-tile ring (X1, X2) and
+    // the value-tile ring, each refilled as soon as its own stage is free (the thread polls
+    // both; the value ring frees much later than the score ring) ----------------
     if (lane == 0) {
       prefetch_tensormap(&maps.r1);
       prefetch_tensormap(&maps.r2);
@@ -215,63 +255,81 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(smem + C::kOffR1 + c * C::kChunkR, &maps.r1, &bars->r_full, c * 64, r0, hh, bb);
         tma_load_4d(smem + C::kOffR2 + c * C::kChunkR, &maps.r2, &bars->r_full, c * 64, r0, hh, bb);
       }
-      int issued = 0;
+      int tk = 0, tv = 0, tq = 0;  // next tile of each ring (tq: the vector ring)
+      const int nq = C::kDKDV ? n_tiles : 0;
       bool ok = true;
-      for (int t = 0; t < n_tiles && ok; ++t) {
-        const int s = t % C::kKS;
-        ok = mbar_wait(&bars->k_empty[s], ((t / C::kKS) & 1) ^ 1, abort_flag, status, kStatusTimeout);
-        if (!ok) break;
-        uint8_t* st = smem + C::kOffK + s * C::kKStage;
-        const int row0 = t * C::kBN;
-        mbar_arrive_expect_tx(&bars->k_full[s], C::kKStage);
-        for (int c = 0; c < C::kDC; ++c) {
-          tma_load_4d(st + c * C::kChunkX, &maps.x1, &bars->k_full[s], c * 64, row0, hh, bb);
-          tma_load_4d(st + (C::kDC + c) * C::kChunkX, &maps.x2, &bars->k_full[s], c * 64, row0, hh, bb);
+      uint64_t t0 = globaltimer_ns();
+      uint32_t idle = 0;
+      while (tk < n_tiles || tv < n_tiles || tq < nq) {
+        bool progressed = false;
+        if (tq < nq && mbar_test_wait(&bars->vec_empty[tq % C::kVecS], ((tq / C::kVecS) & 1) ^ 1)) {
+          const int sq = tq % C::kVecS;
+          float* vec = reinterpret_cast<float*>(smem + C::kOffVec + sq * C::kVecSlot);
+          mbar_arrive_expect_tx(&bars->vec_full[sq], C::kVecSlot);
+          tma_load_2d(vec, &maps.nl2, &bars->vec_full[sq], tq * C::kBN, bh);
+          tma_load_2d(vec + 64, &maps.nd, &bars->vec_full[sq], tq * C::kBN, bh);
+          ++tq;
+          progressed = true;
         }
-        issued = t + 1;
+        if (tk < n_tiles && mbar_test_wait(&bars->k_empty[tk % C::kKS], ((tk / C::kKS) & 1) ^ 1)) {
+          const int s = tk % C::kKS;
+          uint8_t* st = smem + C::kOffK + s * C::kKStage;
+          mbar_arrive_expect_tx(&bars->k_full[s], C::kKStage);
+          for (int c = 0; c < C::kDC; ++c) {
+            tma_load_4d(st + c * C::kChunkX, &maps.x1, &bars->k_full[s], c * 64, tk * C::kBN, hh, bb);
+            tma_load_4d(st + (C::kDC + c) * C::kChunkX, &maps.x2, &bars->k_full[s], c * 64, tk * C::kBN, hh, bb);
+          }
+          ++tk;
+          progressed = true;
+        }
+        if (tv < n_tiles && mbar_test_wait(&bars->v_empty[tv % C::kVS], ((tv / C::kVS) & 1) ^ 1)) {
+          const int sv = tv % C::kVS;
+          const int row0 = tv * C::kBN;
+          uint8_t* vt = smem + C::kOffV + sv * C::kVStage;
+          mbar_arrive_expect_tx(&bars->v_full[sv], C::kVStage);
+          for (int c = 0; c < C::kDC; ++c) {
+            if (C::kDKDV) {  // dO (for dV), then Q (for dK)
+              tma_load_4d(vt + c * C::kChunkX, &maps.x2, &bars->v_full[sv], c * 64, row0, hh, bb);
+              tma_load_4d(vt + (C::kDC + c) * C::kChunkX, &maps.x1, &bars->v_full[sv], c * 64, row0, hh, bb);
+            } else {  // K (for dQ)
+              tma_load_4d(vt + c * C::kChunkX, &maps.x1, &bars->v_full[sv], c * 64, row0, hh, bb);
+            }
+          }
+          ++tv;
+          progressed = true;
+        }
+        if (progressed) {
+          t0 = globaltimer_ns();
+          idle = 0;
+          continue;
+        }
+        __nanosleep(64);
+        // Bounded: a second without either ring moving means a broken protocol.
+        if ((++idle & 15u) == 0u) {
+          if (*abort_flag) {
+            ok = false;
+          } else if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(status, kStatusTimeout);
+            ok = false;
+          }
+          if (!ok) break;
+        }
       }
       if (!ok) {
+        // Let copies still in flight land before the CTA's shared memory goes away.
         volatile int no_abort = 0;
         mbar_wait(&bars->r_full, 0, &no_abort, nullptr, 0);
-        for (int t = issued - C::kKS; t < issued; ++t)
+        for (int t = tk - C::kKS; t < tk; ++t)
           if (t >= 0) mbar_wait(&bars->k_full[t % C::kKS], (t / C::kKS) & 1, &no_abort, nullptr, 0);
-      }
-    }
-  } else if (warp == 2) {
-    // ---------------- TMA producer: the value-tile ring ----------------
-    if (lane == 0) {
-      int issued = 0;
-      bool ok = true;
-      for (int t = 0; t < n_tiles && ok; ++t) {
-        const int s = t % C::kVS;
-        ok = mbar_wait(&bars->v_empty[s], ((t / C::kVS) & 1) ^ 1, abort_flag, status, kStatusTimeout);
-        if (!ok) break;
-        uint8_t* st = smem + C::kOffV + s * C::kVStage;
-        const int row0 = t * C::kBN;
-        mbar_arrive_expect_tx(&bars->v_full[s], C::kVStage - (C::kDKDV ? C::kVecBytes - 512 : 0));
-        for (int c = 0; c < C::kDC; ++c) {
-          if (C::kDKDV) {  // dO (for dV), then Q (for dK)
-            tma_load_4d(st + c * C::kChunkX, &maps.x2, &bars->v_full[s], c * 64, row0, hh, bb);
-            tma_load_4d(st + (C::kDC + c) * C::kChunkX, &maps.x1, &bars->v_full[s], c * 64, row0, hh, bb);
-          } else {  // K (for dQ)
-            tma_load_4d(st + c * C::kChunkX, &maps.x1, &bars->v_full[s], c * 64, row0, hh, bb);
-          }
-        }
-        if (C::kDKDV) {  // the streamed queries' -LSE log2e and -D (256 bytes each)
-          float* vec = reinterpret_cast<float*>(st + 2 * C::kDC * C::kChunkX);
-          tma_load_2d(vec, &maps.nl2, &bars->v_full[s], row0, bh);
-          tma_load_2d(vec + 64, &maps.nd, &bars->v_full[s], row0, bh);
-        }
-        issued = t + 1;
-      }
-      if (!ok) {
-        volatile int no_abort = 0;
-        for (int t = issued - C::kVS; t < issued; ++t)
+        for (int t = tv - C::kVS; t < tv; ++t)
           if (t >= 0) mbar_wait(&bars->v_full[t % C::kVS], (t / C::kVS) & 1, &no_abort, nullptr, 0);
+        for (int t = tq - C::kVecS; t < tq; ++t)
+          if (t >= 0) mbar_wait(&bars->vec_full[t % C::kVecS], (t / C::kVecS) & 1, &no_abort, nullptr, 0);
       }
     }
-  } else if (warp == 1 || warp == 3 || warp == 8) {
-    // ---------------- tcgen05.mma issuers: warp 8 S1, warp 3 S2, warp 1 the value MMAs ----------------
+  } else if (warp >= 1 && warp <= 3) {
+    // ---------------- tcgen05.mma issuers: warp 3 S1, warp 2 S2, warp 1 the value MMAs ----------------
     if (lane == 0) {
       constexpr uint32_t kIdS = make_idesc_bf16_f32(128, C::kBN, false, false);  // both K-major
       constexpr uint32_t kIdPV = make_idesc_bf16_f32(128, D, false, true);      // B N-major
@@ -281,20 +339,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dV0 = make_smem_desc_sw128(smem_u32(smem + C::kOffV), C::kChunkX, 1024);
       auto off = [](uint64_t desc, uint32_t bytes) { return desc + static_cast<uint64_t>(bytes >> 4); };
       volatile int no_abort = 0;
-      if (warp == 8 || warp == 3) {
-        // S1 = R1 X1^T (warp 8) or S2 = R2 X2^T (warp 3), d-deep, N = 64.
-        const bool first = warp == 8;
+      if (warp == 3 || warp == 2) {
+        // S1 = R1 X1^T (warp 3) or S2 = R2 X2^T (warp 2), d-deep, N = 64.
+        const bool first = warp == 3;
         const uint64_t dA = first ? dR1 : dR2;
         const uint32_t xoff = first ? 0u : static_cast<uint32_t>(C::kDC * C::kChunkX);
         bool ok = mbar_wait(&bars->r_full, 0, abort_flag, status, kStatusTimeout);
         for (int t = 0; ok && t < n_tiles; ++t) {
           const int s = t % C::kKS;
           const int b = first ? t % C::kNS : t % C::kNSt;
+          const int bs = first ? t % C::kSBar : b;  // barrier slot
           ok = mbar_wait(&bars->k_full[s], (t / C::kKS) & 1, abort_flag, status, kStatusTimeout);
           // S1 buffers are free once the elementwise warps loaded tile t - NS; S2 buffers
           // hold the packed operands of tile t - NSt until its value MMAs are done.
           if (ok && first && t >= C::kNS)
-            ok = mbar_wait(&bars->s_free[b], ((t - C::kNS) / C::kNS) & 1, abort_flag, status, kStatusTimeout);
+            ok = mbar_wait(&bars->s_free[(t - C::kNS) % C::kSBar], ((t - C::kNS) / C::kSBar) & 1, abort_flag,
+                           status, kStatusTimeout);
           if (ok && !first && t >= C::kNSt)
             ok = mbar_wait(&bars->pv_done[b], ((t - C::kNSt) / C::kNSt) & 1, abort_flag, status, kStatusTimeout);
           if (!ok) break;
@@ -308,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_ss(dst, off(dA, c * C::kChunkR + kk * 32), off(dX, c * C::kChunkX + kk * 32), kIdS,
                      (c | kk) != 0);
           mma_commit(&bars->k_empty[s]);
-          mma_commit(first ? &bars->s_full[b] : &bars->st_full[b]);
+          mma_commit(first ? &bars->s_full[bs] : &bars->st_full[b]);
         }
         uint64_t* drain = first ? &bars->drain_s : &bars->drain_st;
         mma_commit(drain);
@@ -338,13 +398,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(&bars->v_empty[s]);
           mma_commit(&bars->pv_done[bt]);
         }
+        if (ok) mma_commit(&bars->acc_done);
         mma_commit(&bars->drain);
         mbar_wait(&bars->drain, 0, &no_abort, nullptr, 0);
       }
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ---------------- elementwise + epilogue: one resident row per thread ----------------
-    const int quarter = warp - 4;
+  } else {
+    // ---------------- elementwise + epilogue: one resident row per thread; group 0
+    // (warps 4-7) takes the even tiles, group 1 (warps 8-11) the odd ones ----------------
+    const int group = (warp - 4) >> 2;
+    const int quarter = warp & 3;  // TMEM lane quarter a warp may access
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float c2 = geom.scale * kLog2e;
@@ -355,32 +418,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       row_nd = geom.row_nd[ridx];
     }
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
+    for (int j = group; j < n_tiles; j += 2) {
       const int b = j % C::kNS;
+      const int bs = j % C::kSBar;
       const int bt = j % C::kNSt;
-      ok = mbar_wait(&bars->s_full[b], (j / C::kNS) & 1, abort_flag, status, kStatusTimeout) &&
-           mbar_wait(&bars->st_full[bt], (j / C::kNSt) & 1, abort_flag, status, kStatusTimeout);
-      // dK/dV pass: the streamed queries' vectors arrive with the value tiles.
-      if (C::kDKDV && ok)
-        ok = mbar_wait(&bars->v_full[j % C::kVS], (j / C::kVS) & 1, abort_flag, status, kStatusTimeout);
+      // S1 first, and its buffer released at once: the S1 ring is the short one,
+      // and the next tile's S1 MMAs wait for it.
+      ok = mbar_wait(&bars->s_full[bs], (j / C::kSBar) & 1, abort_flag, status, kStatusTimeout);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after_sync();
-      const uint32_t cS = lane_addr + C::kColS + 64u * b;
-      const uint32_t cSt = lane_addr + C::kColSt + 64u * bt;
-      const int valid = min(C::kBN, geom.n_str - j * C::kBN);
-      const float* vec = reinterpret_cast<const float*>(smem + C::kOffV + (j % C::kVS) * C::kVStage +
-                                                        2 * C::kDC * C::kChunkX);
-      if (valid == C::kBN)
-        bwd_tile<kMode, false>(cS, cSt, valid, c2, row_nl2, row_nd, vec, vec + 64, &bars->s_free[b], lane);
-      else
-        bwd_tile<kMode, true>(cS, cSt, valid, c2, row_nl2, row_nd, vec, vec + 64, &bars->s_free[b], lane);
+      uint32_t raw[128];
+      tmem_ld64_wait<0>(lane_addr + C::kColS + 64u * b, raw);
+      tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[bt]);
+      if (lane == 0) mbar_arrive(&bars->s_free[bs]);
+      ok = mbar_wait(&bars->st_full[bt], (j / C::kNSt) & 1, abort_flag, status, kStatusTimeout);
+      // dK/dV pass: the streamed queries' vectors
+      const int sq = j % C::kVecS;
+      if (C::kDKDV && ok)
+        ok = mbar_wait(&bars->vec_full[sq], (j / C::kVecS) & 1, abort_flag, status, kStatusTimeout);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const uint32_t cSt = lane_addr + C::kColSt + 64u * bt;
+      tmem_ld64_wait<64>(cSt, raw);
+      const int valid = min(C::kBN, geom.n_str - j * C::kBN);
+      const float* vec = reinterpret_cast<const float*>(smem + C::kOffVec + sq * C::kVecSlot);
+      if (valid == C::kBN)
+        bwd_tile<kMode, false>(raw, cSt, valid, c2, row_nl2, row_nd, vec, vec + 64);
+      else
+        bwd_tile<kMode, true>(raw, cSt, valid, c2, row_nl2, row_nd, vec, vec + 64);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars->p_full[bt]);
+        if (C::kDKDV) mbar_arrive(&bars->vec_empty[sq]);
+      }
     }
     // ---------------- epilogue ----------------
-    if (ok) ok = mbar_wait(&bars->pv_done[(n_tiles - 1) % C::kNSt], ((n_tiles - 1) / C::kNSt) & 1, abort_flag,
-                           status, kStatusTimeout);
+    if (ok) ok = mbar_wait(&bars->acc_done, 0, abort_flag, status, kStatusTimeout);
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       tc_fence_after_sync();
@@ -388,6 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid_row = rrow < geom.n_res;
       const int64_t obase = (static_cast<int64_t>(bh) * geom.n_res + rrow) * geom.d;
       // dQ pass: ACC1 = dS K, times s.  dK/dV pass: ACC1 = dV, ACC2 = dS^T Q, times s.
+      // The groups take alternate 32-column chunks.
+      int chunk = 0;
 #pragma unroll 1
       for (int acc = 0; acc < (C::kDKDV ? 2 : 1); ++acc) {
         float* out = (C::kDKDV && acc == 1) ? geom.out2 : geom.out1;
@@ -396,6 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ncols = D == 128 ? D : geom.d;
 #pragma unroll 1
         for (int c0 = 0; c0 < ncols; c0 += 32) {
+          if ((chunk++ & 1) != group) continue;
           uint32_t v[32];
           tmem_ld32_wait(lane_addr + col + c0, v);
           if (valid_row) {
