@@ -159,18 +159,7 @@ __device__ __forceinline__ void bwd_tile(uint32_t (&raw)[128], uint32_t cSt, int
   auto f = [&](int i) { return __uint_as_float(raw[i]); };
   const uint64_t c2x2 = f2_pack(c2, c2);
   uint32_t pk[32], dk[32];
-#pragma unroll
-  for (int i = 0; i < 64; i += 2) {
-    uint64_t nl, nd;
-    if (kMode == kModeDQ) {
-      nl = f2_pack(row_nl2, row_nl2);
-      nd = f2_pack(row_nd, row_nd);
-    } else {
-      const float2 a = *reinterpret_cast<const float2*>(col_nl2 + i);
-      const float2 b = *reinterpret_cast<const float2*>(col_nd + i);
-      nl = f2_pack(a.x, a.y);
-      nd = f2_pack(b.x, b.y);
-    }
+  auto step = [&](int i, uint64_t nl, uint64_t nd) {
     float x0, x1;
     f2_unpack(f2_fma(f2_pack(f(i), f(i + 1)), c2x2, nl), x0, x1);
     const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
@@ -178,6 +167,20 @@ __device__ __forceinline__ void bwd_tile(uint32_t (&raw)[128], uint32_t cSt, int
     f2_unpack(f2_mul(f2_pack(p0, p1), f2_add(f2_pack(f(64 + i), f(65 + i)), nd)), d0, d1);
     if (kMode == kModeDKDV) pk[i >> 1] = pack_bf16x2(p0, p1);
     dk[i >> 1] = pack_bf16x2(d0, d1);
+  };
+#pragma unroll
+  for (int i = 0; i < 64; i += 4) {
+    if (kMode == kModeDQ) {
+      const uint64_t nl = f2_pack(row_nl2, row_nl2), nd = f2_pack(row_nd, row_nd);
+      step(i, nl, nd);
+      step(i + 2, nl, nd);
+    } else {
+      // 16-byte broadcast reads (the vector slots are 512-byte aligned)
+      const float4 a = *reinterpret_cast<const float4*>(col_nl2 + i);
+      const float4 b = *reinterpret_cast<const float4*>(col_nd + i);
+      step(i, f2_pack(a.x, a.y), f2_pack(b.x, b.y));
+      step(i + 2, f2_pack(a.z, a.w), f2_pack(b.z, b.w));
+    }
   }
   if (kMode == kModeDKDV) {
     tmem_st32(cSt, pk);
