@@ -141,6 +141,15 @@ def latent_for(name_or_spec, device="cpu", seed=None):
     return x0, eps, t
 
 
+def upstream_gradient(name_or_spec, shape, device="cpu"):
+    """Seeded upstream gradient dO (bf16, N(0,1)) of the backward on a workload's queries."""
+    spec = dict(WORKLOADS[name_or_spec]) if isinstance(name_or_spec, str) else dict(name_or_spec)
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(spec["seed"]) + 777)
+    return torch.randn(shape, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
 def sample_rows(N, count, seed):
     """``count`` distinct query-row indices in [0, N), seeded, always including 0 and N-1."""
     gen = torch.Generator(device="cpu")

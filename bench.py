@@ -151,10 +151,10 @@ def measure_backward(x, spec, o, lse, dev, stream, peaks, reps=5, warmup=2):
     import torch
     from attention_jvp_gb300 import binding
 
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(int(spec["seed"]) + 777)
+    from attention_jvp_gb300 import inputs
+
     q, k, v = x["q"], x["k"], x["v"]
-    dO = torch.randn(q.shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    dO = inputs.upstream_gradient(spec, q.shape, device=dev)
     dq, dk, dv = (torch.empty(t.shape, dtype=torch.float32, device=dev) for t in (q, k, v))
     n = binding.load().attn_bwd_workspace_bytes(q.shape[0], q.shape[1], q.shape[2])
     ws = torch.empty(n, dtype=torch.uint8, device=dev)

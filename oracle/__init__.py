@@ -5,7 +5,8 @@ CPU-baseline leg of ``bench.py`` may import this package.  It shares no code
 with the CUDA library and never imports it; its inputs are plain numpy arrays.
 
 The arithmetic lives in ``attn_jvp_oracle.c`` (plain C, FP64, two-pass
-softmax), following the page "带分数正则的一致性蒸馏" (gitcode.csdn.net):
+softmax; ``attn_bwd_rows``, the backward at sampled rows of full-size heads, is
+plain numpy), following the page "带分数正则的一致性蒸馏" (gitcode.csdn.net):
 section 注意力 (attention) for O = softmax(s Q K^T) V and its JVP
 t_o = P t_v + t_p V, t_p = P (.) t_s - (P t_s^T) P, t_s = (t_q K^T + Q t_k^T) s;
 section 前向 (forward) for the natural-log LSE; section 时间步转换 (timestep
@@ -16,7 +17,7 @@ _process_output, the tangent target with its NaN masks and normalisation, the
 sCM loss) follows section 一致性模型 (consistency model), its 蒸馏代码 listing.
 The primal backward (dQ, dK, dV) follows section 反向 (backward).
 
-Parity pins for every function here are in tests/test_oracle.py; none is unpinned.
+Parity pins for every function here are in tests/test_*oracle.py; none is unpinned.
 """
 import ctypes
 import os
@@ -242,3 +243,49 @@ def attn_bwd(q, k, v, dO, scale):
         if rc != 0:
             raise RuntimeError("oracle_attn_bwd_head failed (%d)" % rc)
     return dq.reshape(q.shape), dk.reshape(k.shape), dv.reshape(v.shape)
+
+
+def attn_bwd_rows(q, k, v, dO, scale, q_rows, k_rows, block=512, with_dq_scale=False):
+    """dQ at the query rows ``q_rows`` and dK, dV at the key rows ``k_rows``, FP64, one head.
+
+    q, dO: [Nq, d]; k, v: [Nk, d].  Every output row is formed from the
+    definition of section 反向 (backward):
+        P_i = softmax_j(s q_i . k_j),  O_i = sum_j P_ij v_j,  D_i = dO_i . O_i,
+        dP_ij = dO_i . v_j,  dS_ij = P_ij (dP_ij - D_i),
+        dQ_i = s sum_j dS_ij k_j,  dV_j = sum_i P_ij dO_i,  dK_j = s sum_i dS_ij q_i.
+    A key row needs every query's softmax normaliser and D_i; those are formed
+    for all queries, ``block`` query rows at a time (the rows are independent),
+    so full-size heads fit in memory.  Plain numpy; the full-head reference is
+    ``attn_bwd``, with which this agrees on every row (tests/test_bwd_oracle.py).
+    Returns (dq [len(q_rows), d], dk [len(k_rows), d], dv [len(k_rows), d]); with
+    ``with_dq_scale`` also s (|dS| @ |K|) at the query rows: the size of the sum
+    behind each dQ element, to which a relative error of every dS_ij contributes."""
+    q, k, v, dO = (_f64(x) for x in (q, k, v, dO))
+    q_rows = np.asarray(q_rows, dtype=np.int64)
+    k_rows = np.asarray(k_rows, dtype=np.int64)
+    Nq = q.shape[0]
+    m = np.empty(Nq)
+    l = np.empty(Nq)
+    D = np.empty(Nq)
+    for a in range(0, Nq, block):
+        b = min(a + block, Nq)
+        S = scale * (q[a:b] @ k.T)
+        m[a:b] = S.max(axis=1)
+        E = np.exp(S - m[a:b, None])
+        l[a:b] = E.sum(axis=1)
+        O = (E @ v) / l[a:b, None]
+        D[a:b] = np.einsum("ij,ij->i", dO[a:b], O)
+    # query rows
+    P = np.exp(scale * (q[q_rows] @ k.T) - m[q_rows, None]) / l[q_rows, None]
+    dS = P * (dO[q_rows] @ v.T - D[q_rows, None])
+    dq = scale * (dS @ k)
+    dq_scale = scale * (np.abs(dS) @ np.abs(k)) if with_dq_scale else None
+    # key rows (columns j of P, dP and dS over every query i)
+    Pt = np.exp(scale * (q @ k[k_rows].T) - m[:, None]) / l[:, None]
+    dSt = Pt * (dO @ v[k_rows].T - D[:, None])
+    dv = Pt.T @ dO
+    dk = scale * (dSt.T @ q)
+    if with_dq_scale:
+        return dq, dk, dv, dq_scale
+    return dq, dk, dv
+

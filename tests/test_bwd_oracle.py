@@ -86,3 +86,23 @@ def test_rowsum_identity_used_by_the_gpu_path():
     P = torch.softmax(torch.from_numpy(q) @ torch.from_numpy(k).transpose(-1, -2) * s, dim=-1).numpy()
     dP = dO @ np.swapaxes(v, -1, -2)
     assert _rel((dP * P).sum(-1), (dO * o).sum(-1)) < 1e-13
+
+
+@pytest.mark.parametrize("nq,nk,d", [(37, 53, 16), (64, 19, 32), (130, 130, 8)])
+def test_sampled_rows_match_the_full_head(nq, nk, d):
+    # The sampled-row oracle (numpy, blocked over queries) against the full-head
+    # one (C) on every row; a block smaller than Nq exercises the blocking.
+    q, k, v, dO = (x[0, 0] for x in _case(B=1, H=1, Nq=nq, Nk=nk, d=d, seed=nq * nk))
+    s = 0.4
+    rq, rk, rv = oracle.attn_bwd(q, k, v, dO, s)
+    gq, gk, gv = oracle.attn_bwd_rows(q, k, v, dO, s, np.arange(nq), np.arange(nk), block=16)
+    assert _rel(gq, rq) < 1e-12 and _rel(gk, rk) < 1e-12 and _rel(gv, rv) < 1e-12
+    sub_q, sub_k = [nq - 1, 0, nq // 2], [nk // 3, nk - 1]
+    hq, hk, hv = oracle.attn_bwd_rows(q, k, v, dO, s, sub_q, sub_k)
+    assert np.allclose(hq, rq[sub_q], rtol=1e-12, atol=1e-14)
+    assert np.allclose(hk, rk[sub_k], rtol=1e-12, atol=1e-14)
+    assert np.allclose(hv, rv[sub_k], rtol=1e-12, atol=1e-14)
+    # the size of each dQ sum bounds the sum itself (triangle inequality)
+    *_, scale_q = oracle.attn_bwd_rows(q, k, v, dO, s, sub_q, sub_k, with_dq_scale=True)
+    assert np.all(scale_q >= np.abs(hq) * (1 - 1e-12)) and np.all(scale_q > 0)
+
