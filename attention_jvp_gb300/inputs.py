@@ -141,6 +141,35 @@ def latent_for(name_or_spec, device="cpu", seed=None):
     return x0, eps, t
 
 
+def epilogue_shape(name_or_spec, min_elems=64 << 20):
+    """[B, C, T, H*W] of a latent batch for the output-side kernels with at least
+    ``min_elems`` elements (more than L2 holds in fp32): 16 channels and 21 frames
+    when the workload's tokens split into 21 frames, else one frame; a sample holds
+    64 * N values (one token per 2x2 patch of a 16-channel latent)."""
+    spec = dict(WORKLOADS[name_or_spec]) if isinstance(name_or_spec, str) else dict(name_or_spec)
+    per = 64 * spec["N"]
+    T = 21 if (4 * spec["N"]) % 21 == 0 else 1
+    HW = per // (16 * T)
+    B = max(1, -(-min_elems // per))
+    return B, 16, T, HW
+
+
+def epilogue_batch(name_or_spec, device="cpu"):
+    """Seeded fp32 latent batch of ``epilogue_shape``: x, n, x_t, n_t ~ N(0,1) and the
+    FP64 [B, T] times t in [0.2, 1.5) and tangents t_t in [0, 1)."""
+    spec = dict(WORKLOADS[name_or_spec]) if isinstance(name_or_spec, str) else dict(name_or_spec)
+    B, C, T, HW = epilogue_shape(spec)
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(spec["seed"]) + 4242)
+    out = {}
+    for name in ("x", "n", "x_t", "n_t"):
+        out[name] = torch.randn((B, C, T, HW), generator=gen, device=device, dtype=torch.float32)
+    out["t"] = torch.rand((B, T), generator=gen, device=device, dtype=torch.float64) * 1.3 + 0.2
+    out["t_t"] = torch.rand((B, T), generator=gen, device=device, dtype=torch.float64)
+    return out
+
+
 def upstream_gradient(name_or_spec, shape, device="cpu"):
     """Seeded upstream gradient dO (bf16, N(0,1)) of the backward on a workload's queries."""
     spec = dict(WORKLOADS[name_or_spec]) if isinstance(name_or_spec, str) else dict(name_or_spec)

@@ -84,35 +84,21 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def epilogue_shape(spec, min_elems=64 << 20):
-    """[B, C, T, H*W] of a latent batch with at least ``min_elems`` elements (more than
-    L2 holds in fp32): 16 channels and 21 frames when the tokens split into 21
-    frames, else one frame; a sample holds 64 * N values."""
-    per = 64 * spec["N"]
-    T = 21 if (4 * spec["N"]) % 21 == 0 else 1
-    HW = per // (16 * T)
-    B = max(1, -(-min_elems // per))
-    return B, 16, T, HW
-
-
 def measure_epilogue(spec, dev, stream, peaks, reps=10, warmup=3):
     """Achieved bandwidth of the two output-side kernels on a latent batch larger than L2.
 
     Algorithmic bytes per element: trigflow_output_jvp reads x, n and their tangents and
     writes F and its tangent (24 B); scm_tangent_loss reads F_theta, F_sg, F_teacher, x and
-    F_t and writes g_n and df_dt (28 B); its second pass over g, F_theta and F_sg (16 B
-    more) is an implementation cost the figure does not credit."""
+    F_t and writes g_n and df_dt (28 B); its in-place normalisation of g (one write and
+    one re-read of the unnormalised g, 8 B more) is an implementation cost the figure
+    does not credit."""
     import torch
-    from attention_jvp_gb300 import binding
+    from attention_jvp_gb300 import binding, inputs
 
-    B, C, T, HW = epilogue_shape(spec)
+    batch = inputs.epilogue_batch(spec, device=dev)
+    x, n, xt, nt, t, tt = (batch[k] for k in ("x", "n", "x_t", "n_t", "t", "t_t"))
+    B, C, T, HW = x.shape
     shape = (B, C, T, HW)
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(int(spec["seed"]) + 4242)
-    make = lambda: torch.randn(shape, generator=gen, device=dev, dtype=torch.float32)
-    x, n, xt, nt = make(), make(), make(), make()
-    t = torch.rand((B, T), generator=gen, device=dev, dtype=torch.float64) * 1.3 + 0.2
-    tt = torch.rand((B, T), generator=gen, device=dev, dtype=torch.float64)
     F, Ft = torch.empty_like(x), torch.empty_like(x)
     ws = binding.scm_workspace(shape, dev)
     elems = B * C * T * HW

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import oracle
-from attention_jvp_gb300 import binding
+from attention_jvp_gb300 import binding, inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -120,3 +120,23 @@ def test_scm_tangent_loss_with_a_dirty_reused_workspace(cuda_lib):
         assert _rel(_np(g)[ok], rg[ok]) < 1e-5
         assert np.all(_np(g)[4] == 0) and _np(loss)[4] == 0.0
         assert np.max(np.abs(_np(loss)[ok] - rl[ok]) / rl[ok]) < 2e-5
+
+
+def test_output_side_on_the_benchmarked_video_batch(cuda_lib):
+    # The batch bench.py times: 33 video latents [33, 16, 21, 6240], 69.2 M
+    # elements per tensor; scm_tangent_loss runs with the persistent grid's
+    # ticket lag in its steady state (33 samples, eight ahead).
+    b = inputs.epilogue_batch("video_dit", device="cuda")
+    x, n, xt, nt, t, tt = (b[k] for k in ("x", "n", "x_t", "n_t", "t", "t_t"))
+    F, Ft = binding.trigflow_output_jvp(x, n, xt, nt, t, tt)
+    g, dfdt, loss, ng, nf = binding.scm_tangent_loss(F, x, n, xt, Ft, t, 0.5)
+    torch.cuda.synchronize()
+    rF, rFt = oracle.process_output_jvp(_np(x), _np(n), _np(xt), _np(nt), _np(t), _np(tt))
+    assert _rel(_np(F), rF) < 2e-6
+    assert _rel(_np(Ft), rFt) < 2e-5
+    del rF, rFt
+    rg, rd, rl, rng, rnf = oracle.scm_tangent_loss(_np(F), _np(x), _np(n), _np(xt), _np(Ft), _np(t), 0.5)
+    assert not ng.any().item() and not nf.any().item() and not rng.any() and not rnf.any()
+    assert _rel(_np(g), rg) < 1e-5
+    assert _rel(_np(dfdt), rd) < 2e-6
+    assert np.max(np.abs(_np(loss) - rl) / rl) < 2e-5
