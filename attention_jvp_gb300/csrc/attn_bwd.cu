@@ -48,7 +48,12 @@ struct BwdCfg {
   static constexpr int kBM = 128;                  // resident rows per CTA (= TMEM lanes)
   static constexpr int kBN = 64;                   // streamed rows per tile
   static constexpr int kDC = D / 64;               // 64-element (128-byte) d-chunks
-  static constexpr int kNS = (kDKDV && D == 128) ? 1 : 3;  // S1 TMEM buffers
+  // dQ pass: the resident Q and dO also live in TMEM (bf16, D/2 columns each) as
+  // the A operands of the score MMAs, which then read only the streamed tiles
+  // from shared memory (with both operands there, a 64-wide score MMA wants
+  // about 1.5x the shared-memory bandwidth).
+  static constexpr bool kRTmem = !kDKDV;
+  static constexpr int kNS = (D == 128) ? 1 : 3;  // S1 TMEM buffers
   static constexpr int kNSt = 3;                            // S2 (then packed operands) TMEM buffers
   // Barrier slots of the S1 ring.  Tiles alternate between the two elementwise
   // groups; with a single buffer, consecutive tiles on one barrier would belong
@@ -82,7 +87,9 @@ struct BwdCfg {
   // TMEM: ACC1 [0, D) (dQ or dV), ACC2 [D, 2D) (dK), S1 buffers, S2 buffers (64 columns each)
   static constexpr uint32_t kColAcc1 = 0;
   static constexpr uint32_t kColAcc2 = D;
-  static constexpr uint32_t kColS = (kDKDV ? 2 : 1) * D;
+  static constexpr uint32_t kColR1 = (kDKDV ? 2 : 1) * D;  // dQ pass: Q, then dO (bf16 pairs)
+  static constexpr uint32_t kColR2 = kColR1 + D / 2;
+  static constexpr uint32_t kColS = kColR1 + (kRTmem ? D : 0);
   static constexpr uint32_t kColSt = kColS + 64 * kNS;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kColSt + 64 * kNSt <= kTmemCols, "TMEM budget");
@@ -118,6 +125,7 @@ struct Barriers {
   uint64_t s_full[3], st_full[3], s_free[3], p_full[3], pv_done[3];
   uint64_t drain, drain_s, drain_st;
   uint64_t acc_done;  // all value MMAs done (single use)
+  uint64_t r_tmem;    // dQ pass: Q and dO copied into TMEM (one arrival per warp of group 0)
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -229,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->drain_s, 1);
     mbar_init(&bars->drain_st, 1);
     mbar_init(&bars->acc_done, 1);
+    mbar_init(&bars->r_tmem, 4);
     for (int s = 0; s < 4; ++s) {
       mbar_init(&bars->vec_full[s], 1);
       mbar_init(&bars->vec_empty[s], 4);  // one arrival per warp of the group that used the slot
@@ -346,8 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // S1 = R1 X1^T (warp 3) or S2 = R2 X2^T (warp 2), d-deep, N = 64.
         const bool first = warp == 3;
         const uint64_t dA = first ? dR1 : dR2;
+        const uint32_t aT = tmem + (first ? C::kColR1 : C::kColR2);  // dQ pass: A in TMEM
         const uint32_t xoff = first ? 0u : static_cast<uint32_t>(C::kDC * C::kChunkX);
-        bool ok = mbar_wait(&bars->r_full, 0, abort_flag, status, kStatusTimeout);
+        bool ok = C::kRTmem ? mbar_wait(&bars->r_tmem, 0, abort_flag, status, kStatusTimeout)
+                            : mbar_wait(&bars->r_full, 0, abort_flag, status, kStatusTimeout);
         for (int t = 0; ok && t < n_tiles; ++t) {
           const int s = t % C::kKS;
           const int b = first ? t % C::kNS : t % C::kNSt;
@@ -367,9 +378,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < C::kDC; ++c)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ss(dst, off(dA, c * C::kChunkR + kk * 32), off(dX, c * C::kChunkX + kk * 32), kIdS,
-                     (c | kk) != 0);
+            for (int kk = 0; kk < 4; ++kk) {
+              if constexpr (C::kRTmem)
+                mma_ts(dst, aT + (c * 4 + kk) * 8, off(dX, c * C::kChunkX + kk * 32), kIdS, (c | kk) != 0);
+              else
+                mma_ss(dst, off(dA, c * C::kChunkR + kk * 32), off(dX, c * C::kChunkX + kk * 32), kIdS,
+                       (c | kk) != 0);
+            }
           mma_commit(&bars->k_empty[s]);
           mma_commit(first ? &bars->s_full[bs] : &bars->st_full[b]);
         }
@@ -421,7 +436,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       row_nd = geom.row_nd[ridx];
     }
     bool ok = true;
-    for (int j = group; j < n_tiles; j += 2) {
+    if (C::kRTmem && group == 0) {
+      // Rows of Q and dO (128-byte-swizzled d-chunks: 16-byte unit u of row r at
+      // unit u ^ (r mod 8)) into this thread's TMEM lane.
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->r_full, 0, abort_flag, status, kStatusTimeout));
+      if (ok) {
+#pragma unroll 1
+        for (int m = 0; m < 2 * C::kDC; ++m) {
+          const int c = m % C::kDC;
+          const uint8_t* src = smem + (m < C::kDC ? C::kOffR1 : C::kOffR2) + c * C::kChunkR + row * 128;
+          uint32_t w[32];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint4 x = *reinterpret_cast<const uint4*>(src + ((u ^ (row & 7)) << 4));
+            w[4 * u] = x.x, w[4 * u + 1] = x.y, w[4 * u + 2] = x.z, w[4 * u + 3] = x.w;
+          }
+          tmem_st32(lane_addr + (m < C::kDC ? C::kColR1 : C::kColR2) + 32 * c, w);
+        }
+        tmem_wait_st();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->r_tmem);
+      }
+    }
+    for (int j = group; ok && j < n_tiles; j += 2) {
       const int b = j % C::kNS;
       const int bs = j % C::kSBar;
       const int bt = j % C::kNSt;
