@@ -10,21 +10,23 @@
 // -LSE log2 e.
 //
 // Two passes, each one CTA per 128 resident rows of one (batch, head), each
-// streaming 64-row tiles of the other side, with the same warp roles and
-// hand-offs as the forward kernel:
+// streaming 64-row tiles of the other side, with hand-offs like the forward
+// kernel's:
 //   dQ pass   (resident Q, dO; streamed K, V):  S1 = Q K^T, S2 = dO V^T,
 //             dS = P (.) (S2 - D) per query row, dQ += dS K.
 //   dK/dV pass (resident K, V; streamed Q, dO and the per-query -LSE log2 e
 //             and -D):  S1 = K Q^T, S2 = V dO^T (both transposed: TMEM lane =
 //             key), P^T and dS^T per key row, dV += P^T dO, dK += dS^T Q.
-// Warps: 0 TMA (resident tiles, then per streamed tile its score stage and its
-// value stage), 1 TMEM + value MMAs, 2 S2 MMAs, 3 S1 MMAs, and two groups of
+// Warps: 0 TMA (resident tiles, then the score ring, the value ring and, in the
+// dK/dV pass, the per-query vector ring, each refilled as soon as it frees),
+// 1 TMEM + value MMAs, 2 S2 MMAs, 3 S1 MMAs, and two groups of
 // elementwise warps (thread = resident row = TMEM lane): 4-7 take the even
 // tiles, 8-11 the odd ones.  One group's per-tile chain (barrier waits, TMEM
 // load, exp2 and packing, TMEM store, arrival) is about as long as the tile's
 // MMAs, so a single group left the tensor pipe idle half the time; with two,
 // one group's waits overlap the other's arithmetic.  The groups split the
-// epilogue by 32-column chunks.  The two passes recompute S and dP (14 d flops
+// epilogue by 32-column chunks.  In the dQ pass the score MMAs take Q and dO
+// from TMEM copies.  The two passes recompute S and dP (14 d flops
 // per (query, key) pair instead of 10) but need no atomics, so results are
 // deterministic.
 #include <cuda_bf16.h>

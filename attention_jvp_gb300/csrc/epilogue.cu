@@ -8,12 +8,13 @@
 // Tensors are [B, C, T, HW] fp32 with the time t given per (b, frame) as FP64
 // [B, T].  The work is HBM-bound.  It is cut into rows of HW elements (one
 // (b, c, frame) each), so every element of a row shares one set of per-frame
-// coefficients, formed once per block in FP64 and rounded to fp32; the
+// coefficients, formed in FP64 (once per block for trigflow_output_jvp, once
+// per frame by a prologue for scm_tangent_loss) and rounded to fp32; the
 // elementwise arithmetic is fp32 (the page's tensors are fp32) with 16-byte
 // accesses when the rows allow them.  The norms and the loss are accumulated to
 // near FP64 accuracy (the page converts g to double before normalising): exact
-// products summed in fp32 pairs per thread, FP64 per block, then per sample in
-// a fixed order, so results are reproducible.
+// products summed as fp32 pairs per thread and across the block, FP64 per item
+// and per sample, in a fixed order, so results are reproducible.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -32,7 +33,7 @@ constexpr int kTgtVecPerThread = 8;
 
 // Row segments: a work item is (row, chunk) with row = (b * C + c) * T + f.
 struct Rows {
-  int64_t HW, chunks, chunk_elems;  // chunk_elems: elements per item (vector: 4 * kChunkVec)
+  int64_t HW, chunks, chunk_elems;  // chunk_elems: elements per item (vector: 4 * threads * groups per thread)
   int T, CT;
   bool vec;
 };
