@@ -525,7 +525,7 @@ def run_gpu(args):
 
     # ---- primal attention backward (not part of the timed step) ----
     bwd = None
-    if not args.skip_backward and rank == 0 and n_chunks == 1:
+    if not args.skip_backward and rank == 0:  # on the (merged) forward's O and LSE
         bwd = measure_backward(x, spec, out, lse, dev, stream, peaks)
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only) ----
