@@ -302,7 +302,11 @@ int trigflow_output_jvp(const float* x, const float* n, const float* x_t, const 
  *   g_n, df_dt     : DEVICE fp32 [B, C, T, HW] outputs (g_n rounded from FP64).
  *   loss           : DEVICE FP64 [B];  nan_g, nan_F: DEVICE int32 [B].
  *   workspace      : DEVICE, 8-byte aligned, scm_tangent_loss_workspace_bytes()
- *                    bytes.  Per-sample sums are reduced in a fixed order, so
+ *                    bytes.  It holds the call's per-item sums and its
+ *                    scheduling counters, which the call resets itself (no
+ *                    zeroing needed); calls that may run at the same time
+ *                    (other streams) need workspaces of their own.  The sums
+ *                    are reduced per sample in a fixed order, so
  *                    results are reproducible run to run.  The loss is formed
  *                    as sum a^2 - 2 s sum a g + s^2 sum g^2 (a = F_theta - F_sg,
  *                    s = 1 / (||g|| + 0.1)), exact algebra on the sum above.
