@@ -245,7 +245,7 @@ def attn_bwd(q, k, v, dO, scale):
     return dq.reshape(q.shape), dk.reshape(k.shape), dv.reshape(v.shape)
 
 
-def attn_bwd_rows(q, k, v, dO, scale, q_rows, k_rows, block=512, with_dq_scale=False):
+def attn_bwd_rows(q, k, v, dO, scale, q_rows, k_rows, block=512, with_scales=False):
     """dQ at the query rows ``q_rows`` and dK, dV at the key rows ``k_rows``, FP64, one head.
 
     q, dO: [Nq, d]; k, v: [Nk, d].  Every output row is formed from the
@@ -258,8 +258,9 @@ def attn_bwd_rows(q, k, v, dO, scale, q_rows, k_rows, block=512, with_dq_scale=F
     so full-size heads fit in memory.  Plain numpy; the full-head reference is
     ``attn_bwd``, with which this agrees on every row (tests/test_bwd_oracle.py).
     Returns (dq [len(q_rows), d], dk [len(k_rows), d], dv [len(k_rows), d]); with
-    ``with_dq_scale`` also s (|dS| @ |K|) at the query rows: the size of the sum
-    behind each dQ element, to which a relative error of every dS_ij contributes."""
+    ``with_scales`` also the size of the sum behind each output element, to which
+    a relative error of every term contributes: (s |dS| |K| at the query rows,
+    s |dS|^T |Q| and P^T |dO| at the key rows)."""
     q, k, v, dO = (_f64(x) for x in (q, k, v, dO))
     q_rows = np.asarray(q_rows, dtype=np.int64)
     k_rows = np.asarray(k_rows, dtype=np.int64)
@@ -279,13 +280,15 @@ def attn_bwd_rows(q, k, v, dO, scale, q_rows, k_rows, block=512, with_dq_scale=F
     P = np.exp(scale * (q[q_rows] @ k.T) - m[q_rows, None]) / l[q_rows, None]
     dS = P * (dO[q_rows] @ v.T - D[q_rows, None])
     dq = scale * (dS @ k)
-    dq_scale = scale * (np.abs(dS) @ np.abs(k)) if with_dq_scale else None
+    sq = scale * (np.abs(dS) @ np.abs(k)) if with_scales else None
     # key rows (columns j of P, dP and dS over every query i)
     Pt = np.exp(scale * (q @ k[k_rows].T) - m[:, None]) / l[:, None]
     dSt = Pt * (dO @ v[k_rows].T - D[:, None])
     dv = Pt.T @ dO
     dk = scale * (dSt.T @ q)
-    if with_dq_scale:
-        return dq, dk, dv, dq_scale
+    if with_scales:
+        sk = scale * (np.abs(dSt).T @ np.abs(q))
+        sv = Pt.T @ np.abs(dO)
+        return dq, dk, dv, (sq, sk, sv)
     return dq, dk, dv
 

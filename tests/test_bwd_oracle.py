@@ -102,7 +102,8 @@ def test_sampled_rows_match_the_full_head(nq, nk, d):
     assert np.allclose(hq, rq[sub_q], rtol=1e-12, atol=1e-14)
     assert np.allclose(hk, rk[sub_k], rtol=1e-12, atol=1e-14)
     assert np.allclose(hv, rv[sub_k], rtol=1e-12, atol=1e-14)
-    # the size of each dQ sum bounds the sum itself (triangle inequality)
-    *_, scale_q = oracle.attn_bwd_rows(q, k, v, dO, s, sub_q, sub_k, with_dq_scale=True)
-    assert np.all(scale_q >= np.abs(hq) * (1 - 1e-12)) and np.all(scale_q > 0)
+    # the size of each sum bounds the sum itself (triangle inequality)
+    *_, (sq, sk, sv) = oracle.attn_bwd_rows(q, k, v, dO, s, sub_q, sub_k, with_scales=True)
+    for size, val in ((sq, hq), (sk, hk), (sv, hv)):
+        assert np.all(size >= np.abs(val) * (1 - 1e-12)) and np.all(size > 0)
 

@@ -109,8 +109,9 @@ def test_backward_full_size_sampled_rows(cuda_lib, name):
     # one head at the longest sequence (its FP64 rows take ~30 s), two elsewhere
     for bh in ((B * H - 1,) if N > 70000 else (0, B * H - 1)):
         b, h = divmod(bh, H)
-        rq, rk, rv, scale_q = oracle.attn_bwd_rows(host64(q[b, h]), host64(k[b, h]), host64(v[b, h]),
-                                                   host64(dO[b, h]), x["scale"], rows, rows, with_dq_scale=True)
+        rq, rk, rv, (scale_q, _, _) = oracle.attn_bwd_rows(host64(q[b, h]), host64(k[b, h]), host64(v[b, h]),
+                                                           host64(dO[b, h]), x["scale"], rows, rows,
+                                                           with_scales=True)
         gq = host64(dq[b, h][rows])
         if name == "stress":
             # The outlier keys carry 96 in coordinate 0 (their +12 logit), so
