@@ -140,3 +140,55 @@ def test_output_side_on_the_benchmarked_video_batch(cuda_lib):
     assert _rel(_np(g), rg) < 1e-5
     assert _rel(_np(dfdt), rd) < 2e-6
     assert np.max(np.abs(_np(loss) - rl) / rl) < 2e-5
+
+
+def _random_epilogue_cases(n=10, seed=77):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        B = int(rng.choice([1, 2, 7, 9, 17, 50]))
+        C = int(rng.integers(1, 5))
+        T = int(rng.integers(1, 6))
+        HW = int(rng.choice([1, 3, 4, 37, 64, 1000, 4097, 8200]))
+        out.append((i, B, C, T, HW, float(rng.uniform(0, 1)), bool(rng.random() < 0.3), bool(rng.random() < 0.4)))
+    return out
+
+
+@pytest.mark.parametrize("case", _random_epilogue_cases(), ids=lambda c: "c%d-B%dC%dT%dHW%d" % c[:5])
+def test_output_side_random_shapes(cuda_lib, case):
+    # Seeded batch sizes around the fused sCM pass's eight-sample ticket lag,
+    # rows that take the 16-byte path or the scalar one (HW % 4, or tensors
+    # offset by one element), and scattered NaNs.
+    i, B, C, T, HW, r, offset, nans = case
+    shape = (B, C, T, HW)
+    n = B * C * T * HW
+
+    def lat(seed, scale=1.0):
+        base = _latent((n + 1,), seed, scale)
+        return (base[1:] if offset else base[:n]).view(shape)
+
+    x, nn, xt, nt = lat(70 + i), lat(80 + i), lat(90 + i), lat(100 + i)
+    t = _times(B, T, 110 + i, 0.05, 1.55)
+    tt = _times(B, T, 120 + i, -1.0, 1.0)
+    F, Ft = binding.trigflow_output_jvp(x, nn, xt, nt, t, tt)
+    Fsg, Ftc = lat(130 + i), lat(140 + i)
+    if nans:
+        flat = Fsg.view(-1)
+        flat[(np.arange(3) * 7919 + i) % n] = float("nan")  # F_sg NaN: g of those elements
+    g, dfdt, loss, ng, nf = binding.scm_tangent_loss(F, Fsg, Ftc, x, Ft, t, r)
+    torch.cuda.synchronize()
+    binding.attn_jvp_status()
+    rF, rFt = oracle.process_output_jvp(_np(x), _np(nn), _np(xt), _np(nt), _np(t), _np(tt))
+    assert _rel(_np(F), rF) < 2e-6
+    assert _rel(_np(Ft), rFt) < 2e-5
+    rg, rd, rl, rng_, rnf = oracle.scm_tangent_loss(_np(F), _np(Fsg), _np(Ftc), _np(x), _np(Ft), _np(t), r)
+    assert ng.cpu().tolist() == rng_.tolist() and nf.cpu().tolist() == rnf.tolist()
+    ok = ~rng_ & ~rnf
+    gl = _np(loss)
+    assert np.all(gl[~ok] == 0.0) and np.all(_np(g)[~ok] == 0)
+    if ok.any():
+        assert _rel(_np(g)[ok], rg[ok]) < 1e-5
+        assert np.max(np.abs(gl[ok] - rl[ok]) / rl[ok]) < 2e-5
+    d = _np(dfdt)
+    fin = np.isfinite(rd)
+    assert np.array_equal(np.isfinite(d), fin) and _rel(d[fin], rd[fin]) < 2e-6
