@@ -100,10 +100,15 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;
 // phase completed; false when the block was asked to abort (``*abort_flag``
 // set by another thread) or the wait ran out of time, in which case it raises
 // ``*abort_flag`` and ORs ``code`` into ``*status``.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status, int code, uint64_t limit_ns = kWaitLimitNs) {
-  if (mbar_test_wait(bar, parity)) return true;  // fast path: phase already complete
-  uint64_t t0 = globaltimer_ns();
+//
+// Only the fast path is inlined: a non-blocking test, then one suspended
+// try_wait, which covers almost every hand-off.  The timed loop lives in one
+// out-of-line function.  Inlined at each of the kernels' twenty-odd wait sites,
+// it made up a third of the fused kernel's machine code, and that kernel's
+// speed falls off a cliff a little above 52 KB (instruction fetch).
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                   int* status, int code, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 15u) == 0u) {
@@ -115,6 +120,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       }
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status, int code, uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_test_wait(bar, parity)) return true;  // phase already complete
+  if (mbar_try_wait(bar, parity)) return true;   // one suspended wait
+  return mbar_wait_slow(bar, parity, abort_flag, status, code, limit_ns);
 }
 
 // ---------------------------------------------------------------------------
