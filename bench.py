@@ -249,6 +249,25 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
                 "samples": len(sm)}
 
+    # Throttle reasons that void a timing; sw_power_cap is normal under a dense load and is kept.
+    REJECT = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+    @classmethod
+    def rejection(cls, summary, locked_frac=0.75):
+        """Why a timed region's clock record voids its number, or None.
+
+        A slowdown or thermal reason seen at any sample voids it.  So does a median SM clock
+        below ``locked_frac`` of the maximum with no reason active, the mark of a clock lock
+        left behind by an earlier user.  No samples (no nvidia-smi) voids nothing.
+        """
+        bad = [r for r in summary.get("reasons", []) if r in cls.REJECT]
+        if bad:
+            return ",".join(bad)
+        sm, mx = summary.get("sm_mhz"), summary.get("sm_max_mhz")
+        if sm and mx and not summary.get("reasons") and sm < locked_frac * mx:
+            return "sm clock %.0f of %.0f MHz with no reason active" % (sm, mx)
+        return None
+
 
 # ---------------------------------------------------------------------------
 # CPU legs: the oracle on a bounded sample of the workload
@@ -418,23 +437,38 @@ def run_gpu(args):
             gpu_index = int(ids[local])
     sampler = ClockSampler(gpu_index)
 
+    def timed_region():
+        attn_events.clear()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        sampler.start()
+        time.sleep(0.3)  # let the sampler take a first idle-to-load sample
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step(record=True)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        sampler.stop()
+        binding.attn_jvp_status()
+        return ev0.elapsed_time(ev1), ClockSampler.summarize(sampler.lines)
+
+    local_ms, clocks = timed_region()
+    # A throttled or clock-locked region is voided and timed once more; any rank's veto counts.
+    why = ClockSampler.rejection(clocks)
+    veto = float(why is not None)
     if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    sampler.start()
-    time.sleep(0.3)  # let the sampler take a first idle-to-load sample
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step(record=True)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    sampler.stop()
-    binding.attn_jvp_status()
-    local_ms = ev0.elapsed_time(ev1)
+        tv = torch.tensor([veto], dtype=torch.float64, device=dev)
+        dist.all_reduce(tv, op=dist.ReduceOp.MAX)
+        veto = float(tv.item())
+    if veto:
+        local_ms, clocks = timed_region()
+        clocks["remeasured"] = why or "another rank's clocks"
+        clocks["rejected_again"] = ClockSampler.rejection(clocks)
     attn_ms = [a.elapsed_time(b) for a, b, _ in attn_events]
     attn_kv = [kv for _, _, kv in attn_events]
 
@@ -539,7 +573,6 @@ def run_gpu(args):
                          % (nrows, N, dt, cores)}
 
     if rank == 0:
-        clocks = ClockSampler.summarize(sampler.lines)
         total_bytes = sum(x[n].numel() * x[n].element_size() for n in inputs.NAMES)
         rec = {
             "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -36,6 +36,31 @@ def test_clock_summary_parses_reasons():
     assert bench.ClockSampler.summarize([])["sm_mhz"] is None
 
 
+def test_clock_rejection_rule():
+    def summary(rows):
+        return bench.ClockSampler.summarize(
+            ["0, %d, 2070, 1000.0, 0x0, Not Active, %s, %s, %s" % r for r in rows])
+
+    ok = lambda sm, pcap="Not Active": (sm, "Not Active", "Not Active", pcap)  # noqa: E731
+    # full clocks, or the power cap holding them near 1.8 GHz: kept
+    assert bench.ClockSampler.rejection(summary([ok(2040)] * 5)) is None
+    assert bench.ClockSampler.rejection(summary([ok(1792, "Active")] * 5)) is None
+    # the power cap explains a low clock too
+    assert bench.ClockSampler.rejection(summary([ok(1200, "Active")] * 5)) is None
+    # a thermal reason at a single sample voids the region
+    rows = [ok(2040)] * 4 + [(2040, "Active", "Not Active", "Not Active")]
+    assert bench.ClockSampler.rejection(summary(rows)) == "hw_thermal_slowdown"
+    rows = [ok(2040)] * 4 + [(1900, "Not Active", "Active", "Active")]
+    assert bench.ClockSampler.rejection(summary(rows)) == "sw_thermal_slowdown"
+    # a low median clock with no reason: a clock lock left behind
+    why = bench.ClockSampler.rejection(summary([ok(1200)] * 5))
+    assert why is not None and "no reason" in why
+    # one idle sample does not move the median
+    assert bench.ClockSampler.rejection(summary([ok(345)] + [ok(2040)] * 4)) is None
+    # no nvidia-smi, no verdict
+    assert bench.ClockSampler.rejection(bench.ClockSampler.summarize([])) is None
+
+
 def test_traffic_record_tracks_kernel_source(tmp_path, monkeypatch):
     rec = {"k": {"w": {"source_sha": bench.kernel_source_sha(), "heads": 4, "dram_bytes_per_launch": 400.0}}}
     path = tmp_path / "traffic.json"
