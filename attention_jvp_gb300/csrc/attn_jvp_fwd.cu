@@ -54,28 +54,35 @@ template <int D>
 struct FwdCfg {
   static constexpr int kBM = 128;                  // query rows per CTA (= TMEM lanes)
   static constexpr int kBN = 64;                   // keys per tile
-  static constexpr int kDC = D / 64;               // 64-element (128-byte) d-chunks
-  static constexpr int kNS = (D == 128) ? 1 : 3;   // S TMEM buffers
+  static constexpr int kDC = D / 64;               // 64-element (128-byte) d-chunks of Q and K
+  // Value columns per CTA.  O and T take 2 kDV TMEM columns; at d = 256 the two
+  // whole would fill TMEM, so two CTAs share a query tile, each accumulating
+  // half of the value columns (and each computing the full scores).
+  static constexpr int kDV = D > 128 ? 128 : D;
+  static constexpr int kVC = kDV / 64;             // 64-element chunks of a value tile
+  static constexpr int kVSplit = D / kDV;          // CTAs per query tile
+  static constexpr int kNS = (D == 64) ? 3 : 1;    // S TMEM buffers
   static constexpr int kNSt = 3;                   // St (then P~/H~) TMEM buffers
-  static constexpr int kKS = (D == 128) ? 2 : 3;   // K/Kt ring stages
-  static constexpr int kVS = (D == 128) ? 2 : 3;   // V/Vt ring stages
+  // K/Kt and V/Vt ring stages (d = 256: one each, as Q and Qt alone take 128 KB)
+  static constexpr int kKS = (D == 64) ? 3 : (D == 128 ? 2 : 1);
+  static constexpr int kVS = (D == 64) ? 3 : (D == 128 ? 2 : 1);
   static constexpr int kChunkQ = kBM * 128;        // one d-chunk of a Q tile (bytes)
   static constexpr int kChunkK = kBN * 128;        // one d-chunk of a key tile (bytes)
   static constexpr int kQBytes = kDC * kChunkQ;    // Q (or Qt) tile
   static constexpr int kKStage = 2 * kDC * kChunkK;  // K chunks, then Kt chunks
-  static constexpr int kVStage = 2 * kDC * kChunkK;  // V chunks, then Vt chunks
+  static constexpr int kVStage = 2 * kVC * kChunkK;  // V chunks, then Vt chunks (this CTA's columns)
   static constexpr int kOffQ = 0;
   static constexpr int kOffQt = kQBytes;
   static constexpr int kOffK = 2 * kQBytes;
   static constexpr int kOffV = kOffK + kKS * kKStage;
   static constexpr int kOffBar = kOffV + kVS * kVStage;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
-  // TMEM columns (fp32 each): O [0,D), T [D,2D), S buffer b [2D+64b, +64),
-  // St buffer c [2D+64NS+64c, +64)
+  // TMEM columns (fp32 each): O [0,DV), T [DV,2DV), S buffer b [2DV+64b, +64),
+  // St buffer c [2DV+64NS+64c, +64)
   static constexpr uint32_t kColO = 0;
-  static constexpr uint32_t kColT = D;
-  static constexpr uint32_t kColS = 2 * D;
-  static constexpr uint32_t kColSt = 2 * D + 64 * kNS;
+  static constexpr uint32_t kColT = kDV;
+  static constexpr uint32_t kColS = 2 * kDV;
+  static constexpr uint32_t kColSt = 2 * kDV + 64 * kNS;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kColSt + 64 * kNSt <= kTmemCols, "TMEM budget");
   static_assert(kNS <= 3 && kNSt <= 3 && kKS <= 3 && kVS <= 3, "barrier arrays");
@@ -215,7 +222,7 @@ __device__ __forceinline__ bool softmax_tile(uint32_t lane_addr, uint32_t cS, ui
     if (!ok) return false;
     tc_fence_after_sync();
 #pragma unroll 1
-    for (int c0 = 0; c0 < 2 * D; c0 += 32) {
+    for (int c0 = 0; c0 < 2 * FwdCfg<D>::kDV; c0 += 32) {
       uint32_t acc[32];
       tmem_ld32_wait(lane_addr + c0, acc);
 #pragma unroll
@@ -231,8 +238,9 @@ __device__ __forceinline__ bool softmax_tile(uint32_t lane_addr, uint32_t cS, ui
 }
 
 // Epilogue of the calling thread's row: O = O~/l, mu = r/l, Ot = T~/l - mu O and
-// LSE = (m + log2 l) ln 2, read from TMEM (O~ in columns 0-D, T~ in D-2D).  The
-// first d columns are written, at element offset ``obase`` of out / out_t.
+// LSE = (m + log2 l) ln 2, read from TMEM (O~ in columns 0-DV, T~ in DV-2DV).
+// The CTA's value columns (the first d of them for d < 64) are written at
+// element offset ``obase`` of out / out_t; LSE and mu where those are non-null.
 template <int D>
 __device__ __forceinline__ void write_row(uint32_t lane_addr, const RowState& st, int64_t ridx, int64_t obase,
                                           bool valid_row, int d, float* __restrict__ out,
@@ -240,20 +248,22 @@ __device__ __forceinline__ void write_row(uint32_t lane_addr, const RowState& st
                                           float* __restrict__ mu_out) {
   const float inv_l = 1.f / st.l;
   const float mu = st.r * inv_l;
-  // d == D except for the 16/32-wide heads run by the D = 64 instantiation.
-  const int ncols = D == 128 ? D : d;
+  // The CTA's kDV value columns, except for the 16/32-wide heads run by the
+  // D = 64 instantiation.
+  constexpr int kDV = FwdCfg<D>::kDV;
+  const int ncols = D == 64 ? d : kDV;
 #pragma unroll 1
   for (int c0 = 0; c0 < ncols; c0 += 32) {
     uint32_t ov[32], tv[32];
     tmem_ld32_wait(lane_addr + c0, ov);
-    tmem_ld32_wait(lane_addr + D + c0, tv);
+    tmem_ld32_wait(lane_addr + kDV + c0, tv);
     if (valid_row) {
       float4* o4 = reinterpret_cast<float4*>(out + obase + c0);
       float4* t4 = reinterpret_cast<float4*>(out_t + obase + c0);
-      const int n4 = D == 128 ? 8 : min(8, (ncols - c0) >> 2);
+      const int n4 = D != 64 ? 8 : min(8, (ncols - c0) >> 2);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        if (D != 128 && i >= n4) break;
+        if (D == 64 && i >= n4) break;
         float4 o, t;
         o.x = __uint_as_float(ov[4 * i + 0]) * inv_l;
         o.y = __uint_as_float(ov[4 * i + 1]) * inv_l;
@@ -294,9 +304,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int n_qtiles = geom.n_qtiles, kv_start = geom.kv_start, kv_len = geom.kv_len;
   const float scale = geom.scale;
-  const int bh = blockIdx.x / n_qtiles;
+  // Both value halves of a query tile (d = 256) are neighbours in the grid, so
+  // they stream the same key tiles through L2 at about the same time.
+  const int vh = blockIdx.x % C::kVSplit;  // which kDV value columns this CTA accumulates
+  const unsigned qb = blockIdx.x / C::kVSplit;  // unsigned: the divisions below stay unsigned
+  const int bh = qb / n_qtiles;
   const int hh = bh % geom.H, bb = bh / geom.H;
-  const int q0 = (blockIdx.x % n_qtiles) * C::kBM;
+  const int q0 = (qb % n_qtiles) * C::kBM;
   const int n_tiles = (kv_len + C::kBN - 1) / C::kBN;
 
 
@@ -376,9 +390,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* st = smem + C::kOffV + s * C::kVStage;
         const int key0 = kv_start + t * C::kBN;
         mbar_arrive_expect_tx(&bars->v_full[s], C::kVStage);
-        for (int c = 0; c < C::kDC; ++c) {
-          tma_load_4d(st + c * C::kChunkK, &maps.v, &bars->v_full[s], c * 64, key0, hh, bb);
-          tma_load_4d(st + (C::kDC + c) * C::kChunkK, &maps.vt, &bars->v_full[s], c * 64, key0, hh, bb);
+        for (int c = 0; c < C::kVC; ++c) {
+          const int col = vh * C::kDV + c * 64;
+          tma_load_4d(st + c * C::kChunkK, &maps.v, &bars->v_full[s], col, key0, hh, bb);
+          tma_load_4d(st + (C::kVC + c) * C::kChunkK, &maps.vt, &bars->v_full[s], col, key0, hh, bb);
         }
         issued = t + 1;
       }
@@ -393,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Independent issuing threads; they meet only through the mbarriers below.
     if (lane == 0) {
       constexpr uint32_t kIdS = make_idesc_bf16_f32(128, C::kBN, false, false);  // Q K^T, both K-major
-      constexpr uint32_t kIdPV = make_idesc_bf16_f32(128, D, false, true);      // P~ V, V is N-major
+      constexpr uint32_t kIdPV = make_idesc_bf16_f32(128, C::kDV, false, true);  // P~ V, V is N-major
       // Descriptors are built once; an operand step adds its byte offset / 16 to the
       // start-address field (every offset here stays inside one CTA's shared memory).
       const uint64_t dQ = make_smem_desc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
@@ -474,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < C::kBN / 16; ++kk) {
             const uint64_t bV = off(dV, kk * 2048);
-            const uint64_t bVt = off(dV, C::kDC * C::kChunkK + kk * 2048);
+            const uint64_t bVt = off(dV, C::kVC * C::kChunkK + kk * 2048);
             const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
             mma_ts(tmem + C::kColO, aP + kk * 8, bV, kIdPV, acc);   // O += P~ V
             mma_ts(tmem + C::kColT, aP + kk * 8, bVt, kIdPV, acc);  // T += P~ Vt
@@ -531,9 +546,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qrow = q0 + row;
       const int64_t obase = static_cast<int64_t>(bb) * geom.o_stride[0] +
                             static_cast<int64_t>(qrow) * geom.o_stride[1] +
-                            static_cast<int64_t>(hh) * geom.o_stride[2];
+                            static_cast<int64_t>(hh) * geom.o_stride[2] + vh * C::kDV;
+      // Every value half computes the same LSE and mu; the first one writes them.
       write_row<D>(lane_addr, st, static_cast<int64_t>(bh) * geom.Nq + qrow, obase, qrow < geom.Nq, geom.d, out,
-                   out_t, lse_out, mu_out);
+                   out_t, vh == 0 ? lse_out : nullptr, vh == 0 ? mu_out : nullptr);
     }
   }
 
@@ -590,15 +606,15 @@ cudaError_t launch_d(const FwdArgs& a, const char** msg) {
     *msg = "cuTensorMapEncodeTiled rejected a tensor (alignment, stride or size)";
     return e;
   }
-  static bool attr_set[2] = {false, false};
+  static bool attr_set = false;  // one per instantiation
   auto kern = attn_jvp_fwd_kernel<D>;
-  if (!attr_set[D == 128]) {
+  if (!attr_set) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) {
       *msg = "cudaFuncSetAttribute(max dynamic shared memory) failed";
       return e;
     }
-    attr_set[D == 128] = true;
+    attr_set = true;
   }
   const int n_qtiles = static_cast<int>((a.Nq + C::kBM - 1) / C::kBM);
   geom.H = static_cast<int>(a.H);
@@ -609,7 +625,7 @@ cudaError_t launch_d(const FwdArgs& a, const char** msg) {
   geom.d = static_cast<int>(a.d);
   geom.scale = a.scale;
   for (int i = 0; i < 3; ++i) geom.o_stride[i] = a.o_stride[i];
-  const int64_t grid = static_cast<int64_t>(n_qtiles) * a.B * a.H;
+  const int64_t grid = static_cast<int64_t>(n_qtiles) * a.B * a.H * C::kVSplit;
   kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, a.stream>>>(maps, geom, a.out, a.out_t, a.lse, a.mu,
                                                                            a.status);
   e = cudaGetLastError();
@@ -620,6 +636,7 @@ cudaError_t launch_d(const FwdArgs& a, const char** msg) {
 }  // namespace
 
 cudaError_t launch_attn_jvp_fwd(const FwdArgs& a, const char** msg) {
+  if (a.d == 256) return launch_d<256>(a, msg);
   if (a.d == 128) return launch_d<128>(a, msg);
   if (a.d == 16 || a.d == 32 || a.d == 64) return launch_d<64>(a, msg);
   *msg = "unsupported head dimension";

@@ -67,13 +67,17 @@ int* status_word(const char** why) {
   return g_status_ptr[dev];
 }
 
-int check_head_dim(int64_t d) {
+// Head dims: 16, 32, 64 and 128 everywhere; 256 in the forward only (two CTAs
+// per query tile, each accumulating half of the value columns).
+int check_head_dim(int64_t d, bool forward) {
   if (d == 16 || d == 32 || d == 64 || d == 128) return ATTNJVP_OK;
+  if (d == 256 && forward) return ATTNJVP_OK;
   if (d == 256)
     return fail(ATTNJVP_EUNSUPPORTED,
-                "head dim 256 not supported: the fp32 O and Ot accumulators of 128 query rows would fill all 512 "
-                "tensor-memory columns, leaving none for the scores");
-  return fail(ATTNJVP_EUNSUPPORTED, "head dim %lld not supported (this build: 16, 32, 64, 128)", (long long)d);
+                "head dim 256 not supported by the backward: the fp32 dK and dV accumulators of 128 keys would "
+                "fill all 512 tensor-memory columns, leaving none for the scores");
+  return fail(ATTNJVP_EUNSUPPORTED, "head dim %lld not supported (16, 32, 64, 128; 256 in the forward)",
+              (long long)d);
 }
 
 int check_attn_args(const void* q, const void* k, const void* v, const void* q_t, const void* k_t, const void* v_t,
@@ -93,10 +97,10 @@ int check_attn_args(const void* q, const void* k, const void* v, const void* q_t
   if (B * H >= (int64_t(1) << 31) || N >= (int64_t(1) << 31))
     return fail(ATTNJVP_EINVAL, "B*H and N must be < 2^31");
   if (!std::isfinite(scale) || !(scale > 0.f)) return fail(ATTNJVP_EINVAL, "scale must be finite and > 0");
-  int rc = check_head_dim(d);
+  int rc = check_head_dim(d, true);
   if (rc != ATTNJVP_OK) return rc;
   const int64_t n_qtiles = (N + 127) / 128;
-  if (n_qtiles * B * H >= (int64_t(1) << 31)) return fail(ATTNJVP_EINVAL, "too many query tiles");
+  if (n_qtiles * B * H * (d == 256 ? 2 : 1) >= (int64_t(1) << 31)) return fail(ATTNJVP_EINVAL, "too many query tiles");
   return ATTNJVP_OK;
 }
 
@@ -310,7 +314,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* dout, cons
   if (B * H >= (int64_t(1) << 31) || N_q >= (int64_t(1) << 31) || N_kv >= (int64_t(1) << 31))
     return fail(ATTNJVP_EINVAL, "B*H, N_q and N_kv must be < 2^31");
   if (!std::isfinite(scale) || !(scale > 0.f)) return fail(ATTNJVP_EINVAL, "scale must be finite and > 0");
-  int rc = check_head_dim(d);
+  int rc = check_head_dim(d, false);
   if (rc != ATTNJVP_OK) return rc;
   if (((N_q + 127) / 128) * B * H >= (int64_t(1) << 31) || ((N_kv + 127) / 128) * B * H >= (int64_t(1) << 31))
     return fail(ATTNJVP_EINVAL, "too many row tiles");

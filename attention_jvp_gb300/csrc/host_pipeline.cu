@@ -110,8 +110,8 @@ Slot slot_layout(int64_t g, int64_t N, int64_t d, int64_t n_chunks) {
 
 int check_shape(int64_t B, int64_t H, int64_t N, int64_t d, int64_t n_chunks, int64_t group_heads) {
   if (B < 1 || H < 1 || N < 1) return reject(ATTNJVP_EINVAL, "B, H, N must be >= 1");
-  if (d != 16 && d != 32 && d != 64 && d != 128)
-    return reject(ATTNJVP_EUNSUPPORTED, "head dim not supported (this build: 16, 32, 64, 128)");
+  if (d != 16 && d != 32 && d != 64 && d != 128 && d != 256)
+    return reject(ATTNJVP_EUNSUPPORTED, "head dim not supported (16, 32, 64, 128, 256)");
   if (n_chunks < 1 || n_chunks > N) return reject(ATTNJVP_EINVAL, "n_chunks must be in [1, N]");
   if (group_heads < 0) return reject(ATTNJVP_EINVAL, "group_heads must be >= 0 (0 = automatic)");
   if (N >= (int64_t(1) << 31) || B * H >= (int64_t(1) << 31)) return reject(ATTNJVP_EINVAL, "B*H and N must be < 2^31");

@@ -54,8 +54,10 @@ extern "C" {
  *   lse, mu                : fp32 [B, H, N] — natural-log LSE and mu; either may be
  *                            NULL when not wanted.
  *   B, H, N                : >= 1 each; B*H < 2^31 and N < 2^31.
- *   d                      : head dimension; 16, 32, 64 or 128 in this build (others,
- *                            including the page's 256: ATTNJVP_EUNSUPPORTED).
+ *   d                      : head dimension: 16, 32, 64, 128 or 256 (the page's set;
+ *                            others: ATTNJVP_EUNSUPPORTED).  At 256 two CTAs share a
+ *                            128-row query tile, each accumulating half of the value
+ *                            columns, so the scores are computed twice.
  *   scale                  : softmax scale s, finite and > 0 (the page's default is d^-1/2).
  */
 int attn_jvp_fwd(const void* q, const void* k, const void* v,
@@ -92,7 +94,7 @@ int attn_jvp_fwd_chunk(const void* q, const void* k, const void* v,
  *   out, out_t          : fp32 O and Ot at the output strides; 16-byte aligned.
  *   lse, mu             : fp32 [B, H, N_q] contiguous, or NULL.
  *   B, H, N_q, N_kv     : >= 1 each (cross-attention when N_q != N_kv).
- *   d                   : 16, 32, 64 or 128.
+ *   d                   : 16, 32, 64, 128 or 256.
  *   strides             : HOST array of 9 element strides — query (batch, seq,
  *                         head), key (batch, seq, head), output (batch, seq,
  *                         head) — or NULL for contiguous [B, H, N, d] everywhere.
@@ -243,7 +245,8 @@ int64_t attn_jvp_fwd_host_workspace_bytes(int64_t B, int64_t H, int64_t N, int64
  *                    write them.  P is rebuilt from lse; rowsum(dP (.) P) is
  *                    taken as rowsum(dO (.) O), equal since O = P V.
  *   dq, dk, dv     : fp32, shaped like q, k, v; 16-byte aligned.
- *   d              : 16, 32, 64 or 128;  scale: the forward's scale.
+ *   d              : 16, 32, 64 or 128 (256: ATTNJVP_EUNSUPPORTED, as dK and dV of
+ *                    128 keys would fill tensor memory);  scale: the forward's scale.
  *   workspace      : DEVICE, 256-byte aligned, attn_bwd_workspace_bytes(B, H, N_q).
  * Two passes (keys resident for dK/dV, queries resident for dQ) recompute the
  * scores instead of accumulating dQ with atomics, so results are reproducible.

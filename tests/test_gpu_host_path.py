@@ -51,6 +51,7 @@ CASES = [
     (1, 7, 517, 64, 1, 3),    # groups of 3, 3 and 1 heads
     (2, 3, 1000, 128, 3, 2),  # split path per item
     (1, 4, 129, 128, 1, 0),   # automatic group size (one item)
+    (1, 3, 300, 256, 2, 2),   # head dim 256, split path, groups of 2 and 1 heads
 ]
 
 

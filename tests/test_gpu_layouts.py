@@ -1,4 +1,4 @@
-"""GPU: strided layouts, cross-attention (N_q != N_kv) and head dims 16/32
+"""GPU: strided layouts, cross-attention (N_q != N_kv) and head dims 16/32/256
 through attn_jvp_fwd_strided, against the FP64 oracle and, where the same
 numbers go through the contiguous path, bit for bit against it.
 
@@ -47,7 +47,7 @@ def _check(got, ref):
     assert np.max(np.abs(host64(got[2]) - ref[2])) <= 1e-3
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_bshd_layout_is_bit_identical_to_contiguous(cuda_lib, d):
     x = inputs.make_inputs(2, 3, 300, d, seed=21, device="cuda", qk="rms", tangent_scale=0.3)
     ref = _contig(x)
@@ -75,7 +75,8 @@ def test_packed_qkv_views_are_bit_identical(cuda_lib):
 
 
 @pytest.mark.parametrize("nq,nkv,d,layout", [(300, 1000, 64, "bhsd"), (1000, 77, 128, "bhsd"),
-                                              (129, 640, 128, "bshd"), (1, 5, 64, "bhsd")])
+                                              (129, 640, 128, "bshd"), (1, 5, 64, "bhsd"),
+                                              (300, 1000, 256, "bshd"), (77, 130, 256, "bhsd")])
 def test_cross_attention_against_oracle(cuda_lib, nq, nkv, d, layout):
     xq = inputs.make_inputs(2, 2, nq, d, seed=30 + nq, device="cuda", qk="rms", tangent_scale=0.3)
     xk = inputs.make_inputs(2, 2, nkv, d, seed=31 + nkv, device="cuda", qk="rms", tangent_scale=0.3)

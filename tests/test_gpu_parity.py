@@ -55,6 +55,10 @@ SMALL = [
     (1, 2, 1000, 128, dict(qk="rms", tangent_scale=0.3)),  # many key tiles, ragged tail
     (1, 1, 700, 64, dict(outlier_frac=0.01)),              # +12 logits: forces rescales
     (2, 1, 517, 128, dict(tangent="student_t3", tangent_scale=0.1)),
+    # head dim 256: two CTAs per query tile, each with half of the value columns
+    (1, 2, 300, 256, dict(qk="rms", tangent_scale=0.3)),
+    (1, 1, 1, 256, {}),
+    (2, 1, 129, 256, dict(outlier_frac=0.01)),
 ]
 
 
@@ -90,8 +94,9 @@ def test_zero_tangents_give_exact_zero(cuda_lib):
     assert torch.all(ot == 0) and torch.all(mu == 0)
 
 
-def test_deterministic(cuda_lib):
-    x = inputs.make_inputs(1, 4, 1100, 64, seed=9, device="cuda")
+@pytest.mark.parametrize("d", [64, 256])
+def test_deterministic(cuda_lib, d):
+    x = inputs.make_inputs(1, 4, 1100, d, seed=9, device="cuda")
     a = _run(x)
     b = _run(x)
     for u, w in zip(a, b):
@@ -107,7 +112,7 @@ def test_optional_row_outputs(cuda_lib):
     assert torch.equal(o, o2) and torch.equal(ot, ot2)
 
 
-@pytest.mark.parametrize("N,d,chunks", [(1000, 128, 4), (611, 64, 3), (300, 128, 1)])
+@pytest.mark.parametrize("N,d,chunks", [(1000, 128, 4), (611, 64, 3), (300, 128, 1), (700, 256, 3)])
 def test_chunks_and_merge(cuda_lib, N, d, chunks):
     x = inputs.make_inputs(1, 2, N, d, seed=11 + chunks, device="cuda", qk="rms", tangent_scale=0.3)
     ws = binding.split_workspace(x["q"].shape, chunks, x["q"].device)
