@@ -47,6 +47,8 @@ def load(path=None):
     lib.attn_jvp_fwd_host.argtypes = [vp] * 6 + [fp] * 4 + [i64] * 4 + [ctypes.c_float, i64, i64, vp, i64, vp]
     lib.attn_jvp_fwd_strided.argtypes = [vp] * 6 + [fp] * 4 + [i64] * 5 + [ctypes.POINTER(i64), ctypes.c_float,
                                                                           i64, i64, vp]
+    lib.attn_jvp_fwd_ex.argtypes = [vp] * 6 + [fp] * 4 + [i64] * 6 + [ctypes.POINTER(i64), ctypes.c_float,
+                                                                    i64, i64, vp]
     lib.attn_jvp_fwd_host_workspace_bytes.argtypes = [i64] * 6
     lib.attn_jvp_fwd_host_workspace_bytes.restype = i64
     lib.trigflow_coeffs_jvp.argtypes = [ctypes.c_double] * 3 + [ctypes.POINTER(ctypes.c_double)]
@@ -64,7 +66,7 @@ def load(path=None):
     lib.attn_jvp_last_error.restype = ctypes.c_char_p
     lib.attn_jvp_version.restype = ctypes.c_char_p
     for name in ("attn_jvp_fwd", "attn_jvp_fwd_chunk", "attn_jvp_merge", "attn_jvp_cast_f32_bf16",
-                 "attn_jvp_fwd_split_noalloc", "attn_jvp_fwd_host", "attn_jvp_fwd_strided",
+                 "attn_jvp_fwd_split_noalloc", "attn_jvp_fwd_host", "attn_jvp_fwd_strided", "attn_jvp_fwd_ex",
                  "trigflow_coeffs_jvp", "trigflow_output_jvp", "scm_tangent_loss", "attn_bwd",
                  "trigflow_coeffs", "trigflow_tangent", "attn_jvp_status", "attn_jvp_selftest_wait"):
         getattr(lib, name).restype = ctypes.c_int
@@ -198,29 +200,36 @@ def attn_jvp_fwd_strided(q, k, v, q_t, k_t, v_t, layout="bhsd", scale=None, out=
     """Strided / cross-attention form.  ``layout`` names the dimension order of every
     tensor's shape: "bhsd" ([B, H, S, D]) or "bshd" ([B, S, H, D], the page's).  Any
     strides are accepted as long as the head dimension is unit-stride; tangents must
-    share their primal's strides.  Outputs O, Ot default to a new contiguous tensor in
-    ``layout``; lse, mu are [B, H, N_q].  ``kv_start``/``kv_len`` select a key range."""
+    share their primal's strides.  V (and Vt) may have a head dim of their own,
+    d_v; O and Ot then have d_v columns.  Outputs O, Ot default to a new contiguous
+    tensor in ``layout``; lse, mu are [B, H, N_q].  ``kv_start``/``kv_len`` select a
+    key range.  Calls attn_jvp_fwd_ex."""
     if layout not in _LAYOUTS:
         raise ValueError("layout must be one of %s" % sorted(_LAYOUTS))
     (B, Nq, H, d), qs = _layout_view(q, "q", layout)
     (Bk, Nkv, Hk, dk), ks = _layout_view(k, "k", layout)
     if (Bk, Hk, dk) != (B, H, d):
         raise ValueError("k must match q in batch, heads and head dim")
-    for n, t, ref in (("q_t", q_t, q), ("v", v, k), ("k_t", k_t, k), ("v_t", v_t, k)):
+    (Bv, Nv, Hv, d_v), vs = _layout_view(v, "v", layout)
+    if (Bv, Nv, Hv) != (B, Nkv, H):
+        raise ValueError("v must match k in batch, sequence length and heads")
+    for n, t, ref in (("q_t", q_t, q), ("k_t", k_t, k), ("v_t", v_t, v)):
         _layout_view(t, n, layout)
         if tuple(t.shape) != tuple(ref.shape) or t.stride() != ref.stride():
-            raise ValueError("%s must have the shape and strides of %s" % (n, "q" if ref is q else "k"))
-    shape_q = tuple(q.shape)
+            raise ValueError("%s must have the shape and strides of %s" % (n, n[0]))
+    ib, isq, ih, _ = _LAYOUTS[layout]
+    shape_o = list(q.shape)
+    shape_o[3] = d_v
+    shape_o = tuple(shape_o)
     if out is None:
-        out = torch.empty(shape_q, dtype=torch.float32, device=q.device)
+        out = torch.empty(shape_o, dtype=torch.float32, device=q.device)
     if out_t is None:
-        out_t = torch.empty(shape_q, dtype=torch.float32, device=q.device)
+        out_t = torch.empty(shape_o, dtype=torch.float32, device=q.device)
     for n, t in (("out", out), ("out_t", out_t)):
-        if not t.is_cuda or t.dtype != torch.float32 or tuple(t.shape) != shape_q or t.stride(3) != 1:
-            raise ValueError("%s must be a float32 CUDA tensor of q's shape with a unit last stride" % n)
+        if not t.is_cuda or t.dtype != torch.float32 or tuple(t.shape) != shape_o or t.stride(3) != 1:
+            raise ValueError("%s must be a float32 CUDA tensor of shape %s with a unit last stride" % (n, shape_o))
     if out_t.stride() != out.stride():
         raise ValueError("out_t must have out's strides")
-    ib, isq, ih, _ = _LAYOUTS[layout]
     os_ = (out.stride(ib), out.stride(isq), out.stride(ih))
     if lse is None and want_rows:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
@@ -232,11 +241,11 @@ def attn_jvp_fwd_strided(q, k, v, q_t, k_t, v_t, layout="bhsd", scale=None, out=
         _req(mu, "mu", torch.float32, (B, H, Nq))
     kv_len = Nkv - kv_start if kv_len is None else int(kv_len)
     scale = d ** -0.5 if scale is None else float(scale)
-    strides = (ctypes.c_int64 * 9)(*qs, *ks, *os_)
-    rc = load().attn_jvp_fwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(q_t), _ptr(k_t), _ptr(v_t),
-                                     _ptr(out), _ptr(out_t), _ptr(lse), _ptr(mu), B, H, Nq, Nkv, d, strides,
-                                     ctypes.c_float(scale), int(kv_start), kv_len, _stream(stream))
-    _check("attn_jvp_fwd_strided", rc)
+    strides = (ctypes.c_int64 * 12)(*qs, *ks, *vs, *os_)
+    rc = load().attn_jvp_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(q_t), _ptr(k_t), _ptr(v_t),
+                                _ptr(out), _ptr(out_t), _ptr(lse), _ptr(mu), B, H, Nq, Nkv, d, d_v, strides,
+                                ctypes.c_float(scale), int(kv_start), kv_len, _stream(stream))
+    _check("attn_jvp_fwd_ex", rc)
     return out, out_t, lse, mu
 
 

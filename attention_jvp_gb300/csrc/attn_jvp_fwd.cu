@@ -50,27 +50,32 @@ namespace {
 
 using namespace ptx;
 
-template <int D>
+// D: Q/K head dim rounded up to a multiple of 64 (16 and 32 run as 64, their
+// missing columns zero-filled by TMA); DVF: the same for V/O.
+template <int D, int DVF>
 struct FwdCfg {
   static constexpr int kBM = 128;                  // query rows per CTA (= TMEM lanes)
   static constexpr int kBN = 64;                   // keys per tile
   static constexpr int kDC = D / 64;               // 64-element (128-byte) d-chunks of Q and K
-  // Value columns per CTA.  O and T take 2 kDV TMEM columns; at d = 256 the two
-  // whole would fill TMEM, so two CTAs share a query tile, each accumulating
-  // half of the value columns (and each computing the full scores).
-  static constexpr int kDV = D > 128 ? 128 : D;
+  // Value columns per CTA.  O and T take 2 kDV TMEM columns; at a value head dim
+  // of 256 the two whole would fill TMEM, so two CTAs share a query tile, each
+  // accumulating half of the value columns (and each computing the full scores).
+  static constexpr int kDV = DVF > 128 ? 128 : DVF;
   static constexpr int kVC = kDV / 64;             // 64-element chunks of a value tile
-  static constexpr int kVSplit = D / kDV;          // CTAs per query tile
-  static constexpr int kNS = (D == 64) ? 3 : 1;    // S TMEM buffers
+  static constexpr int kVSplit = DVF / kDV;        // CTAs per query tile
+  static constexpr bool kSmallV = DVF == 64;       // value heads of 16, 32 or 64 columns
+  static constexpr int kNS = (kDV == 64) ? 3 : 1;  // S TMEM buffers
   static constexpr int kNSt = 3;                   // St (then P~/H~) TMEM buffers
-  // K/Kt and V/Vt ring stages (d = 256: one each, as Q and Qt alone take 128 KB)
-  static constexpr int kKS = (D == 64) ? 3 : (D == 128 ? 2 : 1);
-  static constexpr int kVS = (D == 64) ? 3 : (D == 128 ? 2 : 1);
   static constexpr int kChunkQ = kBM * 128;        // one d-chunk of a Q tile (bytes)
   static constexpr int kChunkK = kBN * 128;        // one d-chunk of a key tile (bytes)
   static constexpr int kQBytes = kDC * kChunkQ;    // Q (or Qt) tile
   static constexpr int kKStage = 2 * kDC * kChunkK;  // K chunks, then Kt chunks
   static constexpr int kVStage = 2 * kVC * kChunkK;  // V chunks, then Vt chunks (this CTA's columns)
+  // K/Kt and V/Vt ring stages: as many as shared memory holds, up to three each
+  // (Q and Qt stay resident: 128 KB at d = 256, which leaves room for one).
+  static constexpr int kRoom = 227 * 1024 - 1280 - 2 * kQBytes;
+  static constexpr int kKS = kRoom >= 3 * (kKStage + kVStage) ? 3 : (kRoom >= 2 * (kKStage + kVStage) ? 2 : 1);
+  static constexpr int kVS = kKS;
   static constexpr int kOffQ = 0;
   static constexpr int kOffQt = kQBytes;
   static constexpr int kOffK = 2 * kQBytes;
@@ -104,7 +109,7 @@ struct FwdMaps {
 // packed QKV tensor, ...) is read in place.
 struct FwdGeom {
   int H, Nq, n_qtiles, kv_start, kv_len;
-  int d;                    // real head dimension; columns d..D-1 of every tile are zero (TMA fill)
+  int d_v;                  // real value head dimension: the output columns written
   float scale;
   int64_t o_stride[3];      // output element strides: batch, sequence, head
 };
@@ -136,7 +141,7 @@ struct RowState {
 // grows by more than the threshold the accumulators O and T (columns 0-2D) are
 // rescaled after ``wait_prev_pv()`` confirms the previous tile's value MMAs are
 // done.  Returns false (warp-uniformly) when a wait gave up.
-template <int D, class OnLoaded, class WaitPrevPv>
+template <class C, class OnLoaded, class WaitPrevPv>
 __device__ __forceinline__ bool softmax_tile(uint32_t lane_addr, uint32_t cS, uint32_t cSt, int valid, bool first,
                                              float c2,
                                              float scale, RowState& st, OnLoaded on_loaded,
@@ -222,7 +227,7 @@ __device__ __forceinline__ bool softmax_tile(uint32_t lane_addr, uint32_t cS, ui
     if (!ok) return false;
     tc_fence_after_sync();
 #pragma unroll 1
-    for (int c0 = 0; c0 < 2 * FwdCfg<D>::kDV; c0 += 32) {
+    for (int c0 = 0; c0 < 2 * C::kDV; c0 += 32) {
       uint32_t acc[32];
       tmem_ld32_wait(lane_addr + c0, acc);
 #pragma unroll
@@ -241,17 +246,16 @@ __device__ __forceinline__ bool softmax_tile(uint32_t lane_addr, uint32_t cS, ui
 // LSE = (m + log2 l) ln 2, read from TMEM (O~ in columns 0-DV, T~ in DV-2DV).
 // The CTA's value columns (the first d of them for d < 64) are written at
 // element offset ``obase`` of out / out_t; LSE and mu where those are non-null.
-template <int D>
+template <class C>
 __device__ __forceinline__ void write_row(uint32_t lane_addr, const RowState& st, int64_t ridx, int64_t obase,
                                           bool valid_row, int d, float* __restrict__ out,
                                           float* __restrict__ out_t, float* __restrict__ lse_out,
                                           float* __restrict__ mu_out) {
   const float inv_l = 1.f / st.l;
   const float mu = st.r * inv_l;
-  // The CTA's kDV value columns, except for the 16/32-wide heads run by the
-  // D = 64 instantiation.
-  constexpr int kDV = FwdCfg<D>::kDV;
-  const int ncols = D == 64 ? d : kDV;
+  // The CTA's kDV value columns, except for the 16/32-wide value heads run as 64.
+  constexpr int kDV = C::kDV;
+  const int ncols = C::kSmallV ? d : kDV;
 #pragma unroll 1
   for (int c0 = 0; c0 < ncols; c0 += 32) {
     uint32_t ov[32], tv[32];
@@ -260,10 +264,10 @@ __device__ __forceinline__ void write_row(uint32_t lane_addr, const RowState& st
     if (valid_row) {
       float4* o4 = reinterpret_cast<float4*>(out + obase + c0);
       float4* t4 = reinterpret_cast<float4*>(out_t + obase + c0);
-      const int n4 = D != 64 ? 8 : min(8, (ncols - c0) >> 2);
+      const int n4 = !C::kSmallV ? 8 : min(8, (ncols - c0) >> 2);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        if (D == 64 && i >= n4) break;
+        if (C::kSmallV && i >= n4) break;
         float4 o, t;
         o.x = __uint_as_float(ov[4 * i + 0]) * inv_l;
         o.y = __uint_as_float(ov[4 * i + 1]) * inv_l;
@@ -284,12 +288,12 @@ __device__ __forceinline__ void write_row(uint32_t lane_addr, const RowState& st
   }
 }
 
-template <int D>
+template <int D, int DVF>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_jvp_fwd_kernel(const __grid_constant__ FwdMaps maps, const __grid_constant__ FwdGeom geom,
                         float* __restrict__ out, float* __restrict__ out_t, float* __restrict__ lse_out,
                         float* __restrict__ mu_out, int* status) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, DVF>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Barriers* bars = reinterpret_cast<Barriers*>(smem + C::kOffBar);
@@ -523,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int valid = min(C::kBN, kv_len - j * C::kBN);
       // Hand-offs arrive once per warp: every lane has fenced its own TMEM
       // accesses, __syncwarp orders them before lane 0's arrival.
-      ok = softmax_tile<D>(
+      ok = softmax_tile<C>(
           lane_addr, cS, cSt, valid, j == 0, c2, scale, st,
           [&]() {
             __syncwarp();
@@ -548,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             static_cast<int64_t>(qrow) * geom.o_stride[1] +
                             static_cast<int64_t>(hh) * geom.o_stride[2] + vh * C::kDV;
       // Every value half computes the same LSE and mu; the first one writes them.
-      write_row<D>(lane_addr, st, static_cast<int64_t>(bh) * geom.Nq + qrow, obase, qrow < geom.Nq, geom.d, out,
+      write_row<C>(lane_addr, st, static_cast<int64_t>(bh) * geom.Nq + qrow, obase, qrow < geom.Nq, geom.d_v, out,
                    out_t, vh == 0 ? lse_out : nullptr, vh == 0 ? mu_out : nullptr);
     }
   }
@@ -589,25 +593,26 @@ cudaError_t make_map(CUtensorMap* map, const void* ptr, int64_t d, int64_t rows,
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D>
+template <int D, int DVF>
 cudaError_t launch_d(const FwdArgs& a, const char** msg) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, DVF>;
   FwdMaps maps;
   FwdGeom geom;
   cudaError_t e = cudaSuccess;
   const void* ptrs[6] = {a.q, a.q_t, a.k, a.k_t, a.v, a.v_t};
   CUtensorMap* dst[6] = {&maps.q, &maps.qt, &maps.k, &maps.kt, &maps.v, &maps.vt};
   for (int i = 0; i < 6 && e == cudaSuccess; ++i) {
-    const bool query = i < 2;
-    e = make_map(dst[i], ptrs[i], a.d, query ? a.Nq : a.Nkv, a.H, a.B, query ? a.q_stride : a.kv_stride,
-                 query ? C::kBM : C::kBN);
+    const int g = i / 2;  // Q and Qt, K and Kt, V and Vt
+    const int64_t* st = g == 0 ? a.q_stride : (g == 1 ? a.k_stride : a.v_stride);
+    e = make_map(dst[i], ptrs[i], g == 2 ? a.d_v : a.d, g == 0 ? a.Nq : a.Nkv, a.H, a.B, st,
+                 g == 0 ? C::kBM : C::kBN);
   }
   if (e != cudaSuccess) {
     *msg = "cuTensorMapEncodeTiled rejected a tensor (alignment, stride or size)";
     return e;
   }
   static bool attr_set = false;  // one per instantiation
-  auto kern = attn_jvp_fwd_kernel<D>;
+  auto kern = attn_jvp_fwd_kernel<D, DVF>;
   if (!attr_set) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) {
@@ -622,7 +627,7 @@ cudaError_t launch_d(const FwdArgs& a, const char** msg) {
   geom.n_qtiles = n_qtiles;
   geom.kv_start = static_cast<int>(a.kv_start);
   geom.kv_len = static_cast<int>(a.kv_len);
-  geom.d = static_cast<int>(a.d);
+  geom.d_v = static_cast<int>(a.d_v);
   geom.scale = a.scale;
   for (int i = 0; i < 3; ++i) geom.o_stride[i] = a.o_stride[i];
   const int64_t grid = static_cast<int64_t>(n_qtiles) * a.B * a.H * C::kVSplit;
@@ -635,12 +640,34 @@ cudaError_t launch_d(const FwdArgs& a, const char** msg) {
 
 }  // namespace
 
+namespace {
+
+// Head dim rounded up to the instantiation that runs it (0: none).
+int padded_dim(int64_t d) {
+  if (d == 16 || d == 32 || d == 64) return 64;
+  if (d == 128 || d == 256) return static_cast<int>(d);
+  return 0;
+}
+
+template <int D>
+cudaError_t launch_dv(const FwdArgs& a, const char** msg) {
+  switch (padded_dim(a.d_v)) {
+    case 64: return launch_d<D, 64>(a, msg);
+    case 128: return launch_d<D, 128>(a, msg);
+    case 256: return launch_d<D, 256>(a, msg);
+    default: *msg = "unsupported value head dimension"; return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
 cudaError_t launch_attn_jvp_fwd(const FwdArgs& a, const char** msg) {
-  if (a.d == 256) return launch_d<256>(a, msg);
-  if (a.d == 128) return launch_d<128>(a, msg);
-  if (a.d == 16 || a.d == 32 || a.d == 64) return launch_d<64>(a, msg);
-  *msg = "unsupported head dimension";
-  return cudaErrorInvalidValue;
+  switch (padded_dim(a.d)) {
+    case 64: return launch_dv<64>(a, msg);
+    case 128: return launch_dv<128>(a, msg);
+    case 256: return launch_dv<256>(a, msg);
+    default: *msg = "unsupported head dimension"; return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace attnjvp

@@ -100,7 +100,8 @@ int check_attn_args(const void* q, const void* k, const void* v, const void* q_t
   int rc = check_head_dim(d, true);
   if (rc != ATTNJVP_OK) return rc;
   const int64_t n_qtiles = (N + 127) / 128;
-  if (n_qtiles * B * H * (d == 256 ? 2 : 1) >= (int64_t(1) << 31)) return fail(ATTNJVP_EINVAL, "too many query tiles");
+  // at a value head dim of 256 two CTAs share each query tile
+  if (n_qtiles * B * H * 2 >= (int64_t(1) << 31)) return fail(ATTNJVP_EINVAL, "too many query tiles");
   return ATTNJVP_OK;
 }
 
@@ -111,9 +112,12 @@ void contiguous_strides(int64_t H, int64_t N, int64_t d, int64_t st[3]) {
   st[2] = N * d;
 }
 
+// ``strides``: 12 element strides (batch, seq, head) of Q, K, V and O, or NULL
+// for contiguous [B, H, N, d] tensors.
 int run_fwd(const void* q, const void* k, const void* v, const void* q_t, const void* k_t, const void* v_t,
             float* out, float* out_t, float* lse, float* mu, int64_t B, int64_t H, int64_t Nq, int64_t Nkv,
-            int64_t d, const int64_t* strides, float scale, int64_t kv_start, int64_t kv_len, void* stream) {
+            int64_t d, int64_t d_v, const int64_t* strides, float scale, int64_t kv_start, int64_t kv_len,
+            void* stream) {
   const char* why = "";
   int* st = status_word(&why);
   if (!st) return fail(ATTNJVP_ECUDA, "no CUDA device / status word: %s", why);
@@ -133,16 +137,19 @@ int run_fwd(const void* q, const void* k, const void* v, const void* q_t, const 
   a.Nq = Nq;
   a.Nkv = Nkv;
   a.d = d;
+  a.d_v = d_v;
   if (strides) {
     for (int i = 0; i < 3; ++i) {
       a.q_stride[i] = strides[i];
-      a.kv_stride[i] = strides[3 + i];
-      a.o_stride[i] = strides[6 + i];
+      a.k_stride[i] = strides[3 + i];
+      a.v_stride[i] = strides[6 + i];
+      a.o_stride[i] = strides[9 + i];
     }
   } else {
     contiguous_strides(H, Nq, d, a.q_stride);
-    contiguous_strides(H, Nkv, d, a.kv_stride);
-    contiguous_strides(H, Nq, d, a.o_stride);
+    contiguous_strides(H, Nkv, d, a.k_stride);
+    contiguous_strides(H, Nkv, d_v, a.v_stride);
+    contiguous_strides(H, Nq, d_v, a.o_stride);
   }
   a.scale = scale;
   a.kv_start = kv_start;
@@ -184,7 +191,7 @@ int attn_jvp_fwd(const void* q, const void* k, const void* v, const void* q_t, c
                  float scale, void* stream) {
   int rc = check_attn_args(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, d, scale);
   if (rc != ATTNJVP_OK) return rc;
-  return run_fwd(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, N, d, nullptr, scale, 0, N, stream);
+  return run_fwd(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, N, d, d, nullptr, scale, 0, N, stream);
 }
 
 int attn_jvp_fwd_chunk(const void* q, const void* k, const void* v, const void* q_t, const void* k_t,
@@ -196,25 +203,27 @@ int attn_jvp_fwd_chunk(const void* q, const void* k, const void* v, const void* 
   if (kv_start < 0 || kv_len < 1 || kv_start + kv_len > N)
     return fail(ATTNJVP_EINVAL, "key range [%lld, %lld) outside [0, %lld) or empty", (long long)kv_start,
                 (long long)(kv_start + kv_len), (long long)N);
-  return run_fwd(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, N, d, nullptr, scale, kv_start, kv_len,
+  return run_fwd(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, N, d, d, nullptr, scale, kv_start, kv_len,
                  stream);
 }
 
-int attn_jvp_fwd_strided(const void* q, const void* k, const void* v, const void* q_t, const void* k_t,
-                         const void* v_t, float* out, float* out_t, float* lse, float* mu, int64_t B, int64_t H,
-                         int64_t Nq, int64_t Nkv, int64_t d, const int64_t* strides, float scale, int64_t kv_start,
-                         int64_t kv_len, void* stream) {
+int attn_jvp_fwd_ex(const void* q, const void* k, const void* v, const void* q_t, const void* k_t, const void* v_t,
+                    float* out, float* out_t, float* lse, float* mu, int64_t B, int64_t H, int64_t Nq, int64_t Nkv,
+                    int64_t d, int64_t d_v, const int64_t* strides, float scale, int64_t kv_start, int64_t kv_len,
+                    void* stream) {
   int rc = check_attn_args(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, Nq, d, scale);
+  if (rc != ATTNJVP_OK) return rc;
+  rc = check_head_dim(d_v, true);
   if (rc != ATTNJVP_OK) return rc;
   if (Nkv < 1 || Nkv >= (int64_t(1) << 31)) return fail(ATTNJVP_EINVAL, "N_kv must be in [1, 2^31)");
   if (kv_start < 0 || kv_len < 1 || kv_start + kv_len > Nkv)
     return fail(ATTNJVP_EINVAL, "key range [%lld, %lld) outside [0, %lld) or empty", (long long)kv_start,
                 (long long)(kv_start + kv_len), (long long)Nkv);
   if (strides) {
-    const char* what[3] = {"q", "kv", "out"};
-    for (int g = 0; g < 3; ++g) {
+    const char* what[4] = {"q", "k", "v", "out"};
+    for (int g = 0; g < 4; ++g) {
       // bf16 inputs: TMA strides are multiples of 16 bytes; fp32 outputs: float4 stores.
-      const int64_t unit = g < 2 ? 8 : 4;
+      const int64_t unit = g < 3 ? 8 : 4;
       for (int i = 0; i < 3; ++i) {
         const int64_t x = strides[3 * g + i];
         if (x < 0 || x % unit != 0 || x >= (int64_t(1) << 38))
@@ -223,8 +232,26 @@ int attn_jvp_fwd_strided(const void* q, const void* k, const void* v, const void
       }
     }
   }
-  return run_fwd(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, Nq, Nkv, d, strides, scale, kv_start, kv_len,
-                 stream);
+  return run_fwd(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, Nq, Nkv, d, d_v, strides, scale, kv_start,
+                 kv_len, stream);
+}
+
+int attn_jvp_fwd_strided(const void* q, const void* k, const void* v, const void* q_t, const void* k_t,
+                         const void* v_t, float* out, float* out_t, float* lse, float* mu, int64_t B, int64_t H,
+                         int64_t Nq, int64_t Nkv, int64_t d, const int64_t* strides, float scale, int64_t kv_start,
+                         int64_t kv_len, void* stream) {
+  // K and V share one stride set here (equal head dims)
+  int64_t st[12];
+  if (strides) {
+    for (int i = 0; i < 3; ++i) {
+      st[i] = strides[i];
+      st[3 + i] = strides[3 + i];
+      st[6 + i] = strides[3 + i];
+      st[9 + i] = strides[6 + i];
+    }
+  }
+  return attn_jvp_fwd_ex(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, Nq, Nkv, d, d, strides ? st : nullptr,
+                         scale, kv_start, kv_len, stream);
 }
 
 int attn_jvp_merge(const float* o_c, const float* ot_c, const float* lse_c, const float* mu_c, int64_t n_chunks,

@@ -14,8 +14,10 @@ constexpr int kStatusTimeout = 1;
 struct FwdArgs {
   const void *q, *k, *v, *q_t, *k_t, *v_t;  // bf16; element (b, s, h, c) at b*st[0] + s*st[1] + h*st[2] + c
   float *out, *out_t, *lse, *mu;            // fp32 O, Ot at the output strides; lse/mu [B, H, Nq] or null
-  int64_t B, H, Nq, Nkv, d;                 // d: the real head dimension (16, 32, 64 or 128)
-  int64_t q_stride[3], kv_stride[3], o_stride[3];  // element strides (batch, seq, head); head-dim stride 1
+  int64_t B, H, Nq, Nkv;
+  int64_t d, d_v;                           // head dims of Q/K and of V/O (each 16, 32, 64, 128 or 256)
+  // element strides (batch, seq, head) of Q (and Qt), K (and Kt), V (and Vt), O (and Ot); head-dim stride 1
+  int64_t q_stride[3], k_stride[3], v_stride[3], o_stride[3];
   float scale;
   int64_t kv_start, kv_len;
   int* status;                               // device status word

@@ -493,7 +493,7 @@ def run_gpu(args):
     flops_launch = sum(attention_flops(spec, kv) for kv in attn_kv) / len(attn_kv)
     achieved = flops_launch / (mean_launch_ms * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops_sustained"])
-    kname = "attn_jvp_fwd_kernel<%d>" % d
+    kname = "attn_jvp_fwd_kernel<%d, %d>" % (d, d)
     traffic = traffic_per_launch(kname, args.workload, H * B)
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": UNIT,
                 "frac": round(achieved / peak, 4), "traffic": traffic,

@@ -118,6 +118,25 @@ int attn_jvp_fwd_strided(const void* q, const void* k, const void* v,
                          int64_t kv_start, int64_t kv_len, void* stream);
 
 /*
+ * Most general form: attn_jvp_fwd_strided with a value head dim of its own.
+ * V, Vt, O and Ot have d_v columns per head, Q, Qt, K and Kt have d; the
+ * page's forward takes d_v != d_qk (its backward does not).
+ *   d, d_v              : 16, 32, 64, 128 or 256 each.
+ *   strides             : HOST array of 12 element strides — query, key, value
+ *                         and output, each (batch, seq, head) — or NULL for
+ *                         contiguous [B, H, N, d] (q, k) and [B, H, N, d_v]
+ *                         (v, out) tensors.  Same rules as attn_jvp_fwd_strided.
+ * Other arguments, ownership and errors as attn_jvp_fwd_strided, which is this
+ * call with d_v = d and the key strides used for the values too.
+ */
+int attn_jvp_fwd_ex(const void* q, const void* k, const void* v,
+                    const void* q_t, const void* k_t, const void* v_t,
+                    float* out, float* out_t, float* lse, float* mu,
+                    int64_t B, int64_t H, int64_t N_q, int64_t N_kv, int64_t d, int64_t d_v,
+                    const int64_t* strides, float scale, int64_t kv_start, int64_t kv_len,
+                    void* stream);
+
+/*
  * Exact merge of C key-chunk partials into the full-row result:
  *   LSE = ln sum_c e^{LSE_c},  w_c = e^{LSE_c - LSE},
  *   O = sum_c w_c O_c,  mu = sum_c w_c mu_c,  Ot = sum_c w_c (Ot_c + mu_c O_c) - mu O.

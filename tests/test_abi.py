@@ -203,6 +203,33 @@ def test_strided_entry_validation_needs_no_gpu(lib):
     assert _strided(lib, scale=0.0) == E.ATTNJVP_EINVAL
 
 
+def _ex(lib, strides=None, d=64, d_v=128, nq=100, nkv=300, scale=0.1):
+    vp = ctypes.c_void_p
+    st = None if strides is None else (ctypes.c_int64 * 12)(*strides)
+    return lib.attn_jvp_fwd_ex(*[vp(256)] * 6, vp(256), vp(256), None, None, 2, 3, nq, nkv, d, d_v, st,
+                               ctypes.c_float(scale), 0, nkv, None)
+
+
+def test_value_head_dim_entry_validation_needs_no_gpu(lib):
+    E = binding
+    assert _ex(lib, d_v=96) == E.ATTNJVP_EUNSUPPORTED
+    assert _ex(lib, d=48, d_v=64) == E.ATTNJVP_EUNSUPPORTED
+    assert _ex(lib, d_v=512) == E.ATTNJVP_EUNSUPPORTED
+    # [B, S, H, D] strides for q (d = 64), k (d = 64), v (d_v = 128), out (d_v = 128)
+    good = [100 * 3 * 64, 3 * 64, 64, 300 * 3 * 64, 3 * 64, 64, 300 * 3 * 128, 3 * 128, 128,
+            100 * 3 * 128, 3 * 128, 128]
+    bad = list(good)
+    bad[7] = 3 * 128 + 4  # value row stride: not a multiple of 8 elements (TMA)
+    assert _ex(lib, bad) == E.ATTNJVP_EINVAL
+    assert b"v stride 1" in lib.attn_jvp_last_error()
+    bad = list(good)
+    bad[10] = 3 * 128 + 2  # output row stride: not a multiple of 4 (float4 stores)
+    assert _ex(lib, bad) == E.ATTNJVP_EINVAL
+    assert b"out stride 1" in lib.attn_jvp_last_error()
+    assert _ex(lib, good, nkv=0) == E.ATTNJVP_EINVAL
+    assert _ex(lib, good, scale=float("nan")) == E.ATTNJVP_EINVAL
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
 def test_valid_strided_call_without_device_reports_cuda_error(lib):
     bshd = [100 * 3 * 16, 3 * 16, 16, 300 * 3 * 16, 3 * 16, 16, 100 * 3 * 16, 3 * 16, 16]

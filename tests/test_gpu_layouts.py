@@ -144,3 +144,26 @@ def test_padded_output_rows_leave_the_padding_untouched(cuda_lib):
     _sync()
     assert torch.equal(got[0], ref[0]) and torch.equal(got[1], ref[1])
     assert torch.isnan(big[..., 64:]).all() and torch.isnan(big_t[..., 64:]).all()
+
+
+@pytest.mark.parametrize("d,d_v,layout,nq,nkv", [
+    (64, 128, "bhsd", 300, 700), (128, 64, "bshd", 129, 640), (32, 128, "bhsd", 200, 333),
+    (128, 256, "bshd", 300, 300), (256, 64, "bhsd", 77, 200), (256, 128, "bhsd", 150, 150),
+    (64, 256, "bshd", 100, 500), (16, 32, "bhsd", 333, 333), (128, 16, "bshd", 100, 260)])
+def test_value_head_dim_of_its_own_against_oracle(cuda_lib, d, d_v, layout, nq, nkv):
+    # The page's forward takes V with d_v columns per head: O and its tangent
+    # then have d_v columns, the scores still d.
+    xq = inputs.make_inputs(2, 2, nq, d, seed=50 + d, device="cuda", qk="rms", tangent_scale=0.3)
+    xk = inputs.make_inputs(2, 2, nkv, d, seed=51 + nkv, device="cuda", qk="rms", tangent_scale=0.3)
+    xv = inputs.make_inputs(2, 2, nkv, d_v, seed=52 + d_v, device="cuda", tangent_scale=0.3)
+    args = [xq["q"], xk["k"], xv["v"], xq["q_t"], xk["k_t"], xv["v_t"]]
+    if layout == "bshd":
+        args = [t.transpose(1, 2).contiguous() for t in args]
+    got = binding.attn_jvp_fwd_strided(*args, layout=layout, scale=xq["scale"])
+    _sync()
+    if layout == "bshd":
+        got = (got[0].transpose(1, 2), got[1].transpose(1, 2), got[2], got[3])
+    assert got[0].shape == (2, 2, nq, d_v)
+    ref = oracle.attn_jvp(host64(xq["q"]), host64(xk["k"]), host64(xv["v"]), host64(xq["q_t"]),
+                          host64(xk["k_t"]), host64(xv["v_t"]), xq["scale"])
+    _check(got, ref)

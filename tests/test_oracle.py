@@ -211,6 +211,26 @@ def test_cross_attention_tangent_matches_autodiff_jvp(nq, nk, d):
     assert _rel(ot, ref_ot.numpy()) < 1e-12
 
 
+@pytest.mark.parametrize("d,dv", [(16, 40), (32, 8)])
+def test_value_head_dim_may_differ_autodiff_jvp(d, dv):
+    # The page's forward lets V have its own head dim: library autodiff of
+    # naive FP64 attention with a wider and a narrower V than Q and K.
+    q, k, _, qt, kt, _ = _case(B=1, H=2, N=19, d=d, seed=47)
+    v, vt = _rand((1, 2, 19, dv), 51), _rand((1, 2, 19, dv), 53, 0.5)
+    s = 0.4
+
+    def attn(q_, k_, v_):
+        return torch.matmul(torch.softmax(torch.matmul(q_, k_.transpose(-1, -2)) * s, dim=-1), v_)
+
+    prim = tuple(torch.from_numpy(x) for x in (q, k, v))
+    tang = tuple(torch.from_numpy(x) for x in (qt, kt, vt))
+    ref_o, ref_ot = torch.func.jvp(attn, prim, tang)
+    o, ot, _, _ = oracle.attn_jvp(q, k, v, qt, kt, vt, s)
+    assert o.shape == (1, 2, 19, dv)
+    assert _rel(o, ref_o.numpy()) < 1e-12
+    assert _rel(ot, ref_ot.numpy()) < 1e-12
+
+
 @pytest.mark.parametrize("chunks", [1, 2, 4, 5])
 def test_key_chunk_merge_equals_unsplit(chunks):
     q, k, v, qt, kt, vt = _case(N=61, seed=37)
