@@ -57,7 +57,7 @@ def test_clock_rejection_rule():
     assert why is not None and "no reason" in why
     # one idle sample does not move the median
     assert bench.ClockSampler.rejection(summary([ok(345)] + [ok(2040)] * 4)) is None
-    # no nvidia-smi, no verdict
+    # no nvidia-smi samples: nothing to reject
     assert bench.ClockSampler.rejection(bench.ClockSampler.summarize([])) is None
 
 
