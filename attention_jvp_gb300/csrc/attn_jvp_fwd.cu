@@ -76,10 +76,18 @@ struct FwdCfg {
   static constexpr int kRoom = 227 * 1024 - 1280 - 2 * kQBytes;
   static constexpr int kKS = kRoom >= 3 * (kKStage + kVStage) ? 3 : (kRoom >= 2 * (kKStage + kVStage) ? 2 : 1);
   static constexpr int kVS = kKS;
+  // K/Kt ring units.  Normally a unit is a whole key tile and the ring holds kKS
+  // of them.  With room for only one tile (Q/K head dim 256) the tile is split
+  // into two units of half its d-chunks, so that the next tile's first half
+  // loads while this tile's second half is in the score MMAs.
+  static constexpr int kUPT = (kKS == 1 && kDC % 2 == 0) ? 2 : 1;  // units per key tile
+  static constexpr int kUC = kDC / kUPT;                           // d-chunks of K (and of Kt) per unit
+  static constexpr int kKU = kKS * kUPT;                           // units in the ring
+  static constexpr int kKUnit = 2 * kUC * kChunkK;                 // K chunks, then Kt chunks
   static constexpr int kOffQ = 0;
   static constexpr int kOffQt = kQBytes;
   static constexpr int kOffK = 2 * kQBytes;
-  static constexpr int kOffV = kOffK + kKS * kKStage;
+  static constexpr int kOffV = kOffK + kKU * kKUnit;
   static constexpr int kOffBar = kOffV + kVS * kVStage;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
   // TMEM columns (fp32 each): O [0,DV), T [DV,2DV), S buffer b [2DV+64b, +64),
@@ -90,7 +98,8 @@ struct FwdCfg {
   static constexpr uint32_t kColSt = 2 * kDV + 64 * kNS;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kColSt + 64 * kNSt <= kTmemCols, "TMEM budget");
-  static_assert(kNS <= 3 && kNSt <= 3 && kKS <= 3 && kVS <= 3, "barrier arrays");
+  static_assert(kNS <= 3 && kNSt <= 3 && kKU <= 3 && kVS <= 3, "barrier arrays");
+  static_assert(kKU * kKUnit == kKS * kKStage, "K ring size");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -357,27 +366,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(smem + C::kOffQ + c * C::kChunkQ, &maps.q, &bars->q_full, c * 64, q0, hh, bb);
         tma_load_4d(smem + C::kOffQt + c * C::kChunkQ, &maps.qt, &bars->q_full, c * 64, q0, hh, bb);
       }
-      int issued = 0;
+      int issued = 0;  // ring units
       bool ok = true;
-      for (int t = 0; t < n_tiles && ok; ++t) {
-        const int s = t % C::kKS;
-        ok = mbar_wait(&bars->k_empty[s], ((t / C::kKS) & 1) ^ 1, abort_flag, status, kStatusTimeout);
+      for (int n = 0; n < n_tiles * C::kUPT && ok; ++n) {
+        const int t = n / C::kUPT, u = n % C::kUPT;  // key tile, unit within it
+        const int s = n % C::kKU;
+        ok = mbar_wait(&bars->k_empty[s], ((n / C::kKU) & 1) ^ 1, abort_flag, status, kStatusTimeout);
         if (!ok) break;
-        uint8_t* st = smem + C::kOffK + s * C::kKStage;
+        uint8_t* st = smem + C::kOffK + s * C::kKUnit;
         const int key0 = kv_start + t * C::kBN;
-        mbar_arrive_expect_tx(&bars->k_full[s], C::kKStage);
-        for (int c = 0; c < C::kDC; ++c) {
-          tma_load_4d(st + c * C::kChunkK, &maps.k, &bars->k_full[s], c * 64, key0, hh, bb);
-          tma_load_4d(st + (C::kDC + c) * C::kChunkK, &maps.kt, &bars->k_full[s], c * 64, key0, hh, bb);
+        mbar_arrive_expect_tx(&bars->k_full[s], C::kKUnit);
+        for (int c = 0; c < C::kUC; ++c) {
+          const int col = (u * C::kUC + c) * 64;
+          tma_load_4d(st + c * C::kChunkK, &maps.k, &bars->k_full[s], col, key0, hh, bb);
+          tma_load_4d(st + (C::kUC + c) * C::kChunkK, &maps.kt, &bars->k_full[s], col, key0, hh, bb);
         }
-        issued = t + 1;
+        issued = n + 1;
       }
       if (!ok) {
         // Let copies still in flight land before the CTA's shared memory goes away.
         volatile int no_abort = 0;
         mbar_wait(&bars->q_full, 0, &no_abort, nullptr, 0);
-        for (int t = issued - C::kKS; t < issued; ++t)
-          if (t >= 0) mbar_wait(&bars->k_full[t % C::kKS], (t / C::kKS) & 1, &no_abort, nullptr, 0);
+        for (int n = issued - C::kKU; n < issued; ++n)
+          if (n >= 0) mbar_wait(&bars->k_full[n % C::kKU], (n / C::kKU) & 1, &no_abort, nullptr, 0);
       }
     }
   } else if (warp == 2) {
@@ -425,23 +436,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = mbar_wait(&bars->q_full, 0, abort_flag, status, kStatusTimeout);
         for (int t = 0; ok && t < n_tiles; ++t) {
           const int b = t % C::kNS;
-          const int s = t % C::kKS;
-          ok = mbar_wait(&bars->k_full[s], (t / C::kKS) & 1, abort_flag, status, kStatusTimeout);
-          // The S buffer is free once the softmax has loaded tile t - NS.
-          if (ok && t >= C::kNS)
-            ok = mbar_wait(&bars->s_free[b], ((t - C::kNS) / C::kNS) & 1, abort_flag, status, kStatusTimeout);
-          if (!ok) break;
-          tc_fence_after_sync();
-          const uint64_t dK = off(dK0, s * C::kKStage);
           const uint32_t dS = tmem + C::kColS + 64u * b;
-          // S_t = Q K_t^T
+#pragma unroll 1
+          for (int u = 0; u < C::kUPT; ++u) {
+            const int n = t * C::kUPT + u;
+            const int s = n % C::kKU;
+            ok = mbar_wait(&bars->k_full[s], (n / C::kKU) & 1, abort_flag, status, kStatusTimeout);
+            // The S buffer is free once the softmax has loaded tile t - NS.
+            if (ok && u == 0 && t >= C::kNS)
+              ok = mbar_wait(&bars->s_free[b], ((t - C::kNS) / C::kNS) & 1, abort_flag, status, kStatusTimeout);
+            if (!ok) break;
+            tc_fence_after_sync();
+            const uint64_t dK = off(dK0, s * C::kKUnit);
+            // S_t = Q K_t^T over this unit's d-chunks
 #pragma unroll
-          for (int c = 0; c < C::kDC; ++c)
+            for (int c = 0; c < C::kUC; ++c)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ss(dS, off(dQ, c * C::kChunkQ + kk * 32), off(dK, c * C::kChunkK + kk * 32), kIdS,
-                     (c | kk) != 0);
-          mma_commit(&bars->k_empty[s]);
+              for (int kk = 0; kk < 4; ++kk)
+                mma_ss(dS, off(dQ, (u * C::kUC + c) * C::kChunkQ + kk * 32), off(dK, c * C::kChunkK + kk * 32),
+                       kIdS, (u | c | kk) != 0);
+            mma_commit(&bars->k_empty[s]);
+          }
+          if (!ok) break;
           mma_commit(&bars->s_full[b]);
         }
         // Nothing may still be reading shared memory or TMEM when the CTA tears down.
@@ -451,29 +467,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = mbar_wait(&bars->q_full, 0, abort_flag, status, kStatusTimeout);
         for (int t = 0; ok && t < n_tiles; ++t) {
           const int bt = t % C::kNSt;
-          const int s = t % C::kKS;
-          ok = mbar_wait(&bars->k_full[s], (t / C::kKS) & 1, abort_flag, status, kStatusTimeout);
-          // The St buffer holds P~/H~ of tile t - NSt until that tile's value MMAs are done.
-          if (ok && t >= C::kNSt)
-            ok = mbar_wait(&bars->pv_done[bt], ((t - C::kNSt) / C::kNSt) & 1, abort_flag, status, kStatusTimeout);
-          if (!ok) break;
-          tc_fence_after_sync();
-          const uint64_t dK = off(dK0, s * C::kKStage);
           const uint32_t dSt = tmem + C::kColSt + 64u * bt;
-          // St_t = [Qt Q] [K_t Kt_t]^T : one accumulator, 2d deep
+#pragma unroll 1
+          for (int u = 0; u < C::kUPT; ++u) {
+            const int n = t * C::kUPT + u;
+            const int s = n % C::kKU;
+            ok = mbar_wait(&bars->k_full[s], (n / C::kKU) & 1, abort_flag, status, kStatusTimeout);
+            // The St buffer holds P~/H~ of tile t - NSt until that tile's value MMAs are done.
+            if (ok && u == 0 && t >= C::kNSt)
+              ok = mbar_wait(&bars->pv_done[bt], ((t - C::kNSt) / C::kNSt) & 1, abort_flag, status,
+                             kStatusTimeout);
+            if (!ok) break;
+            tc_fence_after_sync();
+            const uint64_t dK = off(dK0, s * C::kKUnit);
+            // St_t = [Qt Q] [K_t Kt_t]^T : one accumulator, 2d deep (this unit's d-chunks)
 #pragma unroll
-          for (int c = 0; c < C::kDC; ++c)
+            for (int c = 0; c < C::kUC; ++c)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ss(dSt, off(dQt, c * C::kChunkQ + kk * 32), off(dK, c * C::kChunkK + kk * 32), kIdS,
-                     (c | kk) != 0);
+              for (int kk = 0; kk < 4; ++kk)
+                mma_ss(dSt, off(dQt, (u * C::kUC + c) * C::kChunkQ + kk * 32), off(dK, c * C::kChunkK + kk * 32),
+                       kIdS, (u | c | kk) != 0);
 #pragma unroll
-          for (int c = 0; c < C::kDC; ++c)
+            for (int c = 0; c < C::kUC; ++c)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ss(dSt, off(dQ, c * C::kChunkQ + kk * 32), off(dK, (C::kDC + c) * C::kChunkK + kk * 32), kIdS,
-                     1);
-          mma_commit(&bars->k_empty[s]);
+              for (int kk = 0; kk < 4; ++kk)
+                mma_ss(dSt, off(dQ, (u * C::kUC + c) * C::kChunkQ + kk * 32),
+                       off(dK, (C::kUC + c) * C::kChunkK + kk * 32), kIdS, 1);
+            mma_commit(&bars->k_empty[s]);
+          }
+          if (!ok) break;
           mma_commit(&bars->st_full[bt]);
         }
         mma_commit(&bars->drain_st);
