@@ -199,3 +199,17 @@ def test_long_video_split_kv_sampled_rows(cuda_lib):
     _check_all(x, got, heads=heads, rows=rows)
     del x, got
     torch.cuda.empty_cache()
+
+
+def test_head_dim_256_long_sequence_sampled_rows(cuda_lib):
+    # Two CTAs per query tile and the half-tile K ring over 256 key tiles: seeded
+    # query rows of every head (plus the ragged last tile) against the oracle.
+    x = inputs.make_inputs(1, 3, 16380, 256, seed=61, device="cuda", qk="rms", tangent_scale=0.3)
+    got = _run(x)
+    rng = np.random.default_rng(62)
+    rows = np.unique(np.concatenate([rng.choice(16380, 40, replace=False), np.arange(16375, 16380)]))
+    _check_all(x, got, heads=[0, 1, 2], rows=rows)
+    for t in got:
+        assert bool(torch.isfinite(t).all())
+    del x, got
+    torch.cuda.empty_cache()

@@ -1,5 +1,6 @@
 """GPU: seeded random shapes through the forward and the backward, against the
-FP64 oracle.
+FP64 oracle.  A second seeded set draws the Q/K and the V head dims
+independently from {16, 32, 64, 128, 256} (forward only).
 
 Batch, heads, query and key lengths (cross-attention included), head dims
 16/32/64/128, both memory layouts and softmax scales of 0.5 to 2 times
@@ -96,3 +97,40 @@ def test_backward_random_shape(cuda_lib, case):
             assert rel <= 1e-2, "%s head %d: rel-L2 %.3e" % (name, bh, rel)
             excess = np.abs(g - want) - (2.0 ** -7 * size + 5e-2 * np.sqrt(np.mean(want ** 2)))
             assert np.all(excess <= 0), "%s head %d: %.3e over the operand bound" % (name, bh, excess.max())
+
+
+def _dv_cases(n=12, seed=2027):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        B = int(rng.integers(1, 3))
+        H = int(rng.integers(1, 4))
+        nq = int(rng.integers(1, 500))
+        nkv = int(rng.integers(1, 700))
+        d, d_v = (int(v) for v in rng.choice([16, 32, 64, 128, 256], size=2))
+        layout = "bshd" if rng.random() < 0.5 else "bhsd"
+        out.append((i, B, H, nq, nkv, d, d_v, layout))
+    return out
+
+
+@pytest.mark.parametrize("case", _dv_cases(), ids=lambda c: "c%d-B%dH%d-q%d-k%d-d%d-dv%d-%s" % c)
+def test_forward_random_value_head_dim(cuda_lib, case):
+    # Q/K and V head dims drawn independently from the page's set
+    i, B, H, nq, nkv, d, d_v, layout = case
+    xq = inputs.make_inputs(B, H, nq, d, seed=400 + i, device="cuda", qk="rms", tangent_scale=0.3)
+    xk = inputs.make_inputs(B, H, nkv, d, seed=500 + i, device="cuda", qk="rms", tangent_scale=0.3)
+    xv = inputs.make_inputs(B, H, nkv, d_v, seed=600 + i, device="cuda", tangent_scale=0.3)
+    args = [xq["q"], xk["k"], xv["v"], xq["q_t"], xk["k_t"], xv["v_t"]]
+    if layout == "bshd":
+        args = [t.transpose(1, 2).contiguous() for t in args]
+    o, ot, lse, mu = binding.attn_jvp_fwd_strided(*args, layout=layout, scale=xq["scale"])
+    torch.cuda.synchronize()
+    binding.attn_jvp_status()
+    if layout == "bshd":
+        o, ot = o.transpose(1, 2), ot.transpose(1, 2)
+    ref = oracle.attn_jvp(host64(xq["q"]), host64(xk["k"]), host64(xv["v"]), host64(xq["q_t"]),
+                          host64(xk["k_t"]), host64(xv["v_t"]), xq["scale"])
+    assert_close(host64(o), ref[0], "O")
+    assert_close(host64(ot), ref[1], "Ot")
+    assert_close(host64(mu), ref[3], "mu")
+    assert np.max(np.abs(host64(lse) - ref[2])) <= 1e-3
