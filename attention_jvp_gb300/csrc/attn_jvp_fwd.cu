@@ -39,6 +39,13 @@
 // Lazy rescale: a row keeps its reference max until a tile's max exceeds it by
 // more than 8 (log2 units); only then are O, T, l, r rescaled.  All four share
 // the same reference, so the final normalisation is exact.
+//
+// Head dims (the page's set, 16-256, for Q/K and for V independently): the
+// kernel is a template over both, each rounded up to 64, 128 or 256.  The Q/K
+// dim sets the score MMAs' depth and, through the resident Q and Qt, how many
+// key tiles the rings hold.  The V dim sets the value MMAs and the TMEM layout.
+// At a V dim of 256, O and T of 128 rows would fill TMEM, so two neighbouring
+// CTAs share each query tile and each accumulates 128 of the value columns.
 #include <cuda_runtime.h>
 #include <cstdint>
 

@@ -19,6 +19,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -167,11 +168,17 @@ def measure_backward(x, spec, o, lse, dev, stream, peaks, reps=5, warmup=2):
             "flops_convention": "10 d per (query, key) pair; executed 14 d (two passes)"}
 
 
+_COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
+
+
 def kernel_source_sha():
+    """Hash of the fused kernel's sources with comments removed and whitespace runs folded: a
+    comment edit leaves the compiled kernel, and so its recorded traffic, unchanged; any code
+    edit voids the record."""
     h = hashlib.sha256()
     for path in KERNEL_SOURCES:
-        with open(path, "rb") as f:
-            h.update(f.read())
+        with open(path, encoding="utf-8") as f:
+            h.update(" ".join(_COMMENT.sub(" ", f.read()).split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -61,6 +61,19 @@ def test_clock_rejection_rule():
     assert bench.ClockSampler.rejection(bench.ClockSampler.summarize([])) is None
 
 
+def test_source_hash_ignores_comments_not_code(tmp_path, monkeypatch):
+    src = tmp_path / "k.cu"
+    monkeypatch.setattr(bench, "KERNEL_SOURCES", (str(src),))
+    src.write_text("// kernel\nint f(int a) { return a - -1; }  /* note */\n")
+    base = bench.kernel_source_sha()
+    src.write_text("// kernel, reworded\n// and one more line\n\nint f(int a)  {\n  return a - -1; }\n")
+    assert bench.kernel_source_sha() == base
+    src.write_text("// kernel\nint f(int a) { return a - 1; }\n")
+    assert bench.kernel_source_sha() != base
+    src.write_text("// kernel\nint f(int a) { return a--1; }\n")
+    assert bench.kernel_source_sha() != base
+
+
 def test_traffic_record_tracks_kernel_source(tmp_path, monkeypatch):
     rec = {"k": {"w": {"source_sha": bench.kernel_source_sha(), "heads": 4, "dram_bytes_per_launch": 400.0}}}
     path = tmp_path / "traffic.json"
