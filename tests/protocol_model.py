@@ -1,0 +1,261 @@
+"""CPU model of the fused forward kernel's hand-off protocol (test helper).
+
+The kernel's roles meet only through mbarriers: a TMA thread for Q, Qt and the
+K/Kt ring, a TMA thread for the V/Vt ring, the S, St and value-MMA issuing
+threads, and four softmax warps.  This model runs each role as a generator,
+completes the asynchronous work (TMA copies in any order, each issuing
+thread's MMAs in issue order) at random points, and checks what the GPU
+cannot be asked to show without faulting it:
+
+* every wait uses the hardware's parity test (it passes when the barrier's
+  current phase parity differs from the awaited phase's), and a waiter is
+  never more than one phase behind: a parity test cannot tell phase k from
+  phase k + 2, and passing on phase k - 1 reads data that is not there yet;
+* no deadlock;
+* no buffer is overwritten while an MMA or the softmax still needs it, and
+  each reader finds the tile it expects (shared-memory ring units, the S and
+  St TMEM buffers, the P~/H~ written back into St);
+* O and T are rescaled only when no value MMA is in flight, and every tile's
+  value MMAs land exactly once.
+
+``fwd_config`` restates the kernel's compile-time ring and buffer sizes for a
+pair of (Q/K, V) head dims rounded up to 64, 128 or 256.
+"""
+import random
+
+SMEM = 227 * 1024
+
+
+def fwd_config(D, DVF):
+    """Ring and buffer counts of the fused kernel for padded head dims (D, DVF)."""
+    kDC = D // 64
+    kDV = 128 if DVF > 128 else DVF
+    kVC = kDV // 64
+    NS = 3 if kDV == 64 else 1
+    NSt = 3
+    chunk_q, chunk_k = 128 * 128, 64 * 128
+    q_bytes = kDC * chunk_q
+    k_stage, v_stage = 2 * kDC * chunk_k, 2 * kVC * chunk_k
+    room = SMEM - 1280 - 2 * q_bytes
+    KS = 3 if room >= 3 * (k_stage + v_stage) else (2 if room >= 2 * (k_stage + v_stage) else 1)
+    UPT = 2 if (KS == 1 and kDC % 2 == 0) else 1
+    return dict(NS=NS, NSt=NSt, KS=KS, VS=KS, UPT=UPT, KU=KS * UPT)
+
+
+class ProtocolError(AssertionError):
+    pass
+
+
+class Bar:
+    def __init__(self, name, count):
+        self.name, self.count, self.done, self.pending = name, count, 0, 0
+
+    def arrive(self):
+        self.pending += 1
+        if self.pending > self.count:
+            raise ProtocolError("%s: more arrivals than its count" % self.name)
+        if self.pending == self.count:
+            self.pending = 0
+            self.done += 1
+
+
+class FwdModel:
+    """One CTA's roles over ``n_tiles`` key tiles.  ``mutate`` plants a protocol
+    mistake (for the test that shows the model catches it)."""
+
+    def __init__(self, cfg, n_tiles, seed, mutate=None):
+        self.c = dict(cfg)
+        self.n = n_tiles
+        self.rng = random.Random(seed)
+        self.mutate = mutate
+        c = self.c
+        B = lambda nm, cnt, k: [Bar("%s%d" % (nm, i), cnt) for i in range(k)]  # noqa: E731
+        self.q_full = Bar("q_full", 1)
+        self.k_full, self.k_empty = B("k_full", 1, c["KU"]), B("k_empty", 2, c["KU"])
+        self.v_full, self.v_empty = B("v_full", 1, c["VS"]), B("v_empty", 1, c["VS"])
+        self.s_full, self.s_free = B("s_full", 1, c["NS"]), B("s_free", 4, c["NS"])
+        self.st_full = B("st_full", 1, c["NSt"])
+        self.p_full, self.pv_done = B("p_full", 4, c["NSt"]), B("pv_done", 1, c["NSt"])
+        self.k_unit = [None] * c["KU"]      # (tile, unit) held by each ring unit
+        self.k_readers = [0] * c["KU"]
+        self.v_stage = [None] * c["VS"]
+        self.v_readers = [0] * c["VS"]
+        self.s_buf = [None] * c["NS"]       # ("S", tile) once written
+        self.s_writer = [0] * c["NS"]
+        self.s_loaded = [None] * c["NS"]    # last tile the softmax loaded from each S buffer
+        self.st_buf = [None] * c["NSt"]     # ("St", tile), then ("P", tile)
+        self.st_writer = [0] * c["NSt"]
+        self.st_readers = [0] * c["NSt"]
+        self.pv_in_flight = 0
+        self.pv_landed = []
+        self.pending = []                   # (queue, completion) of asynchronous work
+
+    # -- parity waits ---------------------------------------------------------
+    def wait(self, bar, k):
+        """Wait for phase k (k = -1: the phase before the first, already passed)."""
+        while True:
+            if bar.done >= k + 2:
+                raise ProtocolError("%s: waiter for phase %d is two phases behind (%d done)"
+                                    % (bar.name, k, bar.done))
+            if (bar.done & 1) != (k & 1):
+                if bar.done != k + 1:
+                    raise ProtocolError("%s: parity test for phase %d passed with %d done"
+                                        % (bar.name, k, bar.done))
+                return
+            yield
+
+    def later(self, queue, fn):
+        self.pending.append((queue, fn))
+
+    # -- roles ----------------------------------------------------------------
+    def tma_k(self):
+        c = self.c
+        self.later("tma", self.q_full.arrive)
+        for n in range(self.n * c["UPT"]):
+            t, u, s = n // c["UPT"], n % c["UPT"], n % c["KU"]
+            yield from self.wait(self.k_empty[s], n // c["KU"] - 1)
+            if self.k_readers[s]:
+                raise ProtocolError("K unit %d reloaded while an MMA reads it" % s)
+
+            def land(s=s, t=t, u=u):
+                self.k_unit[s] = (t, u)
+                self.k_full[s].arrive()
+            self.later("tma", land)
+
+    def tma_v(self):
+        c = self.c
+        for t in range(self.n):
+            s = t % c["VS"]
+            yield from self.wait(self.v_empty[s], t // c["VS"] - 1)
+            if self.v_readers[s]:
+                raise ProtocolError("V stage %d reloaded while an MMA reads it" % s)
+
+            def land(s=s, t=t):
+                self.v_stage[s] = t
+                self.v_full[s].arrive()
+            self.later("tma", land)
+
+    def _score_issuer(self, name, NB, full, free_wait, buf, writer):
+        c = self.c
+        yield from self.wait(self.q_full, 0)
+        for t in range(self.n):
+            b = t % NB
+            for u in range(c["UPT"]):
+                n = t * c["UPT"] + u
+                s = n % c["KU"]
+                yield from self.wait(self.k_full[s], n // c["KU"])
+                if u == 0 and t >= NB and self.mutate != name + "_no_free_wait":
+                    yield from free_wait(t - NB)
+                if self.k_unit[s] != (t, u):
+                    raise ProtocolError("%s MMA of tile %d reads K unit holding %s" % (name, t, self.k_unit[s]))
+                if u == 0 and (writer[b] or (name == "St" and self.st_readers[b])):
+                    raise ProtocolError("%s buffer %d overwritten while in use" % (name, b))
+                if u == 0 and t >= NB:
+                    # the buffer's previous tile must be finished with: loaded by the
+                    # softmax (S), or read as P~/H~ by its value MMAs (St)
+                    prev = t - NB
+                    if name == "S" and self.s_loaded[b] != prev:
+                        raise ProtocolError("S buffer %d overwritten before tile %d was loaded" % (b, prev))
+                    if name == "St" and prev not in self.pv_landed:
+                        raise ProtocolError("St buffer %d overwritten before tile %d's value MMAs" % (b, prev))
+                self.k_readers[s] += 1
+                writer[b] += 1
+
+                def done(s=s, b=b):
+                    self.k_readers[s] -= 1
+                    writer[b] -= 1
+                    self.k_empty[s].arrive()
+                self.later(name, done)
+
+            def finished(b=b, t=t):
+                buf[b] = (name, t)
+                full[b].arrive()
+            self.later(name, finished)
+
+    def s_issuer(self):
+        c = self.c
+
+        def free(tp):
+            yield from self.wait(self.s_free[tp % c["NS"]], tp // c["NS"])
+        yield from self._score_issuer("S", c["NS"], self.s_full, free, self.s_buf, self.s_writer)
+
+    def st_issuer(self):
+        c = self.c
+
+        def free(tp):
+            yield from self.wait(self.pv_done[tp % c["NSt"]], tp // c["NSt"])
+        yield from self._score_issuer("St", c["NSt"], self.st_full, free, self.st_buf, self.st_writer)
+
+    def pv_issuer(self):
+        c = self.c
+        for j in range(self.n):
+            b, s = j % c["NSt"], j % c["VS"]
+            yield from self.wait(self.p_full[b], j // c["NSt"])
+            yield from self.wait(self.v_full[s], j // c["VS"])
+            if self.st_buf[b] != ("P", j) or self.v_stage[s] != j:
+                raise ProtocolError("value MMAs of tile %d read %s and V of tile %s"
+                                    % (j, self.st_buf[b], self.v_stage[s]))
+            self.st_readers[b] += 1
+            self.v_readers[s] += 1
+            self.pv_in_flight += 1
+
+            def done(b=b, s=s, j=j):
+                self.st_readers[b] -= 1
+                self.v_readers[s] -= 1
+                self.pv_in_flight -= 1
+                self.pv_landed.append(j)
+                self.v_empty[s].arrive()
+                self.pv_done[b].arrive()
+            self.later("PV", done)
+
+    def softmax_warp(self, w):
+        c = self.c
+        for j in range(self.n):
+            b, bt = j % c["NS"], j % c["NSt"]
+            yield from self.wait(self.s_full[b], j // c["NS"])
+            yield from self.wait(self.st_full[bt], j // c["NSt"])
+            if w == 0 and (self.s_buf[b] != ("S", j) or self.st_buf[bt] != ("St", j)):
+                raise ProtocolError("softmax of tile %d loads %s and %s" % (j, self.s_buf[b], self.st_buf[bt]))
+            if w == 0:
+                self.s_loaded[b] = j
+            yield
+            self.s_free[b].arrive()
+            yield
+            if j >= 1 and self.rng.random() < 0.3:  # the row max grew: rescale O and T
+                if self.mutate != "rescale_no_wait":
+                    yield from self.wait(self.pv_done[(j - 1) % c["NSt"]], (j - 1) // c["NSt"])
+                if self.pv_in_flight:
+                    raise ProtocolError("O and T rescaled while value MMAs are in flight")
+            if w == 0:
+                self.st_buf[bt] = ("P", j)
+            yield
+            self.p_full[bt].arrive()
+        yield from self.wait(self.pv_done[(self.n - 1) % c["NSt"]], (self.n - 1) // c["NSt"])
+        if self.pv_in_flight or sorted(self.pv_landed) != list(range(self.n)):
+            raise ProtocolError("epilogue before every value MMA landed")
+
+    # -- scheduler ------------------------------------------------------------
+    def run(self, max_steps=500000):
+        roles = [self.tma_k(), self.tma_v(), self.s_issuer(), self.st_issuer(), self.pv_issuer()]
+        roles += [self.softmax_warp(w) for w in range(4)]
+        live = list(roles)
+        for _ in range(max_steps):
+            if not live and not self.pending:
+                return
+            if self.pending and (not live or self.rng.random() < 0.4):
+                # any TMA copy may land; an issuing thread's MMAs complete in order
+                heads, seen = [], set()
+                for i, (q, _) in enumerate(self.pending):
+                    if q == "tma" or q not in seen:
+                        heads.append(i)
+                        seen.add(q)
+                _, fn = self.pending.pop(self.rng.choice(heads))
+                fn()
+                continue
+            if live:
+                r = self.rng.choice(live)
+                try:
+                    next(r)
+                except StopIteration:
+                    live.remove(r)
+        raise ProtocolError("deadlock: no progress in %d steps" % max_steps)
