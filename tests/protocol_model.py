@@ -259,3 +259,215 @@ class FwdModel:
                 except StopIteration:
                     live.remove(r)
         raise ProtocolError("deadlock: no progress in %d steps" % max_steps)
+
+
+# ---------------------------------------------------------------------------
+# The backward kernel (both passes)
+# ---------------------------------------------------------------------------
+def bwd_config(D, dkdv):
+    """Ring and buffer counts of the backward kernel for padded head dim D and a pass."""
+    NS = 1 if D == 128 else 3
+    return dict(NS=NS, NSt=3, SBar=2 if NS == 1 else NS, KS=2 if D == 128 else 3,
+                VS=(2 if dkdv else 3) if D == 128 else 3, VecS=4, dkdv=dkdv)
+
+
+class BwdModel(FwdModel):
+    """One CTA of a backward pass: a TMA thread polling the score, value and (dK/dV
+    pass) per-query vector rings; S1, S2 and value-MMA issuers; two groups of four
+    elementwise warps taking even and odd tiles.  In the dQ pass group 0 first
+    copies the resident tiles into TMEM for the score MMAs.  ``mutate``:
+    "one_s1_slot" gives the S1 barriers a single slot (two groups on one slot)."""
+
+    def __init__(self, cfg, n_tiles, seed, mutate=None):
+        self.c = dict(cfg)
+        c = self.c
+        if mutate == "one_s1_slot":
+            c["SBar"] = 1
+        self.n = n_tiles
+        self.rng = random.Random(seed)
+        self.mutate = mutate
+        B = lambda nm, cnt, k: [Bar("%s%d" % (nm, i), cnt) for i in range(k)]  # noqa: E731
+        self.r_full, self.r_tmem = Bar("r_full", 1), Bar("r_tmem", 4)
+        self.k_full, self.k_empty = B("k_full", 1, c["KS"]), B("k_empty", 2, c["KS"])
+        self.v_full, self.v_empty = B("v_full", 1, c["VS"]), B("v_empty", 1, c["VS"])
+        self.vec_full, self.vec_empty = B("vec_full", 1, c["VecS"]), B("vec_empty", 4, c["VecS"])
+        self.s_full, self.s_free = B("s_full", 1, c["SBar"]), B("s_free", 4, c["SBar"])
+        self.st_full = B("st_full", 1, c["NSt"])
+        self.p_full, self.pv_done = B("p_full", 4, c["NSt"]), B("pv_done", 1, c["NSt"])
+        self.acc_done = Bar("acc_done", 1)
+        self.k_stage, self.k_readers = [None] * c["KS"], [0] * c["KS"]
+        self.v_stage, self.v_readers = [None] * c["VS"], [0] * c["VS"]
+        self.vec_slot, self.vec_unread = [None] * c["VecS"], [0] * c["VecS"]
+        self.s1_buf, self.s1_writer, self.s1_loaded = [None] * c["NS"], [0] * c["NS"], [None] * c["NS"]
+        self.s2_buf, self.s2_writer, self.s2_readers = [None] * c["NSt"], [0] * c["NSt"], [0] * c["NSt"]
+        self.r_in_tmem = False
+        self.pv_in_flight = 0
+        self.pv_landed = []
+        self.pending = []
+
+    def test(self, bar, k):
+        """Non-blocking parity test (the producer's poll), held to the same rules as a wait."""
+        if bar.done >= k + 2:
+            raise ProtocolError("%s: poll for phase %d is two phases behind (%d done)" % (bar.name, k, bar.done))
+        if (bar.done & 1) != (k & 1):
+            if bar.done != k + 1:
+                raise ProtocolError("%s: parity poll for phase %d passed with %d done" % (bar.name, k, bar.done))
+            return True
+        return False
+
+    def producer(self):
+        c = self.c
+        self.later("tma", self.r_full.arrive)
+        tk = tv = tq = 0
+        nq = self.n if c["dkdv"] else 0
+        while tk < self.n or tv < self.n or tq < nq:
+            if tq < nq and self.test(self.vec_empty[tq % c["VecS"]], tq // c["VecS"] - 1):
+                s = tq % c["VecS"]
+                if self.vec_unread[s]:
+                    raise ProtocolError("vector slot %d reloaded before a group read it" % s)
+
+                def landq(s=s, t=tq):
+                    self.vec_slot[s] = t
+                    self.vec_unread[s] = 4
+                    self.vec_full[s].arrive()
+                self.later("tma", landq)
+                tq += 1
+            if tk < self.n and self.test(self.k_empty[tk % c["KS"]], tk // c["KS"] - 1):
+                s = tk % c["KS"]
+                if self.k_readers[s]:
+                    raise ProtocolError("score stage %d reloaded while an MMA reads it" % s)
+
+                def landk(s=s, t=tk):
+                    self.k_stage[s] = t
+                    self.k_full[s].arrive()
+                self.later("tma", landk)
+                tk += 1
+            if tv < self.n and self.test(self.v_empty[tv % c["VS"]], tv // c["VS"] - 1):
+                s = tv % c["VS"]
+                if self.v_readers[s]:
+                    raise ProtocolError("value stage %d reloaded while an MMA reads it" % s)
+
+                def landv(s=s, t=tv):
+                    self.v_stage[s] = t
+                    self.v_full[s].arrive()
+                self.later("tma", landv)
+                tv += 1
+            yield
+
+    def score_issuer(self, first):
+        c = self.c
+        name = "S1" if first else "S2"
+        yield from self.wait(self.r_full if c["dkdv"] else self.r_tmem, 0)
+        if not c["dkdv"] and not self.r_in_tmem:
+            raise ProtocolError("score MMAs before the resident tiles are in TMEM")
+        for t in range(self.n):
+            s = t % c["KS"]
+            b = t % (c["NS"] if first else c["NSt"])
+            yield from self.wait(self.k_full[s], t // c["KS"])
+            if first and t >= c["NS"]:
+                tp = t - c["NS"]
+                yield from self.wait(self.s_free[tp % c["SBar"]], tp // c["SBar"])
+                if self.s1_loaded[b] != tp:
+                    raise ProtocolError("S1 buffer %d overwritten before tile %d was loaded" % (b, tp))
+            if not first and t >= c["NSt"]:
+                tp = t - c["NSt"]
+                yield from self.wait(self.pv_done[b], tp // c["NSt"])
+                if tp not in self.pv_landed:
+                    raise ProtocolError("S2 buffer %d overwritten before tile %d's value MMAs" % (b, tp))
+            if self.k_stage[s] != t:
+                raise ProtocolError("%s MMA of tile %d reads stage holding %s" % (name, t, self.k_stage[s]))
+            writer = self.s1_writer if first else self.s2_writer
+            if writer[b] or (not first and self.s2_readers[b]):
+                raise ProtocolError("%s buffer %d overwritten while in use" % (name, b))
+            self.k_readers[s] += 1
+            writer[b] += 1
+
+            def done(s=s, b=b, t=t, first=first, writer=writer):
+                self.k_readers[s] -= 1
+                writer[b] -= 1
+                (self.s1_buf if first else self.s2_buf)[b] = (name, t)
+                self.k_empty[s].arrive()
+                (self.s_full[t % c["SBar"]] if first else self.st_full[b]).arrive()
+            self.later(name, done)
+
+    def value_issuer(self):
+        c = self.c
+        for j in range(self.n):
+            b, s = j % c["NSt"], j % c["VS"]
+            yield from self.wait(self.p_full[b], j // c["NSt"])
+            yield from self.wait(self.v_full[s], j // c["VS"])
+            if self.s2_buf[b] != ("P", j) or self.v_stage[s] != j:
+                raise ProtocolError("value MMAs of tile %d read %s and stage %s" % (j, self.s2_buf[b], self.v_stage[s]))
+            self.s2_readers[b] += 1
+            self.v_readers[s] += 1
+            self.pv_in_flight += 1
+
+            def done(b=b, s=s, j=j):
+                self.s2_readers[b] -= 1
+                self.v_readers[s] -= 1
+                self.pv_in_flight -= 1
+                self.pv_landed.append(j)
+                self.v_empty[s].arrive()
+                self.pv_done[b].arrive()
+            self.later("PV", done)
+        self.later("PV", self.acc_done.arrive)
+
+    def elementwise_warp(self, group, w):
+        c = self.c
+        if not c["dkdv"] and group == 0:
+            yield from self.wait(self.r_full, 0)
+            yield
+            if w == 3:
+                self.r_in_tmem = True  # the last of the four copies (modelled at the last arrival)
+            self.r_tmem.arrive()
+        for j in range(group, self.n, 2):
+            b, bs, bt, sq = j % c["NS"], j % c["SBar"], j % c["NSt"], j % c["VecS"]
+            yield from self.wait(self.s_full[bs], j // c["SBar"])
+            if self.s1_buf[b] != ("S1", j):
+                raise ProtocolError("tile %d loads S1 buffer holding %s" % (j, self.s1_buf[b]))
+            if w == 0:
+                self.s1_loaded[b] = j
+            yield
+            self.s_free[bs].arrive()
+            yield from self.wait(self.st_full[bt], j // c["NSt"])
+            if c["dkdv"]:
+                yield from self.wait(self.vec_full[sq], j // c["VecS"])
+                if self.vec_slot[sq] != j:
+                    raise ProtocolError("tile %d reads vector slot holding %s" % (j, self.vec_slot[sq]))
+                self.vec_unread[sq] -= 1
+            if self.s2_buf[bt] not in (("S2", j), ("P", j)):
+                raise ProtocolError("tile %d loads S2 buffer holding %s" % (j, self.s2_buf[bt]))
+            yield
+            if w == 0:
+                self.s2_buf[bt] = ("P", j)
+            yield
+            self.p_full[bt].arrive()
+            if c["dkdv"]:
+                self.vec_empty[sq].arrive()
+        yield from self.wait(self.acc_done, 0)
+        if self.pv_in_flight or sorted(self.pv_landed) != list(range(self.n)):
+            raise ProtocolError("epilogue before every value MMA landed")
+
+    def run(self, max_steps=500000):
+        roles = [self.producer(), self.score_issuer(True), self.score_issuer(False), self.value_issuer()]
+        roles += [self.elementwise_warp(g, w) for g in range(2) for w in range(4)]
+        live = list(roles)
+        for _ in range(max_steps):
+            if not live and not self.pending:
+                return
+            if self.pending and (not live or self.rng.random() < 0.4):
+                heads, seen = [], set()
+                for i, (q, _) in enumerate(self.pending):
+                    if q == "tma" or q not in seen:
+                        heads.append(i)
+                        seen.add(q)
+                _, fn = self.pending.pop(self.rng.choice(heads))
+                fn()
+                continue
+            if live:
+                r = self.rng.choice(live)
+                try:
+                    next(r)
+                except StopIteration:
+                    live.remove(r)
+        raise ProtocolError("deadlock: no progress in %d steps" % max_steps)

@@ -9,7 +9,7 @@ is there for.
 """
 import pytest
 
-from protocol_model import FwdModel, ProtocolError, fwd_config
+from protocol_model import BwdModel, FwdModel, ProtocolError, bwd_config, fwd_config
 
 PAIRS = [(d, dv) for d in (64, 128, 256) for dv in (64, 128, 256)]
 
@@ -61,3 +61,23 @@ def test_one_barrier_slot_for_two_groups_is_caught():
     bar2 = Bar("early", 1)
     with pytest.raises(ProtocolError):
         list(m.wait(bar2, 1))
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("dkdv", [True, False], ids=["dKdV", "dQ"])
+@pytest.mark.parametrize("n_tiles", [1, 2, 3, 5, 9])
+def test_backward_protocol_is_race_free(D, dkdv, n_tiles):
+    cfg = bwd_config(D, dkdv)
+    for seed in range(12):
+        BwdModel(cfg, n_tiles, seed=1000 * n_tiles + seed).run()
+
+
+def test_backward_two_groups_on_one_s1_slot_is_caught():
+    # the reason the S1 barriers have one slot per tile parity at d = 128
+    hits = 0
+    for seed in range(40):
+        try:
+            BwdModel(bwd_config(128, True), 8, seed=seed, mutate="one_s1_slot").run()
+        except ProtocolError:
+            hits += 1
+    assert hits > 0
