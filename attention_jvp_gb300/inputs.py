@@ -37,6 +37,9 @@ WORKLOADS = {
     "stress": dict(B=4, H=16, N=16384, d=64, dtype=torch.bfloat16, seed=5,
                    qk="normal", tangent="normal", tangent_scale=1.0,
                    outlier_frac=0.01, outlier_logit=12.0),
+    # the largest head dim of the page's set; not one of the benchmark workloads
+    "head_dim_256": dict(B=1, H=16, N=16384, d=256, dtype=torch.bfloat16, seed=6,
+                         qk="rms", tangent="normal", tangent_scale=0.3),
 }
 
 NAMES = ("q", "k", "v", "q_t", "k_t", "v_t")
