@@ -81,3 +81,61 @@ def test_backward_two_groups_on_one_s1_slot_is_caught():
         except ProtocolError:
             hits += 1
     assert hits > 0
+
+
+# ---------------------------------------------------------------------------
+# The model's ring sizes against the kernels' own compile-time configuration
+# ---------------------------------------------------------------------------
+CFG_HARNESS = r"""
+#include <cstdint>
+#include <cstdio>
+constexpr int kModeDQ = 0;
+constexpr int kModeDKDV = 1;
+%s
+%s
+template <int D, int DV> void fwd() {
+  using C = FwdCfg<D, DV>;
+  printf("fwd %%d %%d %%d %%d %%d %%d %%d %%d\n", D, DV, C::kNS, C::kNSt, C::kKS, C::kVS, C::kUPT, C::kKU);
+}
+template <int D, int M> void bwd() {
+  using C = BwdCfg<D, M>;
+  printf("bwd %%d %%d %%d %%d %%d %%d %%d %%d\n", D, M, C::kNS, C::kNSt, C::kSBar, C::kKS, C::kVS, C::kVecS);
+}
+int main() {
+  fwd<64, 64>(); fwd<64, 128>(); fwd<64, 256>(); fwd<128, 64>(); fwd<128, 128>(); fwd<128, 256>();
+  fwd<256, 64>(); fwd<256, 128>(); fwd<256, 256>();
+  bwd<64, 0>(); bwd<64, 1>(); bwd<128, 0>(); bwd<128, 1>();
+  return 0;
+}
+"""
+
+
+def test_model_sizes_are_the_kernels_sizes(tmp_path):
+    import os
+    import re
+    import shutil
+    import subprocess
+    cxx = shutil.which("g++") or shutil.which("c++")
+    if cxx is None:
+        pytest.skip("no host C++ compiler")
+    csrc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "attention_jvp_gb300", "csrc")
+    fwd_src = open(os.path.join(csrc, "attn_jvp_fwd.cu"), encoding="utf-8").read()
+    bwd_src = open(os.path.join(csrc, "attn_bwd.cu"), encoding="utf-8").read()
+    fcfg = re.search(r"template <int D, int DVF>\nstruct FwdCfg \{.*?\n\};\n", fwd_src, re.S)
+    bcfg = re.search(r"template <int D, int kMode>\nstruct BwdCfg \{.*?\n\};\n", bwd_src, re.S)
+    assert fcfg and bcfg, "FwdCfg / BwdCfg not found in the kernel sources"
+    (tmp_path / "cfg.cpp").write_text(CFG_HARNESS % (fcfg.group(0), bcfg.group(0)))
+    exe = tmp_path / "cfg"
+    subprocess.run([cxx, "-std=c++17", str(tmp_path / "cfg.cpp"), "-o", str(exe)], check=True)
+    seen = 0
+    for line in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.splitlines():
+        kind, *v = line.split()
+        v = [int(x) for x in v]
+        if kind == "fwd":
+            want = fwd_config(v[0], v[1])
+            assert (want["NS"], want["NSt"], want["KS"], want["VS"], want["UPT"], want["KU"]) == tuple(v[2:]), line
+        else:
+            want = bwd_config(v[0], v[1] == 1)
+            assert (want["NS"], want["NSt"], want["SBar"], want["KS"], want["VS"], want["VecS"]) == tuple(v[2:]), line
+        seen += 1
+    assert seen == 13
