@@ -286,11 +286,22 @@ def oracle_rows_for(spec, x_host_head, target_s, seed=0):
 
     cores = oracle.default_threads()
     q, k, v, qt, kt, vt = x_host_head
-    rows = inputs.sample_rows(spec["N"], max(cores, 8), seed).numpy()
-    t0 = time.perf_counter()
-    oracle.attn_jvp(q, k, v, qt, kt, vt, spec["scale"], rows=rows, nthreads=cores)
-    per_row = (time.perf_counter() - t0) / len(rows)
-    return int(max(len(rows), min(spec["N"], target_s / max(per_row, 1e-9))))
+    N = spec["N"]
+
+    def per_row(n, s):
+        rows = inputs.sample_rows(N, n, s).numpy()
+        t0 = time.perf_counter()
+        oracle.attn_jvp(q, k, v, qt, kt, vt, spec["scale"], rows=rows, nthreads=cores)
+        return (time.perf_counter() - t0) / len(rows)
+
+    # A row per thread is dominated by thread start-up and overstates the cost of a
+    # row; a second run sized at a tenth of the target, with every thread busy, sets it.
+    n0 = min(N, max(cores, 8))
+    t_row = per_row(n0, seed)
+    n1 = int(min(N, 0.1 * target_s / max(t_row, 1e-9)))
+    if n1 > n0:
+        t_row = per_row(n1, seed + 2)
+    return int(max(n0, min(N, target_s / max(t_row, 1e-9))))
 
 
 def oracle_sample(spec, x_host_head, n_rows, seed=0):

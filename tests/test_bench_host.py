@@ -74,6 +74,23 @@ def test_source_hash_ignores_comments_not_code(tmp_path, monkeypatch):
     assert bench.kernel_source_sha() != base
 
 
+def test_oracle_sample_calibration_discounts_start_up(monkeypatch):
+    # The CPU baseline's sample is sized to a target time from a timed calibration.  With
+    # a fixed start-up cost per call, one row per thread would overstate the cost of a
+    # row several times over; the second, larger calibration must not.
+    import oracle
+    clock = [0.0]
+
+    def fake_oracle(q, k, v, qt, kt, vt, scale, rows=None, nthreads=None):
+        clock[0] += 0.05 + 1e-3 * len(rows)  # start-up + 1 ms a row
+
+    monkeypatch.setattr(oracle, "attn_jvp", fake_oracle)
+    monkeypatch.setattr(bench.time, "perf_counter", lambda: clock[0])
+    n = bench.oracle_rows_for(dict(N=100000, scale=0.1), (None,) * 6, 12.0)
+    assert 9000 <= n <= 12000
+    assert bench.oracle_rows_for(dict(N=500, scale=0.1), (None,) * 6, 12.0) == 500  # capped at N
+
+
 def test_traffic_record_tracks_kernel_source(tmp_path, monkeypatch):
     rec = {"k": {"w": {"source_sha": bench.kernel_source_sha(), "heads": 4, "dram_bytes_per_launch": 400.0}}}
     path = tmp_path / "traffic.json"
