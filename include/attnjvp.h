@@ -119,8 +119,10 @@ int attn_jvp_fwd_strided(const void* q, const void* k, const void* v,
 
 /*
  * Most general form: attn_jvp_fwd_strided with a value head dim of its own.
- * V, Vt, O and Ot have d_v columns per head, Q, Qt, K and Kt have d; the
- * page's forward takes d_v != d_qk (its backward does not).
+ * V, Vt, O and Ot have d_v columns per head, Q, Qt, K and Kt have d.  (The
+ * page's section 前向 (forward) documents v, tv as [B, H, S_kv, d_v] and o, to
+ * as [B, H, S_q, d_v], with d_v free in the forward; its backward needs
+ * d_v = d_qk.)  The default softmax scale there is d^-1/2 of the Q/K dim.
  *   d, d_v              : 16, 32, 64, 128 or 256 each.
  *   strides             : HOST array of 12 element strides — query, key, value
  *                         and output, each (batch, seq, head) — or NULL for
