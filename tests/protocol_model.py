@@ -471,3 +471,174 @@ class BwdModel(FwdModel):
                 except StopIteration:
                     live.remove(r)
         raise ProtocolError("deadlock: no progress in %d steps" % max_steps)
+
+
+# ---------------------------------------------------------------------------
+# The forward kernel's abort path
+# ---------------------------------------------------------------------------
+class AbortFwdModel(FwdModel):
+    """The forward protocol with a bounded wait giving up at a random point.
+
+    As in the kernel: waits in the main loops see the CTA's abort flag and give up;
+    each role then drains what it started (the TMA thread waits for the copies it
+    issued into the last ring units and for Q; each MMA issuer commits to its drain
+    barrier and waits on it) with waits that ignore the flag.  After every role has
+    finished, nothing may still be in flight: no copy landing in, and no MMA
+    reading, memory the CTA is about to release."""
+
+    def __init__(self, cfg, n_tiles, seed, abort_at, strict_teardown=False):
+        super().__init__(cfg, n_tiles, seed)
+        self.abort_at = abort_at
+        self.aborted = False
+        self.drain = {q: Bar("drain_" + q, 1) for q in ("S", "St", "PV")}
+        # A TMA thread that left its loop normally does not wait for its last copies
+        # (the consumers do, unless they abort).  ``strict_teardown`` counts such
+        # copies at teardown too; without it only copies of a thread that gave up
+        # and failed to drain are errors.
+        self.strict_teardown = strict_teardown
+        self.left_normally = {"tmaK": False, "tmaV": False}
+        self.step = 0
+        self.ready = []  # earliest scheduler step of each pending entry
+
+    def later(self, queue, fn):
+        # a copy takes a while to land; MMAs and arrivals are quick
+        self.pending.append((queue, fn))
+        self.ready.append(self.step + (self.rng.randint(20, 200) if queue.startswith("tma") else 0))
+
+    def wait_or_abort(self, bar, k):
+        """Bounded wait: returns False once the abort flag is up."""
+        while True:
+            if self.aborted:
+                return False
+            if bar.done >= k + 2:
+                raise ProtocolError("%s: waiter for phase %d is two phases behind" % (bar.name, k))
+            if (bar.done & 1) != (k & 1):
+                if bar.done != k + 1:
+                    raise ProtocolError("%s: parity test for phase %d passed with %d done" % (bar.name, k, bar.done))
+                return True
+            yield
+
+    def tma_k(self):
+        c = self.c
+        self.later("tmaK", self.q_full.arrive)
+        issued, ok = 0, True
+        for n in range(self.n * c["UPT"]):
+            s = n % c["KU"]
+            ok = yield from self.wait_or_abort(self.k_empty[s], n // c["KU"] - 1)
+            if not ok:
+                break
+            self.later("tmaK", self.k_full[s].arrive)
+            issued = n + 1
+        self.left_normally["tmaK"] = ok
+        if not ok:
+            yield from self.wait(self.q_full, 0)
+            for n in range(max(0, issued - c["KU"]), issued):
+                yield from self.wait(self.k_full[n % c["KU"]], n // c["KU"])
+
+    def tma_v(self):
+        c = self.c
+        issued, ok = 0, True
+        for t in range(self.n):
+            s = t % c["VS"]
+            ok = yield from self.wait_or_abort(self.v_empty[s], t // c["VS"] - 1)
+            if not ok:
+                break
+            self.later("tmaV", self.v_full[s].arrive)
+            issued = t + 1
+        self.left_normally["tmaV"] = ok
+        if not ok:
+            for t in range(max(0, issued - c["VS"]), issued):
+                yield from self.wait(self.v_full[t % c["VS"]], t // c["VS"])
+
+    def _issuer(self, name, NB, full, free_bar):
+        c = self.c
+        ok = yield from self.wait_or_abort(self.q_full, 0)
+        t = 0
+        while ok and t < self.n:
+            for u in range(c["UPT"]):
+                n = t * c["UPT"] + u
+                s = n % c["KU"]
+                ok = yield from self.wait_or_abort(self.k_full[s], n // c["KU"])
+                if ok and u == 0 and t >= NB:
+                    tp = t - NB
+                    ok = yield from self.wait_or_abort(free_bar[tp % NB], tp // NB)
+                if not ok:
+                    break
+                self.later(name, self.k_empty[s].arrive)
+            if not ok:
+                break
+            self.later(name, full[t % NB].arrive)
+            t += 1
+        self.later(name, self.drain[name].arrive)
+        yield from self.wait(self.drain[name], 0)
+
+    def s_issuer(self):
+        yield from self._issuer("S", self.c["NS"], self.s_full, self.s_free)
+
+    def st_issuer(self):
+        yield from self._issuer("St", self.c["NSt"], self.st_full, self.pv_done)
+
+    def pv_issuer(self):
+        c = self.c
+        for j in range(self.n):
+            b, s = j % c["NSt"], j % c["VS"]
+            ok = yield from self.wait_or_abort(self.p_full[b], j // c["NSt"])
+            ok = ok and (yield from self.wait_or_abort(self.v_full[s], j // c["VS"]))
+            if not ok:
+                break
+            self.later("PV", self.v_empty[s].arrive)
+            self.later("PV", self.pv_done[b].arrive)
+        self.later("PV", self.drain["PV"].arrive)
+        yield from self.wait(self.drain["PV"], 0)
+
+    def softmax_warp(self, w):
+        c = self.c
+        ok = True
+        for j in range(self.n):
+            b, bt = j % c["NS"], j % c["NSt"]
+            ok = yield from self.wait_or_abort(self.s_full[b], j // c["NS"])
+            ok = ok and (yield from self.wait_or_abort(self.st_full[bt], j // c["NSt"]))
+            if not ok:
+                break
+            self.s_free[b].arrive()
+            if j >= 1 and self.rng.random() < 0.3:
+                ok = yield from self.wait_or_abort(self.pv_done[(j - 1) % c["NSt"]], (j - 1) // c["NSt"])
+                if not ok:
+                    break
+            self.p_full[bt].arrive()
+        if ok:
+            yield from self.wait_or_abort(self.pv_done[(self.n - 1) % c["NSt"]], (self.n - 1) // c["NSt"])
+
+    def run(self, max_steps=500000):
+        roles = [self.tma_k(), self.tma_v(), self.s_issuer(), self.st_issuer(), self.pv_issuer()]
+        roles += [self.softmax_warp(w) for w in range(4)]
+        live = list(roles)
+        for step in range(max_steps):
+            self.step = step
+            if step == self.abort_at:
+                self.aborted = True
+            if not live:
+                stray = [q for q, _ in self.pending
+                         if self.strict_teardown or not self.left_normally.get(q, False)]
+                if stray:
+                    raise ProtocolError("teardown with %d copies or MMAs still in flight" % len(stray))
+                return
+            if self.pending and self.rng.random() < 0.4:
+                heads, seen = [], set()
+                for i, (q, _) in enumerate(self.pending):
+                    if q.startswith("tma") or q not in seen:
+                        seen.add(q)
+                        if self.ready[i] <= step:
+                            heads.append(i)
+                if heads:
+                    i = self.rng.choice(heads)
+                    self.ready.pop(i)
+                    _, fn = self.pending.pop(i)
+                    fn()
+                    continue
+            r = self.rng.choice(live)
+            try:
+                next(r)
+            except StopIteration:
+                live.remove(r)
+        raise ProtocolError("a role never finished after the abort")
