@@ -612,6 +612,9 @@ class AbortFwdModel(FwdModel):
     def run(self, max_steps=500000):
         roles = [self.tma_k(), self.tma_v(), self.s_issuer(), self.st_issuer(), self.pv_issuer()]
         roles += [self.softmax_warp(w) for w in range(4)]
+        return self.run_roles(roles, max_steps)
+
+    def run_roles(self, roles, max_steps):
         live = list(roles)
         for step in range(max_steps):
             self.step = step
@@ -642,3 +645,120 @@ class AbortFwdModel(FwdModel):
             except StopIteration:
                 live.remove(r)
         raise ProtocolError("a role never finished after the abort")
+
+
+class AbortBwdModel(BwdModel):
+    """The backward protocol with a bounded wait giving up (see AbortFwdModel).  The
+    polling TMA thread drains the resident tiles and the last stage of each ring only
+    when it gave up itself; each MMA issuer drains its own MMAs."""
+
+    def __init__(self, cfg, n_tiles, seed, abort_at, strict_teardown=False):
+        super().__init__(cfg, n_tiles, seed)
+        self.abort_at = abort_at
+        self.aborted = False
+        self.strict_teardown = strict_teardown
+        self.left_normally = {"tma": False}
+        self.drain = {q: Bar("drain_" + q, 1) for q in ("S1", "S2", "PV")}
+        self.step = 0
+        self.ready = []
+
+    later = AbortFwdModel.later
+    wait_or_abort = AbortFwdModel.wait_or_abort
+
+    def producer(self):
+        c = self.c
+        self.later("tma", self.r_full.arrive)
+        tk = tv = tq = 0
+        nq = self.n if c["dkdv"] else 0
+        ok = True
+        while tk < self.n or tv < self.n or tq < nq:
+            if self.aborted:
+                ok = False
+                break
+            if tq < nq and self.test(self.vec_empty[tq % c["VecS"]], tq // c["VecS"] - 1):
+                self.later("tma", self.vec_full[tq % c["VecS"]].arrive)
+                tq += 1
+            if tk < self.n and self.test(self.k_empty[tk % c["KS"]], tk // c["KS"] - 1):
+                self.later("tma", self.k_full[tk % c["KS"]].arrive)
+                tk += 1
+            if tv < self.n and self.test(self.v_empty[tv % c["VS"]], tv // c["VS"] - 1):
+                self.later("tma", self.v_full[tv % c["VS"]].arrive)
+                tv += 1
+            yield
+        self.left_normally["tma"] = ok
+        if not ok:
+            yield from self.wait(self.r_full, 0)
+            for bars, n, k in ((self.k_full, tk, c["KS"]), (self.v_full, tv, c["VS"]),
+                               (self.vec_full, tq, c["VecS"])):
+                for t in range(max(0, n - k), n):
+                    yield from self.wait(bars[t % k], t // k)
+
+    def score_issuer(self, first):
+        c = self.c
+        name = "S1" if first else "S2"
+        ok = yield from self.wait_or_abort(self.r_full if c["dkdv"] else self.r_tmem, 0)
+        for t in range(self.n):
+            if not ok:
+                break
+            s = t % c["KS"]
+            b = t % (c["NS"] if first else c["NSt"])
+            ok = yield from self.wait_or_abort(self.k_full[s], t // c["KS"])
+            if ok and first and t >= c["NS"]:
+                tp = t - c["NS"]
+                ok = yield from self.wait_or_abort(self.s_free[tp % c["SBar"]], tp // c["SBar"])
+            if ok and not first and t >= c["NSt"]:
+                ok = yield from self.wait_or_abort(self.pv_done[b], (t - c["NSt"]) // c["NSt"])
+            if not ok:
+                break
+            self.later(name, self.k_empty[s].arrive)
+            self.later(name, (self.s_full[t % c["SBar"]] if first else self.st_full[b]).arrive)
+        self.later(name, self.drain[name].arrive)
+        yield from self.wait(self.drain[name], 0)
+
+    def value_issuer(self):
+        c = self.c
+        ok = True
+        for j in range(self.n):
+            b, s = j % c["NSt"], j % c["VS"]
+            ok = yield from self.wait_or_abort(self.p_full[b], j // c["NSt"])
+            ok = ok and (yield from self.wait_or_abort(self.v_full[s], j // c["VS"]))
+            if not ok:
+                break
+            self.later("PV", self.v_empty[s].arrive)
+            self.later("PV", self.pv_done[b].arrive)
+        if ok:
+            self.later("PV", self.acc_done.arrive)
+        self.later("PV", self.drain["PV"].arrive)
+        yield from self.wait(self.drain["PV"], 0)
+
+    def elementwise_warp(self, group, w):
+        c = self.c
+        ok = True
+        if not c["dkdv"] and group == 0:
+            ok = yield from self.wait_or_abort(self.r_full, 0)
+            if ok:
+                self.r_tmem.arrive()
+        for j in range(group, self.n, 2):
+            if not ok:
+                break
+            bs, bt, sq = j % c["SBar"], j % c["NSt"], j % c["VecS"]
+            ok = yield from self.wait_or_abort(self.s_full[bs], j // c["SBar"])
+            if not ok:
+                break
+            self.s_free[bs].arrive()
+            ok = yield from self.wait_or_abort(self.st_full[bt], j // c["NSt"])
+            if ok and c["dkdv"]:
+                ok = yield from self.wait_or_abort(self.vec_full[sq], j // c["VecS"])
+            if not ok:
+                break
+            self.p_full[bt].arrive()
+            if c["dkdv"]:
+                self.vec_empty[sq].arrive()
+        if ok:
+            yield from self.wait_or_abort(self.acc_done, 0)
+
+    def run(self, max_steps=500000):
+        roles = [self.producer(), self.score_issuer(True), self.score_issuer(False), self.value_issuer()]
+        roles += [self.elementwise_warp(g, w) for g in range(2) for w in range(4)]
+        self._roles = roles
+        return AbortFwdModel.run_roles(self, roles, max_steps)

@@ -194,3 +194,27 @@ def test_abort_right_after_the_last_copy():
 
     for seed in range(100):
         AbortAfterLastCopy(fwd_config(128, 128), 6, seed=seed, abort_at=-1, strict_teardown=True).run()
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("dkdv", [True, False], ids=["dKdV", "dQ"])
+def test_backward_abort_path_drains_and_terminates(D, dkdv):
+    from protocol_model import AbortBwdModel
+    cfg = bwd_config(D, dkdv)
+    for seed in range(60):
+        AbortBwdModel(cfg, 7, seed=seed, abort_at=seed * 9).run()
+
+
+@pytest.mark.xfail(strict=True, reason="known gap, as in the forward kernel: the polling TMA thread drains "
+                   "only when it gave up itself")
+def test_backward_abort_right_after_the_last_copy():
+    from protocol_model import AbortBwdModel
+
+    class AbortAfterLastCopy(AbortBwdModel):
+        def producer(self):
+            yield from super().producer()
+            if any(q.startswith("tma") for q, _ in self.pending):
+                self.aborted = True
+
+    for seed in range(100):
+        AbortAfterLastCopy(bwd_config(128, True), 7, seed=seed, abort_at=-1, strict_teardown=True).run()
