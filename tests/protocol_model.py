@@ -762,3 +762,137 @@ class AbortBwdModel(BwdModel):
         roles += [self.elementwise_warp(g, w) for g in range(2) for w in range(4)]
         self._roles = roles
         return AbortFwdModel.run_roles(self, roles, max_steps)
+
+
+# ---------------------------------------------------------------------------
+# attn_jvp_fwd_host: items rotating through three workspace slots on streams
+# ---------------------------------------------------------------------------
+class HostPipelineModel:
+    """The host path's stream and event order.
+
+    Streams run their operations in order; ``cudaStreamWaitEvent`` waits for the
+    most recent record of the event enqueued before the wait (none: no wait);
+    copies and kernels take time and may overlap with work on other streams.
+    The enqueue order below follows the host loop of ``attn_jvp_fwd_host``: per
+    item i in slot s = i mod 3, copy-in on the H2D stream after the slot's
+    previous compute, compute on the slot's stream after its copy-in and the
+    slot's previous copy-out, copy-out on the D2H stream after the compute; the
+    caller's stream finally waits for the last copy-out of every slot.  Checked:
+    no copy or kernel touches a slot's buffers while a conflicting one is in
+    progress, every kernel reads its own item's inputs and every copy-out its
+    own item's outputs, and nothing is left when the caller's stream is done.
+    ``mutate``: "no_copied_wait" drops the compute's wait for the slot's previous
+    copy-out, "no_computed_wait" drops the copy-in's wait for the previous
+    compute."""
+
+    SLOTS = 3
+
+    def __init__(self, n_items, seed, mutate=None):
+        self.n = n_items
+        self.rng = random.Random(seed)
+        self.mutate = mutate
+        self.streams = {name: [] for name in ("caller", "h2d", "d2h", "c0", "c1", "c2")}
+        self.enqueued = {}   # event -> versions recorded (enqueued) so far
+        self.completed = {}  # event -> versions completed
+        self.inputs = [None] * self.SLOTS    # item whose inputs the slot holds
+        self.outputs = [None] * self.SLOTS   # item whose outputs the slot holds
+        self.busy_in = [[] for _ in range(self.SLOTS)]   # ops touching the slot's inputs now
+        self.busy_out = [[] for _ in range(self.SLOTS)]
+        self.delivered = set()
+
+    def record(self, stream, ev):
+        v = self.enqueued.get(ev, 0) + 1
+        self.enqueued[ev] = v
+        self.streams[stream].append(("record", ev, v))
+
+    def wait_event(self, stream, ev):
+        v = self.enqueued.get(ev, 0)
+        if v:
+            self.streams[stream].append(("wait", ev, v))
+
+    def enqueue(self):
+        S = self.SLOTS
+        self.record("caller", "entry")
+        for i in range(self.n):
+            s = i % S
+            reuse = i >= S
+            if not (reuse and self.mutate == "no_computed_wait"):
+                self.wait_event("h2d", ("computed", s) if reuse else "entry")
+            self.streams["h2d"].append(("copy_in", s, i))
+            self.record("h2d", ("in_ready", s))
+            cs = "c%d" % s
+            self.wait_event(cs, ("in_ready", s))
+            if reuse and self.mutate != "no_copied_wait":
+                self.wait_event(cs, ("copied", s))
+            self.streams[cs].append(("compute", s, i))
+            self.record(cs, ("computed", s))
+            self.wait_event("d2h", ("computed", s))
+            self.streams["d2h"].append(("copy_out", s, i))
+            self.record("d2h", ("copied", s))
+        for s in range(min(S, self.n)):
+            self.wait_event("caller", ("copied", s))
+        self.streams["caller"].append(("done",))
+
+    def _start(self, op):
+        kind, s, i = op
+        if kind == "copy_in":
+            if self.busy_in[s]:
+                raise ProtocolError("copy-in of item %d over inputs in use by %s" % (i, self.busy_in[s]))
+            self.busy_in[s].append(op)
+        elif kind == "compute":
+            if self.inputs[s] != i or any(o[0] == "copy_in" for o in self.busy_in[s]):
+                raise ProtocolError("compute of item %d reads inputs of item %s" % (i, self.inputs[s]))
+            if self.busy_out[s]:
+                raise ProtocolError("compute of item %d writes outputs in use by %s" % (i, self.busy_out[s]))
+            self.busy_in[s].append(op)
+            self.busy_out[s].append(op)
+        else:
+            if self.outputs[s] != i or any(o[0] == "compute" for o in self.busy_out[s]):
+                raise ProtocolError("copy-out of item %d reads outputs of item %s" % (i, self.outputs[s]))
+            self.busy_out[s].append(op)
+
+    def _finish(self, op):
+        kind, s, i = op
+        if kind == "copy_in":
+            self.busy_in[s].remove(op)
+            self.inputs[s] = i
+        elif kind == "compute":
+            self.busy_in[s].remove(op)
+            self.busy_out[s].remove(op)
+            self.outputs[s] = i
+        else:
+            self.busy_out[s].remove(op)
+            self.delivered.add(i)
+
+    def run(self, max_steps=200000):
+        self.enqueue()
+        running = {}  # stream -> data op in progress
+        for _ in range(max_steps):
+            ready = []
+            for name, q in self.streams.items():
+                if name in running:
+                    ready.append(name)
+                elif q:
+                    head = q[0]
+                    if head[0] == "wait" and self.completed.get(head[1], 0) < head[2]:
+                        continue
+                    ready.append(name)
+            if not ready:
+                if any(self.streams.values()) or running:
+                    raise ProtocolError("streams deadlocked")
+                break
+            name = self.rng.choice(ready)
+            if name in running:
+                self._finish(running.pop(name))
+                continue
+            head = self.streams[name].pop(0)
+            if head[0] == "record":
+                self.completed[head[1]] = max(self.completed.get(head[1], 0), head[2])
+            elif head[0] == "done":
+                if self.delivered != set(range(self.n)):
+                    raise ProtocolError("caller's stream done before every output reached the host")
+                return
+            elif head[0] in ("copy_in", "compute", "copy_out"):
+                self._start(head)
+                running[name] = head
+        raise ProtocolError("no end in %d steps" % max_steps)

@@ -218,3 +218,22 @@ def test_backward_abort_right_after_the_last_copy():
 
     for seed in range(100):
         AbortAfterLastCopy(bwd_config(128, True), 7, seed=seed, abort_at=-1, strict_teardown=True).run()
+
+
+@pytest.mark.parametrize("n_items", [1, 2, 3, 4, 7, 12])
+def test_host_pipeline_streams_are_race_free(n_items):
+    from protocol_model import HostPipelineModel
+    for seed in range(40):
+        HostPipelineModel(n_items, seed).run()
+
+
+@pytest.mark.parametrize("mutate", ["no_copied_wait", "no_computed_wait"])
+def test_host_pipeline_missing_waits_are_caught(mutate):
+    from protocol_model import HostPipelineModel
+    hits = 0
+    for seed in range(60):
+        try:
+            HostPipelineModel(9, seed, mutate=mutate).run()
+        except ProtocolError:
+            hits += 1
+    assert hits > 0
