@@ -31,7 +31,9 @@ if ROOT not in sys.path:
 
 METRIC = "attention-JVP TFLOPS (12·B·H·N²·d) and % of GB300 BF16 tensor peak"
 UNIT = "TFLOP/s"
-DEFAULT_WORKLOAD = "video_dit"
+DEFAULT_WORKLOAD = "long_video"
+# Other workloads timed in the same run, each as a device-timed sub-record.
+DEFAULT_ALSO = "video_dit,stress,image_dit_1k"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # Sources whose change invalidates a recorded DRAM-traffic capture of the fused kernel.
 KERNEL_SOURCES = tuple(os.path.join(ROOT, "attention_jvp_gb300", "csrc", n) for n in ("attn_jvp_fwd.cu", "sm103_ptx.cuh"))
@@ -52,6 +54,9 @@ def parse_args(argv=None):
     p.add_argument("--skip-backward", action="store_true", help="skip the primal-backward line")
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    p.add_argument("--also", default=DEFAULT_ALSO,
+                   help="comma-separated workloads timed after the main one as device-only sub-records ('' = none)")
+    p.add_argument("--sub-steps", type=int, default=10, help="timed steps of each sub-record workload")
     return p.parse_args(argv)
 
 
@@ -374,6 +379,221 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+# Dense bf16 tcgen05 rate of one SM per clock: a 128x128x16 MMA issues every 64
+# clocks (2*128*128*16/64), measured on this GPU with one issuing thread.
+TENSOR_FLOP_PER_CLK_SM = 8192.0
+
+
+def merge_bytes(spec, n_chunks):
+    """Algorithmic bytes of one merge: every chunk's O_c, Ot_c (d floats each) and
+    LSE_c, mu_c are read once, O, Ot, LSE and mu written once."""
+    rows = spec["B"] * spec["H"] * spec["N"]
+    per_row = (2 * spec["d"] + 2) * 4
+    return rows * per_row * (n_chunks + 1)
+
+
+def tangent_bytes(elems):
+    """Algorithmic bytes of trigflow_tangent: read x0 and eps, write the tangent (fp32)."""
+    return 12 * elems
+
+
+def clock_normalised_frac(tflops, sm_count, sm_mhz):
+    """Achieved flops over the tensor pipe's own rate at the sampled SM clock."""
+    if not sm_mhz:
+        return None
+    return tflops * 1e12 / (sm_count * TENSOR_FLOP_PER_CLK_SM * sm_mhz * 1e6)
+
+
+class Path:
+    """One workload's hot path on device-resident inputs: trigflow_coeffs (host,
+    FP64) and trigflow_tangent of the latent batch, then the fused attention JVP
+    (key chunks + exact merge where the workload is split).  ``step(record=True)``
+    brackets every kernel launch with CUDA events on the launching stream."""
+
+    def __init__(self, spec, dev, stream):
+        import torch
+
+        from attention_jvp_gb300 import binding, inputs
+        self.spec, self.dev, self.stream = spec, dev, stream
+        B, H, N, d = spec["B"], spec["H"], spec["N"], spec["d"]
+        self.x = inputs.make_inputs(**spec, device=dev)
+        self.scale = self.x["scale"]
+        self.x0, self.eps, self.t = inputs.latent_for(spec, device=dev)
+        self.t_host = self.t.cpu().tolist()
+        self.dxdt = torch.empty_like(self.x0)
+        self.out = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+        self.out_t = torch.empty_like(self.out)
+        self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        self.mu = torch.empty_like(self.lse)
+        self.n_chunks = spec.get("kv_chunks", 1)
+        self.ws = binding.split_workspace((B, H, N, d), self.n_chunks, dev) if self.n_chunks > 1 else None
+        self.bounds = binding.chunk_bounds(N, self.n_chunks)
+        self.launches_per_step = 1 + (1 if self.n_chunks == 1 else self.n_chunks + 1)
+        self.events = {"attention": [], "merge": [], "tangent": []}  # (start, end, units)
+
+    def _launch(self, kind, units, fn, record):
+        import torch
+        if not record:
+            fn()
+            return
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        fn()
+        e1.record(self.stream)
+        self.events[kind].append((e0, e1, units))
+
+    def step(self, record=False):
+        from attention_jvp_gb300 import binding
+        x, st = self.x, self.stream
+        coeffs = [binding.trigflow_coeffs(tt) for tt in self.t_host]  # FP64, host
+        self._launch("tangent", self.x0.numel(),
+                     lambda: binding.trigflow_tangent(self.x0, self.eps, self.t, out=self.dxdt, stream=st), record)
+        args = (x["q"], x["k"], x["v"], x["q_t"], x["k_t"], x["v_t"])
+        if self.n_chunks == 1:
+            self._launch("attention", self.spec["N"],
+                         lambda: binding.attn_jvp_fwd(*args, scale=self.scale, out=self.out, out_t=self.out_t,
+                                                      lse=self.lse, mu=self.mu, stream=st), record)
+        else:
+            ws = self.ws
+            for c, (a, n) in enumerate(self.bounds):
+                self._launch("attention", n,
+                             lambda c=c, a=a, n=n: binding.attn_jvp_fwd_chunk(
+                                 *args, a, n, scale=self.scale, out=ws[0][c], out_t=ws[1][c], lse=ws[2][c],
+                                 mu=ws[3][c], stream=st), record)
+            self._launch("merge", self.n_chunks,
+                         lambda: binding.attn_jvp_merge(*ws, out=self.out, out_t=self.out_t, lse=self.lse,
+                                                        mu=self.mu, stream=st), record)
+        return coeffs
+
+    def clear_events(self):
+        for v in self.events.values():
+            v.clear()
+
+    def mean_ms(self, kind):
+        ev = self.events[kind]
+        return sum(a.elapsed_time(b) for a, b, _ in ev) / len(ev) if ev else None
+
+
+def timed_region(path, steps, sampler, world):
+    """Times exactly ``steps`` steps between a barrier and a synchronize on each side,
+    with the clocks sampled meanwhile; returns (ms, clock summary)."""
+    import torch
+    import torch.distributed as dist
+
+    from attention_jvp_gb300 import binding
+    path.clear_events()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)  # let the sampler take a first idle-to-load sample
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(path.stream)
+    for _ in range(steps):
+        path.step(record=True)
+    ev1.record(path.stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    sampler.stop()
+    binding.attn_jvp_status()
+    return ev0.elapsed_time(ev1), ClockSampler.summarize(sampler.lines)
+
+
+def measure_path(path, steps, warmup, sampler, world, dev):
+    """Warm up, time, and retake once if the clock record voids the first region."""
+    import torch
+    import torch.distributed as dist
+
+    from attention_jvp_gb300 import binding
+    for _ in range(warmup):
+        path.step()
+    torch.cuda.synchronize()
+    binding.attn_jvp_status()
+    ms, clocks = timed_region(path, steps, sampler, world)
+    why = ClockSampler.rejection(clocks)
+    veto = float(why is not None)
+    if world > 1:  # any rank's veto counts
+        tv = torch.tensor([veto], dtype=torch.float64, device=dev)
+        dist.all_reduce(tv, op=dist.ReduceOp.MAX)
+        veto = float(tv.item())
+    if veto:
+        ms, clocks = timed_region(path, steps, sampler, world)
+        clocks["remeasured"] = why or "another rank's clocks"
+        clocks["rejected_again"] = ClockSampler.rejection(clocks)
+    return ms, clocks
+
+
+def kernel_report(path, workload, peaks, peak_src, clocks, sm_count):
+    """Roofline of the fused attention kernel (tensor-bound) from its own launch events,
+    plus the achieved bandwidth of the HBM-bound kernels of the step."""
+    spec = path.spec
+    B, H, d = spec["B"], spec["H"], spec["d"]
+    ev = path.events["attention"]
+    mean_launch_ms = path.mean_ms("attention")
+    flops_launch = sum(attention_flops(spec, kv) for _, _, kv in ev) / len(ev)
+    achieved = flops_launch / (mean_launch_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops_sustained"])
+    kname = "attn_jvp_fwd_kernel<%d, %d>" % (d, d)
+    traffic = traffic_per_launch(kname, workload, H * B)
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": UNIT,
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_source": "%s bf16_tflops_sustained (kernel timed inside a long step)" % peak_src,
+                "frac_of_burst_peak": round(achieved / float(peaks["bf16_tflops"]), 4),
+                "kernel": kname, "launch_ms": round(mean_launch_ms, 4),
+                "flops_per_launch": flops_launch}
+    cn = clock_normalised_frac(achieved, sm_count, clocks.get("sm_mhz"))
+    if cn is not None:
+        roofline["frac_of_tensor_pipe_at_sampled_clock"] = round(cn, 4)
+        roofline["tensor_pipe_rate"] = ("%d SMs x %.0f flop/clk x %.0f MHz (median sampled) = %.1f TFLOP/s"
+                                        % (sm_count, TENSOR_FLOP_PER_CLK_SM, clocks["sm_mhz"],
+                                           sm_count * TENSOR_FLOP_PER_CLK_SM * clocks["sm_mhz"] * 1e-6))
+    hbm = float(peaks["hbm_gbs"])
+    others = {}
+    t_ms = path.mean_ms("tangent")
+    if t_ms:
+        nb = tangent_bytes(path.x0.numel())
+        others["trigflow_tangent_kernel"] = {
+            "bound": "hbm", "algorithmic_bytes": nb, "launch_ms": round(t_ms, 5),
+            "achieved": round(nb / (t_ms * 1e-3) / 1e9, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(nb / (t_ms * 1e-3) / 1e9 / hbm, 4),
+            "note": "12 B per element; %d elements, %.0f MB (below L2: served partly from cache)"
+                    % (path.x0.numel(), nb / 1e6)}
+    m_ms = path.mean_ms("merge")
+    if m_ms:
+        nb = merge_bytes(spec, path.n_chunks)
+        others["merge_kernel"] = {
+            "bound": "hbm", "algorithmic_bytes": nb, "launch_ms": round(m_ms, 4),
+            "achieved": round(nb / (m_ms * 1e-3) / 1e9, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(nb / (m_ms * 1e-3) / 1e9 / hbm, 4),
+            "note": "%d chunk partials (O_c, Ot_c, LSE_c, mu_c) read, merged O, Ot, LSE, mu written"
+                    % path.n_chunks}
+    return roofline, others
+
+
+def sub_record(name, args, dev, stream, peaks, peak_src, sampler, sm_count):
+    """Device-timed line of another workload (same step, same timing rules), for the
+    JSON line's ``workloads`` object."""
+    import torch
+    spec = workload_spec(name)
+    path = Path(spec, dev, stream)
+    ms, clocks = measure_path(path, args.sub_steps, max(3, args.warmup), sampler, 1, dev)
+    flops = attention_flops(spec) * args.sub_steps
+    value = flops / (ms * 1e-3) / 1e12
+    roofline, others = kernel_report(path, name, peaks, peak_src, clocks, sm_count)
+    rec = {"value": round(value, 3), "unit": UNIT, "steps": args.sub_steps, "warmup": max(3, args.warmup),
+           "ms_per_step": round(ms / args.sub_steps, 4),
+           "config": {"workload": name, "B": spec["B"], "H": spec["H"], "N": spec["N"], "d": spec["d"],
+                      "kv_chunks": path.n_chunks},
+           "roofline": roofline, "hbm_kernels": others, "clocks": clocks,
+           "gpu_launches": path.launches_per_step * args.sub_steps}
+    del path
+    torch.cuda.empty_cache()
+    return rec
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -392,60 +612,13 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     binding.load()
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
 
     spec = workload_spec(args.workload, args.heads)
     B, H, N, d = spec["B"], spec["H"], spec["N"], spec["d"]
-    x = inputs.make_inputs(**spec, device=dev)
-    scale = x["scale"]
-    x0, eps, t = inputs.latent_for(spec, device=dev)
-    t_host = t.cpu().tolist()
-    dxdt = torch.empty_like(x0)
-    out = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
-    out_t = torch.empty_like(out)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    mu = torch.empty_like(lse)
-    n_chunks = spec.get("kv_chunks", 1)
-    ws = binding.split_workspace((B, H, N, d), n_chunks, dev) if n_chunks > 1 else None
-    bounds = binding.chunk_bounds(N, n_chunks)
     stream = torch.cuda.current_stream()
-    attn_events = []  # (start, end, kv_len) per attention-kernel launch in the timed region
-
-    def attention(q, k, v, q_t, k_t, v_t, record):
-        if n_chunks == 1:
-            e0 = torch.cuda.Event(enable_timing=True) if record else None
-            e1 = torch.cuda.Event(enable_timing=True) if record else None
-            if record:
-                e0.record(stream)
-            binding.attn_jvp_fwd(q, k, v, q_t, k_t, v_t, scale=scale, out=out, out_t=out_t, lse=lse, mu=mu,
-                                 stream=stream)
-            if record:
-                e1.record(stream)
-                attn_events.append((e0, e1, N))
-        else:
-            for c, (a, n) in enumerate(bounds):
-                e0 = torch.cuda.Event(enable_timing=True) if record else None
-                e1 = torch.cuda.Event(enable_timing=True) if record else None
-                if record:
-                    e0.record(stream)
-                binding.attn_jvp_fwd_chunk(q, k, v, q_t, k_t, v_t, a, n, scale=scale, out=ws[0][c],
-                                           out_t=ws[1][c], lse=ws[2][c], mu=ws[3][c], stream=stream)
-                if record:
-                    e1.record(stream)
-                    attn_events.append((e0, e1, n))
-            binding.attn_jvp_merge(*ws, out=out, out_t=out_t, lse=lse, mu=mu, stream=stream)
-
-    def step(record=False, xin=x):
-        coeffs = [binding.trigflow_coeffs(tt) for tt in t_host]  # FP64, host
-        binding.trigflow_tangent(x0, eps, t, out=dxdt, stream=stream)
-        attention(xin["q"], xin["k"], xin["v"], xin["q_t"], xin["k_t"], xin["v_t"], record)
-        return coeffs
-
-    launches_per_step = 1 + (1 if n_chunks == 1 else n_chunks + 1)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    binding.attn_jvp_status()
+    path = Path(spec, dev, stream)
+    x, scale, n_chunks = path.x, path.scale, path.n_chunks
 
     gpu_index = local
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
@@ -455,41 +628,7 @@ def run_gpu(args):
             gpu_index = int(ids[local])
     sampler = ClockSampler(gpu_index)
 
-    def timed_region():
-        attn_events.clear()
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        sampler.start()
-        time.sleep(0.3)  # let the sampler take a first idle-to-load sample
-        ev0 = torch.cuda.Event(enable_timing=True)
-        ev1 = torch.cuda.Event(enable_timing=True)
-        ev0.record(stream)
-        for _ in range(args.steps):
-            step(record=True)
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        sampler.stop()
-        binding.attn_jvp_status()
-        return ev0.elapsed_time(ev1), ClockSampler.summarize(sampler.lines)
-
-    local_ms, clocks = timed_region()
-    # A throttled or clock-locked region is voided and timed once more; any rank's veto counts.
-    why = ClockSampler.rejection(clocks)
-    veto = float(why is not None)
-    if world > 1:
-        tv = torch.tensor([veto], dtype=torch.float64, device=dev)
-        dist.all_reduce(tv, op=dist.ReduceOp.MAX)
-        veto = float(tv.item())
-    if veto:
-        local_ms, clocks = timed_region()
-        clocks["remeasured"] = why or "another rank's clocks"
-        clocks["rejected_again"] = ClockSampler.rejection(clocks)
-    attn_ms = [a.elapsed_time(b) for a, b, _ in attn_events]
-    attn_kv = [kv for _, _, kv in attn_events]
-
+    local_ms, clocks = measure_path(path, args.steps, args.warmup, sampler, world, dev)
     flops_step = attention_flops(spec)
 
     def rmax(v):
@@ -505,20 +644,9 @@ def run_gpu(args):
     job_ms, job_flops = aggregate(local_ms, flops_step * args.steps, world, rmax, rsum)
     value = job_flops / (job_ms * 1e-3) / 1e12
 
-    # ---- roofline of the dominant kernel (the fused attention-JVP kernel) ----
     peaks, peak_src = load_peaks()
-    mean_launch_ms = sum(attn_ms) / len(attn_ms)
-    flops_launch = sum(attention_flops(spec, kv) for kv in attn_kv) / len(attn_kv)
-    achieved = flops_launch / (mean_launch_ms * 1e-3) / 1e12
-    peak = float(peaks["bf16_tflops_sustained"])
-    kname = "attn_jvp_fwd_kernel<%d, %d>" % (d, d)
-    traffic = traffic_per_launch(kname, args.workload, H * B)
-    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": UNIT,
-                "frac": round(achieved / peak, 4), "traffic": traffic,
-                "peak_source": "%s bf16_tflops_sustained (kernel timed inside a long step)" % peak_src,
-                "frac_of_burst_peak": round(achieved / float(peaks["bf16_tflops"]), 4),
-                "kernel": kname, "launch_ms": round(mean_launch_ms, 4),
-                "flops_per_launch": flops_launch}
+    roofline, hbm_kernels = kernel_report(path, args.workload, peaks, peak_src, clocks, sm_count)
+    out, lse = path.out, path.lse
 
     # ---- end to end through the C ABI with host buffers ----
     # Every step copies its inputs in from pinned host memory and its results
@@ -527,10 +655,12 @@ def run_gpu(args):
     # attention transfers against compute inside the library.
     e2e = None
     if not args.skip_e2e:
+        x0, eps, t, dxdt, t_host = path.x0, path.eps, path.t, path.dxdt, path.t_host
         host_in = {n: torch.empty(x[n].shape, dtype=x[n].dtype, pin_memory=True) for n in inputs.NAMES}
         for n in inputs.NAMES:
             host_in[n].copy_(x[n])
-        host_out = [torch.empty(tt.shape, dtype=tt.dtype, pin_memory=True) for tt in (out, out_t, lse, mu)]
+        host_out = [torch.empty(tt.shape, dtype=tt.dtype, pin_memory=True)
+                    for tt in (path.out, path.out_t, path.lse, path.mu)]
         lat_in = [torch.empty(tt.shape, dtype=tt.dtype, pin_memory=True) for tt in (x0, eps, t)]
         for hdst, src in zip(lat_in, (x0, eps, t)):
             hdst.copy_(src)
@@ -590,8 +720,19 @@ def run_gpu(args):
                "sample": "%d query rows of head 0 vs all %d keys (%.1f s FP64 on %d host threads)"
                          % (nrows, N, dt, cores)}
 
+    total_bytes = sum(x[n].numel() * x[n].element_size() for n in inputs.NAMES)
+    launches = path.launches_per_step * args.steps
+    del path, x, out, lse
+    torch.cuda.empty_cache()
+
+    # ---- the other workloads, device-timed under the same rules (rank 0, N = 1 only) ----
+    subs = None
+    if rank == 0 and world == 1 and args.also:
+        subs = {}
+        for name in [w for w in args.also.split(",") if w and w != args.workload]:
+            subs[name] = sub_record(name, args, dev, stream, peaks, peak_src, sampler, sm_count)
+
     if rank == 0:
-        total_bytes = sum(x[n].numel() * x[n].element_size() for n in inputs.NAMES)
         rec = {
             "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(job_ms / args.steps, 4), "higher_is_better": True,
@@ -605,12 +746,14 @@ def run_gpu(args):
                             "bf16_burst_%.0f" % float(peaks["bf16_tflops"]):
                             round(100 * value / world / float(peaks["bf16_tflops"]), 2)},
             "roofline": roofline,
+            "hbm_kernels": hbm_kernels,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": launches_per_step * args.steps,
+            "gpu_launches": launches,
             "epilogue": epi,
             "backward": bwd,
             "clocks": clocks,
+            "workloads": subs,
         }
         print(json.dumps(rec))
     if world > 1:

@@ -178,3 +178,28 @@ def test_reference_arm_nonzero_rank_exits_quietly():
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "tiny"],
                          capture_output=True, text=True, timeout=120, cwd=ROOT, env=env)
     assert out.returncode == 0 and out.stdout.strip() == ""
+
+
+def test_merge_and_tangent_algorithmic_bytes():
+    spec = dict(B=1, H=40, N=75600, d=128)
+    # four chunks of (O_c, Ot_c, LSE_c, mu_c) read, one merged set written
+    rows = 40 * 75600
+    assert bench.merge_bytes(spec, 4) == rows * (2 * 128 + 2) * 4 * 5
+    assert bench.tangent_bytes(1000) == 12000
+
+
+def test_clock_normalised_fraction():
+    # 152 SMs x 8192 flop/clk at 2000 MHz is 2490.4 TFLOP/s
+    full = 152 * 8192 * 2000e6 / 1e12
+    assert abs(bench.clock_normalised_frac(full / 2, 152, 2000.0) - 0.5) < 1e-12
+    assert bench.clock_normalised_frac(1000.0, 152, None) is None
+
+
+def test_default_workload_is_the_largest_single_gpu_config():
+    from attention_jvp_gb300 import inputs
+    args = bench.parse_args([])
+    assert args.workload == "long_video" and args.steps >= 1 and args.warmup >= 3
+    big = max((w for w in ("image_dit_1k", "video_dit", "long_video", "stress")),
+              key=lambda w: bench.attention_flops(inputs.WORKLOADS[w]))
+    assert big == args.workload
+    assert set(args.also.split(",")) == {"video_dit", "stress", "image_dit_1k"}
