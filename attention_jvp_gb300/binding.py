@@ -20,6 +20,11 @@ ATTNJVP_EUNSUPPORTED = -2
 ATTNJVP_ECUDA = -3
 ATTNJVP_ETIMEOUT = -4
 
+# input dtype codes of the forward entry points
+ATTNJVP_BF16 = 0
+ATTNJVP_FP32 = 1
+_DTYPE_CODES = {torch.bfloat16: ATTNJVP_BF16, torch.float32: ATTNJVP_FP32}
+
 _lib = None
 
 
@@ -39,16 +44,17 @@ def load(path=None):
         raise RuntimeError("libattnjvp.so not built (%s); run __graft_entry__.build()" % path)
     lib = ctypes.CDLL(path)
     vp, i64, fp = ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p
-    lib.attn_jvp_fwd.argtypes = [vp] * 6 + [fp] * 4 + [i64] * 4 + [ctypes.c_float, vp]
-    lib.attn_jvp_fwd_chunk.argtypes = [vp] * 6 + [fp] * 4 + [i64] * 4 + [ctypes.c_float, i64, i64, vp]
+    ci = ctypes.c_int
+    lib.attn_jvp_fwd.argtypes = [vp] * 6 + [fp] * 4 + [i64] * 4 + [ctypes.c_float, ci, vp]
+    lib.attn_jvp_fwd_chunk.argtypes = [vp] * 6 + [fp] * 4 + [i64] * 4 + [ctypes.c_float, ci, i64, i64, vp]
     lib.attn_jvp_merge.argtypes = [vp] * 4 + [i64] + [vp] * 4 + [i64] * 4 + [vp]
     lib.attn_jvp_cast_f32_bf16.argtypes = [vp, vp, i64, vp]
-    lib.attn_jvp_fwd_split_noalloc.argtypes = [vp] * 6 + [fp] * 4 + [i64] * 4 + [ctypes.c_float, i64, vp]
+    lib.attn_jvp_fwd_split_noalloc.argtypes = [vp] * 6 + [fp] * 4 + [i64] * 4 + [ctypes.c_float, ci, i64, vp]
     lib.attn_jvp_fwd_host.argtypes = [vp] * 6 + [fp] * 4 + [i64] * 4 + [ctypes.c_float, i64, i64, vp, i64, vp]
     lib.attn_jvp_fwd_strided.argtypes = [vp] * 6 + [fp] * 4 + [i64] * 5 + [ctypes.POINTER(i64), ctypes.c_float,
-                                                                          i64, i64, vp]
+                                                                          ci, i64, i64, vp]
     lib.attn_jvp_fwd_ex.argtypes = [vp] * 6 + [fp] * 4 + [i64] * 6 + [ctypes.POINTER(i64), ctypes.c_float,
-                                                                    i64, i64, vp]
+                                                                    ci, i64, i64, vp]
     lib.attn_jvp_fwd_host_workspace_bytes.argtypes = [i64] * 6
     lib.attn_jvp_fwd_host_workspace_bytes.restype = i64
     lib.trigflow_coeffs_jvp.argtypes = [ctypes.c_double] * 3 + [ctypes.POINTER(ctypes.c_double)]
@@ -111,21 +117,22 @@ def attn_jvp_cast_f32_bf16(x, out=None, stream=None):
     return out
 
 
-def _bf16_inputs(tensors, stream):
-    """bf16 views of the six inputs; fp32 inputs are rounded by the library's cast kernel."""
-    res = []
-    for n, t in zip(("q", "k", "v", "q_t", "k_t", "v_t"), tensors):
-        if isinstance(t, torch.Tensor) and t.dtype == torch.float32:
-            _req(t, n, torch.float32)
-            t = attn_jvp_cast_f32_bf16(t, stream=stream)
-        res.append(_req(t, n, torch.bfloat16))
+def _inputs(tensors):
+    """The six contiguous [B, H, N, d] inputs and the library's dtype code for them.
+
+    All six must share one dtype, bf16 or fp32; fp32 inputs are rounded to bf16 by
+    the library itself (the ``dtype`` argument of the C entry points)."""
+    dt = tensors[0].dtype if isinstance(tensors[0], torch.Tensor) else None
+    if dt not in _DTYPE_CODES:
+        raise ValueError("q must be torch.bfloat16 or torch.float32 (got %s)" % dt)
+    res = [_req(t, n, dt) for n, t in zip(("q", "k", "v", "q_t", "k_t", "v_t"), tensors)]
     shape = tuple(res[0].shape)
     if len(shape) != 4:
         raise ValueError("q must be [B, H, N, d]")
     for n, t in zip(("k", "v", "q_t", "k_t", "v_t"), res[1:]):
         if tuple(t.shape) != shape:
             raise ValueError("%s must have q's shape %s (got %s)" % (n, shape, tuple(t.shape)))
-    return res
+    return res, _DTYPE_CODES[dt]
 
 
 def _outputs(shape, device, out, out_t, lse, mu, need_rows):
@@ -150,13 +157,13 @@ def _outputs(shape, device, out, out_t, lse, mu, need_rows):
 def attn_jvp_fwd(q, k, v, q_t, k_t, v_t, scale=None, out=None, out_t=None, lse=None, mu=None,
                  want_rows=True, stream=None):
     """(O, Ot, LSE, mu) of softmax attention and its JVP; inputs [B, H, N, d] bf16 (or fp32)."""
-    q, k, v, q_t, k_t, v_t = _bf16_inputs((q, k, v, q_t, k_t, v_t), stream)
+    (q, k, v, q_t, k_t, v_t), code = _inputs((q, k, v, q_t, k_t, v_t))
     B, H, N, d = q.shape
     scale = d ** -0.5 if scale is None else float(scale)
     out, out_t, lse, mu = _outputs(q.shape, q.device, out, out_t, lse, mu, want_rows)
     rc = load().attn_jvp_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(q_t), _ptr(k_t), _ptr(v_t),
                              _ptr(out), _ptr(out_t), _ptr(lse), _ptr(mu), B, H, N, d,
-                             ctypes.c_float(scale), _stream(stream))
+                             ctypes.c_float(scale), code, _stream(stream))
     _check("attn_jvp_fwd", rc)
     return out, out_t, lse, mu
 
@@ -164,13 +171,13 @@ def attn_jvp_fwd(q, k, v, q_t, k_t, v_t, scale=None, out=None, out_t=None, lse=N
 def attn_jvp_fwd_chunk(q, k, v, q_t, k_t, v_t, kv_start, kv_len, scale=None, out=None, out_t=None,
                        lse=None, mu=None, stream=None):
     """Partials (O_c, Ot_c, LSE_c, mu_c) over keys [kv_start, kv_start + kv_len)."""
-    q, k, v, q_t, k_t, v_t = _bf16_inputs((q, k, v, q_t, k_t, v_t), stream)
+    (q, k, v, q_t, k_t, v_t), code = _inputs((q, k, v, q_t, k_t, v_t))
     B, H, N, d = q.shape
     scale = d ** -0.5 if scale is None else float(scale)
     out, out_t, lse, mu = _outputs(q.shape, q.device, out, out_t, lse, mu, True)
     rc = load().attn_jvp_fwd_chunk(_ptr(q), _ptr(k), _ptr(v), _ptr(q_t), _ptr(k_t), _ptr(v_t),
                                    _ptr(out), _ptr(out_t), _ptr(lse), _ptr(mu), B, H, N, d,
-                                   ctypes.c_float(scale), int(kv_start), int(kv_len), _stream(stream))
+                                   ctypes.c_float(scale), code, int(kv_start), int(kv_len), _stream(stream))
     _check("attn_jvp_fwd_chunk", rc)
     return out, out_t, lse, mu
 
@@ -182,12 +189,12 @@ _LAYOUTS = {
 }
 
 
-def _layout_view(t, name, layout):
-    """(B, S, H, D) and element strides (batch, seq, head) of a bf16 CUDA tensor in ``layout``."""
+def _layout_view(t, name, layout, dtype=torch.bfloat16):
+    """(B, S, H, D) and element strides (batch, seq, head) of a CUDA tensor in ``layout``."""
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % name)
-    if t.dtype != torch.bfloat16:
-        raise ValueError("%s must be torch.bfloat16 (got %s)" % (name, t.dtype))
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s (got %s)" % (name, dtype, t.dtype))
     if t.dim() != 4 or t.stride(3) != 1:
         raise ValueError("%s must be 4-D with a unit stride in the head dimension" % name)
     ib, isq, ih, _ = _LAYOUTS[layout]
@@ -206,15 +213,18 @@ def attn_jvp_fwd_strided(q, k, v, q_t, k_t, v_t, layout="bhsd", scale=None, out=
     key range.  Calls attn_jvp_fwd_ex."""
     if layout not in _LAYOUTS:
         raise ValueError("layout must be one of %s" % sorted(_LAYOUTS))
-    (B, Nq, H, d), qs = _layout_view(q, "q", layout)
-    (Bk, Nkv, Hk, dk), ks = _layout_view(k, "k", layout)
+    dt = q.dtype if isinstance(q, torch.Tensor) else None
+    if dt not in _DTYPE_CODES:
+        raise ValueError("q must be torch.bfloat16 or torch.float32 (got %s)" % dt)
+    (B, Nq, H, d), qs = _layout_view(q, "q", layout, dt)
+    (Bk, Nkv, Hk, dk), ks = _layout_view(k, "k", layout, dt)
     if (Bk, Hk, dk) != (B, H, d):
         raise ValueError("k must match q in batch, heads and head dim")
-    (Bv, Nv, Hv, d_v), vs = _layout_view(v, "v", layout)
+    (Bv, Nv, Hv, d_v), vs = _layout_view(v, "v", layout, dt)
     if (Bv, Nv, Hv) != (B, Nkv, H):
         raise ValueError("v must match k in batch, sequence length and heads")
     for n, t, ref in (("q_t", q_t, q), ("k_t", k_t, k), ("v_t", v_t, v)):
-        _layout_view(t, n, layout)
+        _layout_view(t, n, layout, dt)
         if tuple(t.shape) != tuple(ref.shape) or t.stride() != ref.stride():
             raise ValueError("%s must have the shape and strides of %s" % (n, n[0]))
     ib, isq, ih, _ = _LAYOUTS[layout]
@@ -244,7 +254,7 @@ def attn_jvp_fwd_strided(q, k, v, q_t, k_t, v_t, layout="bhsd", scale=None, out=
     strides = (ctypes.c_int64 * 12)(*qs, *ks, *vs, *os_)
     rc = load().attn_jvp_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(q_t), _ptr(k_t), _ptr(v_t),
                                 _ptr(out), _ptr(out_t), _ptr(lse), _ptr(mu), B, H, Nq, Nkv, d, d_v, strides,
-                                ctypes.c_float(scale), int(kv_start), kv_len, _stream(stream))
+                                ctypes.c_float(scale), _DTYPE_CODES[dt], int(kv_start), kv_len, _stream(stream))
     _check("attn_jvp_fwd_ex", rc)
     return out, out_t, lse, mu
 
@@ -275,7 +285,7 @@ def attn_jvp_split(q, k, v, q_t, k_t, v_t, n_chunks, scale=None, workspace=None,
 
     ``workspace``: optional (o_c, ot_c, lse_c, mu_c) partial buffers to reuse.
     """
-    q, k, v, q_t, k_t, v_t = _bf16_inputs((q, k, v, q_t, k_t, v_t), stream)
+    (q, k, v, q_t, k_t, v_t), _ = _inputs((q, k, v, q_t, k_t, v_t))
     B, H, N, d = q.shape
     if workspace is None:
         workspace = split_workspace(q.shape, n_chunks, q.device)
@@ -290,9 +300,9 @@ def attn_jvp_fwd_split_noalloc(q, k, v, q_t, k_t, v_t, n_chunks, out, out_t, lse
                                stream=None):
     """Split-KV path whose chunk partials live in the library's built-in
     scratch array, for callers that cannot allocate device memory.  All
-    outputs are caller-provided; this wrapper allocates nothing either."""
-    for n, t in zip(("q", "k", "v", "q_t", "k_t", "v_t"), (q, k, v, q_t, k_t, v_t)):
-        _req(t, n, torch.bfloat16, q.shape)
+    outputs are caller-provided; this wrapper allocates nothing either.
+    Inputs are bf16 or fp32 (all six alike)."""
+    (q, k, v, q_t, k_t, v_t), code = _inputs((q, k, v, q_t, k_t, v_t))
     B, H, N, d = q.shape
     _req(out, "out", torch.float32, q.shape)
     _req(out_t, "out_t", torch.float32, q.shape)
@@ -303,7 +313,7 @@ def attn_jvp_fwd_split_noalloc(q, k, v, q_t, k_t, v_t, n_chunks, out, out_t, lse
     scale = d ** -0.5 if scale is None else float(scale)
     rc = load().attn_jvp_fwd_split_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(q_t), _ptr(k_t), _ptr(v_t),
                                            _ptr(out), _ptr(out_t), _ptr(lse), _ptr(mu), B, H, N, d,
-                                           ctypes.c_float(scale), int(n_chunks), _stream(stream))
+                                           ctypes.c_float(scale), code, int(n_chunks), _stream(stream))
     _check("attn_jvp_fwd_split_noalloc", rc)
     return out, out_t, lse, mu
 

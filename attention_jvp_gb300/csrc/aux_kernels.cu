@@ -1,6 +1,6 @@
 // Bandwidth-bound kernels around the fused attention JVP:
 //   * exact merge of key-chunk partials (O_c, Ot_c, LSE_c, mu_c),
-//   * fp32 -> bf16 rounding of inputs,
+//   * fp32 -> bf16 rounding of inputs (contiguous, or gathered from strides),
 //   * the TrigFlow tangent dx_t/dt = -sin t x0 + cos t eps.
 // Each thread moves 16-byte vectors; grids are sized in whole waves of the
 // GPU's SMs by the launchers below.
@@ -92,6 +92,33 @@ __global__ void __launch_bounds__(256) cast_f32_bf16_kernel(const float* __restr
 }
 
 // ---------------------------------------------------------------------------
+// Strided fp32 [b, s, h, c] (element strides sb, ss, sh; unit column stride)
+// -> contiguous bf16 [B, H, S, d], round to nearest even.  One thread moves
+// 4 columns (a float4 in, 8 bytes out), in the output's order so the stores
+// coalesce; grid-stride.  d is a multiple of 4 and every stride a multiple of
+// 4 elements, so each float4 load is 16-byte aligned.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) cast_strided_f32_bf16_kernel(const float* __restrict__ in,
+                                                                    __nv_bfloat16* __restrict__ out, int64_t H,
+                                                                    int64_t S, int q4, int64_t sb, int64_t ss,
+                                                                    int64_t sh, int64_t n4) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    const int64_t r = i / q4;  // output row (b, h, s)
+    const int c4 = static_cast<int>(i - r * q4);
+    const int64_t s = r % S, bh = r / S;
+    const int64_t h = bh % H, b = bh / H;
+    const float4 v = *reinterpret_cast<const float4*>(in + b * sb + s * ss + h * sh + 4 * c4);
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(out)[i] = pk;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // TrigFlow tangent: out[b, i] = -sin(t_b) x0[b, i] + cos(t_b) eps[b, i].
 // Block row y = sample b; sin/cos are taken in FP64 once per block, the
 // element-wise combination in fp32 (the output precision).
@@ -176,6 +203,18 @@ cudaError_t launch_cast_f32_bf16(const float* in, void* out, int64_t n, cudaStre
   const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
   const int64_t blocks = want < 1 ? 1 : (want < cap ? want : cap);
   cast_f32_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(in, static_cast<__nv_bfloat16*>(out), n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cast_strided_f32_bf16(const float* in, void* out, int64_t B, int64_t H, int64_t S, int64_t d,
+                                         const int64_t stride[3], cudaStream_t stream) {
+  const int64_t n4 = B * H * S * (d / 4);
+  if (n4 == 0) return cudaSuccess;
+  const int64_t want = (n4 + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+  const int64_t blocks = want < cap ? want : cap;
+  cast_strided_f32_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      in, static_cast<__nv_bfloat16*>(out), H, S, static_cast<int>(d / 4), stride[0], stride[1], stride[2], n4);
   return cudaGetLastError();
 }
 

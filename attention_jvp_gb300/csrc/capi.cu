@@ -80,21 +80,29 @@ int check_head_dim(int64_t d, bool forward) {
               (long long)d);
 }
 
+}  // namespace
+
 int check_attn_args(const void* q, const void* k, const void* v, const void* q_t, const void* k_t, const void* v_t,
                     const float* out, const float* out_t, const float* lse, const float* mu, int64_t B, int64_t H,
-                    int64_t N, int64_t d, float scale) {
+                    int64_t N, int64_t d, float scale, int dtype) {
+  if (dtype != ATTNJVP_BF16 && dtype != ATTNJVP_FP32)
+    return fail(ATTNJVP_EINVAL, "dtype code %d is neither ATTNJVP_BF16 (%d) nor ATTNJVP_FP32 (%d)", dtype,
+                ATTNJVP_BF16, ATTNJVP_FP32);
   const void* in[6] = {q, k, v, q_t, k_t, v_t};
   const char* names[6] = {"q", "k", "v", "q_t", "k_t", "v_t"};
   for (int i = 0; i < 6; ++i) {
     if (!in[i]) return fail(ATTNJVP_EINVAL, "%s is NULL", names[i]);
-    if (!aligned(in[i], 16)) return fail(ATTNJVP_EINVAL, "%s is not 16-byte aligned (TMA base address)", names[i]);
+    if (!aligned(in[i], 16))
+      return fail(ATTNJVP_EINVAL, "%s is not 16-byte aligned (%s)", names[i],
+                  dtype == ATTNJVP_BF16 ? "TMA base address" : "16-byte loads of the fp32 cast");
   }
   if (!out || !out_t) return fail(ATTNJVP_EINVAL, "out/out_t is NULL");
   if (!aligned(out, 16) || !aligned(out_t, 16)) return fail(ATTNJVP_EINVAL, "out/out_t is not 16-byte aligned");
   if ((lse && !aligned(lse, 4)) || (mu && !aligned(mu, 4))) return fail(ATTNJVP_EINVAL, "lse/mu misaligned");
   if (B < 1 || H < 1 || N < 1) return fail(ATTNJVP_EINVAL, "B, H, N must be >= 1 (got %lld, %lld, %lld)",
                                            (long long)B, (long long)H, (long long)N);
-  if (B * H >= (int64_t(1) << 31) || N >= (int64_t(1) << 31))
+  if (B >= (int64_t(1) << 31) || H >= (int64_t(1) << 31) || B * H >= (int64_t(1) << 31) ||
+      N >= (int64_t(1) << 31))
     return fail(ATTNJVP_EINVAL, "B*H and N must be < 2^31");
   if (!std::isfinite(scale) || !(scale > 0.f)) return fail(ATTNJVP_EINVAL, "scale must be finite and > 0");
   int rc = check_head_dim(d, true);
@@ -105,6 +113,8 @@ int check_attn_args(const void* q, const void* k, const void* v, const void* q_t
   return ATTNJVP_OK;
 }
 
+namespace {
+
 // Element strides (batch, sequence, head) of a contiguous [B, H, N, d] tensor.
 void contiguous_strides(int64_t H, int64_t N, int64_t d, int64_t st[3]) {
   st[0] = H * N * d;
@@ -112,15 +122,12 @@ void contiguous_strides(int64_t H, int64_t N, int64_t d, int64_t st[3]) {
   st[2] = N * d;
 }
 
-// ``strides``: 12 element strides (batch, seq, head) of Q, K, V and O, or NULL
-// for contiguous [B, H, N, d] tensors.
-int run_fwd(const void* q, const void* k, const void* v, const void* q_t, const void* k_t, const void* v_t,
-            float* out, float* out_t, float* lse, float* mu, int64_t B, int64_t H, int64_t Nq, int64_t Nkv,
-            int64_t d, int64_t d_v, const int64_t* strides, float scale, int64_t kv_start, int64_t kv_len,
-            void* stream) {
-  const char* why = "";
-  int* st = status_word(&why);
-  if (!st) return fail(ATTNJVP_ECUDA, "no CUDA device / status word: %s", why);
+// Launches the fused kernel on bf16 inputs.  ``st``: 12 element strides (batch,
+// seq, head) of Q, K, V and O.
+int launch_fwd(const void* q, const void* k, const void* v, const void* q_t, const void* k_t, const void* v_t,
+               float* out, float* out_t, float* lse, float* mu, int64_t B, int64_t H, int64_t Nq, int64_t Nkv,
+               int64_t d, int64_t d_v, const int64_t st[12], float scale, int64_t kv_start, int64_t kv_len,
+               int* status, cudaStream_t stream) {
   FwdArgs a;
   a.q = q;
   a.k = k;
@@ -138,28 +145,84 @@ int run_fwd(const void* q, const void* k, const void* v, const void* q_t, const 
   a.Nkv = Nkv;
   a.d = d;
   a.d_v = d_v;
-  if (strides) {
-    for (int i = 0; i < 3; ++i) {
-      a.q_stride[i] = strides[i];
-      a.k_stride[i] = strides[3 + i];
-      a.v_stride[i] = strides[6 + i];
-      a.o_stride[i] = strides[9 + i];
-    }
-  } else {
-    contiguous_strides(H, Nq, d, a.q_stride);
-    contiguous_strides(H, Nkv, d, a.k_stride);
-    contiguous_strides(H, Nkv, d_v, a.v_stride);
-    contiguous_strides(H, Nq, d_v, a.o_stride);
+  for (int i = 0; i < 3; ++i) {
+    a.q_stride[i] = st[i];
+    a.k_stride[i] = st[3 + i];
+    a.v_stride[i] = st[6 + i];
+    a.o_stride[i] = st[9 + i];
   }
   a.scale = scale;
   a.kv_start = kv_start;
   a.kv_len = kv_len;
-  a.status = st;
-  a.stream = static_cast<cudaStream_t>(stream);
+  a.status = status;
+  a.stream = stream;
   const char* msg = "";
   cudaError_t e = launch_attn_jvp_fwd(a, &msg);
   if (e != cudaSuccess) return fail(ATTNJVP_ECUDA, "%s: %s", msg, cudaGetErrorString(e));
   return ok();
+}
+
+size_t round256(size_t n) { return (n + 255) / 256 * 256; }
+
+// ``strides``: 12 element strides (batch, seq, head) of Q, K, V and O, or NULL
+// for contiguous [B, H, N, d] tensors.  fp32 inputs (``dtype`` ATTNJVP_FP32) are
+// first rounded to bf16 into contiguous [B, H, S, d] copies in stream-ordered
+// device memory (cudaMallocAsync on ``stream``), which is released on the same
+// stream once the kernel has been enqueued after the copies.
+int run_fwd(const void* q, const void* k, const void* v, const void* q_t, const void* k_t, const void* v_t,
+            float* out, float* out_t, float* lse, float* mu, int64_t B, int64_t H, int64_t Nq, int64_t Nkv,
+            int64_t d, int64_t d_v, const int64_t* strides, float scale, int dtype, int64_t kv_start,
+            int64_t kv_len, void* stream) {
+  const char* why = "";
+  int* status = status_word(&why);
+  if (!status) return fail(ATTNJVP_ECUDA, "no CUDA device / status word: %s", why);
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  int64_t st[12];
+  if (strides) {
+    for (int i = 0; i < 12; ++i) st[i] = strides[i];
+  } else {
+    contiguous_strides(H, Nq, d, st);
+    contiguous_strides(H, Nkv, d, st + 3);
+    contiguous_strides(H, Nkv, d_v, st + 6);
+    contiguous_strides(H, Nq, d_v, st + 9);
+  }
+  if (dtype == ATTNJVP_BF16)
+    return launch_fwd(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, Nq, Nkv, d, d_v, st, scale, kv_start,
+                      kv_len, status, cs);
+  // fp32: six bf16 copies, Q and Qt [B, H, Nq, d], K and Kt [B, H, Nkv, d], V and Vt [B, H, Nkv, d_v].
+  const size_t bytes[3] = {round256(size_t(B * H * Nq * d) * 2), round256(size_t(B * H * Nkv * d) * 2),
+                           round256(size_t(B * H * Nkv * d_v) * 2)};
+  void* buf = nullptr;
+  cudaError_t e = cudaMallocAsync(&buf, 2 * (bytes[0] + bytes[1] + bytes[2]), cs);
+  if (e != cudaSuccess)
+    return fail(ATTNJVP_ECUDA, "stream-ordered allocation of the bf16 copies failed: %s", cudaGetErrorString(e));
+  const void* src[6] = {q, q_t, k, k_t, v, v_t};
+  void* dst[6];
+  unsigned char* p = static_cast<unsigned char*>(buf);
+  for (int i = 0; i < 6; ++i) {
+    dst[i] = p;
+    p += bytes[i / 2];
+  }
+  const int64_t rows[3] = {Nq, Nkv, Nkv}, cols[3] = {d, d, d_v};
+  for (int i = 0; i < 6 && e == cudaSuccess; ++i)
+    e = launch_cast_strided_f32_bf16(static_cast<const float*>(src[i]), dst[i], B, H, rows[i / 2], cols[i / 2],
+                                     st + 3 * (i / 2), cs);
+  int rc;
+  if (e != cudaSuccess) {
+    rc = fail(ATTNJVP_ECUDA, "fp32 -> bf16 cast launch failed: %s", cudaGetErrorString(e));
+  } else {
+    int64_t bst[12];
+    contiguous_strides(H, Nq, d, bst);
+    contiguous_strides(H, Nkv, d, bst + 3);
+    contiguous_strides(H, Nkv, d_v, bst + 6);
+    for (int i = 9; i < 12; ++i) bst[i] = st[i];
+    rc = launch_fwd(dst[0], dst[2], dst[4], dst[1], dst[3], dst[5], out, out_t, lse, mu, B, H, Nq, Nkv, d, d_v, bst,
+                    scale, kv_start, kv_len, status, cs);
+  }
+  e = cudaFreeAsync(buf, cs);
+  if (rc == ATTNJVP_OK && e != cudaSuccess)
+    rc = fail(ATTNJVP_ECUDA, "stream-ordered release of the bf16 copies failed: %s", cudaGetErrorString(e));
+  return rc;
 }
 
 }  // namespace
@@ -188,30 +251,31 @@ extern "C" {
 
 int attn_jvp_fwd(const void* q, const void* k, const void* v, const void* q_t, const void* k_t, const void* v_t,
                  float* out, float* out_t, float* lse, float* mu, int64_t B, int64_t H, int64_t N, int64_t d,
-                 float scale, void* stream) {
-  int rc = check_attn_args(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, d, scale);
+                 float scale, int dtype, void* stream) {
+  int rc = check_attn_args(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, d, scale, dtype);
   if (rc != ATTNJVP_OK) return rc;
-  return run_fwd(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, N, d, d, nullptr, scale, 0, N, stream);
+  return run_fwd(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, N, d, d, nullptr, scale, dtype, 0, N,
+                 stream);
 }
 
 int attn_jvp_fwd_chunk(const void* q, const void* k, const void* v, const void* q_t, const void* k_t,
                        const void* v_t, float* out, float* out_t, float* lse, float* mu, int64_t B, int64_t H,
-                       int64_t N, int64_t d, float scale, int64_t kv_start, int64_t kv_len, void* stream) {
-  int rc = check_attn_args(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, d, scale);
+                       int64_t N, int64_t d, float scale, int dtype, int64_t kv_start, int64_t kv_len, void* stream) {
+  int rc = check_attn_args(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, d, scale, dtype);
   if (rc != ATTNJVP_OK) return rc;
   if (!lse || !mu) return fail(ATTNJVP_EINVAL, "chunk mode needs lse and mu (the merge consumes them)");
   if (kv_start < 0 || kv_len < 1 || kv_start + kv_len > N)
     return fail(ATTNJVP_EINVAL, "key range [%lld, %lld) outside [0, %lld) or empty", (long long)kv_start,
                 (long long)(kv_start + kv_len), (long long)N);
-  return run_fwd(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, N, d, d, nullptr, scale, kv_start, kv_len,
-                 stream);
+  return run_fwd(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, N, d, d, nullptr, scale, dtype, kv_start,
+                 kv_len, stream);
 }
 
 int attn_jvp_fwd_ex(const void* q, const void* k, const void* v, const void* q_t, const void* k_t, const void* v_t,
                     float* out, float* out_t, float* lse, float* mu, int64_t B, int64_t H, int64_t Nq, int64_t Nkv,
-                    int64_t d, int64_t d_v, const int64_t* strides, float scale, int64_t kv_start, int64_t kv_len,
-                    void* stream) {
-  int rc = check_attn_args(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, Nq, d, scale);
+                    int64_t d, int64_t d_v, const int64_t* strides, float scale, int dtype, int64_t kv_start,
+                    int64_t kv_len, void* stream) {
+  int rc = check_attn_args(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, Nq, d, scale, dtype);
   if (rc != ATTNJVP_OK) return rc;
   rc = check_head_dim(d_v, true);
   if (rc != ATTNJVP_OK) return rc;
@@ -222,8 +286,9 @@ int attn_jvp_fwd_ex(const void* q, const void* k, const void* v, const void* q_t
   if (strides) {
     const char* what[4] = {"q", "k", "v", "out"};
     for (int g = 0; g < 4; ++g) {
-      // bf16 inputs: TMA strides are multiples of 16 bytes; fp32 outputs: float4 stores.
-      const int64_t unit = g < 3 ? 8 : 4;
+      // bf16 inputs: TMA strides are multiples of 16 bytes; fp32 inputs: 16-byte loads of
+      // the cast; fp32 outputs: float4 stores.
+      const int64_t unit = (g < 3 && dtype == ATTNJVP_BF16) ? 8 : 4;
       for (int i = 0; i < 3; ++i) {
         const int64_t x = strides[3 * g + i];
         if (x < 0 || x % unit != 0 || x >= (int64_t(1) << 38))
@@ -232,14 +297,14 @@ int attn_jvp_fwd_ex(const void* q, const void* k, const void* v, const void* q_t
       }
     }
   }
-  return run_fwd(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, Nq, Nkv, d, d_v, strides, scale, kv_start,
-                 kv_len, stream);
+  return run_fwd(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, Nq, Nkv, d, d_v, strides, scale, dtype,
+                 kv_start, kv_len, stream);
 }
 
 int attn_jvp_fwd_strided(const void* q, const void* k, const void* v, const void* q_t, const void* k_t,
                          const void* v_t, float* out, float* out_t, float* lse, float* mu, int64_t B, int64_t H,
-                         int64_t Nq, int64_t Nkv, int64_t d, const int64_t* strides, float scale, int64_t kv_start,
-                         int64_t kv_len, void* stream) {
+                         int64_t Nq, int64_t Nkv, int64_t d, const int64_t* strides, float scale, int dtype,
+                         int64_t kv_start, int64_t kv_len, void* stream) {
   // K and V share one stride set here (equal head dims)
   int64_t st[12];
   if (strides) {
@@ -251,7 +316,7 @@ int attn_jvp_fwd_strided(const void* q, const void* k, const void* v, const void
     }
   }
   return attn_jvp_fwd_ex(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, Nq, Nkv, d, d, strides ? st : nullptr,
-                         scale, kv_start, kv_len, stream);
+                         scale, dtype, kv_start, kv_len, stream);
 }
 
 int attn_jvp_merge(const float* o_c, const float* ot_c, const float* lse_c, const float* mu_c, int64_t n_chunks,

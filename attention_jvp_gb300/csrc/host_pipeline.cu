@@ -272,7 +272,8 @@ extern "C" int attn_jvp_fwd_host(const void* q, const void* k, const void* v, co
       float* dlse = reinterpret_cast<float*>(base + lay.lse);
       float* dmu = reinterpret_cast<float*>(base + lay.mu);
       if (n_chunks == 1) {
-        rc = attn_jvp_fwd(dq, dk, dv, dqt, dkt, dvt, dout, dout_t, dlse, dmu, 1, gh, N, d, scale, cs_arg);
+        rc = attn_jvp_fwd(dq, dk, dv, dqt, dkt, dvt, dout, dout_t, dlse, dmu, 1, gh, N, d, scale, ATTNJVP_BF16,
+                          cs_arg);
         if (rc != ATTNJVP_OK) return rc;
       } else {
         float* o_c = reinterpret_cast<float*>(base + lay.o_c);
@@ -283,7 +284,8 @@ extern "C" int attn_jvp_fwd_host(const void* q, const void* k, const void* v, co
         for (int64_t c = 0; c < n_chunks; ++c) {
           const int64_t a = (N * c) / n_chunks, z = (N * (c + 1)) / n_chunks;
           rc = attn_jvp_fwd_chunk(dq, dk, dv, dqt, dkt, dvt, o_c + c * rows * d, ot_c + c * rows * d,
-                                  lse_c + c * rows, mu_c + c * rows, 1, gh, N, d, scale, a, z - a, cs_arg);
+                                  lse_c + c * rows, mu_c + c * rows, 1, gh, N, d, scale, ATTNJVP_BF16, a, z - a,
+                                  cs_arg);
           if (rc != ATTNJVP_OK) return rc;
         }
         rc = attn_jvp_merge(o_c, ot_c, lse_c, mu_c, n_chunks, dout, dout_t, dlse, dmu, 1, gh, N, d, cs_arg);

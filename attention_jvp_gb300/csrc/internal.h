@@ -33,6 +33,11 @@ cudaError_t launch_merge(const float* o_c, const float* ot_c, const float* lse_c
 
 cudaError_t launch_cast_f32_bf16(const float* in, void* out, int64_t n, cudaStream_t stream);
 
+// fp32 element (b, s, h, c) at b*stride[0] + s*stride[1] + h*stride[2] + c -> contiguous
+// bf16 [B, H, S, d]; d and the strides are multiples of 4, ``in`` 16-byte aligned.
+cudaError_t launch_cast_strided_f32_bf16(const float* in, void* out, int64_t B, int64_t H, int64_t S, int64_t d,
+                                         const int64_t stride[3], cudaStream_t stream);
+
 cudaError_t launch_trigflow_tangent(const float* x0, const float* eps, const double* t, float* out, int64_t B,
                                     int64_t per_sample, cudaStream_t stream);
 
@@ -62,6 +67,13 @@ cudaError_t launch_scm_tangent_loss(const float* F_theta, const float* F_sg, con
                                     const float* tF, const double* t, double r, float* g_n, float* dfdt,
                                     double* loss, int* nan_g, int* nan_F, int64_t B, int64_t C, int64_t T, int64_t HW,
                                     double* ws, int* status, cudaStream_t stream);
+
+// Argument checks shared by the forward entry points (capi.cu): pointers, alignment,
+// sizes, scale, head dim and the dtype code.  Returns 0 or an ATTNJVP_E* code with
+// attn_jvp_last_error() set; needs no GPU.
+int check_attn_args(const void* q, const void* k, const void* v, const void* q_t, const void* k_t, const void* v_t,
+                    const float* out, const float* out_t, const float* lse, const float* mu, int64_t B, int64_t H,
+                    int64_t N, int64_t d, float scale, int dtype);
 
 // Sets the calling thread's message returned by attn_jvp_last_error().
 void set_last_error(const char* msg);

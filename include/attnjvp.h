@@ -29,6 +29,10 @@
  *     wait).  A wait that runs out records ATTNJVP_ETIMEOUT in a per-device
  *     status word, the kernel releases what it holds and returns early; read
  *     the word with attn_jvp_status() after synchronising the stream.
+ *   - The library looks up the device addresses of its own device arrays (the
+ *     status word, the no-alloc scratch) once per device and keeps them, so it
+ *     does not survive cudaDeviceReset, or any other teardown of a device's
+ *     primary context, while it is loaded.
  */
 #ifndef ATTNJVP_H
 #define ATTNJVP_H
@@ -45,11 +49,17 @@ extern "C" {
 #define ATTNJVP_ECUDA (-3)        /* a CUDA runtime or driver call failed */
 #define ATTNJVP_ETIMEOUT (-4)     /* a kernel's bounded wait ran out (see attn_jvp_status) */
 
+/* Input dtype codes of the forward entry points (the ``dtype`` argument). */
+#define ATTNJVP_BF16 0 /* bfloat16: read in place by the kernels (the timed path) */
+#define ATTNJVP_FP32 1 /* float32: rounded to bf16 (nearest even) on the device first */
+
 /*
  * Fused attention forward + JVP (the operation above) over all N keys.
- *   q, k, v, q_t, k_t, v_t : bf16 [B, H, N, d]; each base 16-byte aligned.
- *                            Tangents have exactly the primals' shape and layout
- *                            (the page's host wrapper asserts equal shape and stride).
+ *   q, k, v, q_t, k_t, v_t : [B, H, N, d] of the type ``dtype`` names; each base
+ *                            16-byte aligned.  Tangents have exactly the primals'
+ *                            shape, layout and type (the page's host wrapper asserts
+ *                            equal shape and stride, and its forward takes q in its
+ *                            own dtype).
  *   out, out_t             : fp32 [B, H, N, d] — O and Ot; 16-byte aligned.
  *   lse, mu                : fp32 [B, H, N] — natural-log LSE and mu; either may be
  *                            NULL when not wanted.
@@ -59,12 +69,22 @@ extern "C" {
  *                            128-row query tile, each accumulating half of the value
  *                            columns, so the scores are computed twice.
  *   scale                  : softmax scale s, finite and > 0 (the page's default is d^-1/2).
+ *   dtype                  : ATTNJVP_BF16 or ATTNJVP_FP32 (any other code:
+ *                            ATTNJVP_EINVAL).  The tensor cores take bf16 operands,
+ *                            so fp32 inputs are rounded to bf16 (nearest even) on
+ *                            the device before the same kernel runs.  The six bf16
+ *                            copies (6 * B * H * N * d * 2 bytes) live in memory
+ *                            the library takes with cudaMallocAsync on ``stream``
+ *                            and gives back with cudaFreeAsync on ``stream`` after
+ *                            the kernel (stream-ordered; no device synchronisation);
+ *                            ATTNJVP_ECUDA if that allocation fails.  The outputs
+ *                            are fp32 either way.
  */
 int attn_jvp_fwd(const void* q, const void* k, const void* v,
                  const void* q_t, const void* k_t, const void* v_t,
                  float* out, float* out_t, float* lse, float* mu,
                  int64_t B, int64_t H, int64_t N, int64_t d,
-                 float scale, void* stream);
+                 float scale, int dtype, void* stream);
 
 /*
  * Same operation restricted to the key range [kv_start, kv_start + kv_len):
@@ -79,7 +99,7 @@ int attn_jvp_fwd_chunk(const void* q, const void* k, const void* v,
                        const void* q_t, const void* k_t, const void* v_t,
                        float* out, float* out_t, float* lse, float* mu,
                        int64_t B, int64_t H, int64_t N, int64_t d,
-                       float scale, int64_t kv_start, int64_t kv_len, void* stream);
+                       float scale, int dtype, int64_t kv_start, int64_t kv_len, void* stream);
 
 /*
  * General form: strided layouts, as many or as few keys as queries, and an
@@ -88,9 +108,11 @@ int attn_jvp_fwd_chunk(const void* q, const void* k, const void* v,
  * elements from its base (the head-dimension stride is 1), so [B, H, S, d],
  * the page's [B, S, H, d], and views such as q/k/v slices of a packed
  * [B, S, 3, H, d] tensor are all accepted without copies.
- *   q, q_t              : bf16, N_q query rows; share the query strides.
- *   k, k_t, v, v_t      : bf16, N_kv key rows; share the key strides (the page's
+ *   q, q_t              : N_q query rows; share the query strides.
+ *   k, k_t, v, v_t      : N_kv key rows; share the key strides (the page's
  *                         wrapper requires tangents to have the primals' strides).
+ *                         All six of the type ``dtype`` names (as attn_jvp_fwd;
+ *                         fp32 inputs are gathered into contiguous bf16 copies).
  *   out, out_t          : fp32 O and Ot at the output strides; 16-byte aligned.
  *   lse, mu             : fp32 [B, H, N_q] contiguous, or NULL.
  *   B, H, N_q, N_kv     : >= 1 each (cross-attention when N_q != N_kv).
@@ -99,8 +121,9 @@ int attn_jvp_fwd_chunk(const void* q, const void* k, const void* v,
  *                         head), key (batch, seq, head), output (batch, seq,
  *                         head) — or NULL for contiguous [B, H, N, d] everywhere.
  *                         Input strides must be non-negative multiples of 8
- *                         elements (16 bytes, a TMA rule), output strides
- *                         multiples of 4; a stride is ignored when its extent is 1.
+ *                         elements for bf16 (16 bytes, a TMA rule) and of 4 for
+ *                         fp32 (16-byte loads), output strides multiples of 4; a
+ *                         stride is ignored when its extent is 1.
  *                         Layouts in which output elements overlap give
  *                         unspecified results.
  *   kv_start, kv_len    : key range [kv_start, kv_start + kv_len) within [0, N_kv);
@@ -114,7 +137,7 @@ int attn_jvp_fwd_strided(const void* q, const void* k, const void* v,
                          const void* q_t, const void* k_t, const void* v_t,
                          float* out, float* out_t, float* lse, float* mu,
                          int64_t B, int64_t H, int64_t N_q, int64_t N_kv, int64_t d,
-                         const int64_t* strides, float scale,
+                         const int64_t* strides, float scale, int dtype,
                          int64_t kv_start, int64_t kv_len, void* stream);
 
 /*
@@ -135,8 +158,8 @@ int attn_jvp_fwd_ex(const void* q, const void* k, const void* v,
                     const void* q_t, const void* k_t, const void* v_t,
                     float* out, float* out_t, float* lse, float* mu,
                     int64_t B, int64_t H, int64_t N_q, int64_t N_kv, int64_t d, int64_t d_v,
-                    const int64_t* strides, float scale, int64_t kv_start, int64_t kv_len,
-                    void* stream);
+                    const int64_t* strides, float scale, int dtype,
+                    int64_t kv_start, int64_t kv_len, void* stream);
 
 /*
  * Exact merge of C key-chunk partials into the full-row result:
@@ -160,23 +183,26 @@ int attn_jvp_merge(const float* o_c, const float* ot_c, const float* lse_c, cons
  * tensors, or a loop where the implicit device synchronisation of
  * cudaMalloc/cudaFree is not allowed.  The pages have no counterpart; this is
  * an interface convenience around the split path above.
- *   Arguments as attn_jvp_fwd, plus n_chunks in [1, N]; lse and mu may be NULL.
+ *   Arguments as attn_jvp_fwd (dtype included), plus n_chunks in [1, N]; lse
+ *   and mu may be NULL.  Every argument is checked before anything is launched.
  *   The chunk partials live in a 16 MiB array built into the library (one per
  *   device that loads it, held until the process exits), so
- *   n_chunks * B * H * N * (2d + 2) * 4 bytes must not exceed 16 MiB;
- *   larger requests return ATTNJVP_EINVAL with the sizes in the message.
- *   No allocator is called.  The first call on a device looks up the array's
- *   device address (cudaGetSymbolAddress); make that first call before any
- *   stream capture.  Every call on a device uses the same array: calls that
- *   can overlap on the GPU (unordered streams, concurrent host threads) race
- *   and must be serialised by the caller.  Each call writes every partial
- *   before reading it, so nothing from an earlier call leaks into a result.
+ *   n_chunks * B * H * N * (2d + 2) * 4 bytes must not exceed 16 MiB; for fp32
+ *   inputs their bf16 copies, 6 * B * H * N * d * 2 bytes, go there too and
+ *   count against the same limit.  Larger requests return ATTNJVP_EINVAL with
+ *   the sizes in the message.  No allocator is called.  The first call on a
+ *   device looks up the array's device address (cudaGetSymbolAddress); make that
+ *   first call before any stream capture.  Every call on a device uses the same
+ *   array: calls that can overlap on the GPU (unordered streams, concurrent host
+ *   threads) race and must be serialised by the caller.  Each call writes every
+ *   partial before reading it, so nothing from an earlier call leaks into a
+ *   result.
  */
 int attn_jvp_fwd_split_noalloc(const void* q, const void* k, const void* v,
                                const void* q_t, const void* k_t, const void* v_t,
                                float* out, float* out_t, float* lse, float* mu,
                                int64_t B, int64_t H, int64_t N, int64_t d,
-                               float scale, int64_t n_chunks, void* stream);
+                               float scale, int dtype, int64_t n_chunks, void* stream);
 
 /*
  * Round fp32 to bf16 (nearest-even) element-wise on the device, so fp32 inputs

@@ -55,11 +55,11 @@ def test_library_targets_sm103a_only():
     assert arches == {"sm_103a"}, arches
 
 
-def _fwd(lib, ptrs=None, B=1, H=1, N=128, d=128, scale=0.1, chunk=None):
+def _fwd(lib, ptrs=None, B=1, H=1, N=128, d=128, scale=0.1, chunk=None, dtype=binding.ATTNJVP_BF16):
     p = [ctypes.c_void_p(256)] * 10 if ptrs is None else ptrs
     if chunk is None:
-        return lib.attn_jvp_fwd(*p, B, H, N, d, ctypes.c_float(scale), None)
-    return lib.attn_jvp_fwd_chunk(*p, B, H, N, d, ctypes.c_float(scale), chunk[0], chunk[1], None)
+        return lib.attn_jvp_fwd(*p, B, H, N, d, ctypes.c_float(scale), dtype, None)
+    return lib.attn_jvp_fwd_chunk(*p, B, H, N, d, ctypes.c_float(scale), dtype, chunk[0], chunk[1], None)
 
 
 def test_argument_validation_needs_no_gpu(lib):
@@ -91,8 +91,8 @@ def test_argument_validation_needs_no_gpu(lib):
     assert lib.trigflow_tangent(vp, vp, vp, vp, 0, 10, None) == E.ATTNJVP_EINVAL
     assert lib.attn_jvp_selftest_wait(10, None) == E.ATTNJVP_EINVAL
     assert lib.attn_jvp_selftest_wait(5_000_000_000, None) == E.ATTNJVP_EINVAL
-    assert lib.attn_jvp_fwd_split_noalloc(*[ctypes.c_void_p(256)] * 10, 1, 1, 64, 128, ctypes.c_float(0.1), 0,
-                                          None) == E.ATTNJVP_EINVAL
+    assert lib.attn_jvp_fwd_split_noalloc(*[ctypes.c_void_p(256)] * 10, 1, 1, 64, 128, ctypes.c_float(0.1),
+                                          E.ATTNJVP_BF16, 0, None) == E.ATTNJVP_EINVAL
     assert lib.trigflow_tangent(vp, vp, vp, vp, 2, 0, None) == E.ATTNJVP_EINVAL
 
 
@@ -173,11 +173,11 @@ def test_trigflow_coeffs_domain(lib):
         binding.trigflow_coeffs(float("nan"))
 
 
-def _strided(lib, strides=None, d=64, nq=100, nkv=300, kv=(0, 300), scale=0.1):
+def _strided(lib, strides=None, d=64, nq=100, nkv=300, kv=(0, 300), scale=0.1, dtype=binding.ATTNJVP_BF16):
     vp = ctypes.c_void_p
     st = None if strides is None else (ctypes.c_int64 * 9)(*strides)
     return lib.attn_jvp_fwd_strided(*[vp(256)] * 6, vp(256), vp(256), None, None, 2, 3, nq, nkv, d, st,
-                                    ctypes.c_float(scale), kv[0], kv[1], None)
+                                    ctypes.c_float(scale), dtype, kv[0], kv[1], None)
 
 
 def test_strided_entry_validation_needs_no_gpu(lib):
@@ -203,11 +203,11 @@ def test_strided_entry_validation_needs_no_gpu(lib):
     assert _strided(lib, scale=0.0) == E.ATTNJVP_EINVAL
 
 
-def _ex(lib, strides=None, d=64, d_v=128, nq=100, nkv=300, scale=0.1):
+def _ex(lib, strides=None, d=64, d_v=128, nq=100, nkv=300, scale=0.1, dtype=binding.ATTNJVP_BF16):
     vp = ctypes.c_void_p
     st = None if strides is None else (ctypes.c_int64 * 12)(*strides)
     return lib.attn_jvp_fwd_ex(*[vp(256)] * 6, vp(256), vp(256), None, None, 2, 3, nq, nkv, d, d_v, st,
-                               ctypes.c_float(scale), 0, nkv, None)
+                               ctypes.c_float(scale), dtype, 0, nkv, None)
 
 
 def test_value_head_dim_entry_validation_needs_no_gpu(lib):
@@ -279,3 +279,52 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(binding, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         binding.load(str(tmp_path / "libattnjvp.so"))
+
+
+def test_dtype_code_is_checked_before_any_cuda_call(lib):
+    """The forward entry points take the inputs' type as a code; anything but
+    ATTNJVP_BF16 or ATTNJVP_FP32 is EINVAL, reported the same with or without a GPU."""
+    E = binding
+    assert (E.ATTNJVP_BF16, E.ATTNJVP_FP32) == (0, 1)
+    for bad in (-1, 2, 7):
+        assert _fwd(lib, dtype=bad) == E.ATTNJVP_EINVAL
+        assert b"dtype code" in lib.attn_jvp_last_error()
+        assert _fwd(lib, chunk=(0, 64), dtype=bad) == E.ATTNJVP_EINVAL
+        assert _strided(lib, dtype=bad) == E.ATTNJVP_EINVAL
+        assert _ex(lib, dtype=bad) == E.ATTNJVP_EINVAL
+        assert lib.attn_jvp_fwd_split_noalloc(*[ctypes.c_void_p(256)] * 10, 1, 1, 64, 128, ctypes.c_float(0.1),
+                                              bad, 2, None) == E.ATTNJVP_EINVAL
+    # fp32 inputs are gathered with 16-byte loads: strides need only be multiples of 4
+    # elements, where bf16 inputs (read by TMA) need multiples of 8.
+    st = [100 * 3 * 64, 3 * 64 + 4, 64, 300 * 3 * 64, 3 * 64, 64, 100 * 3 * 64, 3 * 64, 64]
+    assert _strided(lib, st) == E.ATTNJVP_EINVAL
+    if not torch.cuda.is_available():  # the pointers here are placeholders: never launch with them
+        rc = _strided(lib, st, dtype=E.ATTNJVP_FP32)
+        assert rc == E.ATTNJVP_ECUDA, lib.attn_jvp_last_error()
+    st[1] = 3 * 64 + 2
+    assert _strided(lib, st, dtype=E.ATTNJVP_FP32) == E.ATTNJVP_EINVAL
+
+
+def test_noalloc_checks_every_argument_before_launching(lib):
+    """Sizes that would overflow, and NULL or misaligned outputs, are refused by the
+    no-alloc entry before it computes its scratch layout or launches anything."""
+    E = binding
+    vp = ctypes.c_void_p
+    call = lambda ptrs, B=1, H=1, N=64, d=128, n=2, dtype=E.ATTNJVP_BF16: lib.attn_jvp_fwd_split_noalloc(
+        *ptrs, B, H, N, d, ctypes.c_float(0.1), dtype, n, None)
+    good = [vp(256)] * 8 + [None, None]
+    assert call(good[:6] + [None] + good[7:]) == E.ATTNJVP_EINVAL
+    assert b"out" in lib.attn_jvp_last_error()
+    assert call(good[:7] + [vp(264)] + good[8:]) == E.ATTNJVP_EINVAL
+    assert b"16-byte" in lib.attn_jvp_last_error()
+    assert call(good, B=1 << 40, H=1 << 40) == E.ATTNJVP_EINVAL
+    assert b"2^31" in lib.attn_jvp_last_error()
+    assert call(good, N=1 << 33) == E.ATTNJVP_EINVAL
+    assert call(good, n=65) == E.ATTNJVP_EINVAL
+    # 16 MiB of scratch: 1 x 64 x 128 rows of partials fit at 4 chunks; 64 x 1024 rows do not
+    assert call(good, H=64, N=1024, n=4) == E.ATTNJVP_EINVAL
+    assert b"scratch" in lib.attn_jvp_last_error()
+    # fp32 inputs add their bf16 copies to the same limit
+    msg_bf16 = lib.attn_jvp_last_error()
+    assert call(good, H=64, N=1024, n=4, dtype=E.ATTNJVP_FP32) == E.ATTNJVP_EINVAL
+    assert b"bf16 input copies" in lib.attn_jvp_last_error() and msg_bf16 != lib.attn_jvp_last_error()

@@ -58,6 +58,38 @@ def test_bshd_layout_is_bit_identical_to_contiguous(cuda_lib, d):
     assert torch.equal(got[2], ref[2]) and torch.equal(got[3], ref[3])
 
 
+@pytest.mark.parametrize("d,d_v", [(64, 64), (128, 256), (32, 128)])
+def test_fp32_strided_inputs_equal_the_bf16_path(cuda_lib, d, d_v):
+    """fp32 inputs in the page's [B, S, H, D] layout (packed-QKV views for the
+    queries and keys, head strides that are multiples of 4 but not 8 elements) are
+    gathered and rounded to bf16 inside the library: the result equals, bit for
+    bit, the bf16 path on inputs rounded beforehand, and matches the oracle."""
+    B, H, Nq, Nkv = 2, 3, 200, 333
+    gen = torch.Generator(device="cuda").manual_seed(27 + d + d_v)
+    # [B, S, 2, H, d + 4] buffers: slot 0 holds the primal, slot 1 its tangent, so
+    # both views share one set of strides; the head stride d + 4 is a multiple of 4
+    # elements but not of 8.
+    qk = torch.randn((B, Nq, 2, H, d + 4), generator=gen, device="cuda")
+    kk = torch.randn((B, Nkv, 2, H, d + 4), generator=gen, device="cuda")
+    vv = torch.randn((B, Nkv, 2, H, d_v), generator=gen, device="cuda")
+    qk[:, :, 1] *= 0.3
+    kk[:, :, 1] *= 0.3
+    xs = [qk[:, :, 0, :, :d], kk[:, :, 0, :, :d], vv[:, :, 0], qk[:, :, 1, :, :d], kk[:, :, 1, :, :d], vv[:, :, 1]]
+    scale = d ** -0.5
+    got = binding.attn_jvp_fwd_strided(*xs, layout="bshd", scale=scale)
+    _sync()
+    ref = binding.attn_jvp_fwd_strided(*(t.to(torch.bfloat16) for t in xs), layout="bshd", scale=scale)
+    _sync()
+    for g, r in zip(got, ref):
+        assert torch.equal(g, r)
+    to_bhsd = lambda t: t.transpose(1, 2)
+    xo = {"q": to_bhsd(xs[0]), "k": to_bhsd(xs[1]), "v": to_bhsd(xs[2]), "q_t": to_bhsd(xs[3]),
+          "k_t": to_bhsd(xs[4]), "v_t": to_bhsd(xs[5])}
+    want = _oracle(xo, xo, scale)
+    assert_close(host64(to_bhsd(got[0])), want[0], "O")
+    assert_close(host64(to_bhsd(got[1])), want[1], "Ot")
+
+
 def test_packed_qkv_views_are_bit_identical(cuda_lib):
     B, H, S, d = 1, 4, 257, 128
     x = inputs.make_inputs(B, H, S, d, seed=22, device="cuda", tangent_scale=0.5)

@@ -71,6 +71,44 @@ def test_small_cases_every_row(cuda_lib, B, H, N, d, extra):
     _check_all(x, got)
 
 
+def test_fp32_inputs_through_the_c_abi(cuda_lib):
+    """The tiny fp32 workload's device buffers go straight to attn_jvp_fwd and
+    attn_jvp_fwd_chunk with ATTNJVP_FP32: the library rounds them to bf16 itself.
+    Results match the oracle (on the original fp32 values, within the derived
+    input-rounding bound) and equal, bit for bit, the bf16 path on inputs rounded
+    to bf16 beforehand."""
+    import ctypes
+    lib = binding.load()
+    x = inputs.workload_inputs("tiny", device="cuda")
+    B, H, N, d = x["q"].shape
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    out = torch.empty((B, H, N, d), dtype=torch.float32, device="cuda")
+    out_t, lse, mu = torch.empty_like(out), torch.empty((B, H, N), device="cuda"), torch.empty((B, H, N), device="cuda")
+    rc = lib.attn_jvp_fwd(*(p(x[n]) for n in inputs.NAMES), p(out), p(out_t), p(lse), p(mu), B, H, N, d,
+                          ctypes.c_float(x["scale"]), binding.ATTNJVP_FP32, stream)
+    assert rc == binding.ATTNJVP_OK, lib.attn_jvp_last_error()
+    torch.cuda.synchronize()
+    binding.attn_jvp_status()
+    _check_all(x, (out, out_t, lse, mu))
+    xb = dict(x, **{n: x[n].to(torch.bfloat16) for n in inputs.NAMES})
+    ref = _run(xb)
+    for got, want in zip((out, out_t, lse, mu), ref):
+        assert torch.equal(got, want)
+    # a key chunk, fp32 in
+    a, n = 37, 150
+    co, cot = torch.empty_like(out), torch.empty_like(out)
+    cl, cm = torch.empty_like(lse), torch.empty_like(mu)
+    rc = lib.attn_jvp_fwd_chunk(*(p(x[n_]) for n_ in inputs.NAMES), p(co), p(cot), p(cl), p(cm), B, H, N, d,
+                                ctypes.c_float(x["scale"]), binding.ATTNJVP_FP32, a, n, stream)
+    assert rc == binding.ATTNJVP_OK, lib.attn_jvp_last_error()
+    torch.cuda.synchronize()
+    _check_all(x, (co, cot, cl, cm), kv=(a, n))
+    # any other code is refused before anything runs
+    assert lib.attn_jvp_fwd(*(p(x[n_]) for n_ in inputs.NAMES), p(out), p(out_t), p(lse), p(mu), B, H, N, d,
+                            ctypes.c_float(x["scale"]), 5, stream) == binding.ATTNJVP_EINVAL
+
+
 def test_tiny_workload_fp32_inputs(cuda_lib):
     # fp32 inputs are rounded to bf16 by the library's cast kernel; the oracle
     # sees the original fp32 values, so the error includes the input rounding.
