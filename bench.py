@@ -91,9 +91,11 @@ def load_peaks():
 
 
 def measure_epilogue(spec, dev, stream, peaks, reps=10, warmup=3):
-    """Achieved bandwidth of the two output-side kernels on a latent batch larger than L2.
+    """Achieved bandwidth of the TrigFlow tangent and the two output-side kernels on a
+    latent batch larger than L2.
 
-    Algorithmic bytes per element: trigflow_output_jvp reads x, n and their tangents and
+    Algorithmic bytes per element: trigflow_tangent reads x0 and eps and writes the
+    tangent (12 B); trigflow_output_jvp reads x, n and their tangents and
     writes F and its tangent (24 B); scm_tangent_loss reads F_theta, F_sg, F_teacher, x and
     F_t and writes g_n and df_dt (28 B); its in-place normalisation of g (one write and
     one re-read of the unnormalised g, 8 B more) is an implementation cost the figure
@@ -109,7 +111,12 @@ def measure_epilogue(spec, dev, stream, peaks, reps=10, warmup=3):
     ws = binding.scm_workspace(shape, dev)
     elems = B * C * T * HW
     res = {"shape": [B, C, T, HW], "elements": elems}
+    flat_x, flat_n = x.reshape(B, -1), n.reshape(B, -1)
+    t_b = t[:, 0].contiguous()
+    tangent_out = torch.empty_like(flat_x)
     ops = {
+        "trigflow_tangent": (12, lambda: binding.trigflow_tangent(flat_x, flat_n, t_b, out=tangent_out,
+                                                                  stream=stream)),
         "trigflow_output_jvp": (24, lambda: binding.trigflow_output_jvp(x, n, xt, nt, t, tt, out=F, out_t=Ft,
                                                                          stream=stream)),
         "scm_tangent_loss": (28, lambda: binding.scm_tangent_loss(F, x, n, xt, nt, t, 0.5, workspace=ws,
@@ -559,7 +566,8 @@ def kernel_report(path, workload, peaks, peak_src, clocks, sm_count):
             "bound": "hbm", "algorithmic_bytes": nb, "launch_ms": round(t_ms, 5),
             "achieved": round(nb / (t_ms * 1e-3) / 1e9, 1), "peak": hbm, "unit": "GB/s",
             "frac": round(nb / (t_ms * 1e-3) / 1e9 / hbm, 4),
-            "note": "12 B per element; %d elements, %.0f MB (below L2: served partly from cache)"
+            "note": "in the step: 12 B per element; %d elements, %.0f MB, a few microseconds of work, so "
+                    "launch latency dominates; the epilogue object times it on a batch above L2"
                     % (path.x0.numel(), nb / 1e6)}
     m_ms = path.mean_ms("merge")
     if m_ms:

@@ -49,10 +49,26 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name)
 
 
-def test_library_targets_sm103a_only():
-    out = subprocess.run(["cuobjdump", "--list-elf", binding.LIB_PATH], capture_output=True, text=True).stdout
-    arches = set(re.findall(r"sm_\d+a?", out))
-    assert arches == {"sm_103a"}, arches
+def test_library_is_built_for_sm103a_only(monkeypatch):
+    """Every translation unit and the link step get exactly one -gencode, sm_103a
+    (machine code only: no PTX for a JIT to pick up on another GPU)."""
+    assert _build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    assert not any("gencode" in f or "arch" in f for f in _build.NVCC_FLAGS)
+    seen = []
+
+    class Done(Exception):
+        pass
+
+    def fake_run(cmd, **kw):
+        seen.append(cmd)
+        raise Done
+
+    monkeypatch.setattr(_build.subprocess, "run", fake_run)  # record the commands, compile nothing
+    with pytest.raises(Done):
+        _build.build(force=True)
+    assert seen, "build() ran no compiler"
+    for cmd in seen:
+        assert cmd.count("-gencode") == 1 and "arch=compute_103a,code=sm_103a" in cmd, cmd
 
 
 def _fwd(lib, ptrs=None, B=1, H=1, N=128, d=128, scale=0.1, chunk=None, dtype=binding.ATTNJVP_BF16):
