@@ -15,7 +15,11 @@ The key-chunk merge is exact algebra on those definitions (the pages have no
 key split).  The output side of a consistency step (coefficient JVP, the JVP of
 _process_output, the tangent target with its NaN masks and normalisation, the
 sCM loss) follows section 一致性模型 (consistency model), its 蒸馏代码 listing.
-The primal backward (dQ, dK, dV) follows section 反向 (backward).
+The primal backward (dQ, dK, dV) follows section 反向 (backward).  The QK
+normalisation the student keeps (section 一致性模型) is the per-head RMSNorm of
+the page "Обслуживание Ideogram v4 менее чем за секунду" (dev48.org), section
+on fusing RMSNorm, y = x rsqrt(mean(x^2) + eps) weight; its tangent is the
+chain rule on that definition.
 
 Parity pins for every function here are in tests/test_*oracle.py; none is unpinned.
 """
@@ -53,6 +57,8 @@ def _load():
         lib.oracle_scm_tangent_loss.restype = ctypes.c_int
         lib.oracle_attn_bwd_head.argtypes = [dp] * 4 + [i64] * 3 + [ctypes.c_double] + [dp] * 3
         lib.oracle_attn_bwd_head.restype = ctypes.c_int
+        lib.oracle_rmsnorm_jvp.argtypes = [dp] * 3 + [i64, i64, ctypes.c_double] + [dp] * 2
+        lib.oracle_rmsnorm_jvp.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -292,3 +298,21 @@ def attn_bwd_rows(q, k, v, dO, scale, q_rows, k_rows, block=512, with_scales=Fal
         return dq, dk, dv, (sq, sk, sv)
     return dq, dk, dv
 
+
+
+def rmsnorm_jvp(x, xt, w, eps):
+    """QK normalisation of each row of d values and its tangent, FP64.
+
+    x, xt: [..., d]; w: [d].  Returns (y, yt) shaped like x:
+        y = x rho w,  yt = w (xt rho - x rho^3 mean(x xt)),  rho = 1 / sqrt(mean(x^2) + eps)."""
+    lib = _load()
+    x, xt, w = _f64(x), _f64(xt), _f64(w)
+    d = x.shape[-1]
+    if xt.shape != x.shape or w.shape != (d,):
+        raise ValueError("oracle.rmsnorm_jvp: inconsistent shapes")
+    rows = int(np.prod(x.shape[:-1])) if x.ndim > 1 else 1
+    y, yt = np.empty(x.shape), np.empty(x.shape)
+    rc = lib.oracle_rmsnorm_jvp(_ptr(x), _ptr(xt), _ptr(w), rows, d, float(eps), _ptr(y), _ptr(yt))
+    if rc != 0:
+        raise ValueError("oracle_rmsnorm_jvp failed (%d): rows with no norm or bad eps" % rc)
+    return y, yt

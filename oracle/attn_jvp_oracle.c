@@ -21,6 +21,12 @@
  *     with its warm-up, NaN masks and normalisation, and the sCM loss.
  *   - section 反向 (backward): dV = P^T dO, dP = dO V^T,
  *     dS = P (.) (dP - rowsum(dP (.) P)), dQ = s dS K, dK = s dS^T Q.
+ *   - section 一致性模型 (consistency model): the student keeps its QK
+ *     normalisation (QK正则化), so the tangents of Q and K pass through it
+ *     before the attention.  The norm itself is defined on the page
+ *     "Обслуживание Ideogram v4 менее чем за секунду" (dev48.org), section on
+ *     fusing RMSNorm: per head, y = x rsqrt(mean(x^2) + eps) weight.  Its
+ *     tangent is the chain rule on that definition.
  *
  * Every step below is the plain definition, computed in the order written on
  * the page: two passes over the keys for the softmax (max, then exponentials),
@@ -37,6 +43,10 @@
  * The backward (tests/test_bwd_oracle.py): torch.autograd, a central
  * difference of <O, dO>, one key, key-shift invariance, and the rowsum
  * identity rowsum(dP (.) P) = rowsum(dO (.) O).
+ * The QK normalisation (tests/test_rmsnorm_oracle.py): central differences,
+ * torch.func.jvp of the torch expression, scale invariance at eps = 0, unit
+ * RMS, the tangent orthogonal to x, and attention through the norm against
+ * torch.func.jvp of the whole composition.
  */
 #include <math.h>
 #include <pthread.h>
@@ -448,5 +458,40 @@ int oracle_attn_bwd_head(const double *q, const double *k, const double *v, cons
         }
     free(P);
     free(dS);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* QK normalisation (RMSNorm over each head's d channels) and its tangent    */
+/* ------------------------------------------------------------------------ */
+
+/* For each of ``rows`` rows of d values (one token of one head):
+ *   m   = (1/d) sum_c x_c^2            rho = 1 / sqrt(m + eps)
+ *   y_c = x_c rho w_c
+ * and along the tangent xt (chain rule: d rho = -rho^3 (1/d) sum_c x_c xt_c):
+ *   a    = (1/d) sum_c x_c xt_c
+ *   yt_c = w_c (xt_c rho - x_c rho^3 a)
+ * x, xt, y, yt: [rows, d]; w: [d] (the norm's per-channel weight).          */
+int oracle_rmsnorm_jvp(const double *x, const double *xt, const double *w, int64_t rows, int64_t d,
+                       double eps, double *y, double *yt)
+{
+    if (rows < 0 || d < 1 || !(eps >= 0.0)) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        const double *xr = x + r * d, *xtr = xt + r * d;
+        double m = 0.0, a = 0.0;
+        for (int64_t c = 0; c < d; ++c) {
+            m += xr[c] * xr[c];
+            a += xr[c] * xtr[c];
+        }
+        m /= (double)d;
+        a /= (double)d;
+        if (!(m + eps > 0.0)) return -2;  /* an all-zero row with eps = 0 has no norm */
+        const double rho = 1.0 / sqrt(m + eps);
+        const double rho3 = rho * rho * rho;
+        for (int64_t c = 0; c < d; ++c) {
+            y[r * d + c] = xr[c] * rho * w[c];
+            yt[r * d + c] = w[c] * (xtr[c] * rho - xr[c] * rho3 * a);
+        }
+    }
     return 0;
 }
