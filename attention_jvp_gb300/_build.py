@@ -14,7 +14,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libattnjvp.so")
-SOURCES = ["attn_jvp_fwd.cu", "aux_kernels.cu", "capi.cu", "no_alloc.cu", "host_pipeline.cu", "epilogue.cu", "attn_bwd.cu"]
+SOURCES = ["attn_jvp_fwd.cu", "aux_kernels.cu", "capi.cu", "no_alloc.cu", "host_pipeline.cu", "epilogue.cu",
+           "attn_bwd.cu", "qk_norm.cu"]
 HEADERS = ["sm103_ptx.cuh", "internal.h", os.path.join("..", "..", "include", "attnjvp.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

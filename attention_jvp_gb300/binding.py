@@ -57,6 +57,7 @@ def load(path=None):
                                                                     ci, i64, i64, vp]
     lib.attn_jvp_fwd_host_workspace_bytes.argtypes = [i64] * 6
     lib.attn_jvp_fwd_host_workspace_bytes.restype = i64
+    lib.qk_rmsnorm_jvp.argtypes = [vp] * 10 + [i64] * 3 + [ctypes.c_float, vp]
     lib.trigflow_coeffs_jvp.argtypes = [ctypes.c_double] * 3 + [ctypes.POINTER(ctypes.c_double)]
     lib.trigflow_output_jvp.argtypes = [vp] * 8 + [i64] * 4 + [vp]
     lib.scm_tangent_loss.argtypes = [vp] * 6 + [ctypes.c_double] + [vp] * 5 + [i64] * 4 + [vp, i64, vp]
@@ -73,7 +74,7 @@ def load(path=None):
     lib.attn_jvp_version.restype = ctypes.c_char_p
     for name in ("attn_jvp_fwd", "attn_jvp_fwd_chunk", "attn_jvp_merge", "attn_jvp_cast_f32_bf16",
                  "attn_jvp_fwd_split_noalloc", "attn_jvp_fwd_host", "attn_jvp_fwd_strided", "attn_jvp_fwd_ex",
-                 "trigflow_coeffs_jvp", "trigflow_output_jvp", "scm_tangent_loss", "attn_bwd",
+                 "trigflow_coeffs_jvp", "trigflow_output_jvp", "scm_tangent_loss", "attn_bwd", "qk_rmsnorm_jvp",
                  "trigflow_coeffs", "trigflow_tangent", "attn_jvp_status", "attn_jvp_selftest_wait"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
@@ -316,6 +317,31 @@ def attn_jvp_fwd_split_noalloc(q, k, v, q_t, k_t, v_t, n_chunks, out, out_t, lse
                                            ctypes.c_float(scale), code, int(n_chunks), _stream(stream))
     _check("attn_jvp_fwd_split_noalloc", rc)
     return out, out_t, lse, mu
+
+
+def qk_rmsnorm_jvp(q, q_t, k, k_t, w_q, w_k, eps=1e-6, out=None, stream=None):
+    """QK normalisation and its tangent: (qn, qn_t, kn, kn_t), bf16, shaped like the inputs.
+
+    q, q_t, k, k_t: contiguous bf16 tensors whose last dim is the head dim d (each
+    row of d values one token of one head); w_q, w_k: fp32 [d].  ``out``: optional
+    (qn, qn_t, kn, kn_t) to write into (an input may serve as its own output)."""
+    _req(q, "q", torch.bfloat16)
+    d = q.shape[-1]
+    _req(q_t, "q_t", torch.bfloat16, q.shape)
+    _req(k, "k", torch.bfloat16)
+    if k.shape[-1] != d:
+        raise ValueError("k must have q's head dim %d" % d)
+    _req(k_t, "k_t", torch.bfloat16, k.shape)
+    _req(w_q, "w_q", torch.float32, (d,))
+    _req(w_k, "w_k", torch.float32, (d,))
+    if out is None:
+        out = (torch.empty_like(q), torch.empty_like(q), torch.empty_like(k), torch.empty_like(k))
+    for n, t, ref in zip(("qn", "qn_t", "kn", "kn_t"), out, (q, q, k, k)):
+        _req(t, n, torch.bfloat16, ref.shape)
+    rc = load().qk_rmsnorm_jvp(_ptr(q), _ptr(q_t), _ptr(k), _ptr(k_t), _ptr(w_q), _ptr(w_k), *(_ptr(t) for t in out),
+                               q.numel() // d, k.numel() // d, d, ctypes.c_float(eps), _stream(stream))
+    _check("qk_rmsnorm_jvp", rc)
+    return tuple(out)
 
 
 def _host(t, name, dtype, shape=None):

@@ -353,6 +353,52 @@ int attn_jvp_cast_f32_bf16(const float* in, void* out, int64_t n, void* stream) 
   return ok();
 }
 
+int qk_rmsnorm_jvp(const void* q, const void* q_t, const void* k, const void* k_t, const float* w_q,
+                   const float* w_k, void* qn, void* qn_t, void* kn, void* kn_t, int64_t rows_q, int64_t rows_k,
+                   int64_t d, float eps, void* stream) {
+  if (rows_q < 0 || rows_k < 0) return fail(ATTNJVP_EINVAL, "rows_q and rows_k must be >= 0");
+  if (d != 16 && d != 32 && d != 64 && d != 128 && d != 256)
+    return fail(ATTNJVP_EUNSUPPORTED, "head dim %lld not supported (16, 32, 64, 128 or 256)", (long long)d);
+  if (!std::isfinite(eps) || eps < 0.f) return fail(ATTNJVP_EINVAL, "eps must be finite and >= 0");
+  if (rows_q > (int64_t(1) << 40) / d || rows_k > (int64_t(1) << 40) / d)
+    return fail(ATTNJVP_EINVAL, "too many rows");
+  struct {
+    const void* p;
+    const char* name;
+    bool needed;
+  } ptrs[10] = {{q, "q", rows_q > 0},     {q_t, "q_t", rows_q > 0},   {qn, "qn", rows_q > 0},
+                {qn_t, "qn_t", rows_q > 0}, {w_q, "w_q", rows_q > 0}, {k, "k", rows_k > 0},
+                {k_t, "k_t", rows_k > 0},   {kn, "kn", rows_k > 0},   {kn_t, "kn_t", rows_k > 0},
+                {w_k, "w_k", rows_k > 0}};
+  for (const auto& e : ptrs) {
+    if (!e.needed) continue;
+    if (!e.p) return fail(ATTNJVP_EINVAL, "%s is NULL", e.name);
+    if (!aligned(e.p, 16)) return fail(ATTNJVP_EINVAL, "%s is not 16-byte aligned", e.name);
+  }
+  if (rows_q + rows_k == 0) return ok();
+  int dev;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(ATTNJVP_ECUDA, "no CUDA device: %s", cudaGetErrorString(e));
+  QkNormArgs a;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.q_t = static_cast<const __nv_bfloat16*>(q_t);
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.k_t = static_cast<const __nv_bfloat16*>(k_t);
+  a.w_q = w_q;
+  a.w_k = w_k;
+  a.qn = static_cast<__nv_bfloat16*>(qn);
+  a.qn_t = static_cast<__nv_bfloat16*>(qn_t);
+  a.kn = static_cast<__nv_bfloat16*>(kn);
+  a.kn_t = static_cast<__nv_bfloat16*>(kn_t);
+  a.rows_q = rows_q;
+  a.rows_k = rows_k;
+  a.d = static_cast<int>(d);
+  a.eps = eps;
+  e = launch_qk_rmsnorm_jvp(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(ATTNJVP_ECUDA, "QK-norm launch failed: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 int trigflow_coeffs(double t, double tau, double* c) {
   if (!c) return fail(ATTNJVP_EINVAL, "c is NULL");
   if (!std::isfinite(t) || !std::isfinite(tau)) return fail(ATTNJVP_EINVAL, "t and tau must be finite");

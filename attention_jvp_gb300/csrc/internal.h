@@ -4,6 +4,7 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 namespace attnjvp {
@@ -56,6 +57,17 @@ struct BwdArgs {
 };
 int64_t attn_bwd_workspace_floats(int64_t B, int64_t H, int64_t Nq);
 cudaError_t launch_attn_bwd(const BwdArgs& a, const char** msg);
+
+// QK normalisation and its tangent (qk_norm.cu); rows of d contiguous bf16 values.
+struct QkNormArgs {
+  const __nv_bfloat16 *q, *q_t, *k, *k_t;  // inputs; 16-byte aligned
+  const float *w_q, *w_k;                  // per-channel weights [d]; 16-byte aligned
+  __nv_bfloat16 *qn, *qn_t, *kn, *kn_t;    // outputs (may alias their own input)
+  int64_t rows_q, rows_k;
+  int d;                                   // 16, 32, 64, 128 or 256
+  float eps;
+};
+cudaError_t launch_qk_rmsnorm_jvp(const QkNormArgs& a, cudaStream_t stream);
 
 // Output side of a consistency step (epilogue.cu).
 int64_t epilogue_items(int64_t B, int64_t C, int64_t T, int64_t HW);  // launch blocks

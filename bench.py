@@ -141,6 +141,39 @@ def measure_epilogue(spec, dev, stream, peaks, reps=10, warmup=3):
     return res
 
 
+def measure_qk_norm(x, dev, stream, peaks, reps=10, warmup=3):
+    """Achieved bandwidth of qk_rmsnorm_jvp (the QK normalisation and its tangent) on the
+    workload's Q, K and tangents, written to separate outputs.  Algorithmic bytes: 8 per
+    element of Q and of K (read x and xt, write y and yt, bf16)."""
+    import torch
+    from attention_jvp_gb300 import binding
+    q, qt, k, kt = x["q"], x["q_t"], x["k"], x["k_t"]
+    d = q.shape[-1]
+    w = torch.ones(d, dtype=torch.float32, device=dev)
+    outs = tuple(torch.empty_like(t) for t in (q, qt, k, kt))
+
+    def run():
+        binding.qk_rmsnorm_jvp(q, qt, k, kt, w, w, eps=1e-6, out=outs, stream=stream)
+
+    for _ in range(warmup):
+        run()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    nb = 8 * (q.numel() + k.numel())
+    peak = float(peaks["hbm_gbs"])
+    gbs = nb / (ms * 1e-3) / 1e9
+    del outs
+    return {"bound": "hbm", "algorithmic_bytes": nb, "ms": round(ms, 4), "achieved": round(gbs, 1), "peak": peak,
+            "unit": "GB/s", "frac": round(gbs / peak, 4),
+            "note": "Q and K of the workload with their tangents: 8 B per element (bf16 x, xt in; y, yt out)"}
+
+
 def measure_backward(x, spec, o, lse, dev, stream, peaks, reps=5, warmup=2):
     """Primal attention backward on the workload's Q, K, V with a random upstream gradient.
 
@@ -713,6 +746,11 @@ def run_gpu(args):
     if not args.skip_epilogue and rank == 0:
         epi = measure_epilogue(spec, dev, stream, peaks)
 
+    # ---- QK normalisation JVP (the input side; not part of the timed step) ----
+    qk_norm = None
+    if not args.skip_epilogue and rank == 0:
+        qk_norm = measure_qk_norm(x, dev, stream, peaks)
+
     # ---- primal attention backward (not part of the timed step; head dims up to 128) ----
     bwd = None
     if not args.skip_backward and rank == 0 and d <= 128:  # on the (merged) forward's O and LSE
@@ -759,6 +797,7 @@ def run_gpu(args):
             "e2e": e2e,
             "gpu_launches": launches,
             "epilogue": epi,
+            "qk_norm": qk_norm,
             "backward": bwd,
             "clocks": clocks,
             "workloads": subs,

@@ -205,6 +205,31 @@ int attn_jvp_fwd_split_noalloc(const void* q, const void* k, const void* v,
                                float scale, int dtype, int64_t n_chunks, void* stream);
 
 /*
+ * QK normalisation and its tangent, the input side of the attention JVP for a
+ * student that keeps RMS-normalised queries and keys (page "带分数正则的
+ * 一致性蒸馏", section 一致性模型 (consistency model): QK正则化).  The norm is
+ * the per-head RMSNorm of the page "Обслуживание Ideogram v4 менее чем за
+ * секунду" (dev48.org), section on fusing RMSNorm.  For every row of d values
+ * (one token of one head):
+ *   rho = 1 / sqrt(mean(x^2) + eps),   y = x rho w,
+ *   yt  = w (xt rho - x rho^3 mean(x xt))       (the JVP of y along xt).
+ * One call normalises the Q rows with w_q and the K rows with w_k; the outputs
+ * feed attn_jvp_fwd as its q, q_t, k, k_t.
+ *   q, q_t, k, k_t     : bf16 [rows_q, d] and [rows_k, d]: any layout in which each
+ *                        head's d values are contiguous ([B, H, N, d] and the page's
+ *                        [B, N, H, d] are both B*H*N rows); 16-byte aligned.
+ *   w_q, w_k           : fp32 [d], the norms' per-channel weights; 16-byte aligned.
+ *   qn, qn_t, kn, kn_t : bf16 outputs shaped like their inputs (rounded to nearest
+ *                        even from fp32 arithmetic); each may alias its own input.
+ *   rows_q, rows_k     : >= 0; a zero count leaves that tensor's pointers unused.
+ *   d                  : 16, 32, 64, 128 or 256 (others: ATTNJVP_EUNSUPPORTED).
+ *   eps                : finite and >= 0.
+ */
+int qk_rmsnorm_jvp(const void* q, const void* q_t, const void* k, const void* k_t,
+                   const float* w_q, const float* w_k, void* qn, void* qn_t, void* kn, void* kn_t,
+                   int64_t rows_q, int64_t rows_k, int64_t d, float eps, void* stream);
+
+/*
  * Round fp32 to bf16 (nearest-even) element-wise on the device, so fp32 inputs
  * can be fed to the bf16 kernels.  in: fp32 [n]; out: bf16 [n]; n >= 0.
  * Both 16-byte aligned.

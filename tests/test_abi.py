@@ -37,7 +37,8 @@ def test_header_declares_the_boundary():
                      "attn_jvp_version", "attn_jvp_selftest_wait", "attn_jvp_fwd_split_noalloc",
                      "attn_jvp_fwd_host", "attn_jvp_fwd_host_workspace_bytes", "attn_jvp_fwd_strided",
                      "trigflow_coeffs_jvp", "trigflow_output_jvp", "scm_tangent_loss",
-                     "scm_tangent_loss_workspace_bytes", "attn_bwd", "attn_bwd_workspace_bytes"):
+                     "scm_tangent_loss_workspace_bytes", "attn_bwd", "attn_bwd_workspace_bytes",
+                     "qk_rmsnorm_jvp"):
         assert expected in names
 
 
@@ -344,3 +345,21 @@ def test_noalloc_checks_every_argument_before_launching(lib):
     msg_bf16 = lib.attn_jvp_last_error()
     assert call(good, H=64, N=1024, n=4, dtype=E.ATTNJVP_FP32) == E.ATTNJVP_EINVAL
     assert b"bf16 input copies" in lib.attn_jvp_last_error() and msg_bf16 != lib.attn_jvp_last_error()
+
+
+def test_qk_norm_validation_needs_no_gpu(lib):
+    E = binding
+    vp = ctypes.c_void_p
+    p = vp(256)
+    call = lambda ptrs, rq=10, rk=12, d=128, eps=1e-6: lib.qk_rmsnorm_jvp(*ptrs, rq, rk, d, ctypes.c_float(eps), None)
+    good = [p] * 10
+    assert call(good, d=96) == E.ATTNJVP_EUNSUPPORTED
+    assert call(good, eps=-1.0) == E.ATTNJVP_EINVAL
+    assert call(good, eps=float("nan")) == E.ATTNJVP_EINVAL
+    assert call(good, rq=-1) == E.ATTNJVP_EINVAL
+    assert call([None] + good[1:]) == E.ATTNJVP_EINVAL
+    assert b"q is NULL" in lib.attn_jvp_last_error()
+    assert call(good[:5] + [vp(264)] + good[6:]) == E.ATTNJVP_EINVAL  # w_k misaligned
+    assert b"w_k" in lib.attn_jvp_last_error()
+    # with no K rows the K pointers are not needed; nothing to do at all is a no-op
+    assert call(good[:2] + [None, None] + good[4:5] + [None] + good[6:], rq=0, rk=0) == E.ATTNJVP_OK
