@@ -3,7 +3,10 @@
 The GPU path runs this library's forward to get O and the LSE, then the
 backward; the oracle forms P, dP and dS from q, k, v and dO alone (the same
 bf16 values upcast to FP64).  P and dS enter the tensor cores as bf16, so the
-budget is the forward's: relative L2 <= 1e-2 and max-abs <= 5e-2 RMS(ref).
+budget is the forward's: relative L2 <= 1e-2 and max-abs <= 5e-2 RMS(ref); where
+rounding makes single elements exceed that share (peaked softmax, the stress
+workload's outlier column) a per-element bound derived from the two bf16
+roundings is added, never a measured constant.
 """
 import numpy as np
 import pytest
@@ -62,17 +65,107 @@ def test_backward_against_oracle(cuda_lib, B, H, nq, nkv, d):
         assert_close(host64(g), r, name)
 
 
+U_BF16 = 2.0 ** -8  # unit roundoff of bf16 (8 significant bits, round to nearest)
+
+
+def _bf16_round(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16).double().numpy()
+
+
+def _forward_o_model(q, k, v, s):
+    """O of one head as the forward kernel forms it, in FP64 except for one rounding:
+    the weights P~ = 2^(x - m_ref) that feed the value GEMM are rounded to bf16.  Here
+    x = S s log2(e) and m_ref is the kernel's lazy reference max (the first 64-key
+    tile's max, replaced by a later tile's only when that exceeds it by more than 8);
+    the normaliser l sums the unrounded P~ (page section 前向: p and H~ are cast to the
+    value dtype before the dot products, the sums are taken before the cast)."""
+    x = (q @ k.T) * (s / np.log(2.0))
+    m = x[:, :64].max(axis=1)
+    num = np.zeros((q.shape[0], v.shape[1]))
+    l = np.zeros(q.shape[0])
+    for t0 in range(0, k.shape[0], 64):
+        xt = x[:, t0:t0 + 64]
+        mx = xt.max(axis=1)
+        grow = mx > m + 8.0
+        alpha = np.where(grow, 2.0 ** (m - mx), 1.0)
+        m = np.where(grow, mx, m)
+        num *= alpha[:, None]
+        l *= alpha
+        p = 2.0 ** (xt - m[:, None])
+        l += p.sum(axis=1)
+        num += _bf16_round(p) @ v[t0:t0 + 64]
+    return num / l[:, None]
+
+
+def _backward_model(q, k, v, dO, s):
+    """(dQ, dK, dV) of one head with the backward's own roundings and nothing else:
+    D = rowsum(dO (.) O) from the forward's O (the model above), and P and
+    dS = P (.) (dP - D) rounded to bf16 before they enter the tensor cores."""
+    S = s * (q @ k.T)
+    P = np.exp(S - S.max(axis=1, keepdims=True))
+    P /= P.sum(axis=1, keepdims=True)
+    D = np.einsum("ij,ij->i", dO, _forward_o_model(q, k, v, s))
+    dS = _bf16_round(P * (dO @ v.T - D[:, None]))
+    return s * (dS @ k), s * (dS.T @ q), _bf16_round(P).T @ dO
+
+
+def _operand_bounds(q, k, v, dO, s):
+    """Per-element bound on |kernel - exact| for (dQ, dK, dV) of one head, from the
+    two bf16 roundings the kernels make (unit roundoff u = 2^-8):
+      - dS (and P for dV) rounded to bf16: u s sum_j |dS_ij| |k_j| for dQ,
+        u s sum_i |dS_ij| |q_i| for dK, u sum_i P_ij |dO_i| for dV;
+      - D taken from the forward's O, whose value GEMM used bf16 P~: O_i moves by
+        sum_j d_ij P_ij v_j with |d_ij| <= u, so D_i by at most
+        dD_i = u sum_j P_ij |dP_ij|, and dS_ij by P_ij dD_i: s sum_j P_ij dD_i |k_j|
+        for dQ, s sum_i P_ij dD_i |q_i| for dK (dV does not use D).
+    Exact FP64 quantities throughout (the definitions of section 反向)."""
+    S = s * (q @ k.T)
+    P = np.exp(S - S.max(axis=1, keepdims=True))
+    P /= P.sum(axis=1, keepdims=True)
+    dP = dO @ v.T
+    O = P @ v
+    dS = P * (dP - np.einsum("ij,ij->i", dO, O)[:, None])
+    dD = U_BF16 * np.einsum("ij,ij->i", P, np.abs(dP))
+    Pd = P * dD[:, None]
+    bq = U_BF16 * s * (np.abs(dS) @ np.abs(k)) + s * (Pd @ np.abs(k))
+    bk = U_BF16 * s * (np.abs(dS).T @ np.abs(q)) + s * (Pd.T @ np.abs(q))
+    bv = U_BF16 * (P.T @ np.abs(dO))
+    return bq, bk, bv
+
+
 def test_backward_with_peaked_softmax(cuda_lib):
     # Larger scores: rows dominated by one key (P close to one-hot).  There
-    # dS = P (.) (dP - D) nearly cancels at the dominant key, and D is taken as
-    # rowsum(dO (.) O) with the forward's O, whose value GEMM used bf16 P~
-    # (relative error ~2^-9).  That offset enters dS, hence dQ and dK, at a
-    # few elements as a few percent of RMS (measured: 8.0e-2 for dQ, 7.4e-2
-    # for dK, at rel-L2 3e-3); dV does not involve D and keeps the usual bound.
-    got, ref = _run(1, 2, 400, 400, 128, seed=91, qk_scale=2.5)
-    assert_close(host64(got[0]), ref[0], "dQ", mar=0.15)
-    assert_close(host64(got[1]), ref[1], "dK", mar=0.15)
-    assert_close(host64(got[2]), ref[2], "dV")
+    # dS = P (.) (dP - D) nearly cancels at the dominant key, so two roundings
+    # show at single elements of dQ and dK well above the usual max-abs share:
+    # dS enters the tensor cores as bf16, and D is rowsum(dO (.) O) with the
+    # forward's O, whose value GEMM used bf16 P~.  Two checks, neither with a
+    # constant above the usual tolerances:
+    #   1. an FP64 model that makes exactly those two roundings and nothing else
+    #      (_backward_model) reproduces the kernel's results within the usual
+    #      rel-L2 and max-abs tolerances, so the kernel adds no error of its own;
+    #   2. against the exact oracle, every element stays within the bound derived
+    #      from those roundings (_operand_bounds) plus the usual 5e-2 RMS, and
+    #      rel-L2 within 1e-2.
+    B, H, N, d = 1, 2, 400, 128
+    got, ref = _run(B, H, N, N, d, seed=91, qk_scale=2.5)
+    q, k, v = _bf16((B, H, N, d), 91, 2.5), _bf16((B, H, N, d), 92, 2.5), _bf16((B, H, N, d), 93)
+    dO = _bf16((B, H, N, d), 94)
+    s = d ** -0.5
+    for h in range(H):
+        args = [host64(t[0, h]) for t in (q, k, v, dO)]
+        model = _backward_model(*args, s)
+        bounds = _operand_bounds(*args, s)
+        for i, name in enumerate(("dQ", "dK", "dV")):
+            g, r = host64(got[i][0, h]), ref[i][0, h]
+            e_model = assert_close(g, model[i], "%s head %d vs the rounding model" % (name, h))
+            rel = np.linalg.norm(g - r) / np.linalg.norm(r)
+            assert rel <= 1e-2, "%s head %d: rel-L2 %.3e" % (name, h, rel)
+            excess = np.abs(g - r) - (bounds[i] + 5e-2 * np.sqrt(np.mean(r ** 2)))
+            assert np.all(excess <= 0), "%s head %d: %.3e over the derived bound" % (name, h, excess.max())
+            print("peaked %s head %d: vs oracle rel-L2 %.2e max-abs/RMS %.2e; vs model %.2e / %.2e; "
+                  "model vs oracle max-abs/RMS %.2e" % (name, h, rel, np.abs(g - r).max() / np.sqrt(np.mean(r ** 2)),
+                                                       e_model[0], e_model[1],
+                                                       np.abs(model[i] - r).max() / np.sqrt(np.mean(r ** 2))))
 
 
 def test_backward_is_reproducible(cuda_lib):
