@@ -17,6 +17,9 @@
 //   dK/dV pass (resident K, V; streamed Q, dO and the per-query -LSE log2 e
 //             and -D):  S1 = K Q^T, S2 = V dO^T (both transposed: TMEM lane =
 //             key), P^T and dS^T per key row, dV += P^T dO, dK += dS^T Q.
+// At head dim 256 two CTAs share each resident tile, each accumulating half of
+// the gradient columns (the fp32 dK and dV of 128 keys would fill TMEM); both
+// form the full 256-deep scores.
 // Warps: 0 TMA (resident tiles, then the score ring, the value ring and, in the
 // dK/dV pass, the per-query vector ring, each refilled as soon as it frees),
 // 1 TMEM + value MMAs, 2 S2 MMAs, 3 S1 MMAs, and two groups of
@@ -50,13 +53,23 @@ struct BwdCfg {
   static constexpr int kBM = 128;                  // resident rows per CTA (= TMEM lanes)
   static constexpr int kBN = 64;                   // streamed rows per tile
   static constexpr int kDC = D / 64;               // 64-element (128-byte) d-chunks
+  // Gradient columns per CTA.  At head dim 256 the fp32 accumulators of one
+  // resident tile (dK and dV: 512 columns) would fill TMEM, so two CTAs share
+  // each resident tile, each accumulating half of the gradient columns (and
+  // each forming the full 256-deep scores), as the forward does with O and T.
+  static constexpr int kDV = D > 128 ? 128 : D;
+  static constexpr int kVC = kDV / 64;             // 64-element chunks of a value tile
+  static constexpr int kVSplit = D / kDV;          // CTAs per resident tile
   // dQ pass: the resident Q and dO also live in TMEM (bf16, D/2 columns each) as
   // the A operands of the score MMAs, which then read only the streamed tiles
   // from shared memory (with both operands there, a 64-wide score MMA wants
-  // about 1.5x the shared-memory bandwidth).
-  static constexpr bool kRTmem = !kDKDV;
-  static constexpr int kNS = (D == 128) ? 1 : 3;  // S1 TMEM buffers
-  static constexpr int kNSt = 3;                            // S2 (then packed operands) TMEM buffers
+  // about 1.5x the shared-memory bandwidth).  Not at 256, where they do not fit.
+  static constexpr bool kRTmem = !kDKDV && D <= 128;
+  static constexpr int kNSt = 3;                   // S2 (then packed operands) TMEM buffers
+  // S1 TMEM buffers: as many (up to 3) as the columns left beside the
+  // accumulators, the resident copies and the S2 buffers hold.
+  static constexpr int kFreeCols = 512 - (kDKDV ? 2 : 1) * kDV - (kRTmem ? D : 0) - 64 * kNSt;
+  static constexpr int kNS = kFreeCols >= 192 ? 3 : 1;
   // Barrier slots of the S1 ring.  Tiles alternate between the two elementwise
   // groups; with a single buffer, consecutive tiles on one barrier would belong
   // to different groups, and a group could test a phase parity before the
@@ -65,18 +78,20 @@ struct BwdCfg {
   // finished tile j + 1, so tile j's phase (issued earlier by the same thread)
   // is complete.
   static constexpr int kSBar = kNS == 1 ? 2 : kNS;
-  static constexpr int kKS = (D == 128) ? 2 : 3;   // score-tile ring stages
-  static constexpr int kVS = (D == 128) ? (kDKDV ? 2 : 3) : 3;  // value-tile ring stages
+  // Ring stages: at 256 the resident tiles take 128 KB of shared memory, which
+  // leaves one score stage and one (dK/dV) or two (dQ) value stages.
+  static constexpr int kKS = D == 256 ? 1 : (D == 128 ? 2 : 3);  // score-tile ring stages
+  static constexpr int kVS = D == 256 ? (kDKDV ? 1 : 2) : (D == 128 ? (kDKDV ? 2 : 3) : 3);  // value ring
   static constexpr int kChunkR = kBM * 128;        // one d-chunk of a resident tile (bytes)
   static constexpr int kChunkX = kBN * 128;        // one d-chunk of a streamed tile (bytes)
   static constexpr int kRBytes = kDC * kChunkR;
   static constexpr int kKStage = 2 * kDC * kChunkX;              // X1 chunks, X2 chunks
   static constexpr int kVTensors = kDKDV ? 2 : 1;
-  static constexpr int kVStage = kVTensors * kDC * kChunkX;      // dK/dV: dO, Q;  dQ: K
+  static constexpr int kVStage = kVTensors * kVC * kChunkX;      // dK/dV: dO, Q;  dQ: K (this CTA's columns)
   // dK/dV: the streamed queries' -LSE log2e and -D (64 + 64 floats) in a ring of
   // their own, released by the elementwise warps once read (the value ring is
   // released only by the value MMAs, two tiles later than they need it)
-  static constexpr int kVecS = 4;
+  static constexpr int kVecS = D == 256 ? 2 : 4;
   static constexpr int kVecSlot = 512;
   static constexpr int kVecRing = kDKDV ? kVecS * kVecSlot : 0;
   static constexpr int kOffR1 = 0;
@@ -85,19 +100,21 @@ struct BwdCfg {
   static constexpr int kOffV = kOffK + kKS * kKStage;
   static constexpr int kOffVec = kOffV + kVS * kVStage;
   static constexpr int kOffBar = kOffVec + kVecRing;
-  static constexpr int kSmemBytes = kOffBar + 256 + 1024;
-  // TMEM: ACC1 [0, D) (dQ or dV), ACC2 [D, 2D) (dK), S1 buffers, S2 buffers (64 columns each)
+  static constexpr int kBarBytes = 512;  // the Barriers block below
+  static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
+  // TMEM: ACC1 [0, DV) (dQ or dV), ACC2 [DV, 2DV) (dK), the dQ pass's resident
+  // copies, S1 buffers, S2 buffers (64 columns each)
   static constexpr uint32_t kColAcc1 = 0;
-  static constexpr uint32_t kColAcc2 = D;
-  static constexpr uint32_t kColR1 = (kDKDV ? 2 : 1) * D;  // dQ pass: Q, then dO (bf16 pairs)
+  static constexpr uint32_t kColAcc2 = kDV;
+  static constexpr uint32_t kColR1 = (kDKDV ? 2 : 1) * kDV;  // dQ pass: Q, then dO (bf16 pairs)
   static constexpr uint32_t kColR2 = kColR1 + D / 2;
   static constexpr uint32_t kColS = kColR1 + (kRTmem ? D : 0);
   static constexpr uint32_t kColSt = kColS + 64 * kNS;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kColSt + 64 * kNSt <= kTmemCols, "TMEM budget");
-  static_assert(kSBar <= 3 && kNSt <= 3 && kKS <= 3 && kVS <= 3, "barrier arrays");
+  static_assert(kSBar <= 3 && kNSt <= 3 && kKS <= 3 && kVS <= 3 && kVecS <= 4, "barrier arrays");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-  static_assert(kKStage % 1024 == 0, "stage alignment (128-byte swizzle atoms)");
+  static_assert(kKStage % 1024 == 0 && kVStage % 1024 == 0, "stage alignment (128-byte swizzle atoms)");
 };
 
 constexpr int kThreads = 384;  // 12 warps
@@ -131,6 +148,7 @@ struct Barriers {
   uint32_t tmem_base;
   int abort_flag;
 };
+static_assert(sizeof(Barriers) <= BwdCfg<128, kModeDQ>::kBarBytes, "barrier block");
 
 // 64 TMEM columns of the calling thread's lane into r[kOff .. kOff + 63].
 #define BWD_R8(o) "=r"(r[o + 0]), "=r"(r[o + 1]), "=r"(r[o + 2]), "=r"(r[o + 3]), \
@@ -217,9 +235,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.x / geom.n_rtiles;
+  // Both column halves of a resident tile (head dim 256) are neighbours in the
+  // grid, so they stream the same tiles through L2 at about the same time.
+  const int vh = blockIdx.x % C::kVSplit;       // which kDV gradient columns this CTA accumulates
+  const unsigned rb = blockIdx.x / C::kVSplit;  // unsigned: the divisions below stay unsigned
+  const int bh = rb / geom.n_rtiles;
   const int hh = bh % geom.H, bb = bh / geom.H;
-  const int r0 = (blockIdx.x % geom.n_rtiles) * C::kBM;
+  const int r0 = (rb % geom.n_rtiles) * C::kBM;
   const int n_tiles = (geom.n_str + C::kBN - 1) / C::kBN;
 
   if (threadIdx.x == 0) {
@@ -301,12 +323,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int row0 = tv * C::kBN;
           uint8_t* vt = smem + C::kOffV + sv * C::kVStage;
           mbar_arrive_expect_tx(&bars->v_full[sv], C::kVStage);
-          for (int c = 0; c < C::kDC; ++c) {
+          for (int c = 0; c < C::kVC; ++c) {  // this CTA's gradient columns
+            const int col = vh * C::kDV + c * 64;
             if (C::kDKDV) {  // dO (for dV), then Q (for dK)
-              tma_load_4d(vt + c * C::kChunkX, &maps.x2, &bars->v_full[sv], c * 64, row0, hh, bb);
-              tma_load_4d(vt + (C::kDC + c) * C::kChunkX, &maps.x1, &bars->v_full[sv], c * 64, row0, hh, bb);
+              tma_load_4d(vt + c * C::kChunkX, &maps.x2, &bars->v_full[sv], col, row0, hh, bb);
+              tma_load_4d(vt + (C::kVC + c) * C::kChunkX, &maps.x1, &bars->v_full[sv], col, row0, hh, bb);
             } else {  // K (for dQ)
-              tma_load_4d(vt + c * C::kChunkX, &maps.x1, &bars->v_full[sv], c * 64, row0, hh, bb);
+              tma_load_4d(vt + c * C::kChunkX, &maps.x1, &bars->v_full[sv], col, row0, hh, bb);
             }
           }
           ++tv;
@@ -345,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- tcgen05.mma issuers: warp 3 S1, warp 2 S2, warp 1 the value MMAs ----------------
     if (lane == 0) {
       constexpr uint32_t kIdS = make_idesc_bf16_f32(128, C::kBN, false, false);  // both K-major
-      constexpr uint32_t kIdPV = make_idesc_bf16_f32(128, D, false, true);      // B N-major
+      constexpr uint32_t kIdPV = make_idesc_bf16_f32(128, C::kDV, false, true);  // B N-major
       const uint64_t dR1 = make_smem_desc_sw128(smem_u32(smem + C::kOffR1), 16, 1024);
       const uint64_t dR2 = make_smem_desc_sw128(smem_u32(smem + C::kOffR2), 16, 1024);
       const uint64_t dK0 = make_smem_desc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
@@ -408,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
             if (C::kDKDV) {
               mma_ts(tmem + C::kColAcc1, a0 + kk * 8, off(dV, kk * 2048), kIdPV, acc);  // dV += P^T dO
-              mma_ts(tmem + C::kColAcc2, a0 + 32 + kk * 8, off(dV, C::kDC * C::kChunkX + kk * 2048), kIdPV,
+              mma_ts(tmem + C::kColAcc2, a0 + 32 + kk * 8, off(dV, C::kVC * C::kChunkX + kk * 2048), kIdPV,
                      acc);  // dK += dS^T Q
             } else {
               mma_ts(tmem + C::kColAcc1, a0 + kk * 8, off(dV, kk * 2048), kIdPV, acc);  // dQ += dS K
@@ -504,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const int rrow = r0 + row;
       const bool valid_row = rrow < geom.n_res;
-      const int64_t obase = (static_cast<int64_t>(bh) * geom.n_res + rrow) * geom.d;
+      const int64_t obase = (static_cast<int64_t>(bh) * geom.n_res + rrow) * geom.d + vh * C::kDV;
       // dQ pass: ACC1 = dS K, times s.  dK/dV pass: ACC1 = dV, ACC2 = dS^T Q, times s.
       // The groups take alternate 32-column chunks.
       int chunk = 0;
@@ -513,7 +536,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* out = (C::kDKDV && acc == 1) ? geom.out2 : geom.out1;
         const float mul = (C::kDKDV && acc == 0) ? 1.f : geom.scale;
         const uint32_t col = acc == 0 ? C::kColAcc1 : C::kColAcc2;
-        const int ncols = D == 128 ? D : geom.d;
+        // this CTA's kDV columns, except for the 16/32-wide heads run as 64
+        const int ncols = C::kDV == 128 ? C::kDV : geom.d;
 #pragma unroll 1
         for (int c0 = 0; c0 < ncols; c0 += 32) {
           if ((chunk++ & 1) != group) continue;
@@ -521,10 +545,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32_wait(lane_addr + col + c0, v);
           if (valid_row) {
             float4* o4 = reinterpret_cast<float4*>(out + obase + c0);
-            const int n4 = D == 128 ? 8 : min(8, (ncols - c0) >> 2);
+            const int n4 = C::kDV == 128 ? 8 : min(8, (ncols - c0) >> 2);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              if (D != 128 && i >= n4) break;
+              if (C::kDV != 128 && i >= n4) break;
               o4[i] = make_float4(__uint_as_float(v[4 * i]) * mul, __uint_as_float(v[4 * i + 1]) * mul,
                                   __uint_as_float(v[4 * i + 2]) * mul, __uint_as_float(v[4 * i + 3]) * mul);
             }
@@ -620,15 +644,15 @@ cudaError_t launch_pass(const BwdArgs& a, const float* nl2, const float* nd, con
     maps.nl2 = maps.r1;  // unused by the dQ pass
     maps.nd = maps.r1;
   }
-  static bool attr_set[2][2] = {{false, false}, {false, false}};
+  static bool attr_set = false;  // one per instantiation
   auto kern = attn_bwd_kernel<D, kMode>;
-  if (!attr_set[D == 128][kMode]) {
+  if (!attr_set) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) {
       *msg = "cudaFuncSetAttribute(max dynamic shared memory) failed";
       return e;
     }
-    attr_set[D == 128][kMode] = true;
+    attr_set = true;
   }
   const int n_rtiles = static_cast<int>((n_res + C::kBM - 1) / C::kBM);
   geom.H = static_cast<int>(a.H);
@@ -642,7 +666,7 @@ cudaError_t launch_pass(const BwdArgs& a, const float* nl2, const float* nd, con
   geom.row_nd = nd;
   geom.out1 = dkdv ? a.dv : a.dq;
   geom.out2 = dkdv ? a.dk : nullptr;
-  const int64_t grid = static_cast<int64_t>(n_rtiles) * a.B * a.H;
+  const int64_t grid = static_cast<int64_t>(n_rtiles) * a.B * a.H * C::kVSplit;
   kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, a.stream>>>(maps, geom, a.status);
   e = cudaGetLastError();
   if (e != cudaSuccess) *msg = "attention-backward kernel launch failed";
@@ -674,6 +698,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const char** msg) {
 int64_t attn_bwd_workspace_floats(int64_t B, int64_t H, int64_t Nq) { return 2 * vec_floats(B, H, Nq); }
 
 cudaError_t launch_attn_bwd(const BwdArgs& a, const char** msg) {
+  if (a.d == 256) return launch_bwd_d<256>(a, msg);
   if (a.d == 128) return launch_bwd_d<128>(a, msg);
   if (a.d == 16 || a.d == 32 || a.d == 64) return launch_bwd_d<64>(a, msg);
   *msg = "unsupported head dimension";

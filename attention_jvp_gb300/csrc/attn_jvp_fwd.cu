@@ -139,6 +139,7 @@ struct Barriers {
   uint32_t tmem_base;
   int abort_flag;
 };
+static_assert(sizeof(Barriers) <= 256, "barrier block (256 bytes reserved in FwdCfg::kSmemBytes)");
 
 // Online-softmax state of one query row (log2 units of the scaled scores).
 struct RowState {

@@ -67,17 +67,12 @@ int* status_word(const char** why) {
   return g_status_ptr[dev];
 }
 
-// Head dims: 16, 32, 64 and 128 everywhere; 256 in the forward only (two CTAs
-// per query tile, each accumulating half of the value columns).
-int check_head_dim(int64_t d, bool forward) {
-  if (d == 16 || d == 32 || d == 64 || d == 128) return ATTNJVP_OK;
-  if (d == 256 && forward) return ATTNJVP_OK;
-  if (d == 256)
-    return fail(ATTNJVP_EUNSUPPORTED,
-                "head dim 256 not supported by the backward: the fp32 dK and dV accumulators of 128 keys would "
-                "fill all 512 tensor-memory columns, leaving none for the scores");
-  return fail(ATTNJVP_EUNSUPPORTED, "head dim %lld not supported (16, 32, 64, 128; 256 in the forward)",
-              (long long)d);
+// Head dims: the page's set, 16, 32, 64, 128 and 256, in the forward and the
+// backward (at 256 two CTAs share each row tile, each accumulating half of the
+// output columns).
+int check_head_dim(int64_t d, bool) {
+  if (d == 16 || d == 32 || d == 64 || d == 128 || d == 256) return ATTNJVP_OK;
+  return fail(ATTNJVP_EUNSUPPORTED, "head dim %lld not supported (16, 32, 64, 128 or 256)", (long long)d);
 }
 
 }  // namespace
@@ -454,7 +449,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* dout, cons
   if (!std::isfinite(scale) || !(scale > 0.f)) return fail(ATTNJVP_EINVAL, "scale must be finite and > 0");
   int rc = check_head_dim(d, false);
   if (rc != ATTNJVP_OK) return rc;
-  if (((N_q + 127) / 128) * B * H >= (int64_t(1) << 31) || ((N_kv + 127) / 128) * B * H >= (int64_t(1) << 31))
+  if (((N_q + 127) / 128) * B * H * 2 >= (int64_t(1) << 31) ||
+      ((N_kv + 127) / 128) * B * H * 2 >= (int64_t(1) << 31))
     return fail(ATTNJVP_EINVAL, "too many row tiles");
   const int64_t need = attn_bwd_workspace_floats(B, H, N_q) * 4;
   if (workspace_bytes < need)

@@ -207,10 +207,20 @@ def measure_backward(x, spec, o, lse, dev, stream, peaks, reps=5, warmup=2):
     ms = e0.elapsed_time(e1) / reps
     B, H, N, d = q.shape
     pairs = B * H * float(N) * N
+    executed = backward_executed_flops_per_pair(d)
     return {"ms": round(ms, 4), "tflops": round(10 * d * pairs / (ms * 1e-3) / 1e12, 2),
-            "tflops_executed": round(14 * d * pairs / (ms * 1e-3) / 1e12, 2),
-            "frac_of_sustained_peak": round(14 * d * pairs / (ms * 1e-3) / 1e12 / float(peaks["bf16_tflops_sustained"]), 4),
-            "flops_convention": "10 d per (query, key) pair; executed 14 d (two passes)"}
+            "tflops_executed": round(executed * pairs / (ms * 1e-3) / 1e12, 2),
+            "frac_of_sustained_peak": round(executed * pairs / (ms * 1e-3) / 1e12
+                                            / float(peaks["bf16_tflops_sustained"]), 4),
+            "flops_convention": "10 d per (query, key) pair; executed %d d (two passes%s)"
+                                % (executed // d, ", two CTAs per row tile" if d > 128 else "")}
+
+
+def backward_executed_flops_per_pair(d):
+    """Tensor flops the two backward passes execute per (query, key) pair: each pass forms
+    S and dP (2d + 2d), the dK/dV pass adds dV and dK (4d), the dQ pass dQ (2d): 14 d.
+    At head dim 256 two CTAs share a row tile and each forms the full S and dP: 22 d."""
+    return (22 if d > 128 else 14) * d
 
 
 _COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
@@ -751,9 +761,9 @@ def run_gpu(args):
     if not args.skip_epilogue and rank == 0:
         qk_norm = measure_qk_norm(x, dev, stream, peaks)
 
-    # ---- primal attention backward (not part of the timed step; head dims up to 128) ----
+    # ---- primal attention backward (not part of the timed step) ----
     bwd = None
-    if not args.skip_backward and rank == 0 and d <= 128:  # on the (merged) forward's O and LSE
+    if not args.skip_backward and rank == 0:  # on the (merged) forward's O and LSE
         bwd = measure_backward(x, spec, out, lse, dev, stream, peaks)
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only) ----

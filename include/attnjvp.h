@@ -317,8 +317,9 @@ int64_t attn_jvp_fwd_host_workspace_bytes(int64_t B, int64_t H, int64_t N, int64
  *                    write them.  P is rebuilt from lse; rowsum(dP (.) P) is
  *                    taken as rowsum(dO (.) O), equal since O = P V.
  *   dq, dk, dv     : fp32, shaped like q, k, v; 16-byte aligned.
- *   d              : 16, 32, 64 or 128 (256: ATTNJVP_EUNSUPPORTED, as dK and dV of
- *                    128 keys would fill tensor memory);  scale: the forward's scale.
+ *   d              : 16, 32, 64, 128 or 256 (at 256 two CTAs share each row tile, each
+ *                    accumulating half of the gradient columns, as dK and dV of 128
+ *                    keys would fill tensor memory);  scale: the forward's scale.
  *   workspace      : DEVICE, 256-byte aligned, attn_bwd_workspace_bytes(B, H, N_q).
  * Two passes (keys resident for dK/dV, queries resident for dQ) recompute the
  * scores instead of accumulating dQ with atomics, so results are reproducible.

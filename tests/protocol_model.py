@@ -266,9 +266,14 @@ class FwdModel:
 # ---------------------------------------------------------------------------
 def bwd_config(D, dkdv):
     """Ring and buffer counts of the backward kernel for padded head dim D and a pass."""
-    NS = 1 if D == 128 else 3
-    return dict(NS=NS, NSt=3, SBar=2 if NS == 1 else NS, KS=2 if D == 128 else 3,
-                VS=(2 if dkdv else 3) if D == 128 else 3, VecS=4, dkdv=dkdv)
+    DV = min(D, 128)  # gradient columns per CTA (two CTAs share a row tile at 256)
+    r_tmem = (not dkdv) and D <= 128
+    free = 512 - (2 if dkdv else 1) * DV - (D if r_tmem else 0) - 64 * 3
+    NS = 3 if free >= 192 else 1
+    KS = 1 if D == 256 else (2 if D == 128 else 3)
+    VS = (1 if dkdv else 2) if D == 256 else ((2 if dkdv else 3) if D == 128 else 3)
+    return dict(NS=NS, NSt=3, SBar=2 if NS == 1 else NS, KS=KS, VS=VS, VecS=2 if D == 256 else 4, dkdv=dkdv,
+                r_tmem=r_tmem)
 
 
 class BwdModel(FwdModel):
@@ -357,8 +362,8 @@ class BwdModel(FwdModel):
     def score_issuer(self, first):
         c = self.c
         name = "S1" if first else "S2"
-        yield from self.wait(self.r_full if c["dkdv"] else self.r_tmem, 0)
-        if not c["dkdv"] and not self.r_in_tmem:
+        yield from self.wait(self.r_tmem if c["r_tmem"] else self.r_full, 0)
+        if c["r_tmem"] and not self.r_in_tmem:
             raise ProtocolError("score MMAs before the resident tiles are in TMEM")
         for t in range(self.n):
             s = t % c["KS"]
@@ -414,7 +419,7 @@ class BwdModel(FwdModel):
 
     def elementwise_warp(self, group, w):
         c = self.c
-        if not c["dkdv"] and group == 0:
+        if c["r_tmem"] and group == 0:
             yield from self.wait(self.r_full, 0)
             yield
             if w == 3:
@@ -683,7 +688,7 @@ class AbortBwdModel(BwdModel):
     def score_issuer(self, first):
         c = self.c
         name = "S1" if first else "S2"
-        ok = yield from self.wait_or_abort(self.r_full if c["dkdv"] else self.r_tmem, 0)
+        ok = yield from self.wait_or_abort(self.r_tmem if c["r_tmem"] else self.r_full, 0)
         for t in range(self.n):
             if not ok:
                 break
@@ -721,7 +726,7 @@ class AbortBwdModel(BwdModel):
     def elementwise_warp(self, group, w):
         c = self.c
         ok = True
-        if not c["dkdv"] and group == 0:
+        if c["r_tmem"] and group == 0:
             ok = yield from self.wait_or_abort(self.r_full, 0)
             if ok:
                 self.r_tmem.arrive()

@@ -174,8 +174,11 @@ def test_backward_validation_needs_no_gpu(lib):
     assert call([vp(0)] + good[1:]) == E.ATTNJVP_EINVAL
     assert call(good[:3] + [vp(264)] + good[4:]) == E.ATTNJVP_EINVAL  # dout not 16-byte aligned
     assert b"dout" in lib.attn_jvp_last_error()
-    assert call(good, d=256) == E.ATTNJVP_EUNSUPPORTED  # the forward takes 256, the backward does not
-    assert b"backward" in lib.attn_jvp_last_error()
+    assert call(good, d=512) == E.ATTNJVP_EUNSUPPORTED
+    assert call(good, d=96) == E.ATTNJVP_EUNSUPPORTED
+    assert b"head dim 96" in lib.attn_jvp_last_error()
+    if not torch.cuda.is_available():  # placeholder pointers: never launch with them
+        assert call(good, d=256) == E.ATTNJVP_ECUDA  # 256 passes every argument check
     assert call(good, nkv=0) == E.ATTNJVP_EINVAL
     assert call(good, scale=float("nan")) == E.ATTNJVP_EINVAL
     assert call(good, nbytes=need - 4) == E.ATTNJVP_EINVAL
@@ -201,7 +204,7 @@ def test_strided_entry_validation_needs_no_gpu(lib):
     E = binding
     bshd = [nq * 3 * 64 for nq in (100,)] + [3 * 64, 64] + [300 * 3 * 64, 3 * 64, 64] + [100 * 3 * 64, 3 * 64, 64]
     assert _strided(lib, d=512) == E.ATTNJVP_EUNSUPPORTED
-    assert b"256 in the forward" in lib.attn_jvp_last_error()
+    assert b"16, 32, 64, 128 or 256" in lib.attn_jvp_last_error()
     assert _strided(lib, d=48) == E.ATTNJVP_EUNSUPPORTED
     assert _strided(lib, nkv=0, kv=(0, 1)) == E.ATTNJVP_EINVAL
     assert _strided(lib, kv=(250, 51)) == E.ATTNJVP_EINVAL

@@ -203,3 +203,9 @@ def test_default_workload_is_the_largest_single_gpu_config():
               key=lambda w: bench.attention_flops(inputs.WORKLOADS[w]))
     assert big == args.workload
     assert set(args.also.split(",")) == {"video_dit", "stress", "image_dit_1k"}
+
+
+def test_backward_executed_flops_count():
+    assert bench.backward_executed_flops_per_pair(128) == 14 * 128
+    # two CTAs per row tile at 256: S and dP formed twice in each pass
+    assert bench.backward_executed_flops_per_pair(256) == (2 * 8 + 4 + 2) * 256

@@ -55,6 +55,10 @@ CASES = [
     (1, 1, 700, 129, 64),      # cross-attention, fewer keys
     (2, 2, 333, 333, 32),      # small head dim (zero-padded to 64 on chip)
     (1, 1, 1, 5, 128),         # one query
+    # head dim 256: two CTAs per row tile, each with half of the gradient columns
+    (1, 2, 300, 300, 256),
+    (2, 1, 129, 700, 256),     # cross-attention, more keys
+    (1, 1, 517, 65, 256),      # fewer keys than one tile pair
 ]
 
 
@@ -177,7 +181,7 @@ def test_backward_is_reproducible(cuda_lib):
     assert all(torch.equal(x, y) for x, y in zip(a, b))
 
 
-@pytest.mark.parametrize("name", ["image_dit_1k", "video_dit", "stress", "long_video"])
+@pytest.mark.parametrize("name", ["image_dit_1k", "video_dit", "stress", "long_video", "head_dim_256"])
 def test_backward_full_size_sampled_rows(cuda_lib, name):
     # The workload as bench.py times it: every head launched, O and LSE from this
     # library's forward on the workload inputs, the seeded upstream gradient.

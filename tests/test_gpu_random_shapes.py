@@ -1,6 +1,7 @@
 """GPU: seeded random shapes through the forward and the backward, against the
 FP64 oracle.  A second seeded set draws the Q/K and the V head dims
-independently from {16, 32, 64, 128, 256} (forward only).
+independently from {16, 32, 64, 128, 256} (forward only); a third runs the
+backward at head dim 256.
 
 Batch, heads, query and key lengths (cross-attention included), head dims
 16/32/64/128, both memory layouts and softmax scales of 0.5 to 2 times
@@ -47,6 +48,19 @@ def _cases(n=16, seed=2026):
 CASES = _cases()
 
 
+def _cases_256(n=5, seed=2028):
+    """Seeded backward shapes at head dim 256 (two CTAs per row tile)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        B, H = int(rng.integers(1, 3)), int(rng.integers(1, 3))
+        nq = int(rng.integers(1, 500))
+        nkv = nq if rng.random() < 0.5 else int(rng.integers(1, 700))
+        scale = float(256 ** -0.5 * rng.uniform(0.5, 2.0))
+        out.append((50 + i, B, H, nq, nkv, 256, "bhsd", scale))
+    return out
+
+
 def _inputs(i, B, H, nq, nkv, d):
     xq = inputs.make_inputs(B, H, nq, d, seed=100 + i, device="cuda", qk="rms", tangent_scale=0.3)
     xk = inputs.make_inputs(B, H, nkv, d, seed=200 + i, device="cuda", qk="rms", tangent_scale=0.3)
@@ -77,7 +91,7 @@ def test_forward_random_shape(cuda_lib, case):
     assert np.max(np.abs(host64(lse) - ref[2])) <= 1e-3
 
 
-@pytest.mark.parametrize("case", CASES, ids=lambda c: "c%d-B%dH%d-q%d-k%d-d%d-%s" % c[:7])
+@pytest.mark.parametrize("case", CASES + _cases_256(), ids=lambda c: "c%d-B%dH%d-q%d-k%d-d%d-%s" % c[:7])
 def test_backward_random_shape(cuda_lib, case):
     i, B, H, nq, nkv, d, layout, scale = case
     x = _inputs(i, B, H, nq, nkv, d)
