@@ -251,3 +251,75 @@ def test_head_dim_256_long_sequence_sampled_rows(cuda_lib):
         assert bool(torch.isfinite(t).all())
     del x, got
     torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
+# degenerate cases of the method and the largest key counts
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_uniform_attention_when_queries_are_zero(cuda_lib, d):
+    """Q = 0 makes every score 0: P is uniform over the N keys, so O = mean(V),
+    LSE = ln N exactly, mu = mean_j St_ij = s q_t . mean(K) (q = 0), and
+    Ot = mean(Vt) + mean_j (St_ij - mu) v_j."""
+    x = inputs.make_inputs(1, 2, 777, d, seed=71, device="cuda", tangent_scale=0.5)
+    x["q"] = torch.zeros_like(x["q"])
+    got = _run(x)
+    _check_all(x, got)
+    N = x["q"].shape[2]
+    assert np.max(np.abs(host64(got[2]) - np.log(N))) <= 1e-5 * np.log(N)
+    o_ref = host64(x["v"]).mean(axis=2)
+    assert np.max(np.abs(host64(got[0]) - o_ref[:, :, None, :])) <= 1e-4 * np.abs(o_ref).max() + 1e-6
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_one_hot_softmax_from_huge_logits(cuda_lib, d):
+    """Queries scaled by 60: scores spread over hundreds of log units, so most rows'
+    softmax is one-hot up to underflow and the online rescale fires often.  Nothing
+    may overflow into inf or NaN; O, mu and LSE keep the usual tolerances.
+
+    Ot does not, and cannot: as on the page (section 前向: p and H~ are cast to the
+    value dtype before the dot products), P~ and H~ = P~ (.) St enter the value GEMMs
+    rounded to bf16 (unit roundoff u = 2^-8), and Ot = T / l - mu O.  In a one-hot row
+    |mu| is the dominant key's |St|, far above |Ot|, so the rounding of H~ and of P~
+    in O shows at its full size.  Each element of Ot is held to that arithmetic's
+    bound, u sum_j P_ij (|vt_jc| + (|St_ij| + |mu_i|) |v_jc|), from exact FP64
+    quantities, plus the usual 5e-2 RMS."""
+    x = inputs.make_inputs(1, 2, 640, d, seed=72, device="cuda", tangent_scale=0.2)
+    x["q"] = (x["q"].float() * 60.0).to(torch.bfloat16)
+    got = _run(x)
+    for t in got:
+        assert bool(torch.isfinite(t).all())
+    ref = oracle_on(x)
+    g = [gpu_rows(t, [0, 1]) for t in got]
+    assert_close(g[0], ref[0], "O")
+    assert_close(g[3], ref[3], "mu")
+    assert np.max(np.abs(g[2] - ref[2])) <= LSE_ABS
+    u = 2.0 ** -8
+    q, k, v, qt, kt, vt = (host64(x[n])[0] for n in ("q", "k", "v", "q_t", "k_t", "v_t"))
+    s = x["scale"]
+    S = s * np.einsum("hid,hjd->hij", q, k)
+    St = s * (np.einsum("hid,hjd->hij", qt, k) + np.einsum("hid,hjd->hij", q, kt))
+    P = np.exp(S - S.max(axis=2, keepdims=True))
+    P /= P.sum(axis=2, keepdims=True)
+    mu = np.einsum("hij,hij->hi", P, St)
+    bound = u * (np.einsum("hij,hjc->hic", P, np.abs(vt)) +
+                 np.einsum("hij,hjc->hic", P * (np.abs(St) + np.abs(mu)[:, :, None]), np.abs(v)))
+    rms = np.sqrt(np.mean(ref[1] ** 2))
+    excess = np.abs(g[1] - ref[1]) - (bound + 5e-2 * rms)
+    assert np.all(excess <= 0), "Ot: %.3e over the rounding bound" % excess.max()
+    print("one-hot d=%d: Ot max error / bound %.3f, rel-L2 %.3e" % (
+        d, float(np.max(np.abs(g[1] - ref[1]) / (bound + 5e-2 * rms))), rel_l2(g[1], ref[1])))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_quarter_million_keys_sampled_rows(cuda_lib, d):
+    """One head over 262144 keys (4096 key tiles per CTA, 2048 query tiles), the
+    longest sequence here: seeded sampled rows and the last rows against the oracle;
+    sums over every key of a row stay within the usual tolerances."""
+    N = 1 << 18
+    x = inputs.make_inputs(1, 1, N, d, seed=73, device="cuda", qk="rms", tangent_scale=0.3)
+    got = _run(x)
+    rows = np.unique(np.concatenate([inputs.sample_rows(N, 24, 74).numpy(), np.arange(N - 3, N)]))
+    _check_all(x, got, heads=[0], rows=rows)
+    del x, got
+    torch.cuda.empty_cache()
