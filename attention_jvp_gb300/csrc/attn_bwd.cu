@@ -86,6 +86,13 @@ struct BwdCfg {
   static constexpr int kChunkX = kBN * 128;        // one d-chunk of a streamed tile (bytes)
   static constexpr int kRBytes = kDC * kChunkR;
   static constexpr int kKStage = 2 * kDC * kChunkX;              // X1 chunks, X2 chunks
+  // Score ring units: normally a whole streamed tile; with room for one tile only
+  // (head dim 256) two units of half its d-chunks each, so that the next tile's
+  // first half loads while this tile's second half is in the score MMAs.
+  static constexpr int kUPT = (kKS == 1 && kDC % 2 == 0) ? 2 : 1;  // units per tile
+  static constexpr int kUC = kDC / kUPT;                           // d-chunks of X1 (and X2) per unit
+  static constexpr int kKU = kKS * kUPT;                           // units in the ring
+  static constexpr int kKUnit = 2 * kUC * kChunkX;                 // X1 chunks, then X2 chunks
   static constexpr int kVTensors = kDKDV ? 2 : 1;
   static constexpr int kVStage = kVTensors * kVC * kChunkX;      // dK/dV: dO, Q;  dQ: K (this CTA's columns)
   // dK/dV: the streamed queries' -LSE log2e and -D (64 + 64 floats) in a ring of
@@ -97,7 +104,7 @@ struct BwdCfg {
   static constexpr int kOffR1 = 0;
   static constexpr int kOffR2 = kRBytes;
   static constexpr int kOffK = 2 * kRBytes;
-  static constexpr int kOffV = kOffK + kKS * kKStage;
+  static constexpr int kOffV = kOffK + kKU * kKUnit;
   static constexpr int kOffVec = kOffV + kVS * kVStage;
   static constexpr int kOffBar = kOffVec + kVecRing;
   static constexpr int kBarBytes = 512;  // the Barriers block below
@@ -112,7 +119,8 @@ struct BwdCfg {
   static constexpr uint32_t kColSt = kColS + 64 * kNS;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kColSt + 64 * kNSt <= kTmemCols, "TMEM budget");
-  static_assert(kSBar <= 3 && kNSt <= 3 && kKS <= 3 && kVS <= 3 && kVecS <= 4, "barrier arrays");
+  static_assert(kSBar <= 3 && kNSt <= 3 && kKU <= 3 && kVS <= 3 && kVecS <= 4, "barrier arrays");
+  static_assert(kKU * kKUnit == kKS * kKStage, "score ring size");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static_assert(kKStage % 1024 == 0 && kVStage % 1024 == 0, "stage alignment (128-byte swizzle atoms)");
 };
@@ -296,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       uint64_t t0 = globaltimer_ns();
       uint32_t idle = 0;
-      while (tk < n_tiles || tv < n_tiles || tq < nq) {
+      while (tk < n_tiles * C::kUPT || tv < n_tiles || tq < nq) {
         bool progressed = false;
         if (tq < nq && mbar_test_wait(&bars->vec_empty[tq % C::kVecS], ((tq / C::kVecS) & 1) ^ 1)) {
           const int sq = tq % C::kVecS;
@@ -307,13 +315,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++tq;
           progressed = true;
         }
-        if (tk < n_tiles && mbar_test_wait(&bars->k_empty[tk % C::kKS], ((tk / C::kKS) & 1) ^ 1)) {
-          const int s = tk % C::kKS;
-          uint8_t* st = smem + C::kOffK + s * C::kKStage;
-          mbar_arrive_expect_tx(&bars->k_full[s], C::kKStage);
-          for (int c = 0; c < C::kDC; ++c) {
-            tma_load_4d(st + c * C::kChunkX, &maps.x1, &bars->k_full[s], c * 64, tk * C::kBN, hh, bb);
-            tma_load_4d(st + (C::kDC + c) * C::kChunkX, &maps.x2, &bars->k_full[s], c * 64, tk * C::kBN, hh, bb);
+        // tk counts score-ring units: unit u of streamed tile tk / kUPT
+        if (tk < n_tiles * C::kUPT && mbar_test_wait(&bars->k_empty[tk % C::kKU], ((tk / C::kKU) & 1) ^ 1)) {
+          const int s = tk % C::kKU;
+          const int row0 = (tk / C::kUPT) * C::kBN, u = tk % C::kUPT;
+          uint8_t* st = smem + C::kOffK + s * C::kKUnit;
+          mbar_arrive_expect_tx(&bars->k_full[s], C::kKUnit);
+          for (int c = 0; c < C::kUC; ++c) {
+            const int col = (u * C::kUC + c) * 64;
+            tma_load_4d(st + c * C::kChunkX, &maps.x1, &bars->k_full[s], col, row0, hh, bb);
+            tma_load_4d(st + (C::kUC + c) * C::kChunkX, &maps.x2, &bars->k_full[s], col, row0, hh, bb);
           }
           ++tk;
           progressed = true;
@@ -357,8 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // normal path too (another role may give up right after the last copy was issued).
       volatile int no_abort = 0;
       mbar_wait(&bars->r_full, 0, &no_abort, nullptr, 0);
-      for (int t = tk - C::kKS; t < tk; ++t)
-        if (t >= 0) mbar_wait(&bars->k_full[t % C::kKS], (t / C::kKS) & 1, &no_abort, nullptr, 0);
+      for (int n = tk - C::kKU; n < tk; ++n)
+        if (n >= 0) mbar_wait(&bars->k_full[n % C::kKU], (n / C::kKU) & 1, &no_abort, nullptr, 0);
       for (int t = tv - C::kVS; t < tv; ++t)
         if (t >= 0) mbar_wait(&bars->v_full[t % C::kVS], (t / C::kVS) & 1, &no_abort, nullptr, 0);
       for (int t = tq - C::kVecS; t < tq; ++t)
@@ -380,36 +391,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool first = warp == 3;
         const uint64_t dA = first ? dR1 : dR2;
         const uint32_t aT = tmem + (first ? C::kColR1 : C::kColR2);  // dQ pass: A in TMEM
-        const uint32_t xoff = first ? 0u : static_cast<uint32_t>(C::kDC * C::kChunkX);
+        const uint32_t xoff = first ? 0u : static_cast<uint32_t>(C::kUC * C::kChunkX);
         bool ok = C::kRTmem ? mbar_wait(&bars->r_tmem, 0, abort_flag, status, kStatusTimeout)
                             : mbar_wait(&bars->r_full, 0, abort_flag, status, kStatusTimeout);
         for (int t = 0; ok && t < n_tiles; ++t) {
-          const int s = t % C::kKS;
           const int b = first ? t % C::kNS : t % C::kNSt;
           const int bs = first ? t % C::kSBar : b;  // barrier slot
-          ok = mbar_wait(&bars->k_full[s], (t / C::kKS) & 1, abort_flag, status, kStatusTimeout);
-          // S1 buffers are free once the elementwise warps loaded tile t - NS; S2 buffers
-          // hold the packed operands of tile t - NSt until its value MMAs are done.
-          if (ok && first && t >= C::kNS)
-            ok = mbar_wait(&bars->s_free[(t - C::kNS) % C::kSBar], ((t - C::kNS) / C::kSBar) & 1, abort_flag,
-                           status, kStatusTimeout);
-          if (ok && !first && t >= C::kNSt)
-            ok = mbar_wait(&bars->pv_done[b], ((t - C::kNSt) / C::kNSt) & 1, abort_flag, status, kStatusTimeout);
-          if (!ok) break;
-          tc_fence_after_sync();
-          const uint64_t dX = off(dK0, s * C::kKStage + xoff);
           const uint32_t dst = tmem + (first ? C::kColS : C::kColSt) + 64u * b;
+#pragma unroll 1
+          for (int u = 0; u < C::kUPT; ++u) {
+            const int n = t * C::kUPT + u;
+            const int s = n % C::kKU;
+            ok = mbar_wait(&bars->k_full[s], (n / C::kKU) & 1, abort_flag, status, kStatusTimeout);
+            // S1 buffers are free once the elementwise warps loaded tile t - NS; S2 buffers
+            // hold the packed operands of tile t - NSt until its value MMAs are done.
+            if (ok && u == 0 && first && t >= C::kNS)
+              ok = mbar_wait(&bars->s_free[(t - C::kNS) % C::kSBar], ((t - C::kNS) / C::kSBar) & 1, abort_flag,
+                             status, kStatusTimeout);
+            if (ok && u == 0 && !first && t >= C::kNSt)
+              ok = mbar_wait(&bars->pv_done[b], ((t - C::kNSt) / C::kNSt) & 1, abort_flag, status,
+                             kStatusTimeout);
+            if (!ok) break;
+            tc_fence_after_sync();
+            const uint64_t dX = off(dK0, s * C::kKUnit + xoff);
 #pragma unroll
-          for (int c = 0; c < C::kDC; ++c)
+            for (int c = 0; c < C::kUC; ++c)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              if constexpr (C::kRTmem)
-                mma_ts(dst, aT + (c * 4 + kk) * 8, off(dX, c * C::kChunkX + kk * 32), kIdS, (c | kk) != 0);
-              else
-                mma_ss(dst, off(dA, c * C::kChunkR + kk * 32), off(dX, c * C::kChunkX + kk * 32), kIdS,
-                       (c | kk) != 0);
-            }
-          mma_commit(&bars->k_empty[s]);
+              for (int kk = 0; kk < 4; ++kk) {
+                const int cg = u * C::kUC + c;  // d-chunk of the resident operand
+                if constexpr (C::kRTmem)
+                  mma_ts(dst, aT + (cg * 4 + kk) * 8, off(dX, c * C::kChunkX + kk * 32), kIdS, (u | c | kk) != 0);
+                else
+                  mma_ss(dst, off(dA, cg * C::kChunkR + kk * 32), off(dX, c * C::kChunkX + kk * 32), kIdS,
+                         (u | c | kk) != 0);
+              }
+            mma_commit(&bars->k_empty[s]);
+          }
+          if (!ok) break;
           mma_commit(first ? &bars->s_full[bs] : &bars->st_full[b]);
         }
         uint64_t* drain = first ? &bars->drain_s : &bars->drain_st;

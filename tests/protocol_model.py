@@ -272,8 +272,9 @@ def bwd_config(D, dkdv):
     NS = 3 if free >= 192 else 1
     KS = 1 if D == 256 else (2 if D == 128 else 3)
     VS = (1 if dkdv else 2) if D == 256 else ((2 if dkdv else 3) if D == 128 else 3)
+    UPT = 2 if (KS == 1 and (D // 64) % 2 == 0) else 1  # score-ring units per streamed tile
     return dict(NS=NS, NSt=3, SBar=2 if NS == 1 else NS, KS=KS, VS=VS, VecS=2 if D == 256 else 4, dkdv=dkdv,
-                r_tmem=r_tmem)
+                r_tmem=r_tmem, UPT=UPT, KU=KS * UPT)
 
 
 class BwdModel(FwdModel):
@@ -293,14 +294,14 @@ class BwdModel(FwdModel):
         self.mutate = mutate
         B = lambda nm, cnt, k: [Bar("%s%d" % (nm, i), cnt) for i in range(k)]  # noqa: E731
         self.r_full, self.r_tmem = Bar("r_full", 1), Bar("r_tmem", 4)
-        self.k_full, self.k_empty = B("k_full", 1, c["KS"]), B("k_empty", 2, c["KS"])
+        self.k_full, self.k_empty = B("k_full", 1, c["KU"]), B("k_empty", 2, c["KU"])
         self.v_full, self.v_empty = B("v_full", 1, c["VS"]), B("v_empty", 1, c["VS"])
         self.vec_full, self.vec_empty = B("vec_full", 1, c["VecS"]), B("vec_empty", 4, c["VecS"])
         self.s_full, self.s_free = B("s_full", 1, c["SBar"]), B("s_free", 4, c["SBar"])
         self.st_full = B("st_full", 1, c["NSt"])
         self.p_full, self.pv_done = B("p_full", 4, c["NSt"]), B("pv_done", 1, c["NSt"])
         self.acc_done = Bar("acc_done", 1)
-        self.k_stage, self.k_readers = [None] * c["KS"], [0] * c["KS"]
+        self.k_stage, self.k_readers = [None] * c["KU"], [0] * c["KU"]  # (tile, unit) per ring unit
         self.v_stage, self.v_readers = [None] * c["VS"], [0] * c["VS"]
         self.vec_slot, self.vec_unread = [None] * c["VecS"], [0] * c["VecS"]
         self.s1_buf, self.s1_writer, self.s1_loaded = [None] * c["NS"], [0] * c["NS"], [None] * c["NS"]
@@ -325,7 +326,7 @@ class BwdModel(FwdModel):
         self.later("tma", self.r_full.arrive)
         tk = tv = tq = 0
         nq = self.n if c["dkdv"] else 0
-        while tk < self.n or tv < self.n or tq < nq:
+        while tk < self.n * c["UPT"] or tv < self.n or tq < nq:
             if tq < nq and self.test(self.vec_empty[tq % c["VecS"]], tq // c["VecS"] - 1):
                 s = tq % c["VecS"]
                 if self.vec_unread[s]:
@@ -337,13 +338,14 @@ class BwdModel(FwdModel):
                     self.vec_full[s].arrive()
                 self.later("tma", landq)
                 tq += 1
-            if tk < self.n and self.test(self.k_empty[tk % c["KS"]], tk // c["KS"] - 1):
-                s = tk % c["KS"]
+            # tk counts score-ring units: unit tk % UPT of tile tk // UPT
+            if tk < self.n * c["UPT"] and self.test(self.k_empty[tk % c["KU"]], tk // c["KU"] - 1):
+                s = tk % c["KU"]
                 if self.k_readers[s]:
-                    raise ProtocolError("score stage %d reloaded while an MMA reads it" % s)
+                    raise ProtocolError("score unit %d reloaded while an MMA reads it" % s)
 
-                def landk(s=s, t=tk):
-                    self.k_stage[s] = t
+                def landk(s=s, n=tk):
+                    self.k_stage[s] = divmod(n, c["UPT"])
                     self.k_full[s].arrive()
                 self.later("tma", landk)
                 tk += 1
@@ -366,32 +368,38 @@ class BwdModel(FwdModel):
         if c["r_tmem"] and not self.r_in_tmem:
             raise ProtocolError("score MMAs before the resident tiles are in TMEM")
         for t in range(self.n):
-            s = t % c["KS"]
             b = t % (c["NS"] if first else c["NSt"])
-            yield from self.wait(self.k_full[s], t // c["KS"])
-            if first and t >= c["NS"]:
-                tp = t - c["NS"]
-                yield from self.wait(self.s_free[tp % c["SBar"]], tp // c["SBar"])
-                if self.s1_loaded[b] != tp:
-                    raise ProtocolError("S1 buffer %d overwritten before tile %d was loaded" % (b, tp))
-            if not first and t >= c["NSt"]:
-                tp = t - c["NSt"]
-                yield from self.wait(self.pv_done[b], tp // c["NSt"])
-                if tp not in self.pv_landed:
-                    raise ProtocolError("S2 buffer %d overwritten before tile %d's value MMAs" % (b, tp))
-            if self.k_stage[s] != t:
-                raise ProtocolError("%s MMA of tile %d reads stage holding %s" % (name, t, self.k_stage[s]))
             writer = self.s1_writer if first else self.s2_writer
-            if writer[b] or (not first and self.s2_readers[b]):
-                raise ProtocolError("%s buffer %d overwritten while in use" % (name, b))
-            self.k_readers[s] += 1
-            writer[b] += 1
+            for u in range(c["UPT"]):
+                n = t * c["UPT"] + u
+                s = n % c["KU"]
+                yield from self.wait(self.k_full[s], n // c["KU"])
+                if u == 0 and first and t >= c["NS"]:
+                    tp = t - c["NS"]
+                    yield from self.wait(self.s_free[tp % c["SBar"]], tp // c["SBar"])
+                    if self.s1_loaded[b] != tp:
+                        raise ProtocolError("S1 buffer %d overwritten before tile %d was loaded" % (b, tp))
+                if u == 0 and not first and t >= c["NSt"]:
+                    tp = t - c["NSt"]
+                    yield from self.wait(self.pv_done[b], tp // c["NSt"])
+                    if tp not in self.pv_landed:
+                        raise ProtocolError("S2 buffer %d overwritten before tile %d's value MMAs" % (b, tp))
+                if self.k_stage[s] != (t, u):
+                    raise ProtocolError("%s MMA of tile %d unit %d reads a unit holding %s"
+                                        % (name, t, u, self.k_stage[s]))
+                if u == 0 and (writer[b] or (not first and self.s2_readers[b])):
+                    raise ProtocolError("%s buffer %d overwritten while in use" % (name, b))
+                self.k_readers[s] += 1
+                writer[b] += 1
 
-            def done(s=s, b=b, t=t, first=first, writer=writer):
-                self.k_readers[s] -= 1
-                writer[b] -= 1
+                def unit_done(s=s, b=b, writer=writer):
+                    self.k_readers[s] -= 1
+                    writer[b] -= 1
+                    self.k_empty[s].arrive()
+                self.later(name, unit_done)
+
+            def done(b=b, t=t, first=first):
                 (self.s1_buf if first else self.s2_buf)[b] = (name, t)
-                self.k_empty[s].arrive()
                 (self.s_full[t % c["SBar"]] if first else self.st_full[b]).arrive()
             self.later(name, done)
 
@@ -671,8 +679,8 @@ class AbortBwdModel(BwdModel):
             if tq < nq and self.test(self.vec_empty[tq % c["VecS"]], tq // c["VecS"] - 1):
                 self.later("tma", self.vec_full[tq % c["VecS"]].arrive)
                 tq += 1
-            if tk < self.n and self.test(self.k_empty[tk % c["KS"]], tk // c["KS"] - 1):
-                self.later("tma", self.k_full[tk % c["KS"]].arrive)
+            if tk < self.n * c["UPT"] and self.test(self.k_empty[tk % c["KU"]], tk // c["KU"] - 1):
+                self.later("tma", self.k_full[tk % c["KU"]].arrive)
                 tk += 1
             if tv < self.n and self.test(self.v_empty[tv % c["VS"]], tv // c["VS"] - 1):
                 self.later("tma", self.v_full[tv % c["VS"]].arrive)
@@ -680,7 +688,7 @@ class AbortBwdModel(BwdModel):
             yield
         # as in the kernel: the last copies are waited for whether or not this thread gave up
         yield from self.wait(self.r_full, 0)
-        for bars, n, k in ((self.k_full, tk, c["KS"]), (self.v_full, tv, c["VS"]),
+        for bars, n, k in ((self.k_full, tk, c["KU"]), (self.v_full, tv, c["VS"]),
                            (self.vec_full, tq, c["VecS"])):
             for t in range(max(0, n - k), n):
                 yield from self.wait(bars[t % k], t // k)
@@ -692,17 +700,21 @@ class AbortBwdModel(BwdModel):
         for t in range(self.n):
             if not ok:
                 break
-            s = t % c["KS"]
             b = t % (c["NS"] if first else c["NSt"])
-            ok = yield from self.wait_or_abort(self.k_full[s], t // c["KS"])
-            if ok and first and t >= c["NS"]:
-                tp = t - c["NS"]
-                ok = yield from self.wait_or_abort(self.s_free[tp % c["SBar"]], tp // c["SBar"])
-            if ok and not first and t >= c["NSt"]:
-                ok = yield from self.wait_or_abort(self.pv_done[b], (t - c["NSt"]) // c["NSt"])
+            for u in range(c["UPT"]):
+                n = t * c["UPT"] + u
+                s = n % c["KU"]
+                ok = yield from self.wait_or_abort(self.k_full[s], n // c["KU"])
+                if ok and u == 0 and first and t >= c["NS"]:
+                    tp = t - c["NS"]
+                    ok = yield from self.wait_or_abort(self.s_free[tp % c["SBar"]], tp // c["SBar"])
+                if ok and u == 0 and not first and t >= c["NSt"]:
+                    ok = yield from self.wait_or_abort(self.pv_done[b], (t - c["NSt"]) // c["NSt"])
+                if not ok:
+                    break
+                self.later(name, self.k_empty[s].arrive)
             if not ok:
                 break
-            self.later(name, self.k_empty[s].arrive)
             self.later(name, (self.s_full[t % c["SBar"]] if first else self.st_full[b]).arrive)
         self.later(name, self.drain[name].arrive)
         yield from self.wait(self.drain[name], 0)

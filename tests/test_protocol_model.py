@@ -99,7 +99,8 @@ template <int D, int DV> void fwd() {
 }
 template <int D, int M> void bwd() {
   using C = BwdCfg<D, M>;
-  printf("bwd %%d %%d %%d %%d %%d %%d %%d %%d\n", D, M, C::kNS, C::kNSt, C::kSBar, C::kKS, C::kVS, C::kVecS);
+  printf("bwd %%d %%d %%d %%d %%d %%d %%d %%d %%d %%d\n", D, M, C::kNS, C::kNSt, C::kSBar, C::kKS, C::kVS, C::kVecS,
+         C::kUPT, C::kKU);
 }
 int main() {
   fwd<64, 64>(); fwd<64, 128>(); fwd<64, 256>(); fwd<128, 64>(); fwd<128, 128>(); fwd<128, 256>();
@@ -136,7 +137,8 @@ def test_model_sizes_are_the_kernels_sizes(tmp_path):
             assert (want["NS"], want["NSt"], want["KS"], want["VS"], want["UPT"], want["KU"]) == tuple(v[2:]), line
         else:
             want = bwd_config(v[0], v[1] == 1)
-            assert (want["NS"], want["NSt"], want["SBar"], want["KS"], want["VS"], want["VecS"]) == tuple(v[2:]), line
+            assert (want["NS"], want["NSt"], want["SBar"], want["KS"], want["VS"], want["VecS"], want["UPT"],
+                    want["KU"]) == tuple(v[2:]), line
         seen += 1
     assert seen == 15
 
