@@ -359,11 +359,12 @@ def oracle_rows_for(spec, x_host_head, target_s, seed=0):
     return int(max(n0, min(N, target_s / max(t_row, 1e-9))))
 
 
-def oracle_sample(spec, x_host_head, n_rows, seed=0):
+def oracle_sample(spec, x_host_head, n_rows, seed=0, with_outputs=False):
     """Time the FP64 oracle on ``n_rows`` query rows of one head against all N keys.
 
     Returns (tflops, cores, rows, seconds); flops are the same 12 d per
-    (query, key) pair the GPU metric counts.
+    (query, key) pair the GPU metric counts.  With ``with_outputs`` also the
+    row indices and the oracle's (O, Ot, LSE, mu) at them.
     """
     import oracle
     from attention_jvp_gb300 import inputs
@@ -373,9 +374,27 @@ def oracle_sample(spec, x_host_head, n_rows, seed=0):
     N, d = spec["N"], spec["d"]
     rows = inputs.sample_rows(N, n_rows, seed + 1).numpy()
     t0 = time.perf_counter()
-    oracle.attn_jvp(q, k, v, qt, kt, vt, spec["scale"], rows=rows, nthreads=cores)
+    ref = oracle.attn_jvp(q, k, v, qt, kt, vt, spec["scale"], rows=rows, nthreads=cores)
     dt = time.perf_counter() - t0
-    return 12.0 * len(rows) * N * d / dt / 1e12, cores, len(rows), dt
+    res = (12.0 * len(rows) * N * d / dt / 1e12, cores, len(rows), dt)
+    return res + (rows, ref) if with_outputs else res
+
+
+def parity_on_rows(got, ref):
+    """Errors of the GPU outputs (O, Ot, LSE, mu of one head, as host FP64 arrays at
+    the sampled rows) against the oracle's: rel-L2 and max-abs / RMS(ref) for O, Ot and
+    mu, max-abs for LSE."""
+    import numpy as np
+    out = {}
+    for name, g, r in zip(("O", "Ot", "LSE", "mu"), got, ref):
+        g, r = np.asarray(g, dtype=np.float64), np.asarray(r, dtype=np.float64)
+        if name == "LSE":
+            out[name] = {"max_abs": float(np.max(np.abs(g - r)))}
+            continue
+        rms = float(np.sqrt(np.mean(r * r)))
+        out[name] = {"rel_l2": float(np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-300)),
+                     "max_abs_over_rms": float(np.max(np.abs(g - r)) / max(rms, 1e-300))}
+    return out
 
 
 def host_head(x, h=0):
@@ -771,10 +790,16 @@ def run_gpu(args):
     if rank == 0 and world == 1 and not args.skip_cpu:
         spec_s = dict(spec, scale=scale)
         xh = host_head(x)
-        tf, cores, nrows, dt = oracle_sample(spec_s, xh, oracle_rows_for(spec_s, xh, args.cpu_seconds))
+        tf, cores, nrows, dt, rows, ref = oracle_sample(spec_s, xh, oracle_rows_for(spec_s, xh, args.cpu_seconds),
+                                                        with_outputs=True)
+        # the last timed step's outputs of head 0 at the same rows
+        ridx = torch.as_tensor(rows, device=dev)
+        got = [t.reshape(B * H, N, *t.shape[3:])[0][ridx].to("cpu", torch.float64).numpy()
+               for t in (path.out, path.out_t, path.lse, path.mu)]
         cpu = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": "%d query rows of head 0 vs all %d keys (%.1f s FP64 on %d host threads)"
-                         % (nrows, N, dt, cores)}
+                         % (nrows, N, dt, cores),
+               "parity_of_the_timed_outputs": parity_on_rows(got, ref)}
 
     total_bytes = sum(x[n].numel() * x[n].element_size() for n in inputs.NAMES)
     launches = path.launches_per_step * args.steps

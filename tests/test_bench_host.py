@@ -209,3 +209,12 @@ def test_backward_executed_flops_count():
     assert bench.backward_executed_flops_per_pair(128) == 14 * 128
     # two CTAs per row tile at 256: S and dP formed twice in each pass
     assert bench.backward_executed_flops_per_pair(256) == (2 * 8 + 4 + 2) * 256
+
+
+def test_parity_on_rows_metrics():
+    import numpy as np
+    r = [np.ones((3, 4)), np.full((3, 4), 2.0), np.zeros(3), np.ones(3)]
+    g = [r[0] * 1.01, r[1], r[2] + 1e-4, r[3]]
+    p = bench.parity_on_rows(g, r)
+    assert abs(p["O"]["rel_l2"] - 0.01) < 1e-12 and abs(p["O"]["max_abs_over_rms"] - 0.01) < 1e-12
+    assert p["Ot"]["rel_l2"] == 0.0 and abs(p["LSE"]["max_abs"] - 1e-4) < 1e-12
