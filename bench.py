@@ -57,6 +57,8 @@ def parse_args(argv=None):
     p.add_argument("--also", default=DEFAULT_ALSO,
                    help="comma-separated workloads timed after the main one as device-only sub-records ('' = none)")
     p.add_argument("--sub-steps", type=int, default=10, help="timed steps of each sub-record workload")
+    p.add_argument("--sub-cpu-seconds", type=float, default=3.0,
+                   help="target CPU time of each sub-record workload's oracle sample")
     return p.parse_args(argv)
 
 
@@ -643,6 +645,23 @@ def kernel_report(path, workload, peaks, peak_src, clocks, sm_count):
     return roofline, others
 
 
+def cpu_baseline_leg(path, seconds, dev):
+    """The FP64 oracle on a bounded sample of ``path``'s workload (query rows of head 0
+    against all keys, about ``seconds`` of host time), timed, and compared with the
+    last timed step's outputs at the same rows."""
+    import torch
+    spec = dict(path.spec, scale=path.scale)
+    B, H, N = spec["B"], spec["H"], spec["N"]
+    xh = host_head(path.x)
+    tf, cores, nrows, dt, rows, ref = oracle_sample(spec, xh, oracle_rows_for(spec, xh, seconds), with_outputs=True)
+    ridx = torch.as_tensor(rows, device=dev)
+    got = [t.reshape(B * H, N, *t.shape[3:])[0][ridx].to("cpu", torch.float64).numpy()
+           for t in (path.out, path.out_t, path.lse, path.mu)]
+    return {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "%d query rows of head 0 vs all %d keys (%.1f s FP64 on %d host threads)" % (nrows, N, dt, cores),
+            "parity_of_the_timed_outputs": parity_on_rows(got, ref)}
+
+
 def sub_record(name, args, dev, stream, peaks, peak_src, sampler, sm_count):
     """Device-timed line of another workload (same step, same timing rules), for the
     JSON line's ``workloads`` object."""
@@ -659,6 +678,8 @@ def sub_record(name, args, dev, stream, peaks, peak_src, sampler, sm_count):
                       "kv_chunks": path.n_chunks},
            "roofline": roofline, "hbm_kernels": others, "clocks": clocks,
            "gpu_launches": path.launches_per_step * args.sub_steps}
+    if not args.skip_cpu:
+        rec["cpu_baseline"] = cpu_baseline_leg(path, args.sub_cpu_seconds, dev)
     del path
     torch.cuda.empty_cache()
     return rec
@@ -788,18 +809,7 @@ def run_gpu(args):
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only) ----
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu:
-        spec_s = dict(spec, scale=scale)
-        xh = host_head(x)
-        tf, cores, nrows, dt, rows, ref = oracle_sample(spec_s, xh, oracle_rows_for(spec_s, xh, args.cpu_seconds),
-                                                        with_outputs=True)
-        # the last timed step's outputs of head 0 at the same rows
-        ridx = torch.as_tensor(rows, device=dev)
-        got = [t.reshape(B * H, N, *t.shape[3:])[0][ridx].to("cpu", torch.float64).numpy()
-               for t in (path.out, path.out_t, path.lse, path.mu)]
-        cpu = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": "%d query rows of head 0 vs all %d keys (%.1f s FP64 on %d host threads)"
-                         % (nrows, N, dt, cores),
-               "parity_of_the_timed_outputs": parity_on_rows(got, ref)}
+        cpu = cpu_baseline_leg(path, args.cpu_seconds, dev)
 
     total_bytes = sum(x[n].numel() * x[n].element_size() for n in inputs.NAMES)
     launches = path.launches_per_step * args.steps

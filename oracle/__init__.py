@@ -19,7 +19,9 @@ The primal backward (dQ, dK, dV) follows section 反向 (backward).  The QK
 normalisation the student keeps (section 一致性模型) is the per-head RMSNorm of
 the page "Обслуживание Ideogram v4 менее чем за секунду" (dev48.org), section
 on fusing RMSNorm, y = x rsqrt(mean(x^2) + eps) weight; its tangent is the
-chain rule on that definition.
+chain rule on that definition.  ``attn_jvp_rounding_bound`` is the per-element
+error bound of the forward's two bf16 roundings (P~ and H~ before the value
+sums), written from the same definitions.
 
 Parity pins for every function here are in tests/test_*oracle.py; none is unpinned.
 """
@@ -316,3 +318,26 @@ def rmsnorm_jvp(x, xt, w, eps):
     if rc != 0:
         raise ValueError("oracle_rmsnorm_jvp failed (%d): rows with no norm or bad eps" % rc)
     return y, yt
+
+
+def attn_jvp_rounding_bound(q, k, v, qt, kt, vt, scale, rows=None, u=2.0 ** -8, block=256):
+    """Per-element bound on |Ot_kernel - Ot| for one head from the two roundings of the
+    page's streaming JVP (section 前向: p and H~ = p (.) t_s are cast to the value dtype
+    before the dot products): with P~ and H~ each off by at most a relative u,
+        |dOt_ic| <= u sum_j P_ij (|vt_jc| + (|St_ij| + |mu_i|) |v_jc|),
+    since Ot = T / l - mu O, T = sum P~ vt + sum H~ v and O = sum P~ v / l.  Plain numpy,
+    FP64, from the definitions (S, St, P, mu as in attn_jvp).  q, qt: [Nq, d];
+    k, kt: [Nk, d]; v, vt: [Nk, dv].  Returns [R, dv] for the query rows ``rows``."""
+    q, k, v, qt, kt, vt = (_f64(x) for x in (q, k, v, qt, kt, vt))
+    rows = np.arange(q.shape[0]) if rows is None else np.asarray(rows, dtype=np.int64)
+    av, avt = np.abs(v), np.abs(vt)
+    out = np.empty((len(rows), v.shape[1]))
+    for a in range(0, len(rows), block):
+        r = rows[a:a + block]
+        S = scale * (q[r] @ k.T)
+        St = scale * (qt[r] @ k.T + q[r] @ kt.T)
+        P = np.exp(S - S.max(axis=1, keepdims=True))
+        P /= P.sum(axis=1, keepdims=True)
+        mu = np.einsum("ij,ij->i", P, St)
+        out[a:a + len(r)] = u * (P @ avt + (P * (np.abs(St) + np.abs(mu)[:, None])) @ av)
+    return out

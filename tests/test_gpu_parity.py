@@ -294,16 +294,8 @@ def test_one_hot_softmax_from_huge_logits(cuda_lib, d):
     assert_close(g[0], ref[0], "O")
     assert_close(g[3], ref[3], "mu")
     assert np.max(np.abs(g[2] - ref[2])) <= LSE_ABS
-    u = 2.0 ** -8
-    q, k, v, qt, kt, vt = (host64(x[n])[0] for n in ("q", "k", "v", "q_t", "k_t", "v_t"))
-    s = x["scale"]
-    S = s * np.einsum("hid,hjd->hij", q, k)
-    St = s * (np.einsum("hid,hjd->hij", qt, k) + np.einsum("hid,hjd->hij", q, kt))
-    P = np.exp(S - S.max(axis=2, keepdims=True))
-    P /= P.sum(axis=2, keepdims=True)
-    mu = np.einsum("hij,hij->hi", P, St)
-    bound = u * (np.einsum("hij,hjc->hic", P, np.abs(vt)) +
-                 np.einsum("hij,hjc->hic", P * (np.abs(St) + np.abs(mu)[:, :, None]), np.abs(v)))
+    heads = [host64(x[n])[0] for n in ("q", "k", "v", "q_t", "k_t", "v_t")]
+    bound = np.stack([oracle.attn_jvp_rounding_bound(*(t[h] for t in heads), x["scale"]) for h in range(2)])
     rms = np.sqrt(np.mean(ref[1] ** 2))
     excess = np.abs(g[1] - ref[1]) - (bound + 5e-2 * rms)
     assert np.all(excess <= 0), "Ot: %.3e over the rounding bound" % excess.max()

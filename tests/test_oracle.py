@@ -253,3 +253,29 @@ def test_outlier_recipe_adds_exact_logit():
     assert torch.all(k[..., 0][out] * s == 12.0)
     assert torch.all(q[..., 0] == 1.0)
     assert torch.all(x["q_t"][..., 0] == 0) and torch.all(x["k_t"][..., 0] == 0)
+
+
+def test_rounding_bound_covers_a_model_with_exactly_those_roundings():
+    """The per-element Ot bound of oracle.attn_jvp_rounding_bound holds for an FP64 model
+    that rounds P~ and H~ = P~ St to bf16 (unit roundoff 2^-8) before the value sums, on
+    rows from diffuse to one-hot, and is not vacuous (the model's error reaches a fair
+    share of it somewhere)."""
+    import torch
+    rng = np.random.default_rng(11)
+    N, d = 300, 32
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16).double().numpy()
+    for qs in (1.0, 8.0, 40.0):
+        q, k, v = rng.standard_normal((N, d)) * qs, rng.standard_normal((N, d)), rng.standard_normal((N, d))
+        qt, kt, vt = (rng.standard_normal((N, d)) * 0.3 for _ in range(3))
+        s = d ** -0.5
+        ref = oracle.attn_jvp(q, k, v, qt, kt, vt, s)[1]
+        S, St = s * q @ k.T, s * (qt @ k.T + q @ kt.T)
+        Pt = np.exp(S - S.max(axis=1, keepdims=True))
+        l = Pt.sum(axis=1, keepdims=True)
+        O = bf(Pt) @ v / l
+        T = (bf(Pt) @ vt + bf(Pt * St) @ v) / l
+        model = T - ((Pt * St).sum(axis=1, keepdims=True) / l) * O
+        bound = oracle.attn_jvp_rounding_bound(q, k, v, qt, kt, vt, s)
+        ratio = np.abs(model - ref) / bound
+        assert ratio.max() <= 1.0, (qs, ratio.max())
+        assert ratio.max() >= 0.05, (qs, ratio.max())
