@@ -20,8 +20,10 @@
 // At head dim 256 two CTAs share each resident tile, each accumulating half of
 // the gradient columns (the fp32 dK and dV of 128 keys would fill TMEM); both
 // form the full 256-deep scores.
-// Warps: 0 TMA (resident tiles, then the score ring, the value ring and, in the
-// dK/dV pass, the per-query vector ring, each refilled as soon as it frees),
+// Warps: 0 TMA (resident tiles, then the ring of streamed tiles, which up to
+// head dim 128 feeds both the score and the value MMAs, the value ring of its
+// own at 256 and, in the dK/dV pass, the per-query vector ring, each refilled
+// as soon as it frees),
 // 1 TMEM + value MMAs, 2 S2 MMAs, 3 S1 MMAs, and two groups of
 // elementwise warps (thread = resident row = TMEM lane): 4-7 take the even
 // tiles, 8-11 the odd ones.  One group's per-tile chain (barrier waits, TMEM
@@ -78,10 +80,18 @@ struct BwdCfg {
   // finished tile j + 1, so tile j's phase (issued earlier by the same thread)
   // is complete.
   static constexpr int kSBar = kNS == 1 ? 2 : kNS;
-  // Ring stages: at 256 the resident tiles take 128 KB of shared memory, which
-  // leaves one score stage and one (dK/dV) or two (dQ) value stages.
-  static constexpr int kKS = D == 256 ? 1 : (D == 128 ? 2 : 3);  // score-tile ring stages
-  static constexpr int kVS = D == 256 ? (kDKDV ? 1 : 2) : (D == 128 ? (kDKDV ? 2 : 3) : 3);  // value ring
+  // Up to head dim 128 one ring serves both MMA kinds: the value MMAs take their
+  // B operands (dK/dV pass: dO and Q; dQ pass: K) from the same stage as the
+  // score MMAs, which then stays until the value MMAs of its tile are done.  A
+  // second ring would load every streamed tile twice, and shared memory is what
+  // bounds the 64-wide score MMAs (their operands, the value MMAs' B operands
+  // and the TMA writes all go through it).
+  // At 256 the resident tiles take 128 KB of shared memory, which leaves one
+  // score stage and a value ring of its own with one (dK/dV) or two (dQ) stages
+  // of this CTA's gradient columns only.
+  static constexpr bool kShared = D <= 128;
+  static constexpr int kKS = D == 256 ? 1 : (D == 128 ? 4 : 6);  // score-tile ring stages
+  static constexpr int kVS = kShared ? 1 : (kDKDV ? 1 : 2);        // own value ring (head dim 256)
   static constexpr int kChunkR = kBM * 128;        // one d-chunk of a resident tile (bytes)
   static constexpr int kChunkX = kBN * 128;        // one d-chunk of a streamed tile (bytes)
   static constexpr int kRBytes = kDC * kChunkR;
@@ -105,7 +115,7 @@ struct BwdCfg {
   static constexpr int kOffR2 = kRBytes;
   static constexpr int kOffK = 2 * kRBytes;
   static constexpr int kOffV = kOffK + kKU * kKUnit;
-  static constexpr int kOffVec = kOffV + kVS * kVStage;
+  static constexpr int kOffVec = kOffV + (kShared ? 0 : kVS * kVStage);
   static constexpr int kOffBar = kOffVec + kVecRing;
   static constexpr int kBarBytes = 512;  // the Barriers block below
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
@@ -119,13 +129,23 @@ struct BwdCfg {
   static constexpr uint32_t kColSt = kColS + 64 * kNS;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kColSt + 64 * kNSt <= kTmemCols, "TMEM budget");
-  static_assert(kSBar <= 3 && kNSt <= 3 && kKU <= 3 && kVS <= 3 && kVecS <= 4, "barrier arrays");
+  static_assert(kSBar <= 3 && kNSt <= 3 && kKU <= 6 && kVS <= 3 && kVecS <= 4, "barrier arrays");
+  static_assert(!kShared || (kUPT == 1 && kVC == kDC), "a shared stage holds whole tiles of every column");
   static_assert(kKU * kKUnit == kKS * kKStage, "score ring size");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static_assert(kKStage % 1024 == 0 && kVStage % 1024 == 0, "stage alignment (128-byte swizzle atoms)");
 };
 
 constexpr int kThreads = 384;  // 12 warps
+// Registers per thread after the split at the start of the kernel: the TMA and
+// MMA warpgroup gives up what the elementwise warpgroups take.  The block's pool
+// is its threads x the registers per thread it was launched with (the launch
+// bounds allow 168), and ``setmaxnreg.inc`` waits until the pool has room, so
+// the launch checks that the compiled count leaves enough.
+constexpr int kRegsIssue = 88;
+constexpr int kRegsElem = 208;
+constexpr int kRegPoolNeeded = 128 * kRegsIssue + 256 * kRegsElem;
+static_assert(kRegPoolNeeded <= kThreads * 168, "register split above the launch pool");
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct BwdMaps {
@@ -146,7 +166,7 @@ struct BwdGeom {
 
 struct Barriers {
   uint64_t r_full;
-  uint64_t k_full[3], k_empty[3];
+  uint64_t k_full[6], k_empty[6];
   uint64_t v_full[3], v_empty[3];
   uint64_t vec_full[4], vec_empty[4];
   uint64_t s_full[3], st_full[3], s_free[3], p_full[3], pv_done[3];
@@ -194,35 +214,39 @@ __device__ __forceinline__ void bwd_tile(uint32_t (&raw)[128], uint32_t cSt, int
   }
   auto f = [&](int i) { return __uint_as_float(raw[i]); };
   const uint64_t c2x2 = f2_pack(c2, c2);
-  uint32_t pk[32], dk[32];
-  auto step = [&](int i, uint64_t nl, uint64_t nd) {
+  auto step = [&](int i, uint64_t nl, uint64_t nd, uint32_t& pw, uint32_t& dw) {
     float x0, x1;
     f2_unpack(f2_fma(f2_pack(f(i), f(i + 1)), c2x2, nl), x0, x1);
     const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
     float d0, d1;
     f2_unpack(f2_mul(f2_pack(p0, p1), f2_add(f2_pack(f(64 + i), f(65 + i)), nd)), d0, d1);
-    if (kMode == kModeDKDV) pk[i >> 1] = pack_bf16x2(p0, p1);
-    dk[i >> 1] = pack_bf16x2(d0, d1);
+    if (kMode == kModeDKDV) pw = pack_bf16x2(p0, p1);
+    dw = pack_bf16x2(d0, d1);
   };
+  if (kMode == kModeDQ) {
+    uint32_t pk[32], dk[32];
+    const uint64_t nl = f2_pack(row_nl2, row_nl2), nd = f2_pack(row_nd, row_nd);
 #pragma unroll
-  for (int i = 0; i < 64; i += 4) {
-    if (kMode == kModeDQ) {
-      const uint64_t nl = f2_pack(row_nl2, row_nl2), nd = f2_pack(row_nd, row_nd);
-      step(i, nl, nd);
-      step(i + 2, nl, nd);
-    } else {
-      // 16-byte broadcast reads (the vector slots are 512-byte aligned)
-      const float4 a = *reinterpret_cast<const float4*>(col_nl2 + i);
-      const float4 b = *reinterpret_cast<const float4*>(col_nd + i);
-      step(i, f2_pack(a.x, a.y), f2_pack(b.x, b.y));
-      step(i + 2, f2_pack(a.z, a.w), f2_pack(b.z, b.w));
-    }
-  }
-  if (kMode == kModeDKDV) {
-    tmem_st32(cSt, pk);
-    tmem_st32(cSt + 32, dk);
-  } else {
+    for (int i = 0; i < 64; i += 2) step(i, nl, nd, pk[i >> 1], dk[i >> 1]);
     tmem_st32(cSt, dk);
+  } else {
+    // Two halves of 32 columns, each stored as soon as it is packed, so that the
+    // packed words of the first half are not live across the second.
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t pk[16], dk[16];
+#pragma unroll
+      for (int i = 32 * h; i < 32 * h + 32; i += 4) {
+        // 16-byte broadcast reads (the vector slots are 512-byte aligned)
+        const float4 a = *reinterpret_cast<const float4*>(col_nl2 + i);
+        const float4 b = *reinterpret_cast<const float4*>(col_nd + i);
+        const int w = (i - 32 * h) >> 1;
+        step(i, f2_pack(a.x, a.y), f2_pack(b.x, b.y), pk[w], dk[w]);
+        step(i + 2, f2_pack(a.z, a.w), f2_pack(b.z, b.w), pk[w + 1], dk[w + 1]);
+      }
+      tmem_st16(cSt + 16 * h, pk);
+      tmem_st16(cSt + 32 + 16 * h, dk);
+    }
   }
   tmem_wait_st();
   tc_fence_before_sync();
@@ -254,9 +278,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->r_full, 1);
-    for (int s = 0; s < 3; ++s) {
+    for (int s = 0; s < 6; ++s) {
       mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_empty[s], 2);  // one commit from each score issuer
+      // one commit from each score issuer, and one from the value issuer when
+      // its B operands come from the same stage
+      mbar_init(&bars->k_empty[s], C::kShared ? 3 : 2);
+    }
+    for (int s = 0; s < 3; ++s) {
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
       mbar_init(&bars->s_full[s], 1);
@@ -285,6 +313,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
 
+  // Registers: the TMA and MMA warps need few, the elementwise warps hold a
+  // whole tile of scores per thread (fewer spills; about 1 % faster).
+  if (warp < 4)
+    setmaxnreg_dec<kRegsIssue>();
+  else
+    setmaxnreg_inc<kRegsElem>();
+
   if (warp == 0) {
     // ---------------- TMA producer: resident tiles, then the score-tile ring (X1, X2) and
     // the value-tile ring, each refilled as soon as its own stage is free (the thread polls
@@ -301,10 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int tk = 0, tv = 0, tq = 0;  // next tile of each ring (tq: the vector ring)
       const int nq = C::kDKDV ? n_tiles : 0;
+      const int nv = C::kShared ? 0 : n_tiles;  // tiles of the value ring of its own
       bool ok = true;
       uint64_t t0 = globaltimer_ns();
       uint32_t idle = 0;
-      while (tk < n_tiles * C::kUPT || tv < n_tiles || tq < nq) {
+      while (tk < n_tiles * C::kUPT || tv < nv || tq < nq) {
         bool progressed = false;
         if (tq < nq && mbar_test_wait(&bars->vec_empty[tq % C::kVecS], ((tq / C::kVecS) & 1) ^ 1)) {
           const int sq = tq % C::kVecS;
@@ -329,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++tk;
           progressed = true;
         }
-        if (tv < n_tiles && mbar_test_wait(&bars->v_empty[tv % C::kVS], ((tv / C::kVS) & 1) ^ 1)) {
+        if (tv < nv && mbar_test_wait(&bars->v_empty[tv % C::kVS], ((tv / C::kVS) & 1) ^ 1)) {
           const int sv = tv % C::kVS;
           const int row0 = tv * C::kBN;
           uint8_t* vt = smem + C::kOffV + sv * C::kVStage;
@@ -383,7 +419,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dR1 = make_smem_desc_sw128(smem_u32(smem + C::kOffR1), 16, 1024);
       const uint64_t dR2 = make_smem_desc_sw128(smem_u32(smem + C::kOffR2), 16, 1024);
       const uint64_t dK0 = make_smem_desc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
-      const uint64_t dV0 = make_smem_desc_sw128(smem_u32(smem + C::kOffV), C::kChunkX, 1024);
+      // B operands of the value MMAs: a stage of the shared ring (X1 chunks, then X2
+      // chunks) or of the value ring of its own
+      const uint64_t dV0 =
+          make_smem_desc_sw128(smem_u32(smem + (C::kShared ? C::kOffK : C::kOffV)), C::kChunkX, 1024);
       auto off = [](uint64_t desc, uint32_t bytes) { return desc + static_cast<uint64_t>(bytes >> 4); };
       volatile int no_abort = 0;
       if (warp == 3 || warp == 2) {
@@ -437,25 +476,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int j = 0; ok && j < n_tiles; ++j) {
           const int bt = j % C::kNSt;
-          const int s = j % C::kVS;
+          const int s = j % (C::kShared ? C::kKS : C::kVS);
+          const uint32_t sphase = (j / (C::kShared ? C::kKS : C::kVS)) & 1;
           ok = mbar_wait(&bars->p_full[bt], (j / C::kNSt) & 1, abort_flag, status, kStatusTimeout) &&
-               mbar_wait(&bars->v_full[s], (j / C::kVS) & 1, abort_flag, status, kStatusTimeout);
+               mbar_wait(C::kShared ? &bars->k_full[s] : &bars->v_full[s], sphase, abort_flag, status,
+                         kStatusTimeout);
           if (!ok) break;
           tc_fence_after_sync();
-          const uint64_t dV = off(dV0, s * C::kVStage);
+          // dK/dV pass: dO, then Q (shared stage: X2 = dO after X1 = Q).  dQ pass: K (X1).
+          const uint64_t dV = off(dV0, C::kShared ? s * C::kKUnit : s * C::kVStage);
+          const uint32_t dO_off = C::kShared ? C::kUC * C::kChunkX : 0;
+          const uint32_t q_off = C::kShared ? 0 : C::kVC * C::kChunkX;
           const uint32_t a0 = tmem + C::kColSt + 64u * bt;  // dQ: dS;  dK/dV: P^T (then dS^T at +32)
 #pragma unroll
           for (int kk = 0; kk < C::kBN / 16; ++kk) {
             const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
             if (C::kDKDV) {
-              mma_ts(tmem + C::kColAcc1, a0 + kk * 8, off(dV, kk * 2048), kIdPV, acc);  // dV += P^T dO
-              mma_ts(tmem + C::kColAcc2, a0 + 32 + kk * 8, off(dV, C::kVC * C::kChunkX + kk * 2048), kIdPV,
+              mma_ts(tmem + C::kColAcc1, a0 + kk * 8, off(dV, dO_off + kk * 2048), kIdPV, acc);  // dV += P^T dO
+              mma_ts(tmem + C::kColAcc2, a0 + 32 + kk * 8, off(dV, q_off + kk * 2048), kIdPV,
                      acc);  // dK += dS^T Q
             } else {
               mma_ts(tmem + C::kColAcc1, a0 + kk * 8, off(dV, kk * 2048), kIdPV, acc);  // dQ += dS K
             }
           }
-          mma_commit(&bars->v_empty[s]);
+          mma_commit(C::kShared ? &bars->k_empty[s] : &bars->v_empty[s]);
           mma_commit(&bars->pv_done[bt]);
         }
         if (ok) mma_commit(&bars->acc_done);
@@ -481,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (C::kRTmem && group == 0) {
       // Rows of Q and dO (128-byte-swizzled d-chunks: 16-byte unit u of row r at
       // unit u ^ (r mod 8)) into this thread's TMEM lane.
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->r_full, 0, abort_flag, status, kStatusTimeout));
+      ok = __all_sync(0xffffffffu, mbar_wait<1>(&bars->r_full, 0, abort_flag, status, kStatusTimeout));
       if (ok) {
 #pragma unroll 1
         for (int m = 0; m < 2 * C::kDC; ++m) {
@@ -507,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int bt = j % C::kNSt;
       // S1 first, and its buffer released at once: the S1 ring is the short one,
       // and the next tile's S1 MMAs wait for it.
-      ok = mbar_wait(&bars->s_full[bs], (j / C::kSBar) & 1, abort_flag, status, kStatusTimeout);
+      ok = mbar_wait<1>(&bars->s_full[bs], (j / C::kSBar) & 1, abort_flag, status, kStatusTimeout);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after_sync();
@@ -516,11 +560,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->s_free[bs]);
-      ok = mbar_wait(&bars->st_full[bt], (j / C::kNSt) & 1, abort_flag, status, kStatusTimeout);
+      ok = mbar_wait<1>(&bars->st_full[bt], (j / C::kNSt) & 1, abort_flag, status, kStatusTimeout);
       // dK/dV pass: the streamed queries' vectors
       const int sq = j % C::kVecS;
       if (C::kDKDV && ok)
-        ok = mbar_wait(&bars->vec_full[sq], (j / C::kVecS) & 1, abort_flag, status, kStatusTimeout);
+        ok = mbar_wait<1>(&bars->vec_full[sq], (j / C::kVecS) & 1, abort_flag, status, kStatusTimeout);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after_sync();
@@ -539,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // ---------------- epilogue ----------------
-    if (ok) ok = mbar_wait(&bars->acc_done, 0, abort_flag, status, kStatusTimeout);
+    if (ok) ok = mbar_wait<1>(&bars->acc_done, 0, abort_flag, status, kStatusTimeout);
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       tc_fence_after_sync();
@@ -669,6 +713,14 @@ cudaError_t launch_pass(const BwdArgs& a, const float* nl2, const float* nd, con
     if (e != cudaSuccess) {
       *msg = "cudaFuncSetAttribute(max dynamic shared memory) failed";
       return e;
+    }
+    // The warpgroups' register split must fit the pool the block launches with
+    // (see kRegsIssue); a smaller compiled count would leave setmaxnreg.inc waiting.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess || fa.numRegs * kThreads < kRegPoolNeeded) {
+      *msg = "backward kernel compiled with fewer registers than its warpgroup split needs";
+      return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
     }
     attr_set = true;
   }

@@ -106,6 +106,11 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;
 // out-of-line function.  Inlined at each of the kernels' twenty-odd wait sites,
 // it made up a third of the fused kernel's machine code, and that kernel's
 // speed falls off a cliff a little above 52 KB (instruction fetch).
+//
+// kRegion: one copy of the out-of-line loop per register budget.  A kernel that
+// moves registers between its warpgroups (setmaxnreg) calls a separate copy
+// from each side, since one function body is compiled for one register count.
+template <int kRegion = 0>
 static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                                    int* status, int code, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
@@ -122,11 +127,27 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
   }
 }
 
+template <int kRegion = 0>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           int* status, int code, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_test_wait(bar, parity)) return true;  // phase already complete
   if (mbar_try_wait(bar, parity)) return true;   // one suspended wait
-  return mbar_wait_slow(bar, parity, abort_flag, status, code, limit_ns);
+  return mbar_wait_slow<kRegion>(bar, parity, abort_flag, status, code, limit_ns);
+}
+
+// Per-warp register budget changes (all four warps of a warpgroup execute the
+// same one).  ``inc`` blocks until enough registers are free in the block's
+// pool (its threads x registers per thread at launch), so the counts of all
+// warpgroups must add up to at most that pool.
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  static_assert(kRegs % 8 == 0 && kRegs >= 24 && kRegs <= 256, "setmaxnreg count");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  static_assert(kRegs % 8 == 0 && kRegs >= 24 && kRegs <= 256, "setmaxnreg count");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
 
 // ---------------------------------------------------------------------------

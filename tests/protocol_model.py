@@ -270,19 +270,25 @@ def bwd_config(D, dkdv):
     r_tmem = (not dkdv) and D <= 128
     free = 512 - (2 if dkdv else 1) * DV - (D if r_tmem else 0) - 64 * 3
     NS = 3 if free >= 192 else 1
-    KS = 1 if D == 256 else (2 if D == 128 else 3)
-    VS = (1 if dkdv else 2) if D == 256 else ((2 if dkdv else 3) if D == 128 else 3)
+    # up to 128 the value MMAs read their B operands from the score ring's stage
+    shared = D <= 128
+    KS = 1 if D == 256 else (4 if D == 128 else 6)
+    VS = 1 if shared else (1 if dkdv else 2)
     UPT = 2 if (KS == 1 and (D // 64) % 2 == 0) else 1  # score-ring units per streamed tile
     return dict(NS=NS, NSt=3, SBar=2 if NS == 1 else NS, KS=KS, VS=VS, VecS=2 if D == 256 else 4, dkdv=dkdv,
-                r_tmem=r_tmem, UPT=UPT, KU=KS * UPT)
+                r_tmem=r_tmem, UPT=UPT, KU=KS * UPT, shared=shared)
 
 
 class BwdModel(FwdModel):
     """One CTA of a backward pass: a TMA thread polling the score, value and (dK/dV
     pass) per-query vector rings; S1, S2 and value-MMA issuers; two groups of four
     elementwise warps taking even and odd tiles.  In the dQ pass group 0 first
-    copies the resident tiles into TMEM for the score MMAs.  ``mutate``:
-    "one_s1_slot" gives the S1 barriers a single slot (two groups on one slot)."""
+    copies the resident tiles into TMEM for the score MMAs.  Up to head dim 128
+    (``shared``) the value MMAs take their B operands from the score ring's stage of
+    the same tile, which the value issuer releases as a third arrival on k_empty.
+    ``mutate``: "one_s1_slot" gives the S1 barriers a single slot (two groups on one
+    slot); "shared_stage_two_arrivals" leaves the value issuer's release out of the
+    shared stage's count."""
 
     def __init__(self, cfg, n_tiles, seed, mutate=None):
         self.c = dict(cfg)
@@ -294,7 +300,8 @@ class BwdModel(FwdModel):
         self.mutate = mutate
         B = lambda nm, cnt, k: [Bar("%s%d" % (nm, i), cnt) for i in range(k)]  # noqa: E731
         self.r_full, self.r_tmem = Bar("r_full", 1), Bar("r_tmem", 4)
-        self.k_full, self.k_empty = B("k_full", 1, c["KU"]), B("k_empty", 2, c["KU"])
+        self.k_full = B("k_full", 1, c["KU"])
+        self.k_empty = B("k_empty", 3 if c["shared"] and mutate != "shared_stage_two_arrivals" else 2, c["KU"])
         self.v_full, self.v_empty = B("v_full", 1, c["VS"]), B("v_empty", 1, c["VS"])
         self.vec_full, self.vec_empty = B("vec_full", 1, c["VecS"]), B("vec_empty", 4, c["VecS"])
         self.s_full, self.s_free = B("s_full", 1, c["SBar"]), B("s_free", 4, c["SBar"])
@@ -326,7 +333,8 @@ class BwdModel(FwdModel):
         self.later("tma", self.r_full.arrive)
         tk = tv = tq = 0
         nq = self.n if c["dkdv"] else 0
-        while tk < self.n * c["UPT"] or tv < self.n or tq < nq:
+        nv = 0 if c["shared"] else self.n
+        while tk < self.n * c["UPT"] or tv < nv or tq < nq:
             if tq < nq and self.test(self.vec_empty[tq % c["VecS"]], tq // c["VecS"] - 1):
                 s = tq % c["VecS"]
                 if self.vec_unread[s]:
@@ -349,7 +357,7 @@ class BwdModel(FwdModel):
                     self.k_full[s].arrive()
                 self.later("tma", landk)
                 tk += 1
-            if tv < self.n and self.test(self.v_empty[tv % c["VS"]], tv // c["VS"] - 1):
+            if tv < nv and self.test(self.v_empty[tv % c["VS"]], tv // c["VS"] - 1):
                 s = tv % c["VS"]
                 if self.v_readers[s]:
                     raise ProtocolError("value stage %d reloaded while an MMA reads it" % s)
@@ -405,22 +413,30 @@ class BwdModel(FwdModel):
 
     def value_issuer(self):
         c = self.c
+        sh = c["shared"]
         for j in range(self.n):
-            b, s = j % c["NSt"], j % c["VS"]
+            b, s = j % c["NSt"], j % (c["KU"] if sh else c["VS"])
             yield from self.wait(self.p_full[b], j // c["NSt"])
-            yield from self.wait(self.v_full[s], j // c["VS"])
-            if self.s2_buf[b] != ("P", j) or self.v_stage[s] != j:
-                raise ProtocolError("value MMAs of tile %d read %s and stage %s" % (j, self.s2_buf[b], self.v_stage[s]))
+            if sh:
+                yield from self.wait(self.k_full[s], j // c["KU"])
+                stage, readers, empty = self.k_stage[s], self.k_readers, self.k_empty
+                ok = stage == (j, 0)
+            else:
+                yield from self.wait(self.v_full[s], j // c["VS"])
+                stage, readers, empty = self.v_stage[s], self.v_readers, self.v_empty
+                ok = stage == j
+            if self.s2_buf[b] != ("P", j) or not ok:
+                raise ProtocolError("value MMAs of tile %d read %s and stage %s" % (j, self.s2_buf[b], stage))
             self.s2_readers[b] += 1
-            self.v_readers[s] += 1
+            readers[s] += 1
             self.pv_in_flight += 1
 
-            def done(b=b, s=s, j=j):
+            def done(b=b, s=s, j=j, readers=readers, empty=empty):
                 self.s2_readers[b] -= 1
-                self.v_readers[s] -= 1
+                readers[s] -= 1
                 self.pv_in_flight -= 1
                 self.pv_landed.append(j)
-                self.v_empty[s].arrive()
+                empty[s].arrive()
                 self.pv_done[b].arrive()
             self.later("PV", done)
         self.later("PV", self.acc_done.arrive)
@@ -671,8 +687,9 @@ class AbortBwdModel(BwdModel):
         self.later("tma", self.r_full.arrive)
         tk = tv = tq = 0
         nq = self.n if c["dkdv"] else 0
+        nv = 0 if c["shared"] else self.n
         ok = True
-        while tk < self.n or tv < self.n or tq < nq:
+        while tk < self.n * c["UPT"] or tv < nv or tq < nq:
             if self.aborted:
                 ok = False
                 break
@@ -682,7 +699,7 @@ class AbortBwdModel(BwdModel):
             if tk < self.n * c["UPT"] and self.test(self.k_empty[tk % c["KU"]], tk // c["KU"] - 1):
                 self.later("tma", self.k_full[tk % c["KU"]].arrive)
                 tk += 1
-            if tv < self.n and self.test(self.v_empty[tv % c["VS"]], tv // c["VS"] - 1):
+            if tv < nv and self.test(self.v_empty[tv % c["VS"]], tv // c["VS"] - 1):
                 self.later("tma", self.v_full[tv % c["VS"]].arrive)
                 tv += 1
             yield
@@ -722,13 +739,17 @@ class AbortBwdModel(BwdModel):
     def value_issuer(self):
         c = self.c
         ok = True
+        sh = c["shared"]
         for j in range(self.n):
-            b, s = j % c["NSt"], j % c["VS"]
+            b, s = j % c["NSt"], j % (c["KU"] if sh else c["VS"])
             ok = yield from self.wait_or_abort(self.p_full[b], j // c["NSt"])
-            ok = ok and (yield from self.wait_or_abort(self.v_full[s], j // c["VS"]))
+            if sh:
+                ok = ok and (yield from self.wait_or_abort(self.k_full[s], j // c["KU"]))
+            else:
+                ok = ok and (yield from self.wait_or_abort(self.v_full[s], j // c["VS"]))
             if not ok:
                 break
-            self.later("PV", self.v_empty[s].arrive)
+            self.later("PV", (self.k_empty if sh else self.v_empty)[s].arrive)
             self.later("PV", self.pv_done[b].arrive)
         if ok:
             self.later("PV", self.acc_done.arrive)

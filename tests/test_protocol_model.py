@@ -72,6 +72,19 @@ def test_backward_protocol_is_race_free(D, dkdv, n_tiles):
         BwdModel(cfg, n_tiles, seed=1000 * n_tiles + seed).run()
 
 
+def test_backward_shared_stage_without_the_value_release_is_caught():
+    # the score ring's stage also feeds the value MMAs up to head dim 128; released
+    # after the two score issuers alone, it would be reloaded under the value MMAs
+    for D in (64, 128):
+        hits = 0
+        for seed in range(40):
+            try:
+                BwdModel(bwd_config(D, True), 9, seed=seed, mutate="shared_stage_two_arrivals").run()
+            except ProtocolError:
+                hits += 1
+        assert hits > 0, D
+
+
 def test_backward_two_groups_on_one_s1_slot_is_caught():
     # the reason the S1 barriers have one slot per tile parity at d = 128
     hits = 0
@@ -99,8 +112,8 @@ template <int D, int DV> void fwd() {
 }
 template <int D, int M> void bwd() {
   using C = BwdCfg<D, M>;
-  printf("bwd %%d %%d %%d %%d %%d %%d %%d %%d %%d %%d\n", D, M, C::kNS, C::kNSt, C::kSBar, C::kKS, C::kVS, C::kVecS,
-         C::kUPT, C::kKU);
+  printf("bwd %%d %%d %%d %%d %%d %%d %%d %%d %%d %%d %%d\n", D, M, C::kNS, C::kNSt, C::kSBar, C::kKS, C::kVS,
+         C::kVecS, C::kUPT, C::kKU, int(C::kShared));
 }
 int main() {
   fwd<64, 64>(); fwd<64, 128>(); fwd<64, 256>(); fwd<128, 64>(); fwd<128, 128>(); fwd<128, 256>();
@@ -138,7 +151,7 @@ def test_model_sizes_are_the_kernels_sizes(tmp_path):
         else:
             want = bwd_config(v[0], v[1] == 1)
             assert (want["NS"], want["NSt"], want["SBar"], want["KS"], want["VS"], want["VecS"], want["UPT"],
-                    want["KU"]) == tuple(v[2:]), line
+                    want["KU"], int(want["shared"])) == tuple(v[2:]), line
         seen += 1
     assert seen == 15
 
