@@ -95,6 +95,7 @@ struct FwdCfg {
   static constexpr int kOffQt = kQBytes;
   static constexpr int kOffK = 2 * kQBytes;
   static constexpr int kOffV = kOffK + kKU * kKUnit;
+  static_assert(kKU * kKUnit >= 4 * 8192, "the key ring also holds the four 8 KB epilogue stages");
   static constexpr int kOffBar = kOffV + kVS * kVStage;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
   // TMEM columns (fp32 each): O [0,DV), T [DV,2DV), S buffer b [2DV+64b, +64),
@@ -259,47 +260,67 @@ __device__ __forceinline__ bool softmax_tile(uint32_t lane_addr, uint32_t cS, ui
   return true;
 }
 
-// Epilogue of the calling thread's row: O = O~/l, mu = r/l, Ot = T~/l - mu O and
-// LSE = (m + log2 l) ln 2, read from TMEM (O~ in columns 0-DV, T~ in DV-2DV).
-// The CTA's value columns (the first d of them for d < 64) are written at
-// element offset ``obase`` of out / out_t; LSE and mu where those are non-null.
+// Epilogue of one softmax warp's 32 rows: O = O~/l, mu = r/l, Ot = T~/l - mu O
+// and LSE = (m + log2 l) ln 2, read from TMEM (O~ in columns 0-DV, T~ in DV-2DV).
+// Each thread forms its own row 32 columns at a time, but stores from one thread
+// per row would touch 32 rows (32 cache lines) per warp instruction, and the
+// store path, not the bandwidth, bounds that.  So the warp passes each 32-column
+// chunk through ``stage`` (its own 8 KB of shared memory: O, then Ot, 32 x 32
+// floats each, 16-byte unit u of row r at unit u ^ (r mod 8), which spreads both
+// the row-wise writes and the read-back over all banks) and writes it back four
+// rows per instruction, eight lanes per 128-byte row segment.
+// ``obase0``: element offset of the warp's first row in out / out_t (this CTA's
+// value columns); ``ostride``: elements between rows; ``valid_rows``: rows of the
+// warp that exist (the last query tile may be partial).  The CTA's value columns
+// (the first d of them for d < 64) are written; LSE and mu where non-null.
 template <class C>
-__device__ __forceinline__ void write_row(uint32_t lane_addr, const RowState& st, int64_t ridx, int64_t obase,
-                                          bool valid_row, int d, float* __restrict__ out,
-                                          float* __restrict__ out_t, float* __restrict__ lse_out,
-                                          float* __restrict__ mu_out) {
+__device__ __forceinline__ void write_rows(uint32_t lane_addr, const RowState& st, int64_t ridx, int64_t obase0,
+                                           int64_t ostride, int valid_rows, int d, float* stage,
+                                           float* __restrict__ out, float* __restrict__ out_t,
+                                           float* __restrict__ lse_out, float* __restrict__ mu_out) {
+  const int lane = threadIdx.x & 31;
   const float inv_l = 1.f / st.l;
   const float mu = st.r * inv_l;
   // The CTA's kDV value columns, except for the 16/32-wide value heads run as 64.
   constexpr int kDV = C::kDV;
   const int ncols = C::kSmallV ? d : kDV;
+  float4* so = reinterpret_cast<float4*>(stage);        // [32 rows][8 units]
+  float4* stt = reinterpret_cast<float4*>(stage + 1024);
+  const int ru = lane & 7;   // read-back: unit of the row segment
+  const int rr = lane >> 3;  // read-back: first row (then every fourth)
 #pragma unroll 1
   for (int c0 = 0; c0 < ncols; c0 += 32) {
     uint32_t ov[32], tv[32];
     tmem_ld32_wait(lane_addr + c0, ov);
     tmem_ld32_wait(lane_addr + kDV + c0, tv);
-    if (valid_row) {
-      float4* o4 = reinterpret_cast<float4*>(out + obase + c0);
-      float4* t4 = reinterpret_cast<float4*>(out_t + obase + c0);
-      const int n4 = !C::kSmallV ? 8 : min(8, (ncols - c0) >> 2);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (C::kSmallV && i >= n4) break;
-        float4 o, t;
-        o.x = __uint_as_float(ov[4 * i + 0]) * inv_l;
-        o.y = __uint_as_float(ov[4 * i + 1]) * inv_l;
-        o.z = __uint_as_float(ov[4 * i + 2]) * inv_l;
-        o.w = __uint_as_float(ov[4 * i + 3]) * inv_l;
-        t.x = __uint_as_float(tv[4 * i + 0]) * inv_l - mu * o.x;
-        t.y = __uint_as_float(tv[4 * i + 1]) * inv_l - mu * o.y;
-        t.z = __uint_as_float(tv[4 * i + 2]) * inv_l - mu * o.z;
-        t.w = __uint_as_float(tv[4 * i + 3]) * inv_l - mu * o.w;
-        o4[i] = o;
-        t4[i] = t;
+    for (int i = 0; i < 8; ++i) {
+      float4 o, t;
+      o.x = __uint_as_float(ov[4 * i + 0]) * inv_l;
+      o.y = __uint_as_float(ov[4 * i + 1]) * inv_l;
+      o.z = __uint_as_float(ov[4 * i + 2]) * inv_l;
+      o.w = __uint_as_float(ov[4 * i + 3]) * inv_l;
+      t.x = __uint_as_float(tv[4 * i + 0]) * inv_l - mu * o.x;
+      t.y = __uint_as_float(tv[4 * i + 1]) * inv_l - mu * o.y;
+      t.z = __uint_as_float(tv[4 * i + 2]) * inv_l - mu * o.z;
+      t.w = __uint_as_float(tv[4 * i + 3]) * inv_l - mu * o.w;
+      so[lane * 8 + (i ^ (lane & 7))] = o;
+      stt[lane * 8 + (i ^ (lane & 7))] = t;
+    }
+    __syncwarp();
+    const bool col_ok = !C::kSmallV || c0 + 4 * ru < ncols;
+#pragma unroll 1
+    for (int i = 0; i < 8; ++i) {
+      const int r = rr + 4 * i;
+      if (col_ok && r < valid_rows) {
+        const int64_t off = obase0 + static_cast<int64_t>(r) * ostride + c0 + 4 * ru;
+        *reinterpret_cast<float4*>(out + off) = so[r * 8 + (ru ^ (r & 7))];
+        *reinterpret_cast<float4*>(out_t + off) = stt[r * 8 + (ru ^ (r & 7))];
       }
     }
+    __syncwarp();  // the next chunk overwrites the stage
   }
-  if (valid_row) {
+  if (lane < valid_rows) {
     if (lse_out) lse_out[ridx] = (st.m + __log2f(st.l)) * kLn2;
     if (mu_out) mu_out[ridx] = mu;
   }
@@ -575,13 +596,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       tc_fence_after_sync();
+      // Every MMA and copy of the CTA is done: the key ring's shared memory is free
+      // and holds each softmax warp's 8 KB epilogue stage.
+      fence_proxy_async_smem();
       const int qrow = q0 + row;
-      const int64_t obase = static_cast<int64_t>(bb) * geom.o_stride[0] +
-                            static_cast<int64_t>(qrow) * geom.o_stride[1] +
-                            static_cast<int64_t>(hh) * geom.o_stride[2] + vh * C::kDV;
+      const int wrow0 = q0 + quarter * 32;  // the warp's first query row
+      const int64_t obase0 = static_cast<int64_t>(bb) * geom.o_stride[0] +
+                             static_cast<int64_t>(wrow0) * geom.o_stride[1] +
+                             static_cast<int64_t>(hh) * geom.o_stride[2] + vh * C::kDV;
+      float* stage = reinterpret_cast<float*>(smem + C::kOffK + quarter * 8192);
       // Every value half computes the same LSE and mu; the first one writes them.
-      write_row<C>(lane_addr, st, static_cast<int64_t>(bh) * geom.Nq + qrow, obase, qrow < geom.Nq, geom.d_v, out,
-                   out_t, vh == 0 ? lse_out : nullptr, vh == 0 ? mu_out : nullptr);
+      write_rows<C>(lane_addr, st, static_cast<int64_t>(bh) * geom.Nq + qrow, obase0, geom.o_stride[1],
+                    min(32, geom.Nq - wrow0), geom.d_v, stage, out, out_t, vh == 0 ? lse_out : nullptr,
+                    vh == 0 ? mu_out : nullptr);
     }
   }
 
