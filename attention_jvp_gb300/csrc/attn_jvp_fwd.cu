@@ -46,8 +46,14 @@
 // key tiles the rings hold.  The V dim sets the value MMAs and the TMEM layout.
 // At a V dim of 256, O and T of 128 rows would fill TMEM, so two neighbouring
 // CTAs share each query tile and each accumulates 128 of the value columns.
+//
+// Waves: each CTA holds all of an SM's TMEM, so the grid runs in waves of the
+// SM count.  A last wave at most half full would leave most SMs idle for a
+// whole CTA's time, so its units are cut into pieces over the keys, written as
+// partials and merged by merge_pieces_kernel (see FwdGeom).
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <mutex>
 
 #include "internal.h"
 #include "sm103_ptx.cuh"
@@ -129,6 +135,17 @@ struct FwdGeom {
   int d_v;                  // real value head dimension: the output columns written
   float scale;
   int64_t o_stride[3];      // output element strides: batch, sequence, head
+  // Balance of a short last wave: the grid's units (query tile, value half) from
+  // n_main on are each cut into ``split`` pieces over consecutive key ranges, one
+  // CTA per piece; piece c takes key tiles [piece_t[c], piece_t[c + 1]) of the
+  // launch's range.  A piece writes its normalised O, Ot (kDV columns per row,
+  // 128 rows) and its LSE and mu to the ``part_*`` arrays, slot
+  // (unit - n_main) * split + c, and merge_pieces_kernel combines them.
+  // split == 1: no pieces, n_main is the grid.
+  static constexpr int kMaxSplit = 16;
+  int n_main, split;
+  int piece_t[kMaxSplit + 1];
+  float *part_o, *part_ot, *part_lse, *part_mu;
 };
 
 struct Barriers {
@@ -344,12 +361,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_qtiles = geom.n_qtiles, kv_start = geom.kv_start, kv_len = geom.kv_len;
+  const int n_qtiles = geom.n_qtiles;
+  int kv_start = geom.kv_start, kv_len = geom.kv_len;
   const float scale = geom.scale;
+  // A CTA past n_main is one piece of a unit of the last wave: that unit's key
+  // tiles [t0, t1) of the launch's range.
+  unsigned unit = blockIdx.x;
+  int piece = -1;  // this CTA's partial-output slot, or -1 (outputs in place)
+  if (unit >= static_cast<unsigned>(geom.n_main)) {
+    piece = static_cast<int>(unit - geom.n_main);
+    const unsigned u = static_cast<unsigned>(piece) / static_cast<unsigned>(geom.split);
+    const int c = piece - static_cast<int>(u) * geom.split;
+    unit = geom.n_main + u;
+    const int k0 = geom.piece_t[c] * C::kBN;
+    kv_len = min(geom.piece_t[c + 1] * C::kBN, kv_len) - k0;
+    kv_start += k0;
+  }
   // Both value halves of a query tile (d = 256) are neighbours in the grid, so
   // they stream the same key tiles through L2 at about the same time.
-  const int vh = blockIdx.x % C::kVSplit;  // which kDV value columns this CTA accumulates
-  const unsigned qb = blockIdx.x / C::kVSplit;  // unsigned: the divisions below stay unsigned
+  const int vh = unit % C::kVSplit;  // which kDV value columns this CTA accumulates
+  const unsigned qb = unit / C::kVSplit;  // unsigned: the divisions below stay unsigned
   const int bh = qb / n_qtiles;
   const int hh = bh % geom.H, bb = bh / geom.H;
   const int q0 = (qb % n_qtiles) * C::kBM;
@@ -601,14 +632,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       const int qrow = q0 + row;
       const int wrow0 = q0 + quarter * 32;  // the warp's first query row
-      const int64_t obase0 = static_cast<int64_t>(bb) * geom.o_stride[0] +
-                             static_cast<int64_t>(wrow0) * geom.o_stride[1] +
-                             static_cast<int64_t>(hh) * geom.o_stride[2] + vh * C::kDV;
       float* stage = reinterpret_cast<float*>(smem + C::kOffK + quarter * 8192);
-      // Every value half computes the same LSE and mu; the first one writes them.
-      write_rows<C>(lane_addr, st, static_cast<int64_t>(bh) * geom.Nq + qrow, obase0, geom.o_stride[1],
-                    min(32, geom.Nq - wrow0), geom.d_v, stage, out, out_t, vh == 0 ? lse_out : nullptr,
-                    vh == 0 ? mu_out : nullptr);
+      // In place; or a piece's partial slot of 128 rows of kDV columns.  Every value
+      // half computes the same LSE and mu; in place, the first one writes them.
+      const bool part = piece >= 0;
+      const int64_t slot = static_cast<int64_t>(piece) * C::kBM;
+      const int64_t obase0 = part ? (slot + quarter * 32) * C::kDV
+                                  : static_cast<int64_t>(bb) * geom.o_stride[0] +
+                                        static_cast<int64_t>(wrow0) * geom.o_stride[1] +
+                                        static_cast<int64_t>(hh) * geom.o_stride[2] + vh * C::kDV;
+      write_rows<C>(lane_addr, st, part ? slot + row : static_cast<int64_t>(bh) * geom.Nq + qrow, obase0,
+                    part ? C::kDV : geom.o_stride[1], min(32, geom.Nq - wrow0), geom.d_v, stage,
+                    part ? geom.part_o : out, part ? geom.part_ot : out_t,
+                    part ? geom.part_lse : (vh == 0 ? lse_out : nullptr),
+                    part ? geom.part_mu : (vh == 0 ? mu_out : nullptr));
     }
   }
 
@@ -646,6 +683,115 @@ cudaError_t make_map(CUtensorMap* map, const void* ptr, int64_t d, int64_t rows,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Combines the pieces of each split unit (see FwdGeom) into its outputs, by the
+// exact merge of key ranges: LSE = ln sum_c e^{LSE_c}, w_c = e^{LSE_c - LSE},
+// O = sum_c w_c O_c, mu = sum_c w_c mu_c, Ot = sum_c w_c (Ot_c + mu_c O_c) - mu O.
+// One thread per 4 columns of one row of one unit.
+template <class C>
+__global__ void __launch_bounds__(256) merge_pieces_kernel(const __grid_constant__ FwdGeom geom, int n_units,
+                                                           int ncols, float* __restrict__ out,
+                                                           float* __restrict__ out_t, float* __restrict__ lse,
+                                                           float* __restrict__ mu) {
+  const int tpr = ncols >> 2;
+  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t rowid = gtid / tpr;  // unit * 128 + row
+  if (rowid >= static_cast<int64_t>(n_units) * C::kBM) return;
+  const int col = static_cast<int>(gtid % tpr) * 4;
+  const int u = static_cast<int>(rowid / C::kBM), r = static_cast<int>(rowid % C::kBM);
+  const unsigned unit = geom.n_main + u;
+  const int vh = unit % C::kVSplit;
+  const unsigned qb = unit / C::kVSplit;
+  const int bh = qb / geom.n_qtiles;
+  const int hh = bh % geom.H, bb = bh / geom.H;
+  const int qrow = (qb % geom.n_qtiles) * C::kBM + r;
+  if (qrow >= geom.Nq) return;
+  const int split = geom.split;
+  const int64_t s0 = static_cast<int64_t>(u) * split * C::kBM + r;  // slot row of piece 0
+  float mx = -INFINITY;
+  for (int c = 0; c < split; ++c) mx = fmaxf(mx, geom.part_lse[s0 + c * C::kBM]);
+  float sum = 0.f;
+  for (int c = 0; c < split; ++c) sum += expf(geom.part_lse[s0 + c * C::kBM] - mx);
+  const float L = mx + logf(sum);
+  float mu_row = 0.f;
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f), t = o;
+  for (int c = 0; c < split; ++c) {
+    const int64_t sr = s0 + c * C::kBM;
+    const float w = expf(geom.part_lse[sr] - L);
+    const float mc = geom.part_mu[sr];
+    mu_row += w * mc;
+    const float4 oc = *reinterpret_cast<const float4*>(geom.part_o + sr * C::kDV + col);
+    const float4 tc = *reinterpret_cast<const float4*>(geom.part_ot + sr * C::kDV + col);
+    o.x += w * oc.x;
+    o.y += w * oc.y;
+    o.z += w * oc.z;
+    o.w += w * oc.w;
+    t.x += w * (tc.x + mc * oc.x);
+    t.y += w * (tc.y + mc * oc.y);
+    t.z += w * (tc.z + mc * oc.z);
+    t.w += w * (tc.w + mc * oc.w);
+  }
+  t.x -= mu_row * o.x;
+  t.y -= mu_row * o.y;
+  t.z -= mu_row * o.z;
+  t.w -= mu_row * o.w;
+  const int64_t off = static_cast<int64_t>(bb) * geom.o_stride[0] + static_cast<int64_t>(qrow) * geom.o_stride[1] +
+                      static_cast<int64_t>(hh) * geom.o_stride[2] + vh * C::kDV + col;
+  *reinterpret_cast<float4*>(out + off) = o;
+  *reinterpret_cast<float4*>(out_t + off) = t;
+  if (col == 0 && vh == 0) {
+    const int64_t ridx = static_cast<int64_t>(bh) * geom.Nq + qrow;
+    if (lse) lse[ridx] = L;
+    if (mu) mu[ridx] = mu_row;
+  }
+}
+
+// A stream-ordered memory pool per device for the last wave's partial outputs.
+// Its release threshold keeps the memory mapped between calls: a pool that gives
+// its memory back at every synchronisation maps it again on the next call, which
+// costs more than the cut saves.  It holds at most the largest set of partials a
+// call has needed (SMs x 128 rows x (2 x 128 + 2) floats, about 20 MB on 152 SMs)
+// and lives as long as the process.
+cudaError_t piece_pool(cudaMemPool_t* pool) {
+  constexpr int kMaxDev = 64;
+  static std::mutex mu;
+  static cudaMemPool_t pools[kMaxDev] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!pools[dev]) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t p = nullptr;
+    e = cudaMemPoolCreate(&p, &props);
+    if (e != cudaSuccess) return e;
+    uint64_t keep = ~uint64_t(0);
+    e = cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep);
+    if (e != cudaSuccess) {
+      cudaMemPoolDestroy(p);
+      return e;
+    }
+    pools[dev] = p;
+  }
+  *pool = pools[dev];
+  return cudaSuccess;
+}
+
+int sm_count_fwd() {
+  static int cached = 0;
+  if (cached == 0) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return 0;
+    cached = n;
+  }
+  return cached;
 }
 
 template <int D, int DVF>
@@ -686,10 +832,59 @@ cudaError_t launch_d(const FwdArgs& a, const char** msg) {
   geom.scale = a.scale;
   for (int i = 0; i < 3; ++i) geom.o_stride[i] = a.o_stride[i];
   const int64_t grid = static_cast<int64_t>(n_qtiles) * a.B * a.H * C::kVSplit;
-  kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, a.stream>>>(maps, geom, a.out, a.out_t, a.lse, a.mu,
-                                                                           a.status);
+  // One CTA per SM (the kernel takes all of TMEM), so the grid runs in waves of
+  // the SM count.  When the last wave is at most half full, its units are cut
+  // into pieces over the keys that spread over the whole GPU (at least four key
+  // tiles each), merged afterwards.
+  geom.n_main = static_cast<int>(grid);
+  geom.split = 1;
+  geom.part_o = geom.part_ot = geom.part_lse = geom.part_mu = nullptr;
+  const int n_sm = sm_count_fwd();
+  const int64_t tail = n_sm > 0 ? grid % n_sm : 0;
+  const int64_t nt = (a.kv_len + C::kBN - 1) / C::kBN;
+  int64_t split = tail > 0 ? n_sm / tail : 0;
+  if (split > nt / 4) split = nt / 4;
+  if (split > FwdGeom::kMaxSplit) split = FwdGeom::kMaxSplit;
+  void* ws = nullptr;
+  if (a.balance_tail && grid >= n_sm && tail > 0 && 2 * tail <= n_sm && split >= 2) {
+    const int64_t slots = tail * split * C::kBM;
+    cudaMemPool_t pool = nullptr;
+    e = piece_pool(&pool);
+    if (e == cudaSuccess)
+      e = cudaMallocFromPoolAsync(&ws, static_cast<size_t>(slots) * (2 * C::kDV + 2) * sizeof(float), pool,
+                                  a.stream);
+    if (e != cudaSuccess) {
+      *msg = "stream-ordered allocation of the last wave's partial outputs failed";
+      return e;
+    }
+    geom.n_main = static_cast<int>(grid - tail);
+    geom.split = static_cast<int>(split);
+    for (int c = 0; c <= split; ++c) geom.piece_t[c] = static_cast<int>(c * nt / split);
+    geom.part_o = static_cast<float*>(ws);
+    geom.part_ot = geom.part_o + slots * C::kDV;
+    geom.part_lse = geom.part_ot + slots * C::kDV;
+    geom.part_mu = geom.part_lse + slots;
+  }
+  const int64_t launched = geom.n_main + (grid - geom.n_main) * geom.split;
+  kern<<<static_cast<unsigned>(launched), kThreads, C::kSmemBytes, a.stream>>>(maps, geom, a.out, a.out_t, a.lse,
+                                                                               a.mu, a.status);
   e = cudaGetLastError();
   if (e != cudaSuccess) *msg = "attention-JVP kernel launch failed";
+  if (ws) {
+    if (e == cudaSuccess) {
+      const int ncols = C::kSmallV ? static_cast<int>(a.d_v) : C::kDV;
+      const int64_t threads = tail * C::kBM * (ncols / 4);
+      merge_pieces_kernel<C><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, a.stream>>>(
+          geom, static_cast<int>(tail), ncols, a.out, a.out_t, a.lse, a.mu);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) *msg = "merge of the last wave's pieces failed to launch";
+    }
+    const cudaError_t f = cudaFreeAsync(ws, a.stream);
+    if (e == cudaSuccess && f != cudaSuccess) {
+      *msg = "stream-ordered release of the last wave's partial outputs failed";
+      e = f;
+    }
+  }
   return e;
 }
 

@@ -122,7 +122,7 @@ void contiguous_strides(int64_t H, int64_t N, int64_t d, int64_t st[3]) {
 int launch_fwd(const void* q, const void* k, const void* v, const void* q_t, const void* k_t, const void* v_t,
                float* out, float* out_t, float* lse, float* mu, int64_t B, int64_t H, int64_t Nq, int64_t Nkv,
                int64_t d, int64_t d_v, const int64_t st[12], float scale, int64_t kv_start, int64_t kv_len,
-               int* status, cudaStream_t stream) {
+               bool balance, int* status, cudaStream_t stream) {
   FwdArgs a;
   a.q = q;
   a.k = k;
@@ -151,6 +151,7 @@ int launch_fwd(const void* q, const void* k, const void* v, const void* q_t, con
   a.kv_len = kv_len;
   a.status = status;
   a.stream = stream;
+  a.balance_tail = balance;
   const char* msg = "";
   cudaError_t e = launch_attn_jvp_fwd(a, &msg);
   if (e != cudaSuccess) return fail(ATTNJVP_ECUDA, "%s: %s", msg, cudaGetErrorString(e));
@@ -160,14 +161,15 @@ int launch_fwd(const void* q, const void* k, const void* v, const void* q_t, con
 size_t round256(size_t n) { return (n + 255) / 256 * 256; }
 
 // ``strides``: 12 element strides (batch, seq, head) of Q, K, V and O, or NULL
-// for contiguous [B, H, N, d] tensors.  fp32 inputs (``dtype`` ATTNJVP_FP32) are
+// for contiguous [B, H, N, d] tensors.  ``balance``: the kernel may cut the units
+// of a short last wave into pieces over the keys (see FwdArgs::balance_tail).  fp32 inputs (``dtype`` ATTNJVP_FP32) are
 // first rounded to bf16 into contiguous [B, H, S, d] copies in stream-ordered
 // device memory (cudaMallocAsync on ``stream``), which is released on the same
 // stream once the kernel has been enqueued after the copies.
 int run_fwd(const void* q, const void* k, const void* v, const void* q_t, const void* k_t, const void* v_t,
             float* out, float* out_t, float* lse, float* mu, int64_t B, int64_t H, int64_t Nq, int64_t Nkv,
             int64_t d, int64_t d_v, const int64_t* strides, float scale, int dtype, int64_t kv_start,
-            int64_t kv_len, void* stream) {
+            int64_t kv_len, bool balance, void* stream) {
   const char* why = "";
   int* status = status_word(&why);
   if (!status) return fail(ATTNJVP_ECUDA, "no CUDA device / status word: %s", why);
@@ -183,7 +185,7 @@ int run_fwd(const void* q, const void* k, const void* v, const void* q_t, const 
   }
   if (dtype == ATTNJVP_BF16)
     return launch_fwd(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, Nq, Nkv, d, d_v, st, scale, kv_start,
-                      kv_len, status, cs);
+                      kv_len, balance, status, cs);
   // fp32: six bf16 copies, Q and Qt [B, H, Nq, d], K and Kt [B, H, Nkv, d], V and Vt [B, H, Nkv, d_v].
   const size_t bytes[3] = {round256(size_t(B * H * Nq * d) * 2), round256(size_t(B * H * Nkv * d) * 2),
                            round256(size_t(B * H * Nkv * d_v) * 2)};
@@ -212,7 +214,7 @@ int run_fwd(const void* q, const void* k, const void* v, const void* q_t, const 
     contiguous_strides(H, Nkv, d_v, bst + 6);
     for (int i = 9; i < 12; ++i) bst[i] = st[i];
     rc = launch_fwd(dst[0], dst[2], dst[4], dst[1], dst[3], dst[5], out, out_t, lse, mu, B, H, Nq, Nkv, d, d_v, bst,
-                    scale, kv_start, kv_len, status, cs);
+                    scale, kv_start, kv_len, balance, status, cs);
   }
   e = cudaFreeAsync(buf, cs);
   if (rc == ATTNJVP_OK && e != cudaSuccess)
@@ -250,7 +252,7 @@ int attn_jvp_fwd(const void* q, const void* k, const void* v, const void* q_t, c
   int rc = check_attn_args(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, d, scale, dtype);
   if (rc != ATTNJVP_OK) return rc;
   return run_fwd(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, N, d, d, nullptr, scale, dtype, 0, N,
-                 stream);
+                 true, stream);
 }
 
 int attn_jvp_fwd_chunk(const void* q, const void* k, const void* v, const void* q_t, const void* k_t,
@@ -263,7 +265,7 @@ int attn_jvp_fwd_chunk(const void* q, const void* k, const void* v, const void* 
     return fail(ATTNJVP_EINVAL, "key range [%lld, %lld) outside [0, %lld) or empty", (long long)kv_start,
                 (long long)(kv_start + kv_len), (long long)N);
   return run_fwd(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, N, N, d, d, nullptr, scale, dtype, kv_start,
-                 kv_len, stream);
+                 kv_len, false, stream);
 }
 
 int attn_jvp_fwd_ex(const void* q, const void* k, const void* v, const void* q_t, const void* k_t, const void* v_t,
@@ -293,7 +295,7 @@ int attn_jvp_fwd_ex(const void* q, const void* k, const void* v, const void* q_t
     }
   }
   return run_fwd(q, k, v, q_t, k_t, v_t, out, out_t, lse, mu, B, H, Nq, Nkv, d, d_v, strides, scale, dtype,
-                 kv_start, kv_len, stream);
+                 kv_start, kv_len, kv_start == 0 && kv_len == Nkv, stream);
 }
 
 int attn_jvp_fwd_strided(const void* q, const void* k, const void* v, const void* q_t, const void* k_t,

@@ -23,6 +23,10 @@ struct FwdArgs {
   int64_t kv_start, kv_len;
   int* status;                               // device status word
   cudaStream_t stream;
+  // Cut the units of a short last wave into pieces over the keys (stream-ordered
+  // allocation of their partial outputs and one merge launch).  Off for callers
+  // that must not allocate and for key chunks, which are merged by their callers.
+  bool balance_tail = false;
 };
 
 // Returns cudaSuccess or the failing CUDA error; ``*msg`` gets a static message.

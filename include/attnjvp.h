@@ -32,7 +32,9 @@
  *   - The library looks up the device addresses of its own device arrays (the
  *     status word, the no-alloc scratch) once per device and keeps them, so it
  *     does not survive cudaDeviceReset, or any other teardown of a device's
- *     primary context, while it is loaded.
+ *     primary context, while it is loaded.  For the same lifetime it keeps, per
+ *     device, one stream-ordered memory pool for the partial outputs of a cut
+ *     last wave (see attn_jvp_fwd), which it does not give back to the system.
  */
 #ifndef ATTNJVP_H
 #define ATTNJVP_H
@@ -79,6 +81,16 @@ extern "C" {
  *                            the kernel (stream-ordered; no device synchronisation);
  *                            ATTNJVP_ECUDA if that allocation fails.  The outputs
  *                            are fp32 either way.
+ * Last wave: the kernel runs one CTA per SM, so its units (a 128-row query tile,
+ * or a value half of one at d = 256) run in waves of the SM count.  When the
+ * last wave would be at most half full, each of its units is cut into 2 to 16
+ * pieces over consecutive key ranges (at least four 64-key tiles each), which
+ * spread over the whole GPU, and one more kernel merges them exactly (the
+ * key-chunk merge).  The pieces' partial outputs, at most SMs x 128 rows x
+ * (2 min(d, 128) + 2) floats, come from the library's stream-ordered pool on
+ * ``stream``.  A cut row rounds P~ against its piece's own maximum, so it can
+ * differ from an uncut computation in the last bits (within the tolerances
+ * above); every other row is computed exactly as without the cut.
  */
 int attn_jvp_fwd(const void* q, const void* k, const void* v,
                  const void* q_t, const void* k_t, const void* v_t,
@@ -93,6 +105,8 @@ int attn_jvp_fwd(const void* q, const void* k, const void* v,
  * chunks exactly.  Arguments as attn_jvp_fwd, plus:
  *   lse, mu   : required (not NULL) — the merge needs them.
  *   kv_start  : >= 0;  kv_len >= 1;  kv_start + kv_len <= N.
+ * A chunk is never cut into pieces (its caller merges chunks), so this call
+ * takes no memory of its own for bf16 inputs.
  * (The page has no key split; chunking is exact algebra on the definitions above.)
  */
 int attn_jvp_fwd_chunk(const void* q, const void* k, const void* v,
@@ -127,8 +141,9 @@ int attn_jvp_fwd_chunk(const void* q, const void* k, const void* v,
  *                         Layouts in which output elements overlap give
  *                         unspecified results.
  *   kv_start, kv_len    : key range [kv_start, kv_start + kv_len) within [0, N_kv);
- *                         the whole range gives the full result, a sub-range the
- *                         chunk partials of attn_jvp_fwd_chunk.
+ *                         the whole range gives the full result (with the cut of
+ *                         a short last wave of attn_jvp_fwd), a sub-range the
+ *                         chunk partials of attn_jvp_fwd_chunk (never cut).
  * (The page's host wrapper hands [B, S, H, D] tensors to its kernel as
  * transposed views together with their strides; its section 前向 (forward)
  * allows seqlen_q != seqlen_kv and head dims {16, 32, 64, 128, 256}.)
@@ -288,8 +303,10 @@ int trigflow_tangent(const float* x0, const float* eps, const double* t, float* 
  * On return the work is enqueued; once ``stream`` has been synchronised every
  * output is in host memory.  Inputs must stay unchanged, and outputs unread,
  * until then.  Calls that share a workspace must be ordered on one stream.
- * Each item runs the device entry points on a [group, N, d] slice, so the
- * results equal a device-resident call bit for bit.
+ * Each item runs the device entry points on a [group, N, d] slice, so its
+ * results equal a device-resident call on that slice bit for bit, and a call
+ * on the whole tensor wherever neither call cuts a short last wave (see
+ * attn_jvp_fwd).
  */
 int attn_jvp_fwd_host(const void* q, const void* k, const void* v,
                       const void* q_t, const void* k_t, const void* v_t,

@@ -1,0 +1,98 @@
+"""GPU: the cut of a short last wave into pieces over the keys.
+
+The fused kernel runs one CTA per SM, so a grid of (query tile, value half)
+units runs in waves of the SM count.  When the last wave is at most half full,
+attn_jvp_fwd cuts each of its units into pieces over consecutive key ranges
+(at least four key tiles each) and merges them exactly afterwards.  The shapes
+here are chosen from the device's SM count so that the grid is one wave plus a
+short tail; the units of the tail are then the last heads' query tiles.
+
+The cut heads are checked against the FP64 oracle with the usual tolerances.
+They are not compared bit for bit with an uncut run: each piece rounds its own
+P~ = 2^(S - m) to bf16 against its own running maximum, so the roundings differ
+(both runs stay within the oracle's tolerance).  Every head whose units all ran
+in the first wave must equal the uncut run (the chunk entry point over the whole
+key range, which never cuts) bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+from attention_jvp_gb300 import binding, inputs
+from helpers import assert_close, gpu_rows, oracle_on
+
+pytestmark = pytest.mark.gpu
+
+
+def _sm_count():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def _shape(d, n_qtiles):
+    """(B, H) with B*H*n_qtiles*(2 if d == 256) units: one wave plus a tail of
+    at most a quarter of the SMs, so the tail is cut (n_qtiles divides the
+    units, so the tail is whole heads' worth of query tiles)."""
+    per_head = n_qtiles * (2 if d == 256 else 1)
+    n_sm = _sm_count()
+    heads = n_sm // per_head + 1
+    assert 0 < heads * per_head - n_sm <= n_sm // 4
+    return 1, heads
+
+
+def _whole_range(x):
+    N = x["q"].shape[2]
+    out = binding.attn_jvp_fwd_chunk(*(x[n] for n in inputs.NAMES), 0, N, scale=x["scale"])
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("d,N", [(64, 1000), (128, 1000), (256, 1000), (32, 777)])
+def test_cut_tail_matches_oracle_and_uncut_path(cuda_lib, d, N):
+    n_qtiles = (N + 127) // 128
+    B, H = _shape(d, n_qtiles)
+    x = inputs.make_inputs(B, H, N, d, seed=70 + d, device="cuda", qk="rms", tangent_scale=0.3)
+    got = binding.attn_jvp_fwd(*(x[n] for n in inputs.NAMES), scale=x["scale"])
+    torch.cuda.synchronize()
+    binding.attn_jvp_status()
+    ref = _whole_range(x)
+    # the cut units are those past the first wave: the last heads' query tiles
+    per_head = n_qtiles * (2 if d == 256 else 1)
+    first_cut = _sm_count() // per_head
+    for name, g, r in zip(("O", "Ot", "LSE", "mu"), got, ref):
+        assert torch.equal(g[:, :first_cut], r[:, :first_cut]), name
+    heads = list(range(first_cut, B * H))
+    o = oracle_on(x, heads=heads)
+    assert_close(gpu_rows(got[0], heads), o[0], "O")
+    assert_close(gpu_rows(got[1], heads), o[1], "Ot")
+    assert_close(gpu_rows(got[3], heads), o[3], "mu")
+    assert np.max(np.abs(gpu_rows(got[2], heads) - o[2])) <= 1e-3
+
+
+def test_cut_tail_with_strided_outputs_and_no_row_outputs(cuda_lib):
+    d, N = 128, 1000
+    B, H = _shape(d, (N + 127) // 128)
+    x = inputs.make_inputs(B, H, N, d, seed=81, device="cuda", qk="rms", tangent_scale=0.3)
+    ref = binding.attn_jvp_fwd(*(x[n] for n in inputs.NAMES), scale=x["scale"])
+    # the same values in [B, N, H, d]; outputs in that layout too
+    xs = {n: x[n].transpose(1, 2).contiguous() for n in inputs.NAMES}
+    got = binding.attn_jvp_fwd_strided(*(xs[n] for n in inputs.NAMES), layout="bshd", scale=x["scale"])
+    only = binding.attn_jvp_fwd(*(x[n] for n in inputs.NAMES), scale=x["scale"], want_rows=False)
+    torch.cuda.synchronize()
+    binding.attn_jvp_status()
+    assert torch.equal(got[0].transpose(1, 2), ref[0]) and torch.equal(got[1].transpose(1, 2), ref[1])
+    assert torch.equal(got[2], ref[2]) and torch.equal(got[3], ref[3])
+    assert only[2] is None and only[3] is None
+    assert torch.equal(only[0], ref[0]) and torch.equal(only[1], ref[1])
+
+
+def test_cut_tail_with_fp32_inputs(cuda_lib):
+    d, N = 64, 1000
+    B, H = _shape(d, (N + 127) // 128)
+    x = inputs.make_inputs(B, H, N, d, seed=83, device="cuda", dtype=torch.float32)
+    got = binding.attn_jvp_fwd(*(x[n] for n in inputs.NAMES), scale=x["scale"])
+    xb = {n: x[n].to(torch.bfloat16) for n in inputs.NAMES}
+    ref = binding.attn_jvp_fwd(*(xb[n] for n in inputs.NAMES), scale=x["scale"])
+    torch.cuda.synchronize()
+    binding.attn_jvp_status()
+    for g, r in zip(got, ref):
+        assert torch.equal(g, r)
