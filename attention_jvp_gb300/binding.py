@@ -58,6 +58,7 @@ def load(path=None):
     lib.attn_jvp_fwd_host_workspace_bytes.argtypes = [i64] * 6
     lib.attn_jvp_fwd_host_workspace_bytes.restype = i64
     lib.qk_rmsnorm_jvp.argtypes = [vp] * 10 + [i64] * 3 + [ctypes.c_float, vp]
+    lib.attn_jvp_fwd_last_wave_split.argtypes = [i64] * 5 + [ctypes.POINTER(i64)]
     lib.trigflow_coeffs_jvp.argtypes = [ctypes.c_double] * 3 + [ctypes.POINTER(ctypes.c_double)]
     lib.trigflow_output_jvp.argtypes = [vp] * 8 + [i64] * 4 + [vp]
     lib.scm_tangent_loss.argtypes = [vp] * 6 + [ctypes.c_double] + [vp] * 5 + [i64] * 4 + [vp, i64, vp]
@@ -167,6 +168,15 @@ def attn_jvp_fwd(q, k, v, q_t, k_t, v_t, scale=None, out=None, out_t=None, lse=N
                              ctypes.c_float(scale), code, _stream(stream))
     _check("attn_jvp_fwd", rc)
     return out, out_t, lse, mu
+
+
+def attn_jvp_fwd_last_wave_split(B, H, N_q, N_kv, d_v):
+    """Pieces per unit into which attn_jvp_fwd cuts the last wave of this shape on the
+    current device (1: no cut; otherwise the call launches a second, merging kernel)."""
+    out = ctypes.c_int64(0)
+    _check("attn_jvp_fwd_last_wave_split",
+           load().attn_jvp_fwd_last_wave_split(int(B), int(H), int(N_q), int(N_kv), int(d_v), ctypes.byref(out)))
+    return out.value
 
 
 def attn_jvp_fwd_chunk(q, k, v, q_t, k_t, v_t, kv_start, kv_len, scale=None, out=None, out_t=None,

@@ -782,6 +782,23 @@ cudaError_t piece_pool(cudaMemPool_t* pool) {
   return cudaSuccess;
 }
 
+}  // namespace
+
+// Pieces per unit of the last wave (1: no cut) for a grid of ``grid`` units over
+// kv_len keys on n_sm SMs: only a last wave at most half full is cut, into as
+// many pieces as spread it over all SMs, at least four 64-key tiles each and at
+// most FwdGeom::kMaxSplit.
+int64_t last_wave_split(int64_t grid, int64_t kv_len, int n_sm) {
+  if (n_sm <= 0 || grid < n_sm) return 1;
+  const int64_t tail = grid % n_sm;
+  if (tail == 0 || 2 * tail > n_sm) return 1;
+  int64_t split = n_sm / tail;
+  const int64_t nt = (kv_len + 63) / 64;
+  if (split > nt / 4) split = nt / 4;
+  if (split > FwdGeom::kMaxSplit) split = FwdGeom::kMaxSplit;
+  return split >= 2 ? split : 1;
+}
+
 int sm_count_fwd() {
   static int cached = 0;
   if (cached == 0) {
@@ -793,6 +810,8 @@ int sm_count_fwd() {
   }
   return cached;
 }
+
+namespace {
 
 template <int D, int DVF>
 cudaError_t launch_d(const FwdArgs& a, const char** msg) {
@@ -842,11 +861,9 @@ cudaError_t launch_d(const FwdArgs& a, const char** msg) {
   const int n_sm = sm_count_fwd();
   const int64_t tail = n_sm > 0 ? grid % n_sm : 0;
   const int64_t nt = (a.kv_len + C::kBN - 1) / C::kBN;
-  int64_t split = tail > 0 ? n_sm / tail : 0;
-  if (split > nt / 4) split = nt / 4;
-  if (split > FwdGeom::kMaxSplit) split = FwdGeom::kMaxSplit;
+  const int64_t split = a.balance_tail ? last_wave_split(grid, a.kv_len, n_sm) : 1;
   void* ws = nullptr;
-  if (a.balance_tail && grid >= n_sm && tail > 0 && 2 * tail <= n_sm && split >= 2) {
+  if (split > 1) {
     const int64_t slots = tail * split * C::kBM;
     cudaMemPool_t pool = nullptr;
     e = piece_pool(&pool);

@@ -316,6 +316,20 @@ int attn_jvp_fwd_strided(const void* q, const void* k, const void* v, const void
                          scale, dtype, kv_start, kv_len, stream);
 }
 
+int attn_jvp_fwd_last_wave_split(int64_t B, int64_t H, int64_t N_q, int64_t N_kv, int64_t d_v, int64_t* split) {
+  if (!split) return fail(ATTNJVP_EINVAL, "split is NULL");
+  if (B < 1 || H < 1 || N_q < 1 || N_kv < 1 || B * H >= (int64_t(1) << 31) || N_q >= (int64_t(1) << 31) ||
+      N_kv >= (int64_t(1) << 31))
+    return fail(ATTNJVP_EINVAL, "B, H, N_q, N_kv must be >= 1 (B*H, N_q and N_kv below 2^31)");
+  const int rc = check_head_dim(d_v, true);
+  if (rc != ATTNJVP_OK) return rc;
+  const int n_sm = sm_count_fwd();
+  if (n_sm <= 0) return fail(ATTNJVP_ECUDA, "no CUDA device to size the grid for");
+  const int64_t grid = (N_q + 127) / 128 * B * H * (d_v > 128 ? 2 : 1);
+  *split = last_wave_split(grid, N_kv, n_sm);
+  return ok();
+}
+
 int attn_jvp_merge(const float* o_c, const float* ot_c, const float* lse_c, const float* mu_c, int64_t n_chunks,
                    float* out, float* out_t, float* lse, float* mu, int64_t B, int64_t H, int64_t N, int64_t d,
                    void* stream) {

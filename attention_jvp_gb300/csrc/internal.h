@@ -32,6 +32,12 @@ struct FwdArgs {
 // Returns cudaSuccess or the failing CUDA error; ``*msg`` gets a static message.
 cudaError_t launch_attn_jvp_fwd(const FwdArgs& a, const char** msg);
 
+// Pieces per unit into which a balanced launch cuts the last wave of a grid of
+// ``grid`` units over kv_len keys on n_sm SMs (1: no cut); the current device's
+// SM count (0 if unknown).
+int64_t last_wave_split(int64_t grid, int64_t kv_len, int n_sm);
+int sm_count_fwd();
+
 cudaError_t launch_merge(const float* o_c, const float* ot_c, const float* lse_c, const float* mu_c,
                          int64_t n_chunks, float* out, float* out_t, float* lse, float* mu, int64_t rows,
                          int64_t d, cudaStream_t stream);

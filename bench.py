@@ -499,7 +499,10 @@ class Path:
         self.n_chunks = spec.get("kv_chunks", 1)
         self.ws = binding.split_workspace((B, H, N, d), self.n_chunks, dev) if self.n_chunks > 1 else None
         self.bounds = binding.chunk_bounds(N, self.n_chunks)
-        self.launches_per_step = 1 + (1 if self.n_chunks == 1 else self.n_chunks + 1)
+        # attn_jvp_fwd cuts a short last wave into pieces and merges them in a second launch
+        self.pieces = binding.attn_jvp_fwd_last_wave_split(B, H, N, N, d) if self.n_chunks == 1 else 1
+        fwd_launches = 1 + (self.pieces > 1) if self.n_chunks == 1 else self.n_chunks + 1
+        self.launches_per_step = 1 + fwd_launches
         self.events = {"attention": [], "merge": [], "tangent": []}  # (start, end, units)
 
     def _launch(self, kind, units, fn, record):
@@ -615,6 +618,9 @@ def kernel_report(path, workload, peaks, peak_src, clocks, sm_count):
                 "frac_of_burst_peak": round(achieved / float(peaks["bf16_tflops"]), 4),
                 "kernel": kname, "launch_ms": round(mean_launch_ms, 4),
                 "flops_per_launch": flops_launch}
+    if path.pieces > 1:
+        roofline["last_wave"] = ("cut into %d pieces per unit; launch_ms brackets the whole call, the fused "
+                                 "kernel and the merge of the pieces" % path.pieces)
     cn = clock_normalised_frac(achieved, sm_count, clocks.get("sm_mhz"))
     if cn is not None:
         roofline["frac_of_tensor_pipe_at_sampled_clock"] = round(cn, 4)

@@ -99,6 +99,20 @@ int attn_jvp_fwd(const void* q, const void* k, const void* v,
                  float scale, int dtype, void* stream);
 
 /*
+ * Pieces per unit into which attn_jvp_fwd (and attn_jvp_fwd_ex / _strided over
+ * the whole key range) cuts the last wave of this shape on the current device
+ * (see "Last wave" above): 1 when it does not cut.  When it cuts, such a call
+ * makes two kernel launches (the fused kernel, then the merge of the pieces)
+ * instead of one.
+ *   B, H, N_q, N_kv : >= 1 (B*H, N_q and N_kv below 2^31).
+ *   d_v             : the value head dim (16, 32, 64, 128 or 256).
+ *   split           : HOST; receives the count.
+ * Returns ATTNJVP_ECUDA without a CUDA device.  Launches nothing.
+ */
+int attn_jvp_fwd_last_wave_split(int64_t B, int64_t H, int64_t N_q, int64_t N_kv,
+                                 int64_t d_v, int64_t* split);
+
+/*
  * Same operation restricted to the key range [kv_start, kv_start + kv_len):
  * every query row attends only to those keys.  The outputs are the chunk's
  * own normalised partials (O_c, Ot_c, LSE_c, mu_c); attn_jvp_merge combines

@@ -38,7 +38,7 @@ def test_header_declares_the_boundary():
                      "attn_jvp_fwd_host", "attn_jvp_fwd_host_workspace_bytes", "attn_jvp_fwd_strided",
                      "trigflow_coeffs_jvp", "trigflow_output_jvp", "scm_tangent_loss",
                      "scm_tangent_loss_workspace_bytes", "attn_bwd", "attn_bwd_workspace_bytes",
-                     "qk_rmsnorm_jvp"):
+                     "qk_rmsnorm_jvp", "attn_jvp_fwd_last_wave_split"):
         assert expected in names
 
 
@@ -366,3 +366,14 @@ def test_qk_norm_validation_needs_no_gpu(lib):
     assert b"w_k" in lib.attn_jvp_last_error()
     # with no K rows the K pointers are not needed; nothing to do at all is a no-op
     assert call(good[:2] + [None, None] + good[4:5] + [None] + good[6:], rq=0, rk=0) == E.ATTNJVP_OK
+
+
+def test_last_wave_query_validation_needs_no_gpu(lib):
+    out = ctypes.c_int64(-7)
+    for args in ((0, 1, 100, 100, 64), (1, 1, 0, 100, 64), (1, 1, 100, 0, 64), (1 << 16, 1 << 15, 10, 10, 64)):
+        assert lib.attn_jvp_fwd_last_wave_split(*args, ctypes.byref(out)) == binding.ATTNJVP_EINVAL
+    assert lib.attn_jvp_fwd_last_wave_split(1, 1, 100, 100, 48, ctypes.byref(out)) == binding.ATTNJVP_EUNSUPPORTED
+    assert lib.attn_jvp_fwd_last_wave_split(1, 1, 100, 100, 64, None) == binding.ATTNJVP_EINVAL
+    if not torch.cuda.is_available():
+        assert lib.attn_jvp_fwd_last_wave_split(1, 1, 100, 100, 64, ctypes.byref(out)) == binding.ATTNJVP_ECUDA
+    assert out.value == -7

@@ -96,3 +96,29 @@ def test_cut_tail_with_fp32_inputs(cuda_lib):
     binding.attn_jvp_status()
     for g, r in zip(got, ref):
         assert torch.equal(g, r)
+
+
+
+def _documented_split(grid, kv_len, n_sm):
+    # the header's rule: cut only a last wave at most half full, into as many
+    # pieces as spread it over the SMs, each at least four 64-key tiles, at most 16
+    tail = grid % n_sm
+    if grid < n_sm or tail == 0 or 2 * tail > n_sm:
+        return 1
+    split = min(n_sm // tail, ((kv_len + 63) // 64) // 4, 16)
+    return split if split >= 2 else 1
+
+
+def test_last_wave_query_follows_the_documented_rule(cuda_lib):
+    n_sm = _sm_count()
+    seen = set()
+    for B, H, Nq, Nkv, dv in [(1, n_sm // 8 + 1, 1000, 1000, 128), (1, n_sm, 128, 1000, 128),
+                              (1, 1, 128, 1000, 128), (1, n_sm + 1, 128, 100, 128),
+                              (1, n_sm + 1, 128, 4096, 128), (1, n_sm + n_sm // 2 + 1, 128, 4096, 128),
+                              (2, 24, 4096, 4096, 128), (1, 40, 32760, 32760, 128), (4, 16, 16384, 16384, 64),
+                              (1, n_sm // 2 + 1, 128, 4096, 256), (1, 7, 777, 300, 32)]:
+        grid = (Nq + 127) // 128 * B * H * (2 if dv > 128 else 1)
+        want = _documented_split(grid, Nkv, n_sm)
+        assert binding.attn_jvp_fwd_last_wave_split(B, H, Nq, Nkv, dv) == want, (B, H, Nq, Nkv, dv)
+        seen.add(want > 1)
+    assert seen == {True, False}
