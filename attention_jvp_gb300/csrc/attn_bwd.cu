@@ -33,7 +33,8 @@
 // epilogue by 32-column chunks.  In the dQ pass the score MMAs take Q and dO
 // from TMEM copies.  The two passes recompute S and dP (14 d flops
 // per (query, key) pair instead of 10) but need no atomics, so results are
-// deterministic.
+// deterministic.  A last wave at most half full is cut into pieces over the
+// streamed rows, as in the forward, and a second kernel adds their partial sums.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
@@ -162,6 +163,16 @@ struct BwdGeom {
   const float* row_nd;
   float* out1;                    // dQ pass: dQ;  dK/dV pass: dV
   float* out2;                    // dK/dV pass: dK
+  // Balance of a short last wave, as in the forward: the units (resident tile,
+  // column half) from n_main on are cut into ``split`` pieces over the streamed
+  // rows, piece c taking streamed tiles [piece_t[c], piece_t[c + 1]).  A piece
+  // writes its partial sums (already scaled) to part1 / part2, slot
+  // (unit - n_main) * split + c of 128 rows x kDV columns, and
+  // bwd_merge_pieces_kernel adds the pieces of each unit.  split == 1: no pieces.
+  static constexpr int kMaxSplit = 16;
+  int n_main, split;
+  int piece_t[kMaxSplit + 1];
+  float *part1, *part2;
 };
 
 struct Barriers {
@@ -252,7 +263,9 @@ __device__ __forceinline__ void bwd_tile(uint32_t (&raw)[128], uint32_t cSt, int
   tc_fence_before_sync();
 }
 
-template <int D, int kMode>
+// kCut: the grid's last wave is cut into pieces (see BwdGeom).  A separate
+// instantiation, so that grids without a cut run the plain code.
+template <int D, int kMode, bool kCut>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const __grid_constant__ BwdGeom geom, int* status) {
   using C = BwdCfg<D, kMode>;
@@ -269,12 +282,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   // Both column halves of a resident tile (head dim 256) are neighbours in the
   // grid, so they stream the same tiles through L2 at about the same time.
-  const int vh = blockIdx.x % C::kVSplit;       // which kDV gradient columns this CTA accumulates
-  const unsigned rb = blockIdx.x / C::kVSplit;  // unsigned: the divisions below stay unsigned
+  // A CTA past n_main is one piece of a unit of the last wave: that unit's
+  // streamed tiles [piece_t[c], piece_t[c + 1]).
+  unsigned unit = blockIdx.x;
+  int piece = -1;  // this CTA's partial-output slot, or -1 (outputs in place)
+  int t_first = 0, n_tiles = (geom.n_str + C::kBN - 1) / C::kBN;
+  if (kCut && unit >= static_cast<unsigned>(geom.n_main)) {
+    piece = static_cast<int>(unit - geom.n_main);
+    const unsigned u = static_cast<unsigned>(piece) / static_cast<unsigned>(geom.split);
+    const int c = piece - static_cast<int>(u) * geom.split;
+    unit = geom.n_main + u;
+    t_first = geom.piece_t[c];
+    n_tiles = geom.piece_t[c + 1] - t_first;
+  }
+  const int str0 = t_first * C::kBN;  // first streamed row of this CTA
+  const int vh = unit % C::kVSplit;       // which kDV gradient columns this CTA accumulates
+  const unsigned rb = unit / C::kVSplit;  // unsigned: the divisions below stay unsigned
   const int bh = rb / geom.n_rtiles;
   const int hh = bh % geom.H, bb = bh / geom.H;
   const int r0 = (rb % geom.n_rtiles) * C::kBM;
-  const int n_tiles = (geom.n_str + C::kBN - 1) / C::kBN;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->r_full, 1);
@@ -346,15 +372,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int sq = tq % C::kVecS;
           float* vec = reinterpret_cast<float*>(smem + C::kOffVec + sq * C::kVecSlot);
           mbar_arrive_expect_tx(&bars->vec_full[sq], C::kVecSlot);
-          tma_load_2d(vec, &maps.nl2, &bars->vec_full[sq], tq * C::kBN, bh);
-          tma_load_2d(vec + 64, &maps.nd, &bars->vec_full[sq], tq * C::kBN, bh);
+          tma_load_2d(vec, &maps.nl2, &bars->vec_full[sq], str0 + tq * C::kBN, bh);
+          tma_load_2d(vec + 64, &maps.nd, &bars->vec_full[sq], str0 + tq * C::kBN, bh);
           ++tq;
           progressed = true;
         }
         // tk counts score-ring units: unit u of streamed tile tk / kUPT
         if (tk < n_tiles * C::kUPT && mbar_test_wait(&bars->k_empty[tk % C::kKU], ((tk / C::kKU) & 1) ^ 1)) {
           const int s = tk % C::kKU;
-          const int row0 = (tk / C::kUPT) * C::kBN, u = tk % C::kUPT;
+          const int row0 = str0 + (tk / C::kUPT) * C::kBN, u = tk % C::kUPT;
           uint8_t* st = smem + C::kOffK + s * C::kKUnit;
           mbar_arrive_expect_tx(&bars->k_full[s], C::kKUnit);
           for (int c = 0; c < C::kUC; ++c) {
@@ -367,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (tv < nv && mbar_test_wait(&bars->v_empty[tv % C::kVS], ((tv / C::kVS) & 1) ^ 1)) {
           const int sv = tv % C::kVS;
-          const int row0 = tv * C::kBN;
+          const int row0 = str0 + tv * C::kBN;
           uint8_t* vt = smem + C::kOffV + sv * C::kVStage;
           mbar_arrive_expect_tx(&bars->v_full[sv], C::kVStage);
           for (int c = 0; c < C::kVC; ++c) {  // this CTA's gradient columns
@@ -570,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const uint32_t cSt = lane_addr + C::kColSt + 64u * bt;
       tmem_ld64_wait<64>(cSt, raw);
-      const int valid = min(C::kBN, geom.n_str - j * C::kBN);
+      const int valid = min(C::kBN, geom.n_str - str0 - j * C::kBN);
       const float* vec = reinterpret_cast<const float*>(smem + C::kOffVec + sq * C::kVecSlot);
       if (valid == C::kBN)
         bwd_tile<kMode, false>(raw, cSt, valid, c2, row_nl2, row_nd, vec, vec + 64);
@@ -589,13 +615,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const int rrow = r0 + row;
       const bool valid_row = rrow < geom.n_res;
-      const int64_t obase = (static_cast<int64_t>(bh) * geom.n_res + rrow) * geom.d + vh * C::kDV;
+      // in place, or a piece's slot of 128 rows of kDV columns
+      const bool part = kCut && piece >= 0;
+      const int64_t obase = part ? (static_cast<int64_t>(piece) * C::kBM + row) * C::kDV
+                                 : (static_cast<int64_t>(bh) * geom.n_res + rrow) * geom.d + vh * C::kDV;
       // dQ pass: ACC1 = dS K, times s.  dK/dV pass: ACC1 = dV, ACC2 = dS^T Q, times s.
       // The groups take alternate 32-column chunks.
       int chunk = 0;
 #pragma unroll 1
       for (int acc = 0; acc < (C::kDKDV ? 2 : 1); ++acc) {
-        float* out = (C::kDKDV && acc == 1) ? geom.out2 : geom.out1;
+        float* out = (C::kDKDV && acc == 1) ? (part ? geom.part2 : geom.out2) : (part ? geom.part1 : geom.out1);
         const float mul = (C::kDKDV && acc == 0) ? 1.f : geom.scale;
         const uint32_t col = acc == 0 ? C::kColAcc1 : C::kColAcc2;
         // this CTA's kDV columns, except for the 16/32-wide heads run as 64
@@ -645,6 +674,40 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
     const int64_t w = (r / nq) * nq_pad + r % nq;
     nl2[w] = -lse[r] * kLog2e;
     nd[w] = -s;
+  }
+}
+
+// Adds the pieces of each cut unit (see BwdGeom) into its outputs: one thread per
+// 4 columns of one row of one unit, both accumulators in the dK/dV pass.
+template <class C>
+__global__ void __launch_bounds__(256) bwd_merge_pieces_kernel(const __grid_constant__ BwdGeom geom, int n_units,
+                                                               int ncols) {
+  const int tpr = ncols >> 2;
+  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t rowid = gtid / tpr;  // unit * 128 + row
+  if (rowid >= static_cast<int64_t>(n_units) * C::kBM) return;
+  const int col = static_cast<int>(gtid % tpr) * 4;
+  const int u = static_cast<int>(rowid / C::kBM), r = static_cast<int>(rowid % C::kBM);
+  const unsigned unit = geom.n_main + u;
+  const int vh = unit % C::kVSplit;
+  const unsigned rb = unit / C::kVSplit;
+  const int bh = rb / geom.n_rtiles;
+  const int rrow = (rb % geom.n_rtiles) * C::kBM + r;
+  if (rrow >= geom.n_res) return;
+  const int64_t off = (static_cast<int64_t>(bh) * geom.n_res + rrow) * geom.d + vh * C::kDV + col;
+#pragma unroll 1
+  for (int acc = 0; acc < (C::kDKDV ? 2 : 1); ++acc) {
+    const float* part = acc == 0 ? geom.part1 : geom.part2;
+    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = 0; c < geom.split; ++c) {
+      const float4 x = *reinterpret_cast<const float4*>(
+          part + ((static_cast<int64_t>(u) * geom.split + c) * C::kBM + r) * C::kDV + col);
+      sum.x += x.x;
+      sum.y += x.y;
+      sum.z += x.z;
+      sum.w += x.w;
+    }
+    *reinterpret_cast<float4*>((acc == 0 ? geom.out1 : geom.out2) + off) = sum;
   }
 }
 
@@ -706,9 +769,15 @@ cudaError_t launch_pass(const BwdArgs& a, const float* nl2, const float* nd, con
     maps.nl2 = maps.r1;  // unused by the dQ pass
     maps.nd = maps.r1;
   }
-  static bool attr_set = false;  // one per instantiation
-  auto kern = attn_bwd_kernel<D, kMode>;
-  if (!attr_set) {
+  // A short last wave is cut into pieces over the streamed rows (the forward's
+  // rule), whose partial sums a second kernel adds.
+  const int n_rtiles = static_cast<int>((n_res + C::kBM - 1) / C::kBM);
+  const int64_t grid = static_cast<int64_t>(n_rtiles) * a.B * a.H * C::kVSplit;
+  const int n_sm = sm_count_fwd();
+  const int64_t split = last_wave_split(grid, n_str, n_sm);
+  static bool attr_set[2] = {false, false};  // per instantiation
+  auto kern = split > 1 ? attn_bwd_kernel<D, kMode, true> : attn_bwd_kernel<D, kMode, false>;
+  if (!attr_set[split > 1]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) {
       *msg = "cudaFuncSetAttribute(max dynamic shared memory) failed";
@@ -722,9 +791,8 @@ cudaError_t launch_pass(const BwdArgs& a, const float* nl2, const float* nd, con
       *msg = "backward kernel compiled with fewer registers than its warpgroup split needs";
       return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
     }
-    attr_set = true;
+    attr_set[split > 1] = true;
   }
-  const int n_rtiles = static_cast<int>((n_res + C::kBM - 1) / C::kBM);
   geom.H = static_cast<int>(a.H);
   geom.n_rtiles = n_rtiles;
   geom.n_res = static_cast<int>(n_res);
@@ -736,10 +804,46 @@ cudaError_t launch_pass(const BwdArgs& a, const float* nl2, const float* nd, con
   geom.row_nd = nd;
   geom.out1 = dkdv ? a.dv : a.dq;
   geom.out2 = dkdv ? a.dk : nullptr;
-  const int64_t grid = static_cast<int64_t>(n_rtiles) * a.B * a.H * C::kVSplit;
-  kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, a.stream>>>(maps, geom, a.status);
+  const int64_t tail = split > 1 ? grid % n_sm : 0;
+  geom.n_main = static_cast<int>(grid - tail);
+  geom.split = static_cast<int>(split);
+  geom.part1 = geom.part2 = nullptr;
+  void* ws = nullptr;
+  if (split > 1) {
+    const int64_t nt = (n_str + C::kBN - 1) / C::kBN;
+    for (int c = 0; c <= split; ++c) geom.piece_t[c] = static_cast<int>(c * nt / split);
+    const int64_t slot_floats = tail * split * C::kBM * C::kDV;
+    cudaMemPool_t pool = nullptr;
+    e = piece_pool(&pool);
+    if (e == cudaSuccess)
+      e = cudaMallocFromPoolAsync(&ws, static_cast<size_t>(slot_floats) * (dkdv ? 2 : 1) * sizeof(float), pool,
+                                  a.stream);
+    if (e != cudaSuccess) {
+      *msg = "stream-ordered allocation of the last wave's partial sums failed";
+      return e;
+    }
+    geom.part1 = static_cast<float*>(ws);
+    geom.part2 = dkdv ? geom.part1 + slot_floats : nullptr;
+  }
+  const int64_t launched = geom.n_main + tail * split;
+  kern<<<static_cast<unsigned>(launched), kThreads, C::kSmemBytes, a.stream>>>(maps, geom, a.status);
   e = cudaGetLastError();
   if (e != cudaSuccess) *msg = "attention-backward kernel launch failed";
+  if (ws) {
+    if (e == cudaSuccess) {
+      const int ncols = C::kDV == 128 ? C::kDV : static_cast<int>(a.d);
+      const int64_t threads = tail * C::kBM * (ncols / 4);
+      bwd_merge_pieces_kernel<C><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, a.stream>>>(
+          geom, static_cast<int>(tail), ncols);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) *msg = "merge of the backward's last-wave pieces failed to launch";
+    }
+    const cudaError_t f = cudaFreeAsync(ws, a.stream);
+    if (e == cudaSuccess && f != cudaSuccess) {
+      *msg = "stream-ordered release of the last wave's partial sums failed";
+      e = f;
+    }
+  }
   return e;
 }
 

@@ -747,6 +747,8 @@ __global__ void __launch_bounds__(256) merge_pieces_kernel(const __grid_constant
   }
 }
 
+}  // namespace
+
 // A stream-ordered memory pool per device for the last wave's partial outputs.
 // Its release threshold keeps the memory mapped between calls: a pool that gives
 // its memory back at every synchronisation maps it again on the next call, which
@@ -781,8 +783,6 @@ cudaError_t piece_pool(cudaMemPool_t* pool) {
   *pool = pools[dev];
   return cudaSuccess;
 }
-
-}  // namespace
 
 // Pieces per unit of the last wave (1: no cut) for a grid of ``grid`` units over
 // kv_len keys on n_sm SMs: only a last wave at most half full is cut, into as

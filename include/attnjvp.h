@@ -354,6 +354,11 @@ int64_t attn_jvp_fwd_host_workspace_bytes(int64_t B, int64_t H, int64_t N, int64
  *   workspace      : DEVICE, 256-byte aligned, attn_bwd_workspace_bytes(B, H, N_q).
  * Two passes (keys resident for dK/dV, queries resident for dQ) recompute the
  * scores instead of accumulating dQ with atomics, so results are reproducible.
+ * Each pass cuts a short last wave as attn_jvp_fwd does, over its streamed rows
+ * (queries for dK/dV, keys for dQ), and adds the pieces' partial sums in a
+ * second kernel; the partial sums come from the library's stream-ordered pool on
+ * ``stream``.  The pieces fix the order of those additions, so results stay
+ * reproducible for a given shape and GPU.
  */
 int attn_bwd(const void* q, const void* k, const void* v, const void* dout,
              const float* out, const float* lse, float* dq, float* dk, float* dv,

@@ -122,3 +122,35 @@ def test_last_wave_query_follows_the_documented_rule(cuda_lib):
         assert binding.attn_jvp_fwd_last_wave_split(B, H, Nq, Nkv, dv) == want, (B, H, Nq, Nkv, dv)
         seen.add(want > 1)
     assert seen == {True, False}
+
+
+@pytest.mark.parametrize("d,N", [(128, 1000), (64, 777), (256, 1000)])
+def test_backward_cut_tail_matches_oracle_and_uncut_heads(cuda_lib, d, N):
+    """The backward's two passes cut a short last wave the same way, over their
+    streamed rows (queries in the dK/dV pass, keys in the dQ pass), and add the
+    pieces' partial sums.  Heads whose units all ran in the first wave equal a
+    run over those heads alone (whole waves, no cut) bit for bit; the cut heads
+    are checked against the FP64 oracle."""
+    import oracle
+    from helpers import host64
+    n_qtiles = (N + 127) // 128
+    B, H = _shape(d, n_qtiles)
+    per_head = n_qtiles * (2 if d == 256 else 1)
+    assert binding.attn_jvp_fwd_last_wave_split(B, H, N, N, d) > 1  # the backward uses the same rule
+    g = torch.Generator(device="cuda").manual_seed(90 + d)
+    q, k, v, dO = (torch.randn((B, H, N, d), generator=g, device="cuda").to(torch.bfloat16) for _ in range(4))
+    scale = d ** -0.5
+    z = torch.zeros_like(q)
+    o, _, lse, _ = binding.attn_jvp_fwd_chunk(q, k, v, z, z, z, 0, N, scale=scale)
+    got = binding.attn_bwd(q, k, v, dO, o, lse, scale=scale)
+    first_cut = _sm_count() // per_head
+    sub = lambda t: t[:, :first_cut].contiguous()  # noqa: E731
+    ref = binding.attn_bwd(sub(q), sub(k), sub(v), sub(dO), sub(o), sub(lse), scale=scale)
+    torch.cuda.synchronize()
+    binding.attn_jvp_status()
+    for name, a, b in zip(("dQ", "dK", "dV"), got, ref):
+        assert torch.equal(a[:, :first_cut], b), name
+    for h in range(first_cut, H):
+        want = oracle.attn_bwd(host64(q[0, h]), host64(k[0, h]), host64(v[0, h]), host64(dO[0, h]), scale)
+        for name, a, r in zip(("dQ", "dK", "dV"), got, want):
+            assert_close(host64(a[0, h]), r, "%s head %d" % (name, h))
