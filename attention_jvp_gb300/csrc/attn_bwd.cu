@@ -134,6 +134,7 @@ struct BwdCfg {
   static_assert(!kShared || (kUPT == 1 && kVC == kDC), "a shared stage holds whole tiles of every column");
   static_assert(kKU * kKUnit == kKS * kKStage, "score ring size");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(kKU * kKUnit >= 8 * 4096, "the streamed-tile ring also holds the eight 4 KB epilogue stages");
   static_assert(kKStage % 1024 == 0 && kVStage % 1024 == 0, "stage alignment (128-byte swizzle atoms)");
 };
 
@@ -613,12 +614,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       tc_fence_after_sync();
-      const int rrow = r0 + row;
-      const bool valid_row = rrow < geom.n_res;
+      // Every MMA and copy of the CTA is done: the streamed-tile ring's shared
+      // memory is free and holds each elementwise warp's 4 KB epilogue stage.
+      // Stores from one thread per row would touch 32 rows per warp instruction,
+      // so a warp passes each 32-column chunk through its stage (16-byte unit u of
+      // row r at unit u ^ (r mod 8), conflict-free both ways) and writes it back
+      // four rows per instruction, eight lanes per 128-byte row segment.
+      fence_proxy_async_smem();
+      float4* stage = reinterpret_cast<float4*>(smem + C::kOffK + (group * 4 + quarter) * 4096);
+      const int ru = lane & 7, rr = lane >> 3;
       // in place, or a piece's slot of 128 rows of kDV columns
       const bool part = kCut && piece >= 0;
-      const int64_t obase = part ? (static_cast<int64_t>(piece) * C::kBM + row) * C::kDV
-                                 : (static_cast<int64_t>(bh) * geom.n_res + rrow) * geom.d + vh * C::kDV;
+      const int64_t rstride = part ? C::kDV : geom.d;
+      const int64_t obase0 = part ? (static_cast<int64_t>(piece) * C::kBM + quarter * 32) * C::kDV
+                                  : (static_cast<int64_t>(bh) * geom.n_res + r0 + quarter * 32) * geom.d +
+                                        vh * C::kDV;
+      const int valid_rows = min(32, geom.n_res - (r0 + quarter * 32));
       // dQ pass: ACC1 = dS K, times s.  dK/dV pass: ACC1 = dV, ACC2 = dS^T Q, times s.
       // The groups take alternate 32-column chunks.
       int chunk = 0;
@@ -634,16 +645,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           if ((chunk++ & 1) != group) continue;
           uint32_t v[32];
           tmem_ld32_wait(lane_addr + col + c0, v);
-          if (valid_row) {
-            float4* o4 = reinterpret_cast<float4*>(out + obase + c0);
-            const int n4 = C::kDV == 128 ? 8 : min(8, (ncols - c0) >> 2);
 #pragma unroll
+          for (int i = 0; i < 8; ++i)
+            stage[lane * 8 + (i ^ (lane & 7))] =
+                make_float4(__uint_as_float(v[4 * i]) * mul, __uint_as_float(v[4 * i + 1]) * mul,
+                            __uint_as_float(v[4 * i + 2]) * mul, __uint_as_float(v[4 * i + 3]) * mul);
+          __syncwarp();
+          if (c0 + 4 * ru < ncols) {
+#pragma unroll 1
             for (int i = 0; i < 8; ++i) {
-              if (C::kDV != 128 && i >= n4) break;
-              o4[i] = make_float4(__uint_as_float(v[4 * i]) * mul, __uint_as_float(v[4 * i + 1]) * mul,
-                                  __uint_as_float(v[4 * i + 2]) * mul, __uint_as_float(v[4 * i + 3]) * mul);
+              const int r = rr + 4 * i;
+              if (r < valid_rows)
+                *reinterpret_cast<float4*>(out + obase0 + r * rstride + c0 + 4 * ru) = stage[r * 8 + (ru ^ (r & 7))];
             }
           }
+          __syncwarp();  // the next chunk overwrites the stage
         }
       }
     }
