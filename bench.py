@@ -767,15 +767,22 @@ def run_gpu(args):
         h2d = sum(tt.numel() * tt.element_size() for tt in list(host_in.values()) + lat_in)
         d2h = sum(tt.numel() * tt.element_size() for tt in host_out + [lat_out])
 
+        # The latent batch's copies and tangent are independent of the attention, so
+        # they run on a stream of their own beside the host path; the step ends when
+        # both have (the caller's stream waits for the latent stream's last copy).
+        lat_stream = torch.cuda.Stream(device=dev)
+
         def e2e_step():
-            with torch.cuda.stream(stream):
+            lat_stream.wait_stream(stream)
+            with torch.cuda.stream(lat_stream):
                 for hsrc, ddst in zip(lat_in, lat_dev):
                     ddst.copy_(hsrc, non_blocking=True)
                 coeffs = [binding.trigflow_coeffs(tt) for tt in t_host]  # FP64, host
-                binding.trigflow_tangent(lat_dev[0], lat_dev[1], lat_dev[2], out=dxdt, stream=stream)
+                binding.trigflow_tangent(lat_dev[0], lat_dev[1], lat_dev[2], out=dxdt, stream=lat_stream)
                 lat_out.copy_(dxdt, non_blocking=True)
             binding.attn_jvp_fwd_host(*(host_in[n] for n in inputs.NAMES), *host_out, scale=scale,
                                       n_chunks=n_chunks, workspace=ws_host, stream=stream)
+            stream.wait_stream(lat_stream)
             return coeffs
 
         e2e_step()
