@@ -655,8 +655,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
             for (int i = 0; i < 8; ++i) {
               const int r = rr + 4 * i;
-              if (r < valid_rows)
-                *reinterpret_cast<float4*>(out + obase0 + r * rstride + c0 + 4 * ru) = stage[r * 8 + (ru ^ (r & 7))];
+              if (r < valid_rows)  // streaming stores: the gradients are not read again here
+                __stcs(reinterpret_cast<float4*>(out + obase0 + r * rstride + c0 + 4 * ru), stage[r * 8 + (ru ^ (r & 7))]);
             }
           }
           __syncwarp();  // the next chunk overwrites the stage

@@ -331,8 +331,10 @@ __device__ __forceinline__ void write_rows(uint32_t lane_addr, const RowState& s
       const int r = rr + 4 * i;
       if (col_ok && r < valid_rows) {
         const int64_t off = obase0 + static_cast<int64_t>(r) * ostride + c0 + 4 * ru;
-        *reinterpret_cast<float4*>(out + off) = so[r * 8 + (ru ^ (r & 7))];
-        *reinterpret_cast<float4*>(out_t + off) = stt[r * 8 + (ru ^ (r & 7))];
+        // streaming stores: the outputs are not read again, so they should not
+        // push the key and value tiles out of L2
+        __stcs(reinterpret_cast<float4*>(out + off), so[r * 8 + (ru ^ (r & 7))]);
+        __stcs(reinterpret_cast<float4*>(out_t + off), stt[r * 8 + (ru ^ (r & 7))]);
       }
     }
     __syncwarp();  // the next chunk overwrites the stage
@@ -738,8 +740,8 @@ __global__ void __launch_bounds__(256) merge_pieces_kernel(const __grid_constant
   t.w -= mu_row * o.w;
   const int64_t off = static_cast<int64_t>(bb) * geom.o_stride[0] + static_cast<int64_t>(qrow) * geom.o_stride[1] +
                       static_cast<int64_t>(hh) * geom.o_stride[2] + vh * C::kDV + col;
-  *reinterpret_cast<float4*>(out + off) = o;
-  *reinterpret_cast<float4*>(out_t + off) = t;
+  __stcs(reinterpret_cast<float4*>(out + off), o);
+  __stcs(reinterpret_cast<float4*>(out_t + off), t);
   if (col == 0 && vh == 0) {
     const int64_t ridx = static_cast<int64_t>(bh) * geom.Nq + qrow;
     if (lse) lse[ridx] = L;
