@@ -829,11 +829,7 @@ cudaError_t launch_pass(const BwdArgs& a, const float* nl2, const float* nd, con
     const int64_t nt = (n_str + C::kBN - 1) / C::kBN;
     for (int c = 0; c <= split; ++c) geom.piece_t[c] = static_cast<int>(c * nt / split);
     const int64_t slot_floats = tail * split * C::kBM * C::kDV;
-    cudaMemPool_t pool = nullptr;
-    e = piece_pool(&pool);
-    if (e == cudaSuccess)
-      e = cudaMallocFromPoolAsync(&ws, static_cast<size_t>(slot_floats) * (dkdv ? 2 : 1) * sizeof(float), pool,
-                                  a.stream);
+    e = piece_alloc(&ws, static_cast<size_t>(slot_floats) * (dkdv ? 2 : 1) * sizeof(float), a.stream);
     if (e != cudaSuccess) {
       *msg = "stream-ordered allocation of the last wave's partial sums failed";
       return e;

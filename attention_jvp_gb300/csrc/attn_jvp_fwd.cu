@@ -757,7 +757,7 @@ __global__ void __launch_bounds__(256) merge_pieces_kernel(const __grid_constant
 // costs more than the cut saves.  It holds at most the largest set of partials a
 // call has needed (SMs x 128 rows x (2 x 128 + 2) floats, about 20 MB on 152 SMs)
 // and lives as long as the process.
-cudaError_t piece_pool(cudaMemPool_t* pool) {
+static cudaError_t piece_pool(cudaMemPool_t* pool) {
   constexpr int kMaxDev = 64;
   static std::mutex mu;
   static cudaMemPool_t pools[kMaxDev] = {};
@@ -784,6 +784,19 @@ cudaError_t piece_pool(cudaMemPool_t* pool) {
   }
   *pool = pools[dev];
   return cudaSuccess;
+}
+
+cudaError_t piece_alloc(void** ptr, size_t bytes, cudaStream_t stream) {
+  // A stream being captured into a CUDA graph takes the allocation as a graph
+  // memory node from the device's default pool; otherwise the library's pool.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) return e;
+  if (cap != cudaStreamCaptureStatusNone) return cudaMallocAsync(ptr, bytes, stream);
+  cudaMemPool_t pool = nullptr;
+  e = piece_pool(&pool);
+  if (e != cudaSuccess) return e;
+  return cudaMallocFromPoolAsync(ptr, bytes, pool, stream);
 }
 
 // Pieces per unit of the last wave (1: no cut) for a grid of ``grid`` units over
@@ -867,11 +880,7 @@ cudaError_t launch_d(const FwdArgs& a, const char** msg) {
   void* ws = nullptr;
   if (split > 1) {
     const int64_t slots = tail * split * C::kBM;
-    cudaMemPool_t pool = nullptr;
-    e = piece_pool(&pool);
-    if (e == cudaSuccess)
-      e = cudaMallocFromPoolAsync(&ws, static_cast<size_t>(slots) * (2 * C::kDV + 2) * sizeof(float), pool,
-                                  a.stream);
+    e = piece_alloc(&ws, static_cast<size_t>(slots) * (2 * C::kDV + 2) * sizeof(float), a.stream);
     if (e != cudaSuccess) {
       *msg = "stream-ordered allocation of the last wave's partial outputs failed";
       return e;

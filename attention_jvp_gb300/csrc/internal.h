@@ -37,9 +37,11 @@ cudaError_t launch_attn_jvp_fwd(const FwdArgs& a, const char** msg);
 // SM count (0 if unknown).
 int64_t last_wave_split(int64_t grid, int64_t kv_len, int n_sm);
 int sm_count_fwd();
-// The current device's stream-ordered pool for the last wave's partial outputs
-// (memory kept mapped between calls; lives as long as the process).
-cudaError_t piece_pool(cudaMemPool_t* pool);
+// Stream-ordered allocation of the last wave's partial outputs on ``stream``: from
+// a per-device pool that keeps its memory mapped between calls (and lives as
+// long as the process), or, while the stream is being captured into a CUDA
+// graph, from the default pool as a graph memory node.  Freed with cudaFreeAsync.
+cudaError_t piece_alloc(void** ptr, size_t bytes, cudaStream_t stream);
 
 cudaError_t launch_merge(const float* o_c, const float* ot_c, const float* lse_c, const float* mu_c,
                          int64_t n_chunks, float* out, float* out_t, float* lse, float* mu, int64_t rows,

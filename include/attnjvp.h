@@ -35,6 +35,11 @@
  *     primary context, while it is loaded.  For the same lifetime it keeps, per
  *     device, one stream-ordered memory pool for the partial outputs of a cut
  *     last wave (see attn_jvp_fwd), which it does not give back to the system.
+ *   - Calls may be captured into a CUDA graph once the same entry point has run
+ *     on the device outside capture (the first call looks up the device state
+ *     above, which capture does not allow).  Under capture, the stream-ordered
+ *     allocations of the fp32 path and of a cut last wave become graph memory
+ *     nodes from the device's default pool.
  */
 #ifndef ATTNJVP_H
 #define ATTNJVP_H
