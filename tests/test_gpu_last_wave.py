@@ -154,3 +154,40 @@ def test_backward_cut_tail_matches_oracle_and_uncut_heads(cuda_lib, d, N):
         want = oracle.attn_bwd(host64(q[0, h]), host64(k[0, h]), host64(v[0, h]), host64(dO[0, h]), scale)
         for name, a, r in zip(("dQ", "dK", "dV"), got, want):
             assert_close(host64(a[0, h]), r, "%s head %d" % (name, h))
+
+
+def test_cut_tail_cross_attention_with_own_value_dim(cuda_lib):
+    """N_q != N_kv and d_v != d through the general entry point over the whole key
+    range: the forward cuts (its units are query tiles); the backward's dQ pass cuts
+    and its dK/dV pass (fewer key tiles than one wave) does not."""
+    import oracle
+    from helpers import host64
+    d, dv, Nq, Nkv = 128, 64, 1000, 700
+    B, H = _shape(128, (Nq + 127) // 128)
+    assert binding.attn_jvp_fwd_last_wave_split(B, H, Nq, Nkv, dv) > 1
+    g = torch.Generator(device="cuda").manual_seed(97)
+    mk = lambda n, c: (torch.randn((B, H, n, c), generator=g, device="cuda") * 0.8).to(torch.bfloat16)  # noqa: E731
+    q, qt, k, kt = mk(Nq, d), mk(Nq, d), mk(Nkv, d), mk(Nkv, d)
+    v, vt = mk(Nkv, dv), mk(Nkv, dv)
+    s = d ** -0.5
+    got = binding.attn_jvp_fwd_strided(q, k, v, qt, kt, vt, scale=s)
+    torch.cuda.synchronize()
+    binding.attn_jvp_status()
+    first_cut = _sm_count() // ((Nq + 127) // 128)
+    for h in range(first_cut, H):
+        o = oracle.attn_jvp(host64(q[0, h]), host64(k[0, h]), host64(v[0, h]), host64(qt[0, h]),
+                            host64(kt[0, h]), host64(vt[0, h]), s)
+        assert_close(host64(got[0][0, h]), o[0], "O head %d" % h)
+        assert_close(host64(got[1][0, h]), o[1], "Ot head %d" % h)
+        assert_close(host64(got[3][0, h]), o[3], "mu head %d" % h)
+    # backward (d_v = d required): the dQ pass cuts, the dK/dV pass does not
+    v2, dO = mk(Nkv, d), mk(Nq, d)
+    z = torch.zeros_like
+    o2, _, lse2, _ = binding.attn_jvp_fwd_strided(q, k, v2, z(q), z(k), z(v2), scale=s)
+    dq, dk, dv_ = binding.attn_bwd(q, k, v2, dO, o2, lse2, scale=s)
+    torch.cuda.synchronize()
+    binding.attn_jvp_status()
+    for h in range(first_cut, H):
+        want = oracle.attn_bwd(host64(q[0, h]), host64(k[0, h]), host64(v2[0, h]), host64(dO[0, h]), s)
+        for name, a, r in zip(("dQ", "dK", "dV"), (dq, dk, dv_), want):
+            assert_close(host64(a[0, h]), r, "%s head %d" % (name, h))
