@@ -758,6 +758,16 @@ cudaError_t make_vec_map(CUtensorMap* map, const float* ptr, int64_t rows, int64
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Registers per thread the kernel was compiled with (-1 if unknown); looked up once.
+template <int D, int kMode, bool kCut>
+int compiled_regs() {
+  static const int regs = [] {
+    cudaFuncAttributes fa;
+    return cudaFuncGetAttributes(&fa, attn_bwd_kernel<D, kMode, kCut>) == cudaSuccess ? fa.numRegs : -1;
+  }();
+  return regs;
+}
+
 template <int D, int kMode>
 cudaError_t launch_pass(const BwdArgs& a, const float* nl2, const float* nd, const char** msg) {
   using C = BwdCfg<D, kMode>;
@@ -789,25 +799,21 @@ cudaError_t launch_pass(const BwdArgs& a, const float* nl2, const float* nd, con
   // rule), whose partial sums a second kernel adds.
   const int n_rtiles = static_cast<int>((n_res + C::kBM - 1) / C::kBM);
   const int64_t grid = static_cast<int64_t>(n_rtiles) * a.B * a.H * C::kVSplit;
-  const int n_sm = sm_count_fwd();
+  const int n_sm = device_sm_count();
   const int64_t split = last_wave_split(grid, n_str, n_sm);
-  static bool attr_set[2] = {false, false};  // per instantiation
   auto kern = split > 1 ? attn_bwd_kernel<D, kMode, true> : attn_bwd_kernel<D, kMode, false>;
-  if (!attr_set[split > 1]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) {
-      *msg = "cudaFuncSetAttribute(max dynamic shared memory) failed";
-      return e;
-    }
-    // The warpgroups' register split must fit the pool the block launches with
-    // (see kRegsIssue); a smaller compiled count would leave setmaxnreg.inc waiting.
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, kern);
-    if (e != cudaSuccess || fa.numRegs * kThreads < kRegPoolNeeded) {
-      *msg = "backward kernel compiled with fewer registers than its warpgroup split needs";
-      return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
-    }
-    attr_set[split > 1] = true;
+  // The warpgroups' register split must fit the pool the block launches with
+  // (see kRegsIssue); a smaller compiled count would leave setmaxnreg.inc waiting.
+  const int regs = split > 1 ? compiled_regs<D, kMode, true>() : compiled_regs<D, kMode, false>();
+  if (regs * kThreads < kRegPoolNeeded) {
+    *msg = "backward kernel compiled with fewer registers than its warpgroup split needs";
+    return cudaErrorInvalidConfiguration;
+  }
+  bool first = false;
+  e = ensure_smem_limit(reinterpret_cast<const void*>(kern), C::kSmemBytes, &first);
+  if (e != cudaSuccess) {
+    *msg = "cudaFuncSetAttribute(max dynamic shared memory) failed";
+    return e;
   }
   geom.H = static_cast<int>(a.H);
   geom.n_rtiles = n_rtiles;

@@ -814,17 +814,6 @@ int64_t last_wave_split(int64_t grid, int64_t kv_len, int n_sm) {
   return split >= 2 ? split : 1;
 }
 
-int sm_count_fwd() {
-  static int cached = 0;
-  if (cached == 0) {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      return 0;
-    cached = n;
-  }
-  return cached;
-}
 
 namespace {
 
@@ -846,15 +835,12 @@ cudaError_t launch_d(const FwdArgs& a, const char** msg) {
     *msg = "cuTensorMapEncodeTiled rejected a tensor (alignment, stride or size)";
     return e;
   }
-  static bool attr_set = false;  // one per instantiation
   auto kern = attn_jvp_fwd_kernel<D, DVF>;
-  if (!attr_set) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) {
-      *msg = "cudaFuncSetAttribute(max dynamic shared memory) failed";
-      return e;
-    }
-    attr_set = true;
+  bool first = false;
+  e = ensure_smem_limit(reinterpret_cast<const void*>(kern), C::kSmemBytes, &first);
+  if (e != cudaSuccess) {
+    *msg = "cudaFuncSetAttribute(max dynamic shared memory) failed";
+    return e;
   }
   const int n_qtiles = static_cast<int>((a.Nq + C::kBM - 1) / C::kBM);
   geom.H = static_cast<int>(a.H);
@@ -873,7 +859,7 @@ cudaError_t launch_d(const FwdArgs& a, const char** msg) {
   geom.n_main = static_cast<int>(grid);
   geom.split = 1;
   geom.part_o = geom.part_ot = geom.part_lse = geom.part_mu = nullptr;
-  const int n_sm = sm_count_fwd();
+  const int n_sm = device_sm_count();
   const int64_t tail = n_sm > 0 ? grid % n_sm : 0;
   const int64_t nt = (a.kv_len + C::kBN - 1) / C::kBN;
   const int64_t split = a.balance_tail ? last_wave_split(grid, a.kv_len, n_sm) : 1;

@@ -172,16 +172,8 @@ __global__ void wait_selftest_kernel(int* status, uint64_t limit_ns) {
 }
 
 int sm_count() {
-  static int cached = 0;
-  if (cached == 0) {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
-      cached = n;
-    else
-      return 148;
-  }
-  return cached;
+  const int n = device_sm_count();
+  return n > 0 ? n : 148;
 }
 
 }  // namespace

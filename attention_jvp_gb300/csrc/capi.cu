@@ -10,6 +10,8 @@
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "../../include/attnjvp.h"
 #include "internal.h"
@@ -66,6 +68,40 @@ int* status_word(const char** why) {
   }
   return g_status_ptr[dev];
 }
+
+int g_sm_count[kMaxDevices] = {};
+std::vector<std::pair<const void*, int>> g_smem_set;  // (kernel, device) pairs done
+
+}  // namespace
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 0;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+cudaError_t ensure_smem_limit(const void* func, int bytes, bool* first) {
+  *first = false;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (const auto& fd : g_smem_set)
+    if (fd.first == func && fd.second == dev) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  g_smem_set.emplace_back(func, dev);
+  *first = true;
+  return cudaSuccess;
+}
+
+namespace {
 
 // Head dims: the page's set, 16, 32, 64, 128 and 256, in the forward and the
 // backward (at 256 two CTAs share each row tile, each accumulating half of the
@@ -323,7 +359,7 @@ int attn_jvp_fwd_last_wave_split(int64_t B, int64_t H, int64_t N_q, int64_t N_kv
     return fail(ATTNJVP_EINVAL, "B, H, N_q, N_kv must be >= 1 (B*H, N_q and N_kv below 2^31)");
   const int rc = check_head_dim(d_v, true);
   if (rc != ATTNJVP_OK) return rc;
-  const int n_sm = sm_count_fwd();
+  const int n_sm = device_sm_count();
   if (n_sm <= 0) return fail(ATTNJVP_ECUDA, "no CUDA device to size the grid for");
   const int64_t grid = (N_q + 127) / 128 * B * H * (d_v > 128 ? 2 : 1);
   *split = last_wave_split(grid, N_kv, n_sm);

@@ -36,7 +36,13 @@ cudaError_t launch_attn_jvp_fwd(const FwdArgs& a, const char** msg);
 // ``grid`` units over kv_len keys on n_sm SMs (1: no cut); the current device's
 // SM count (0 if unknown).
 int64_t last_wave_split(int64_t grid, int64_t kv_len, int n_sm);
-int sm_count_fwd();
+
+// The current device's SM count, looked up once per device (0 if unknown).
+int device_sm_count();
+// Raises ``func``'s dynamic shared-memory limit to ``bytes`` on the current
+// device, once per (kernel, device); ``*first`` tells whether this call did it.
+// Thread-safe.
+cudaError_t ensure_smem_limit(const void* func, int bytes, bool* first);
 // Stream-ordered allocation of the last wave's partial outputs on ``stream``: from
 // a per-device pool that keeps its memory mapped between calls (and lives as
 // long as the process), or, while the stream is being captured into a CUDA

@@ -105,16 +105,8 @@ __global__ void __launch_bounds__(256) qk_rmsnorm_jvp_kernel(QkNormArgs a) {
 }
 
 int sm_count_cached() {
-  static int cached = 0;
-  if (cached == 0) {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
-      cached = n;
-    else
-      return 148;
-  }
-  return cached;
+  const int n = device_sm_count();
+  return n > 0 ? n : 148;
 }
 
 template <int G>
