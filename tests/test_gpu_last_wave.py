@@ -191,3 +191,36 @@ def test_cut_tail_cross_attention_with_own_value_dim(cuda_lib):
         want = oracle.attn_bwd(host64(q[0, h]), host64(k[0, h]), host64(v2[0, h]), host64(dO[0, h]), s)
         for name, a, r in zip(("dQ", "dK", "dV"), (dq, dk, dv_), want):
             assert_close(host64(a[0, h]), r, "%s head %d" % (name, h))
+
+
+def test_image_dit_workload_cut_rows_at_full_size(cuda_lib):
+    """The image DiT 1K workload (B=2, H=24, N=4096, d=128) as the benchmark runs it: on a
+    152-SM GB300 its 1536 units leave a 16-unit last wave, which is cut.  Seeded rows of
+    the cut units (the last head's second half, on such a GPU) against the oracle."""
+    from helpers import gpu_rows, oracle_on
+    spec = inputs.WORKLOADS["image_dit_1k"]
+    B, H, N, d = spec["B"], spec["H"], spec["N"], spec["d"]
+    n_sm = _sm_count()
+    grid = B * H * (N // 128)
+    pieces = binding.attn_jvp_fwd_last_wave_split(B, H, N, N, d)
+    tail = grid % n_sm
+    if pieces == 1:
+        pytest.skip("this GPU's SM count (%d) leaves no short last wave for this workload" % n_sm)
+    x = inputs.workload_inputs("image_dit_1k", device="cuda")
+    got = binding.attn_jvp_fwd(*(x[n] for n in inputs.NAMES), scale=x["scale"])
+    torch.cuda.synchronize()
+    binding.attn_jvp_status()
+    # cut units: the last ``tail`` (query tile) units, i.e. flat heads / tiles at the end
+    first_unit = grid - tail
+    units = range(first_unit, grid)
+    heads = sorted(set(u // (N // 128) for u in units))
+    rng = np.random.default_rng(101)
+    for h in heads:
+        tiles = [u % (N // 128) for u in units if u // (N // 128) == h]
+        rows = np.unique(np.concatenate([rng.integers(t * 128, t * 128 + 128, 6) for t in tiles]))
+        ref = oracle_on(x, heads=[h], rows=rows)
+        g = [gpu_rows(t, [h], rows) for t in got]
+        assert_close(g[0], ref[0], "O")
+        assert_close(g[1], ref[1], "Ot")
+        assert_close(g[3], ref[3], "mu")
+        assert np.max(np.abs(g[2] - ref[2])) <= 1e-3
