@@ -341,200 +341,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
 
   // Registers: the TMA and MMA warps need few, the elementwise warps hold a
-  // whole tile of scores per thread (fewer spills; about 1 % faster).
-  if (warp < 4)
-    setmaxnreg_dec<kRegsIssue>();
-  else
+  // whole tile of scores per thread.  Each setmaxnreg is the first instruction of
+  // the region it governs (all warps of a warpgroup execute the same one), so the
+  // compiler allocates each region within its own count.
+  if (warp >= 4) {
     setmaxnreg_inc<kRegsElem>();
-
-  if (warp == 0) {
-    // ---------------- TMA producer: resident tiles, then the score-tile ring (X1, X2) and
-    // the value-tile ring, each refilled as soon as its own stage is free (the thread polls
-    // both; the value ring frees much later than the score ring) ----------------
-    if (lane == 0) {
-      prefetch_tensormap(&maps.r1);
-      prefetch_tensormap(&maps.r2);
-      prefetch_tensormap(&maps.x1);
-      prefetch_tensormap(&maps.x2);
-      mbar_arrive_expect_tx(&bars->r_full, 2 * C::kRBytes);
-      for (int c = 0; c < C::kDC; ++c) {
-        tma_load_4d(smem + C::kOffR1 + c * C::kChunkR, &maps.r1, &bars->r_full, c * 64, r0, hh, bb);
-        tma_load_4d(smem + C::kOffR2 + c * C::kChunkR, &maps.r2, &bars->r_full, c * 64, r0, hh, bb);
-      }
-      int tk = 0, tv = 0, tq = 0;  // next tile of each ring (tq: the vector ring)
-      const int nq = C::kDKDV ? n_tiles : 0;
-      const int nv = C::kShared ? 0 : n_tiles;  // tiles of the value ring of its own
-      bool ok = true;
-      uint64_t t0 = globaltimer_ns();
-      uint32_t idle = 0;
-      while (tk < n_tiles * C::kUPT || tv < nv || tq < nq) {
-        bool progressed = false;
-        if (tq < nq && mbar_test_wait(&bars->vec_empty[tq % C::kVecS], ((tq / C::kVecS) & 1) ^ 1)) {
-          const int sq = tq % C::kVecS;
-          float* vec = reinterpret_cast<float*>(smem + C::kOffVec + sq * C::kVecSlot);
-          mbar_arrive_expect_tx(&bars->vec_full[sq], C::kVecSlot);
-          tma_load_2d(vec, &maps.nl2, &bars->vec_full[sq], str0 + tq * C::kBN, bh);
-          tma_load_2d(vec + 64, &maps.nd, &bars->vec_full[sq], str0 + tq * C::kBN, bh);
-          ++tq;
-          progressed = true;
-        }
-        // tk counts score-ring units: unit u of streamed tile tk / kUPT
-        if (tk < n_tiles * C::kUPT && mbar_test_wait(&bars->k_empty[tk % C::kKU], ((tk / C::kKU) & 1) ^ 1)) {
-          const int s = tk % C::kKU;
-          const int row0 = str0 + (tk / C::kUPT) * C::kBN, u = tk % C::kUPT;
-          uint8_t* st = smem + C::kOffK + s * C::kKUnit;
-          mbar_arrive_expect_tx(&bars->k_full[s], C::kKUnit);
-          for (int c = 0; c < C::kUC; ++c) {
-            const int col = (u * C::kUC + c) * 64;
-            tma_load_4d(st + c * C::kChunkX, &maps.x1, &bars->k_full[s], col, row0, hh, bb);
-            tma_load_4d(st + (C::kUC + c) * C::kChunkX, &maps.x2, &bars->k_full[s], col, row0, hh, bb);
-          }
-          ++tk;
-          progressed = true;
-        }
-        if (tv < nv && mbar_test_wait(&bars->v_empty[tv % C::kVS], ((tv / C::kVS) & 1) ^ 1)) {
-          const int sv = tv % C::kVS;
-          const int row0 = str0 + tv * C::kBN;
-          uint8_t* vt = smem + C::kOffV + sv * C::kVStage;
-          mbar_arrive_expect_tx(&bars->v_full[sv], C::kVStage);
-          for (int c = 0; c < C::kVC; ++c) {  // this CTA's gradient columns
-            const int col = vh * C::kDV + c * 64;
-            if (C::kDKDV) {  // dO (for dV), then Q (for dK)
-              tma_load_4d(vt + c * C::kChunkX, &maps.x2, &bars->v_full[sv], col, row0, hh, bb);
-              tma_load_4d(vt + (C::kVC + c) * C::kChunkX, &maps.x1, &bars->v_full[sv], col, row0, hh, bb);
-            } else {  // K (for dQ)
-              tma_load_4d(vt + c * C::kChunkX, &maps.x1, &bars->v_full[sv], col, row0, hh, bb);
-            }
-          }
-          ++tv;
-          progressed = true;
-        }
-        if (progressed) {
-          t0 = globaltimer_ns();
-          idle = 0;
-          continue;
-        }
-        __nanosleep(64);
-        // Bounded: a second without either ring moving means a broken protocol.
-        if ((++idle & 15u) == 0u) {
-          if (*abort_flag) {
-            ok = false;
-          } else if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            *abort_flag = 1;
-            atomicOr(status, kStatusTimeout);
-            ok = false;
-          }
-          if (!ok) break;
-        }
-      }
-      // Let copies still in flight land before the CTA's shared memory goes away, on the
-      // normal path too (another role may give up right after the last copy was issued).
-      volatile int no_abort = 0;
-      mbar_wait(&bars->r_full, 0, &no_abort, nullptr, 0);
-      for (int n = tk - C::kKU; n < tk; ++n)
-        if (n >= 0) mbar_wait(&bars->k_full[n % C::kKU], (n / C::kKU) & 1, &no_abort, nullptr, 0);
-      for (int t = tv - C::kVS; t < tv; ++t)
-        if (t >= 0) mbar_wait(&bars->v_full[t % C::kVS], (t / C::kVS) & 1, &no_abort, nullptr, 0);
-      for (int t = tq - C::kVecS; t < tq; ++t)
-        if (t >= 0) mbar_wait(&bars->vec_full[t % C::kVecS], (t / C::kVecS) & 1, &no_abort, nullptr, 0);
-    }
-  } else if (warp >= 1 && warp <= 3) {
-    // ---------------- tcgen05.mma issuers: warp 3 S1, warp 2 S2, warp 1 the value MMAs ----------------
-    if (lane == 0) {
-      constexpr uint32_t kIdS = make_idesc_bf16_f32(128, C::kBN, false, false);  // both K-major
-      constexpr uint32_t kIdPV = make_idesc_bf16_f32(128, C::kDV, false, true);  // B N-major
-      const uint64_t dR1 = make_smem_desc_sw128(smem_u32(smem + C::kOffR1), 16, 1024);
-      const uint64_t dR2 = make_smem_desc_sw128(smem_u32(smem + C::kOffR2), 16, 1024);
-      const uint64_t dK0 = make_smem_desc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
-      // B operands of the value MMAs: a stage of the shared ring (X1 chunks, then X2
-      // chunks) or of the value ring of its own
-      const uint64_t dV0 =
-          make_smem_desc_sw128(smem_u32(smem + (C::kShared ? C::kOffK : C::kOffV)), C::kChunkX, 1024);
-      auto off = [](uint64_t desc, uint32_t bytes) { return desc + static_cast<uint64_t>(bytes >> 4); };
-      volatile int no_abort = 0;
-      if (warp == 3 || warp == 2) {
-        // S1 = R1 X1^T (warp 3) or S2 = R2 X2^T (warp 2), d-deep, N = 64.
-        const bool first = warp == 3;
-        const uint64_t dA = first ? dR1 : dR2;
-        const uint32_t aT = tmem + (first ? C::kColR1 : C::kColR2);  // dQ pass: A in TMEM
-        const uint32_t xoff = first ? 0u : static_cast<uint32_t>(C::kUC * C::kChunkX);
-        bool ok = C::kRTmem ? mbar_wait(&bars->r_tmem, 0, abort_flag, status, kStatusTimeout)
-                            : mbar_wait(&bars->r_full, 0, abort_flag, status, kStatusTimeout);
-        for (int t = 0; ok && t < n_tiles; ++t) {
-          const int b = first ? t % C::kNS : t % C::kNSt;
-          const int bs = first ? t % C::kSBar : b;  // barrier slot
-          const uint32_t dst = tmem + (first ? C::kColS : C::kColSt) + 64u * b;
-#pragma unroll 1
-          for (int u = 0; u < C::kUPT; ++u) {
-            const int n = t * C::kUPT + u;
-            const int s = n % C::kKU;
-            ok = mbar_wait(&bars->k_full[s], (n / C::kKU) & 1, abort_flag, status, kStatusTimeout);
-            // S1 buffers are free once the elementwise warps loaded tile t - NS; S2 buffers
-            // hold the packed operands of tile t - NSt until its value MMAs are done.
-            if (ok && u == 0 && first && t >= C::kNS)
-              ok = mbar_wait(&bars->s_free[(t - C::kNS) % C::kSBar], ((t - C::kNS) / C::kSBar) & 1, abort_flag,
-                             status, kStatusTimeout);
-            if (ok && u == 0 && !first && t >= C::kNSt)
-              ok = mbar_wait(&bars->pv_done[b], ((t - C::kNSt) / C::kNSt) & 1, abort_flag, status,
-                             kStatusTimeout);
-            if (!ok) break;
-            tc_fence_after_sync();
-            const uint64_t dX = off(dK0, s * C::kKUnit + xoff);
-#pragma unroll
-            for (int c = 0; c < C::kUC; ++c)
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const int cg = u * C::kUC + c;  // d-chunk of the resident operand
-                if constexpr (C::kRTmem)
-                  mma_ts(dst, aT + (cg * 4 + kk) * 8, off(dX, c * C::kChunkX + kk * 32), kIdS, (u | c | kk) != 0);
-                else
-                  mma_ss(dst, off(dA, cg * C::kChunkR + kk * 32), off(dX, c * C::kChunkX + kk * 32), kIdS,
-                         (u | c | kk) != 0);
-              }
-            mma_commit(&bars->k_empty[s]);
-          }
-          if (!ok) break;
-          mma_commit(first ? &bars->s_full[bs] : &bars->st_full[b]);
-        }
-        uint64_t* drain = first ? &bars->drain_s : &bars->drain_st;
-        mma_commit(drain);
-        mbar_wait(drain, 0, &no_abort, nullptr, 0);
-      } else {
-        bool ok = true;
-        for (int j = 0; ok && j < n_tiles; ++j) {
-          const int bt = j % C::kNSt;
-          const int s = j % (C::kShared ? C::kKS : C::kVS);
-          const uint32_t sphase = (j / (C::kShared ? C::kKS : C::kVS)) & 1;
-          ok = mbar_wait(&bars->p_full[bt], (j / C::kNSt) & 1, abort_flag, status, kStatusTimeout) &&
-               mbar_wait(C::kShared ? &bars->k_full[s] : &bars->v_full[s], sphase, abort_flag, status,
-                         kStatusTimeout);
-          if (!ok) break;
-          tc_fence_after_sync();
-          // dK/dV pass: dO, then Q (shared stage: X2 = dO after X1 = Q).  dQ pass: K (X1).
-          const uint64_t dV = off(dV0, C::kShared ? s * C::kKUnit : s * C::kVStage);
-          const uint32_t dO_off = C::kShared ? C::kUC * C::kChunkX : 0;
-          const uint32_t q_off = C::kShared ? 0 : C::kVC * C::kChunkX;
-          const uint32_t a0 = tmem + C::kColSt + 64u * bt;  // dQ: dS;  dK/dV: P^T (then dS^T at +32)
-#pragma unroll
-          for (int kk = 0; kk < C::kBN / 16; ++kk) {
-            const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
-            if (C::kDKDV) {
-              mma_ts(tmem + C::kColAcc1, a0 + kk * 8, off(dV, dO_off + kk * 2048), kIdPV, acc);  // dV += P^T dO
-              mma_ts(tmem + C::kColAcc2, a0 + 32 + kk * 8, off(dV, q_off + kk * 2048), kIdPV,
-                     acc);  // dK += dS^T Q
-            } else {
-              mma_ts(tmem + C::kColAcc1, a0 + kk * 8, off(dV, kk * 2048), kIdPV, acc);  // dQ += dS K
-            }
-          }
-          mma_commit(C::kShared ? &bars->k_empty[s] : &bars->v_empty[s]);
-          mma_commit(&bars->pv_done[bt]);
-        }
-        if (ok) mma_commit(&bars->acc_done);
-        mma_commit(&bars->drain);
-        mbar_wait(&bars->drain, 0, &no_abort, nullptr, 0);
-      }
-    }
-  } else {
     // ---------------- elementwise + epilogue: one resident row per thread; group 0
     // (warps 4-7) takes the even tiles, group 1 (warps 8-11) the odd ones ----------------
     const int group = (warp - 4) >> 2;
@@ -660,6 +471,196 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           __syncwarp();  // the next chunk overwrites the stage
+        }
+      }
+    }
+  } else {
+    setmaxnreg_dec<kRegsIssue>();
+    if (warp == 0) {
+      // ---------------- TMA producer: resident tiles, then the score-tile ring (X1, X2) and
+      // the value-tile ring, each refilled as soon as its own stage is free (the thread polls
+      // both; the value ring frees much later than the score ring) ----------------
+      if (lane == 0) {
+        prefetch_tensormap(&maps.r1);
+        prefetch_tensormap(&maps.r2);
+        prefetch_tensormap(&maps.x1);
+        prefetch_tensormap(&maps.x2);
+        mbar_arrive_expect_tx(&bars->r_full, 2 * C::kRBytes);
+        for (int c = 0; c < C::kDC; ++c) {
+          tma_load_4d(smem + C::kOffR1 + c * C::kChunkR, &maps.r1, &bars->r_full, c * 64, r0, hh, bb);
+          tma_load_4d(smem + C::kOffR2 + c * C::kChunkR, &maps.r2, &bars->r_full, c * 64, r0, hh, bb);
+        }
+        int tk = 0, tv = 0, tq = 0;  // next tile of each ring (tq: the vector ring)
+        const int nq = C::kDKDV ? n_tiles : 0;
+        const int nv = C::kShared ? 0 : n_tiles;  // tiles of the value ring of its own
+        bool ok = true;
+        uint64_t t0 = globaltimer_ns();
+        uint32_t idle = 0;
+        while (tk < n_tiles * C::kUPT || tv < nv || tq < nq) {
+          bool progressed = false;
+          if (tq < nq && mbar_test_wait(&bars->vec_empty[tq % C::kVecS], ((tq / C::kVecS) & 1) ^ 1)) {
+            const int sq = tq % C::kVecS;
+            float* vec = reinterpret_cast<float*>(smem + C::kOffVec + sq * C::kVecSlot);
+            mbar_arrive_expect_tx(&bars->vec_full[sq], C::kVecSlot);
+            tma_load_2d(vec, &maps.nl2, &bars->vec_full[sq], str0 + tq * C::kBN, bh);
+            tma_load_2d(vec + 64, &maps.nd, &bars->vec_full[sq], str0 + tq * C::kBN, bh);
+            ++tq;
+            progressed = true;
+          }
+          // tk counts score-ring units: unit u of streamed tile tk / kUPT
+          if (tk < n_tiles * C::kUPT && mbar_test_wait(&bars->k_empty[tk % C::kKU], ((tk / C::kKU) & 1) ^ 1)) {
+            const int s = tk % C::kKU;
+            const int row0 = str0 + (tk / C::kUPT) * C::kBN, u = tk % C::kUPT;
+            uint8_t* st = smem + C::kOffK + s * C::kKUnit;
+            mbar_arrive_expect_tx(&bars->k_full[s], C::kKUnit);
+            for (int c = 0; c < C::kUC; ++c) {
+              const int col = (u * C::kUC + c) * 64;
+              tma_load_4d(st + c * C::kChunkX, &maps.x1, &bars->k_full[s], col, row0, hh, bb);
+              tma_load_4d(st + (C::kUC + c) * C::kChunkX, &maps.x2, &bars->k_full[s], col, row0, hh, bb);
+            }
+            ++tk;
+            progressed = true;
+          }
+          if (tv < nv && mbar_test_wait(&bars->v_empty[tv % C::kVS], ((tv / C::kVS) & 1) ^ 1)) {
+            const int sv = tv % C::kVS;
+            const int row0 = str0 + tv * C::kBN;
+            uint8_t* vt = smem + C::kOffV + sv * C::kVStage;
+            mbar_arrive_expect_tx(&bars->v_full[sv], C::kVStage);
+            for (int c = 0; c < C::kVC; ++c) {  // this CTA's gradient columns
+              const int col = vh * C::kDV + c * 64;
+              if (C::kDKDV) {  // dO (for dV), then Q (for dK)
+                tma_load_4d(vt + c * C::kChunkX, &maps.x2, &bars->v_full[sv], col, row0, hh, bb);
+                tma_load_4d(vt + (C::kVC + c) * C::kChunkX, &maps.x1, &bars->v_full[sv], col, row0, hh, bb);
+              } else {  // K (for dQ)
+                tma_load_4d(vt + c * C::kChunkX, &maps.x1, &bars->v_full[sv], col, row0, hh, bb);
+              }
+            }
+            ++tv;
+            progressed = true;
+          }
+          if (progressed) {
+            t0 = globaltimer_ns();
+            idle = 0;
+            continue;
+          }
+          __nanosleep(64);
+          // Bounded: a second without either ring moving means a broken protocol.
+          if ((++idle & 15u) == 0u) {
+            if (*abort_flag) {
+              ok = false;
+            } else if (globaltimer_ns() - t0 > kWaitLimitNs) {
+              *abort_flag = 1;
+              atomicOr(status, kStatusTimeout);
+              ok = false;
+            }
+            if (!ok) break;
+          }
+        }
+        // Let copies still in flight land before the CTA's shared memory goes away, on the
+        // normal path too (another role may give up right after the last copy was issued).
+        volatile int no_abort = 0;
+        mbar_wait(&bars->r_full, 0, &no_abort, nullptr, 0);
+        for (int n = tk - C::kKU; n < tk; ++n)
+          if (n >= 0) mbar_wait(&bars->k_full[n % C::kKU], (n / C::kKU) & 1, &no_abort, nullptr, 0);
+        for (int t = tv - C::kVS; t < tv; ++t)
+          if (t >= 0) mbar_wait(&bars->v_full[t % C::kVS], (t / C::kVS) & 1, &no_abort, nullptr, 0);
+        for (int t = tq - C::kVecS; t < tq; ++t)
+          if (t >= 0) mbar_wait(&bars->vec_full[t % C::kVecS], (t / C::kVecS) & 1, &no_abort, nullptr, 0);
+      }
+    } else {
+      // ---------------- tcgen05.mma issuers: warp 3 S1, warp 2 S2, warp 1 the value MMAs ----------------
+      if (lane == 0) {
+        constexpr uint32_t kIdS = make_idesc_bf16_f32(128, C::kBN, false, false);  // both K-major
+        constexpr uint32_t kIdPV = make_idesc_bf16_f32(128, C::kDV, false, true);  // B N-major
+        const uint64_t dR1 = make_smem_desc_sw128(smem_u32(smem + C::kOffR1), 16, 1024);
+        const uint64_t dR2 = make_smem_desc_sw128(smem_u32(smem + C::kOffR2), 16, 1024);
+        const uint64_t dK0 = make_smem_desc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
+        // B operands of the value MMAs: a stage of the shared ring (X1 chunks, then X2
+        // chunks) or of the value ring of its own
+        const uint64_t dV0 =
+            make_smem_desc_sw128(smem_u32(smem + (C::kShared ? C::kOffK : C::kOffV)), C::kChunkX, 1024);
+        auto off = [](uint64_t desc, uint32_t bytes) { return desc + static_cast<uint64_t>(bytes >> 4); };
+        volatile int no_abort = 0;
+        if (warp == 3 || warp == 2) {
+          // S1 = R1 X1^T (warp 3) or S2 = R2 X2^T (warp 2), d-deep, N = 64.
+          const bool first = warp == 3;
+          const uint64_t dA = first ? dR1 : dR2;
+          const uint32_t aT = tmem + (first ? C::kColR1 : C::kColR2);  // dQ pass: A in TMEM
+          const uint32_t xoff = first ? 0u : static_cast<uint32_t>(C::kUC * C::kChunkX);
+          bool ok = C::kRTmem ? mbar_wait(&bars->r_tmem, 0, abort_flag, status, kStatusTimeout)
+                              : mbar_wait(&bars->r_full, 0, abort_flag, status, kStatusTimeout);
+          for (int t = 0; ok && t < n_tiles; ++t) {
+            const int b = first ? t % C::kNS : t % C::kNSt;
+            const int bs = first ? t % C::kSBar : b;  // barrier slot
+            const uint32_t dst = tmem + (first ? C::kColS : C::kColSt) + 64u * b;
+  #pragma unroll 1
+            for (int u = 0; u < C::kUPT; ++u) {
+              const int n = t * C::kUPT + u;
+              const int s = n % C::kKU;
+              ok = mbar_wait(&bars->k_full[s], (n / C::kKU) & 1, abort_flag, status, kStatusTimeout);
+              // S1 buffers are free once the elementwise warps loaded tile t - NS; S2 buffers
+              // hold the packed operands of tile t - NSt until its value MMAs are done.
+              if (ok && u == 0 && first && t >= C::kNS)
+                ok = mbar_wait(&bars->s_free[(t - C::kNS) % C::kSBar], ((t - C::kNS) / C::kSBar) & 1, abort_flag,
+                               status, kStatusTimeout);
+              if (ok && u == 0 && !first && t >= C::kNSt)
+                ok = mbar_wait(&bars->pv_done[b], ((t - C::kNSt) / C::kNSt) & 1, abort_flag, status,
+                               kStatusTimeout);
+              if (!ok) break;
+              tc_fence_after_sync();
+              const uint64_t dX = off(dK0, s * C::kKUnit + xoff);
+  #pragma unroll
+              for (int c = 0; c < C::kUC; ++c)
+  #pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                  const int cg = u * C::kUC + c;  // d-chunk of the resident operand
+                  if constexpr (C::kRTmem)
+                    mma_ts(dst, aT + (cg * 4 + kk) * 8, off(dX, c * C::kChunkX + kk * 32), kIdS, (u | c | kk) != 0);
+                  else
+                    mma_ss(dst, off(dA, cg * C::kChunkR + kk * 32), off(dX, c * C::kChunkX + kk * 32), kIdS,
+                           (u | c | kk) != 0);
+                }
+              mma_commit(&bars->k_empty[s]);
+            }
+            if (!ok) break;
+            mma_commit(first ? &bars->s_full[bs] : &bars->st_full[b]);
+          }
+          uint64_t* drain = first ? &bars->drain_s : &bars->drain_st;
+          mma_commit(drain);
+          mbar_wait(drain, 0, &no_abort, nullptr, 0);
+        } else {
+          bool ok = true;
+          for (int j = 0; ok && j < n_tiles; ++j) {
+            const int bt = j % C::kNSt;
+            const int s = j % (C::kShared ? C::kKS : C::kVS);
+            const uint32_t sphase = (j / (C::kShared ? C::kKS : C::kVS)) & 1;
+            ok = mbar_wait(&bars->p_full[bt], (j / C::kNSt) & 1, abort_flag, status, kStatusTimeout) &&
+                 mbar_wait(C::kShared ? &bars->k_full[s] : &bars->v_full[s], sphase, abort_flag, status,
+                           kStatusTimeout);
+            if (!ok) break;
+            tc_fence_after_sync();
+            // dK/dV pass: dO, then Q (shared stage: X2 = dO after X1 = Q).  dQ pass: K (X1).
+            const uint64_t dV = off(dV0, C::kShared ? s * C::kKUnit : s * C::kVStage);
+            const uint32_t dO_off = C::kShared ? C::kUC * C::kChunkX : 0;
+            const uint32_t q_off = C::kShared ? 0 : C::kVC * C::kChunkX;
+            const uint32_t a0 = tmem + C::kColSt + 64u * bt;  // dQ: dS;  dK/dV: P^T (then dS^T at +32)
+  #pragma unroll
+            for (int kk = 0; kk < C::kBN / 16; ++kk) {
+              const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+              if (C::kDKDV) {
+                mma_ts(tmem + C::kColAcc1, a0 + kk * 8, off(dV, dO_off + kk * 2048), kIdPV, acc);  // dV += P^T dO
+                mma_ts(tmem + C::kColAcc2, a0 + 32 + kk * 8, off(dV, q_off + kk * 2048), kIdPV,
+                       acc);  // dK += dS^T Q
+              } else {
+                mma_ts(tmem + C::kColAcc1, a0 + kk * 8, off(dV, kk * 2048), kIdPV, acc);  // dQ += dS K
+              }
+            }
+            mma_commit(C::kShared ? &bars->k_empty[s] : &bars->v_empty[s]);
+            mma_commit(&bars->pv_done[bt]);
+          }
+          if (ok) mma_commit(&bars->acc_done);
+          mma_commit(&bars->drain);
+          mbar_wait(&bars->drain, 0, &no_abort, nullptr, 0);
         }
       }
     }
