@@ -31,8 +31,8 @@ def fwd_config(D, DVF):
     kDC = D // 64
     kDV = 128 if DVF > 128 else DVF
     kVC = kDV // 64
-    NS = 3 if kDV == 64 else 1
-    NSt = 3
+    NS = 1
+    NSt = 5 if kDV == 64 else 3
     chunk_q, chunk_k = 128 * 128, 64 * 128
     q_bytes = kDC * chunk_q
     k_stage, v_stage = 2 * kDC * chunk_k, 2 * kVC * chunk_k

@@ -17,7 +17,7 @@ PAIRS = [(d, dv) for d in (64, 128, 256) for dv in (64, 128, 256)]
 def test_configs_match_the_kernel_sizes():
     # the combinations the design notes list: 3 stages at 64, 2 at 128, one
     # tile in two units at 256 (Q/K dim), and the TMEM buffers by value dim
-    assert fwd_config(64, 64) == dict(NS=3, NSt=3, KS=3, VS=3, UPT=1, KU=3)
+    assert fwd_config(64, 64) == dict(NS=1, NSt=5, KS=3, VS=3, UPT=1, KU=3)
     assert fwd_config(128, 128) == dict(NS=1, NSt=3, KS=2, VS=2, UPT=1, KU=2)
     assert fwd_config(256, 256) == dict(NS=1, NSt=3, KS=1, VS=1, UPT=2, KU=2)
     assert fwd_config(256, 64)["KS"] == 1 and fwd_config(128, 64)["KS"] == 3
