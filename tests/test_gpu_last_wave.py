@@ -224,3 +224,31 @@ def test_image_dit_workload_cut_rows_at_full_size(cuda_lib):
         assert_close(g[1], ref[1], "Ot")
         assert_close(g[3], ref[3], "mu")
         assert np.max(np.abs(g[2] - ref[2])) <= 1e-3
+
+
+def test_cut_into_the_most_pieces(cuda_lib):
+    """One unit past a whole wave, over 4096 keys: the lone unit is cut into the most
+    pieces (16 of four key tiles each).  Its rows against the oracle, and a second
+    identical call bit for bit (the cut and its merge are deterministic)."""
+    import oracle
+    from helpers import host64
+    n_sm = _sm_count()
+    B, H, Nq, Nkv, d = 1, n_sm + 1, 128, 4096, 64
+    assert binding.attn_jvp_fwd_last_wave_split(B, H, Nq, Nkv, d) == 16
+    g = torch.Generator(device="cuda").manual_seed(131)
+    mk = lambda n: torch.randn((B, H, n, d), generator=g, device="cuda").to(torch.bfloat16)  # noqa: E731
+    q, qt, k, kt, v, vt = mk(Nq), mk(Nq), mk(Nkv), mk(Nkv), mk(Nkv), mk(Nkv)
+    s = d ** -0.5
+    got = binding.attn_jvp_fwd_strided(q, k, v, qt, kt, vt, scale=s)
+    ref = binding.attn_jvp_fwd_strided(q, k, v, qt, kt, vt, scale=s, kv_start=0, kv_len=Nkv)
+    torch.cuda.synchronize()
+    binding.attn_jvp_status()
+    h = H - 1
+    o = oracle.attn_jvp(host64(q[0, h]), host64(k[0, h]), host64(v[0, h]), host64(qt[0, h]), host64(kt[0, h]),
+                        host64(vt[0, h]), s)
+    assert_close(host64(got[0][0, h]), o[0], "O")
+    assert_close(host64(got[1][0, h]), o[1], "Ot")
+    assert_close(host64(got[3][0, h]), o[3], "mu")
+    assert np.max(np.abs(host64(got[2][0, h]) - o[2])) <= 1e-3
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)  # the same call twice: the cut is deterministic
